@@ -1,0 +1,342 @@
+/*
+ * oracle.c -- CPU reference for the batch-invariant linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path (the
+ * CUDA library and its Python binding) never calls it and shares no code with
+ * it: no headers, helpers, tables or constants.
+ *
+ * What it computes, and the passages it follows:
+ *   - bf16 storage, fp32 arithmetic.  A bf16 value is the top 16 bits of an
+ *     IEEE binary32 value, so decoding is exact.
+ *   - GEMM  Y = X . W^T  (the nn.Linear layout) with fp32 accumulation.  Every
+ *     output element is one dot product summed sequentially in ascending k:
+ *     acc = 0; acc = acc + x_k * w_k.  This is the "a+b+c+d" chain of
+ *     CoRun (Padding is Simple and Efficient for Deterministic LLM Inference),
+ *     Sec. III-A, Fig. 3, and the non-split reduction of LLM-42, Sec. 2.2,
+ *     Fig. 3.  A product of two bf16 values has at most 16 significant bits,
+ *     so it is exact in fp32; only the additions round.
+ *   - RMSNorm, a per-token reduction over the hidden dimension (LLM-42,
+ *     Sec. 2.1).  The pages name the operator but never write its formula; the
+ *     reading used here is the usual one:
+ *        ss = sum_h x_h^2 (sequential fp32), r = 1 / sqrt(ss / H + eps),
+ *        y_h = bf16_rne((x_h * r) * g_h)
+ *     with one rounding to bf16 at the end.
+ *   - The fused layer RMSNorm -> GEMM is the composition through the bf16
+ *     normalised activations.
+ *   - One decode layer of a Llama-style stack (for the linear-stack
+ *     workload): RMSNorm, qkv projection, an attention stand-in for context
+ *     length 1 (softmax over one key is exactly 1, so each query head's output
+ *     is the value vector of its key/value group), output projection,
+ *     residual, RMSNorm, gate/up projection, SiLU(gate) * up, down projection,
+ *     residual.
+ *
+ * Every output row is computed from that row's inputs alone, so the results
+ * cannot depend on the number of rows or on the other rows (batch invariance
+ * as defined in CoRun, Sec. III-B, Def. 1, and Detent, Sec. 3, Eq. 2, holds by
+ * construction).
+ *
+ * Build with -ffp-contract=off so that no multiply-add is fused: each product
+ * and each sum is rounded to fp32 separately, exactly as written.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> fp32                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Exact widening: the bf16 bits become the high half of a binary32. */
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Round-to-nearest-even narrowing of a binary32 to bf16.
+ * NaN stays NaN (its quiet bit is forced on); everything else adds half an
+ * ulp of the 16 dropped bits, plus one more when the kept part is odd (ties go
+ * to even), and truncates.  Values past the largest bf16 round to infinity. */
+uint16_t oracle_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) {
+    return (uint16_t)((u >> 16) | 0x0040u);
+  }
+  uint32_t keep_lsb = (u >> 16) & 1u;
+  u = u + 0x7fffu + keep_lsb;
+  return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------ */
+/* A tiny fork/join helper: split [0, total) into nthreads contiguous parts. */
+/* Each output element is computed by exactly one thread with the same code */
+/* as the single-threaded loop, so the thread count cannot change any bit.  */
+/* ------------------------------------------------------------------------ */
+
+typedef void (*range_fn)(void* ctx, int64_t lo, int64_t hi);
+
+typedef struct {
+  range_fn fn;
+  void* ctx;
+  int64_t lo, hi;
+} range_job;
+
+static void* range_thread(void* p) {
+  range_job* j = (range_job*)p;
+  j->fn(j->ctx, j->lo, j->hi);
+  return NULL;
+}
+
+static void parallel_for(range_fn fn, void* ctx, int64_t total, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > total) nthreads = (int)(total > 0 ? total : 1);
+  if (nthreads == 1) {
+    fn(ctx, 0, total);
+    return;
+  }
+  pthread_t tid[256];
+  range_job job[256];
+  int started[256];
+  for (int t = 0; t < nthreads; ++t) {
+    job[t].fn = fn;
+    job[t].ctx = ctx;
+    job[t].lo = total * t / nthreads;
+    job[t].hi = total * (t + 1) / nthreads;
+    started[t] = pthread_create(&tid[t], NULL, range_thread, &job[t]) == 0;
+    if (!started[t]) range_thread(&job[t]); /* no thread: do it inline */
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* One row: ss accumulates x_h * x_h in ascending h; the mean divides by H;
+ * r = 1 / sqrt(mean + eps) with the correctly rounded sqrt and division of
+ * IEEE binary32; y_h = bf16_rne((x_h * r) * g_h). */
+static void rmsnorm_row(const uint16_t* x, const uint16_t* g, uint16_t* y, int64_t H,
+                        float eps) {
+  float ss = 0.0f;
+  for (int64_t h = 0; h < H; ++h) {
+    float xh = oracle_bf16_to_f32(x[h]);
+    float sq = xh * xh;
+    ss = ss + sq;
+  }
+  float mean = ss / (float)H;
+  float r = 1.0f / sqrtf(mean + eps);
+  for (int64_t h = 0; h < H; ++h) {
+    float xh = oracle_bf16_to_f32(x[h]);
+    float scaled = xh * r;
+    float v = scaled * oracle_bf16_to_f32(g[h]);
+    y[h] = oracle_bf16_rne(v);
+  }
+}
+
+/* The inverse RMS of one row, as used inside rmsnorm_row. */
+float oracle_rmsnorm_inv_rms(const uint16_t* x, int64_t H, float eps) {
+  float ss = 0.0f;
+  for (int64_t h = 0; h < H; ++h) {
+    float xh = oracle_bf16_to_f32(x[h]);
+    float sq = xh * xh;
+    ss = ss + sq;
+  }
+  float mean = ss / (float)H;
+  return 1.0f / sqrtf(mean + eps);
+}
+
+typedef struct {
+  const uint16_t *X, *g;
+  uint16_t* Y;
+  int64_t H;
+  float eps;
+} rms_ctx;
+
+static void rms_range(void* p, int64_t lo, int64_t hi) {
+  rms_ctx* c = (rms_ctx*)p;
+  for (int64_t m = lo; m < hi; ++m) rmsnorm_row(c->X + m * c->H, c->g, c->Y + m * c->H, c->H, c->eps);
+}
+
+/* X [M,H] bf16, g [H] bf16 -> Y [M,H] bf16. */
+void oracle_rmsnorm(const uint16_t* X, const uint16_t* g, uint16_t* Y, int64_t M, int64_t H,
+                    float eps, int nthreads) {
+  rms_ctx c = {X, g, Y, H, eps};
+  parallel_for(rms_range, &c, M, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* GEMM  Y = X . W^T                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* One output element: the sequential ascending-k fp32 chain. */
+static float dot_row(const uint16_t* x, const uint16_t* w, int64_t K) {
+  float acc = 0.0f;
+  for (int64_t k = 0; k < K; ++k) {
+    float p = oracle_bf16_to_f32(x[k]) * oracle_bf16_to_f32(w[k]);
+    acc = acc + p;
+  }
+  return acc;
+}
+
+typedef struct {
+  const uint16_t *X, *W;
+  float* Yf;
+  uint16_t* Yb;
+  int64_t N, K;
+} gemm_ctx;
+
+static void gemm_range(void* p, int64_t lo, int64_t hi) {
+  gemm_ctx* c = (gemm_ctx*)p;
+  for (int64_t e = lo; e < hi; ++e) {
+    int64_t m = e / c->N, n = e % c->N;
+    float acc = dot_row(c->X + m * c->K, c->W + n * c->K, c->K);
+    if (c->Yf) c->Yf[e] = acc;
+    if (c->Yb) c->Yb[e] = oracle_bf16_rne(acc);
+  }
+}
+
+/* X [M,K] bf16, W [N,K] bf16 -> Yf [M,N] fp32 (may be NULL) and
+ * Yb [M,N] bf16 = bf16_rne(Yf) (may be NULL). */
+void oracle_gemm(const uint16_t* X, const uint16_t* W, float* Yf, uint16_t* Yb, int64_t M,
+                 int64_t N, int64_t K, int nthreads) {
+  gemm_ctx c = {X, W, Yf, Yb, N, K};
+  parallel_for(gemm_range, &c, M * N, nthreads);
+}
+
+typedef struct {
+  const uint16_t *X, *W;
+  const int64_t *rows, *cols;
+  float* out;
+  int64_t K;
+} sample_ctx;
+
+static void sample_range(void* p, int64_t lo, int64_t hi) {
+  sample_ctx* c = (sample_ctx*)p;
+  for (int64_t i = lo; i < hi; ++i)
+    c->out[i] = dot_row(c->X + c->rows[i] * c->K, c->W + c->cols[i] * c->K, c->K);
+}
+
+/* The fp32 result of chosen elements only: out[i] = Y[rows[i], cols[i]].
+ * Used to check full-size launches element by element. */
+void oracle_gemm_sampled(const uint16_t* X, const uint16_t* W, const int64_t* rows,
+                         const int64_t* cols, float* out, int64_t count, int64_t K,
+                         int nthreads) {
+  sample_ctx c = {X, W, rows, cols, out, K};
+  parallel_for(sample_range, &c, count, nthreads);
+}
+
+/* Fused layer: Xhat = RMSNorm(X; g, eps) in bf16, then Y = Xhat . W^T.
+ * Xhat_out may be NULL; otherwise it receives the bf16 normalised rows. */
+void oracle_rmsnorm_gemm(const uint16_t* X, const uint16_t* g, const uint16_t* W, float* Yf,
+                         uint16_t* Yb, uint16_t* Xhat_out, int64_t M, int64_t N, int64_t K,
+                         float eps, int nthreads) {
+  uint16_t* xh = Xhat_out ? Xhat_out : (uint16_t*)malloc((size_t)(M * K) * sizeof(uint16_t));
+  if (!xh) return;
+  oracle_rmsnorm(X, g, xh, M, K, eps, nthreads);
+  oracle_gemm(xh, W, Yf, Yb, M, N, K, nthreads);
+  if (!Xhat_out) free(xh);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode-layer glue                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* out = bf16_rne(a + b), both operands widened to fp32. */
+void oracle_residual_add(const uint16_t* a, const uint16_t* b, uint16_t* out, int64_t count) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = oracle_bf16_rne(oracle_bf16_to_f32(a[i]) + oracle_bf16_to_f32(b[i]));
+}
+
+/* SwiGLU activation on a [M, 2*I] gate/up block (gate = columns 0..I-1,
+ * up = columns I..2I-1):  out[m,i] = bf16_rne(silu(gate) * up), with
+ * silu(v) = v / (1 + exp(-v)) evaluated in fp32. */
+void oracle_silu_mul(const uint16_t* gu, uint16_t* out, int64_t M, int64_t I) {
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t i = 0; i < I; ++i) {
+      float gate = oracle_bf16_to_f32(gu[m * 2 * I + i]);
+      float up = oracle_bf16_to_f32(gu[m * 2 * I + I + i]);
+      float e = expf(-gate);
+      float den = 1.0f + e;
+      float s = gate / den;
+      float v = s * up;
+      out[m * I + i] = oracle_bf16_rne(v);
+    }
+  }
+}
+
+/* Attention stand-in at context length 1: the qkv row is
+ * [q (nq*D) | k (nkv*D) | v (nkv*D)]; query head j reads key/value group
+ * j / (nq / nkv), and with one key its softmax weight is exactly 1, so the
+ * head's output is that group's v vector copied unchanged. */
+void oracle_attention_ctx1(const uint16_t* qkv, uint16_t* out, int64_t M, int64_t nq,
+                           int64_t nkv, int64_t D) {
+  int64_t width = (nq + 2 * nkv) * D;
+  int64_t group = nq / nkv;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t j = 0; j < nq; ++j) {
+      const uint16_t* v = qkv + m * width + (nq + nkv) * D + (j / group) * D;
+      for (int64_t d = 0; d < D; ++d) out[m * nq * D + j * D + d] = v[d];
+    }
+  }
+}
+
+/* One decode layer, x_in [M,Hd] -> x_out [M,Hd]:
+ *   xn  = RMSNorm(x_in; g_attn)
+ *   qkv = xn . Wqkv^T                      Wqkv [(nq+2nkv)*D, Hd]
+ *   a   = attention_ctx1(qkv)              [M, nq*D]
+ *   o   = a . Wo^T                         Wo [Hd, nq*D]
+ *   h   = x_in + o
+ *   hn  = RMSNorm(h; g_mlp)
+ *   gu  = hn . Wgu^T                       Wgu [2I, Hd]
+ *   s   = silu(gate) * up                  [M, I]
+ *   d   = s . Wd^T                         Wd [Hd, I]
+ *   x_out = h + d
+ * Every intermediate is stored as bf16, as a layer of the stack stores it. */
+int oracle_decode_layer(const uint16_t* x_in, uint16_t* x_out, const uint16_t* g_attn,
+                        const uint16_t* Wqkv, const uint16_t* Wo, const uint16_t* g_mlp,
+                        const uint16_t* Wgu, const uint16_t* Wd, int64_t M, int64_t Hd,
+                        int64_t nq, int64_t nkv, int64_t D, int64_t I, float eps,
+                        int nthreads) {
+  int64_t qkv_w = (nq + 2 * nkv) * D;
+  uint16_t* xn = (uint16_t*)malloc((size_t)(M * Hd) * 2);
+  uint16_t* qkv = (uint16_t*)malloc((size_t)(M * qkv_w) * 2);
+  uint16_t* att = (uint16_t*)malloc((size_t)(M * nq * D) * 2);
+  uint16_t* o = (uint16_t*)malloc((size_t)(M * Hd) * 2);
+  uint16_t* h = (uint16_t*)malloc((size_t)(M * Hd) * 2);
+  uint16_t* hn = (uint16_t*)malloc((size_t)(M * Hd) * 2);
+  uint16_t* gu = (uint16_t*)malloc((size_t)(M * 2 * I) * 2);
+  uint16_t* s = (uint16_t*)malloc((size_t)(M * I) * 2);
+  uint16_t* d = (uint16_t*)malloc((size_t)(M * Hd) * 2);
+  int ok = xn && qkv && att && o && h && hn && gu && s && d;
+  if (ok) {
+    oracle_rmsnorm(x_in, g_attn, xn, M, Hd, eps, nthreads);
+    oracle_gemm(xn, Wqkv, NULL, qkv, M, qkv_w, Hd, nthreads);
+    oracle_attention_ctx1(qkv, att, M, nq, nkv, D);
+    oracle_gemm(att, Wo, NULL, o, M, Hd, nq * D, nthreads);
+    oracle_residual_add(x_in, o, h, M * Hd);
+    oracle_rmsnorm(h, g_mlp, hn, M, Hd, eps, nthreads);
+    oracle_gemm(hn, Wgu, NULL, gu, M, 2 * I, Hd, nthreads);
+    oracle_silu_mul(gu, s, M, I);
+    oracle_gemm(s, Wd, NULL, d, M, Hd, I, nthreads);
+    oracle_residual_add(h, d, x_out, M * Hd);
+  }
+  free(xn); free(qkv); free(att); free(o); free(h); free(hn); free(gu); free(s); free(d);
+  return ok ? 0 : -1;
+}
+
+/* Array forms of the two conversions, for callers that hold whole tensors. */
+void oracle_bf16_rne_array(const float* in, uint16_t* out, int64_t count) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_bf16_rne(in[i]);
+}
+
+void oracle_bf16_to_f32_array(const uint16_t* in, float* out, int64_t count) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_bf16_to_f32(in[i]);
+}

@@ -1,0 +1,442 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test fixes the oracle to an independent fact -- a hand-derived bit
+pattern, an exact integer result, a closed form, a textbook error bound against
+an fp64 brute force, or a worked summation-order example -- chosen so that a
+plausible mistake (a dropped term, a wrong sign or index, a transposed operand,
+a different summation order, a wrong rounding mode, eps outside the sqrt)
+fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from invariant_bi_gemm_bf16_gb300 import inputs
+
+U = 2.0 ** -24  # unit roundoff of binary32
+
+
+def f32_bits(x: float) -> int:
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+
+
+def bits_to_f32(b: int) -> float:
+    return float(np.array([b], dtype=np.uint32).view(np.float32)[0])
+
+
+def bf16_val(bits16) -> np.ndarray:
+    b = np.asarray(bits16, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+def gamma(n: int) -> float:
+    return n * U / (1 - n * U)
+
+
+def ordered(bits16: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> integers ordered like the values (sign-magnitude)."""
+    b = bits16.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def bf16_of_f64(x: np.ndarray) -> np.ndarray:
+    """Exact round-to-nearest-even of float64 values to bf16, via Fractions
+    (independent of the oracle's bit trick and of numpy's float32 cast)."""
+    out = []
+    for v in np.asarray(x, dtype=np.float64).ravel():
+        if v == 0:
+            out.append(0x8000 if math.copysign(1, v) < 0 else 0)
+            continue
+        s = 0x8000 if v < 0 else 0
+        a = Fraction(abs(float(v)))
+        e = math.floor(math.log2(a))
+        while Fraction(2) ** e > a:
+            e -= 1
+        while Fraction(2) ** (e + 1) <= a:
+            e += 1
+        # 8 significant bits: quantum 2^(e-7)
+        q = Fraction(2) ** (e - 7)
+        n = a / q
+        fl = math.floor(n)
+        rem = n - fl
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+            fl += 1
+        val = fl * q
+        fbits = f32_bits(float(val))
+        out.append(s | (fbits >> 16))
+    return np.array(out, dtype=np.uint16).reshape(np.shape(x))
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("f32_in, bf16_out", [
+    (0x3F800000, 0x3F80),   # 1.0
+    (0x3F808000, 0x3F80),   # 1 + 2^-8: exact tie, kept part even -> down
+    (0x3F818000, 0x3F82),   # 1 + 3*2^-8: exact tie, kept part odd -> up
+    (0x3F808001, 0x3F81),   # just above the tie -> up
+    (0x3F807FFF, 0x3F80),   # just below the tie -> down
+    (0xBF808001, 0xBF81),   # sign is carried
+    (0x80000000, 0x8000),   # -0
+    (0x7F800000, 0x7F80),   # +inf
+    (0xFF800000, 0xFF80),   # -inf
+    (0x7F7FFFFF, 0x7F80),   # FLT_MAX rounds past the largest bf16 -> inf
+    (0x7FC00000, 0x7FC0),   # quiet NaN
+    (0x7F800001, 0x7FC0),   # signalling NaN whose payload would truncate to inf -> stays NaN
+    (0x00010000, 0x0001),   # subnormal kept exactly
+    (0x00008000, 0x0000),   # smallest subnormal tie -> even (0)
+])
+def test_bf16_rne_bits(oracle, f32_in, bf16_out):
+    got = oracle.bf16_rne(np.array([bits_to_f32(f32_in)], dtype=np.float32))
+    assert int(got[0]) == bf16_out
+
+
+def test_bf16_rne_matches_exact_rounding(oracle):
+    r = np.random.default_rng(123)
+    x = (r.standard_normal(4000) * np.exp(r.uniform(-20, 20, 4000))).astype(np.float32)
+    got = oracle.bf16_rne(x)
+    want = bf16_of_f64(x.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# GEMM
+# ---------------------------------------------------------------------------
+
+def test_gemm_integer_inputs_exact(oracle):
+    """Integer inputs with small magnitudes: every partial sum is an integer below
+    2^24, so every summation order gives the exact integer product."""
+    X = inputs.integers((7, 300), -8, 8, seed=1, stream=0)
+    W = inputs.integers((13, 300), -8, 8, seed=1, stream=1)
+    Yf, Yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    exact = X.float().numpy().astype(np.int64) @ W.float().numpy().astype(np.int64).T
+    assert np.array_equal(Yf.astype(np.int64), exact)
+    assert np.array_equal(Yf, exact.astype(np.float32))
+
+
+def test_gemm_summation_order_worked_example(oracle):
+    """The order of the fp32 chain is the sequential a+b+c+d of CoRun Fig. 3.
+    With x = [1, 2^-24, 2^-24, 2^-24] and w = 1:
+      sequential ((1 + 2^-24) + 2^-24) + 2^-24: each step is a tie that rounds to
+        the even value 1, so the result is exactly 1;
+      the split-K tree (1 + 2^-24) + (2^-24 + 2^-24) gives 1 + 2^-23;
+      the reversed chain gives 1 + 3*2^-24, a tie that rounds to 1 + 2^-22.
+    Values derived by hand above; only the sequential order yields 1.0."""
+    x = np.array([[1.0, 2.0 ** -24, 2.0 ** -24, 2.0 ** -24]], dtype=np.float32)
+    w = np.ones((1, 4), dtype=np.float32)
+    Yf, _ = oracle.gemm(inputs.bits(inputs.to_bf16(x)), inputs.bits(inputs.to_bf16(w)))
+    assert Yf[0, 0] == np.float32(1.0)
+    # and the other orders really do differ (so the example is discriminating)
+    assert np.float32(1.0) + np.float32(2.0 ** -23) != np.float32(1.0)
+
+
+def test_gemm_identity_weights(oracle):
+    X = inputs.normal((9, 64), seed=2, stream=0)
+    Wf = np.eye(64, dtype=np.float32)
+    Yf, Yb = oracle.gemm(inputs.bits(X), inputs.bits(inputs.to_bf16(Wf)))
+    assert np.array_equal(Yb, inputs.bits(X))
+
+
+def test_gemm_permutation_weights(oracle):
+    X = inputs.normal((5, 48), seed=3, stream=0)
+    perm = np.random.default_rng(3).permutation(48)
+    Wf = np.zeros((48, 48), dtype=np.float32)
+    Wf[np.arange(48), perm] = 1.0  # y[n] = x[perm[n]]
+    _, Yb = oracle.gemm(inputs.bits(X), inputs.bits(inputs.to_bf16(Wf)))
+    assert np.array_equal(Yb, inputs.bits(X)[:, perm])
+
+
+def test_gemm_one_hot_rows(oracle):
+    """One non-zero per X row: y[m,n] = x[m,k_m] * w[n,k_m], a single exact product."""
+    K, M, N = 40, 6, 11
+    r = np.random.default_rng(4)
+    W = inputs.normal((N, K), std=0.02, seed=4, stream=1)
+    Xf = np.zeros((M, K), dtype=np.float32)
+    ks = r.integers(0, K, size=M)
+    Xf[np.arange(M), ks] = r.standard_normal(M).astype(np.float32)
+    X = inputs.to_bf16(Xf)
+    Yf, Yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    xv = X.double().numpy()
+    wv = W.double().numpy()
+    for m in range(M):
+        exact = xv[m, ks[m]] * wv[:, ks[m]]
+        assert np.array_equal(Yf[m].astype(np.float64), exact)
+        assert np.array_equal(Yb[m], bf16_of_f64(exact))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 17), (4, 7, 256), (2, 3, 4096)])
+def test_gemm_higham_bound(oracle, M, N, K):
+    """Recursive summation of K exact products: |fl(sum) - sum| <= gamma_{K-1} sum|p_k|
+    (Higham, Accuracy and Stability of Numerical Algorithms, Sec. 4.2)."""
+    X = inputs.normal((M, K), seed=5, stream=0)
+    W = inputs.normal((N, K), std=0.02, seed=5, stream=1)
+    Yf, Yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    xv = X.double().numpy()
+    wv = W.double().numpy()
+    exact = xv @ wv.T                    # products exact in fp64; fp64 sum error ~1e-16 relative
+    absdot = np.abs(xv) @ np.abs(wv).T
+    bound = gamma(max(K - 1, 0)) * absdot + 1e-300
+    assert np.all(np.abs(Yf.astype(np.float64) - exact) <= bound * (1 + 1e-9) + 1e-30)
+    # the bf16 output is the round-to-nearest-even of the fp32 result
+    assert np.array_equal(Yb, bf16_of_f64(Yf.astype(np.float64)))
+
+
+def test_gemm_transposition_and_dropped_term(oracle):
+    """A non-square case where X.W (instead of X.W^T) or a skipped last k fails."""
+    X = inputs.integers((2, 3), -3, 3, seed=6, stream=0)
+    W = inputs.integers((4, 3), -3, 3, seed=6, stream=1)
+    Yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    xv = X.float().numpy().astype(int)
+    wv = W.float().numpy().astype(int)
+    for m in range(2):
+        for n in range(4):
+            assert Yf[m, n] == sum(xv[m, k] * wv[n, k] for k in range(3))
+
+
+def test_gemm_sampled_matches_full(oracle):
+    X = inputs.normal((6, 96), seed=7, stream=0)
+    W = inputs.normal((10, 96), std=0.02, seed=7, stream=1)
+    Yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    rows = np.array([0, 5, 3, 3])
+    cols = np.array([9, 0, 4, 5])
+    s = oracle.gemm_sampled(inputs.bits(X), inputs.bits(W), rows, cols)
+    assert np.array_equal(s, Yf[rows, cols])
+
+
+def test_gemm_thread_count_does_not_change_bits(oracle):
+    X = inputs.normal((5, 512), seed=8, stream=0)
+    W = inputs.normal((37, 512), std=0.02, seed=8, stream=1)
+    a = oracle.gemm(inputs.bits(X), inputs.bits(W), nthreads=1)[0]
+    b = oracle.gemm(inputs.bits(X), inputs.bits(W), nthreads=7)[0]
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_gemm_batch_invariance_by_construction(oracle):
+    """Def. 1 of CoRun Sec. III-B on the oracle: a row's bits do not depend on
+    the batch size, its position, or its co-runners (including inf/nan rows)."""
+    K, N = 128, 24
+    W = inputs.bits(inputs.normal((N, K), std=0.02, seed=9, stream=1))
+    target = inputs.normal((3, K), seed=9, stream=0)
+    ref = oracle.gemm(inputs.bits(target), W)[0]
+    for batch, fill in [(3, None), (17, None), (64, float("nan")), (40, float("inf")), (33, 65504.0)]:
+        full, pos = inputs.scatter_rows(target, batch, seed=batch, corunner_fill=fill)
+        got = oracle.gemm(inputs.bits(full), W)[0]
+        assert np.array_equal(got[pos].view(np.uint32), ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+EPS = 1e-5
+
+
+def test_rmsnorm_zero_row(oracle):
+    X = np.zeros((2, 64), dtype=np.uint16)
+    g = inputs.bits(inputs.normal((64,), std=0.1, mean=1.0, seed=10, stream=2))
+    Y = oracle.rmsnorm(X, g, EPS)
+    assert np.all(bf16_val(Y) == 0)
+
+
+def test_rmsnorm_unit_rows_are_fixed_points(oracle):
+    """Rows of +-1 with gain 1: mean(x^2) = 1 exactly, r = 1/sqrt(1 + 1e-5) =
+    0.999995..., and bf16 rounds +-0.999995 to +-1 (the next bf16 below 1 is
+    0.99609375).  So Y == X bit for bit."""
+    r = np.random.default_rng(11)
+    Xf = np.where(r.random((4, 256)) < 0.5, -1.0, 1.0).astype(np.float32)
+    X = inputs.bits(inputs.to_bf16(Xf))
+    g = inputs.bits(inputs.to_bf16(np.ones(256, dtype=np.float32)))
+    assert np.array_equal(oracle.rmsnorm(X, g, EPS), X)
+
+
+@pytest.mark.parametrize("c", [1.0, 4.0, 0.0625, 1024.0])
+def test_rmsnorm_constant_magnitude_rows(oracle, c):
+    """Rows of +-c with gain 0.5: y = +-0.5 * c / sqrt(c^2 + eps), which rounds
+    to +-0.5 for these c (|c/sqrt(c^2+eps) - 1| < 2^-10)."""
+    r = np.random.default_rng(12)
+    sign = np.where(r.random((3, 128)) < 0.5, -1.0, 1.0)
+    X = inputs.bits(inputs.to_bf16((sign * c).astype(np.float32)))
+    g = inputs.bits(inputs.to_bf16(np.full(128, 0.5, dtype=np.float32)))
+    Y = bf16_val(oracle.rmsnorm(X, g, EPS))
+    assert np.array_equal(Y, (0.5 * sign).astype(np.float32))
+
+
+def test_rmsnorm_eps_inside_sqrt(oracle):
+    """Tiny rows where eps dominates: y = x / sqrt(x^2 + eps) * g.  With x = 2^-10:
+    mean = 2^-20, r = 1/sqrt(2^-20 + 1e-5) ~ 302.5 (eps outside the sqrt, or added
+    to the root, gives very different values)."""
+    x = 2.0 ** -10
+    X = inputs.bits(inputs.to_bf16(np.full((1, 64), x, dtype=np.float32)))
+    g = inputs.bits(inputs.to_bf16(np.ones(64, dtype=np.float32)))
+    Y = oracle.rmsnorm(X, g, EPS)
+    want = bf16_of_f64(np.array([x / math.sqrt(x * x + float(np.float32(EPS)))]))
+    diff = np.abs(ordered(Y[0]) - int(ordered(want)[0]))
+    assert diff.max() <= 1
+
+
+@pytest.mark.parametrize("H", [8, 256, 4096])
+def test_rmsnorm_fp64_brute_force(oracle, H):
+    """Against an fp64 evaluation of the same formula: within one bf16 ulp, and
+    the inverse RMS within Higham's bound for the sum of squares plus the few
+    roundings of the mean, sqrt and division."""
+    X = inputs.rows_loguniform(16, H, seed=13, stream=0)
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=13, stream=2)
+    Y = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
+    xv = X.double().numpy()
+    gv = g.double().numpy()
+    eps32 = float(np.float32(EPS))
+    ss = (xv * xv).sum(axis=1)
+    r_exact = 1.0 / np.sqrt(ss / H + eps32)
+    want = bf16_of_f64((xv * r_exact[:, None]) * gv[None, :])
+    assert np.abs(ordered(Y) - ordered(want)).max() <= 1
+    for m in range(16):
+        r_or = float(oracle.inv_rms(inputs.bits(X[m]), EPS))
+        rel = abs(r_or - r_exact[m]) / r_exact[m]
+        assert rel <= 0.5 * gamma(H - 1) + 4 * U
+
+
+def test_rmsnorm_row_independence(oracle):
+    H = 256
+    g = inputs.bits(inputs.normal((H,), std=0.1, mean=1.0, seed=14, stream=2))
+    target = inputs.rows_loguniform(2, H, seed=14, stream=0)
+    ref = oracle.rmsnorm(inputs.bits(target), g, EPS)
+    full, pos = inputs.scatter_rows(target, 37, seed=14, corunner_fill=float("nan"))
+    got = oracle.rmsnorm(inputs.bits(full), g, EPS)
+    assert np.array_equal(got[pos], ref)
+
+
+def test_rmsnorm_gemm_is_the_composition(oracle):
+    X = inputs.normal((5, 256), seed=15, stream=0)
+    g = inputs.normal((256,), std=0.1, mean=1.0, seed=15, stream=2)
+    W = inputs.normal((64, 256), std=0.02, seed=15, stream=1)
+    Yf, Yb, Xh = oracle.rmsnorm_gemm(inputs.bits(X), inputs.bits(g), inputs.bits(W), EPS)
+    Xh2 = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
+    assert np.array_equal(Xh, Xh2)
+    Yf2, Yb2 = oracle.gemm(Xh2, inputs.bits(W))
+    assert np.array_equal(Yf.view(np.uint32), Yf2.view(np.uint32))
+    assert np.array_equal(Yb, Yb2)
+
+
+def test_rmsnorm_gemm_closed_form(oracle):
+    """+-1 rows, gain 1 (normalisation is the identity, see above) into identity
+    weights: the fused layer returns X."""
+    r = np.random.default_rng(16)
+    Xf = np.where(r.random((3, 64)) < 0.5, -1.0, 1.0).astype(np.float32)
+    X = inputs.bits(inputs.to_bf16(Xf))
+    g = inputs.bits(inputs.to_bf16(np.ones(64, dtype=np.float32)))
+    W = inputs.bits(inputs.to_bf16(np.eye(64, dtype=np.float32)))
+    _, Yb, _ = oracle.rmsnorm_gemm(X, g, W, EPS)
+    assert np.array_equal(Yb, X)
+
+
+# ---------------------------------------------------------------------------
+# decode-layer glue
+# ---------------------------------------------------------------------------
+
+def test_silu_mul_closed_forms(oracle):
+    gate = np.array([[0.0, 20.0, -20.0, 1.0, -1.0, 2.0]], dtype=np.float32)
+    up = np.array([[3.0, 1.0, 1.0, 1.0, 1.0, -0.5]], dtype=np.float32)
+    gu = inputs.bits(inputs.to_bf16(np.concatenate([gate, up], axis=1)))
+    got = oracle.silu_mul(gu)
+    g64 = gate.astype(np.float64)
+    want = bf16_of_f64(g64 / (1 + np.exp(-g64)) * up.astype(np.float64))
+    assert np.abs(ordered(got) - ordered(want)).max() <= 1
+    assert bf16_val(got)[0, 0] == 0.0          # silu(0) = 0
+    assert bf16_val(got)[0, 1] == 20.0         # silu(20) = 20 / (1 + 2e-9) rounds to 20
+
+
+def test_residual_add_exact(oracle):
+    a = inputs.integers((4, 32), -100, 100, seed=17, stream=0)
+    b = inputs.integers((4, 32), -100, 100, seed=17, stream=1)
+    got = bf16_val(oracle.residual_add(inputs.bits(a), inputs.bits(b)))
+    assert np.array_equal(got, (a.float() + b.float()).numpy())
+
+
+def test_attention_ctx1_routing(oracle):
+    """nq=4 query heads, nkv=2 groups, D=2: heads 0,1 read v group 0 and heads 2,3
+    read v group 1 (hand-written expectation)."""
+    q = [1, 2, 3, 4, 5, 6, 7, 8]
+    k = [9, 10, 11, 12]
+    v = [13, 14, 15, 16]
+    qkv = inputs.bits(inputs.to_bf16(np.array([q + k + v], dtype=np.float32)))
+    got = bf16_val(oracle.attention_ctx1(qkv, 4, 2, 2))
+    assert got.tolist() == [[13, 14, 13, 14, 15, 16, 15, 16]]
+
+
+def _layer(Hd, nq, nkv, D, I, seed, zero=False):
+    def w(shape, stream):
+        if zero:
+            return inputs.bits(inputs.to_bf16(np.zeros(shape, dtype=np.float32)))
+        return inputs.bits(inputs.normal(shape, std=0.02, seed=seed, stream=stream))
+    return {
+        "g_attn": inputs.bits(inputs.normal((Hd,), std=0.1, mean=1.0, seed=seed, stream=2)),
+        "g_mlp": inputs.bits(inputs.normal((Hd,), std=0.1, mean=1.0, seed=seed, stream=3)),
+        "Wqkv": w(((nq + 2 * nkv) * D, Hd), 4),
+        "Wo": w((Hd, nq * D), 5),
+        "Wgu": w((2 * I, Hd), 6),
+        "Wd": w((Hd, I), 7),
+    }
+
+
+def test_decode_layer_zero_weights_is_identity(oracle):
+    x = inputs.bits(inputs.normal((3, 32), seed=18, stream=0))
+    layer = _layer(32, 4, 2, 8, 48, seed=18, zero=True)
+    assert np.array_equal(oracle.stack(x, [layer, layer], 4, 2, 8, EPS), x)
+
+
+def test_decode_layer_attention_path_wiring(oracle):
+    """Wgu = Wd = 0 and selector weights: Wqkv's v rows copy the normalised
+    input, Wo sums head copies onto the hidden dims.  Then
+    out = x + bf16(sum over heads of the routed v), checked against numpy."""
+    Hd, nq, nkv, D, I = 8, 4, 2, 4, 16
+    layer = _layer(Hd, nq, nkv, D, I, seed=19, zero=True)
+    Wqkv = np.zeros(((nq + 2 * nkv) * D, Hd), dtype=np.float32)
+    for j in range(nkv * D):                     # v rows: v = xn (hidden 8 = nkv*D)
+        Wqkv[(nq + nkv) * D + j, j] = 1.0
+    Wo = np.zeros((Hd, nq * D), dtype=np.float32)
+    for j in range(nq):                          # o[d] = head j's v[d] for heads 0 and 2
+        if j % 2 == 0:
+            for d in range(D):
+                Wo[(j // 2) * D + d, j * D + d] = 1.0
+    layer["Wqkv"] = inputs.bits(inputs.to_bf16(Wqkv))
+    layer["Wo"] = inputs.bits(inputs.to_bf16(Wo))
+    x = inputs.bits(inputs.normal((2, Hd), seed=19, stream=0))
+    out = oracle.decode_layer(x, layer, nq, nkv, D, EPS)
+    xn = oracle.rmsnorm(x, layer["g_attn"], EPS)
+    # head 0 reads group 0 = xn[:, 0:4]; head 2 reads group 1 = xn[:, 4:8]
+    o = np.concatenate([xn[:, 0:4], xn[:, 4:8]], axis=1)
+    want = bf16_of_f64(bf16_val(x).astype(np.float64) + bf16_val(o).astype(np.float64))
+    assert np.array_equal(out, want)
+
+
+def test_rmsnorm_single_final_rounding(oracle):
+    """The reading adopted for RMSNorm rounds once, after the gain: bf16((x*r)*g).
+    The alternative (round x*r to bf16, then multiply by g and round again) gives
+    a different value for some gains.  Rows of +-2^-6 make x*r = 1/sqrt(1 +
+    eps/c^2) ~ 0.98013, visibly below 1; a gain is searched (in fp64, by exact
+    rounding, independent of the oracle) for which the two readings differ with
+    a wide margin, and the oracle must give the single-rounding value."""
+    c = 2.0 ** -6
+    eps32 = float(np.float32(EPS))
+    xr = c / math.sqrt(c * c + eps32)            # ~0.98013, not near a bf16 midpoint
+    xr_b = float(bf16_val(bf16_of_f64(np.array([xr])))[0])
+    chosen = None
+    for k in range(128):
+        gv = 1.0 + k / 128.0                      # bf16 values in [1, 2)
+        single = bf16_of_f64(np.array([xr * gv]))[0]
+        double = bf16_of_f64(np.array([xr_b * gv]))[0]
+        q = 2.0 ** -7                             # bf16 quantum in [1, 2)
+        frac = (xr * gv / q) % 1.0
+        if single != double and abs(frac - 0.5) > 0.01:
+            chosen = (gv, single, double)
+            break
+    assert chosen is not None
+    gv, single, double = chosen
+    X = inputs.bits(inputs.to_bf16(np.full((1, 64), c, dtype=np.float32)))
+    g = inputs.bits(inputs.to_bf16(np.full(64, gv, dtype=np.float32)))
+    Y = oracle.rmsnorm(X, g, EPS)
+    assert np.all(Y == single) and single != double
