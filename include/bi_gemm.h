@@ -1,0 +1,225 @@
+/*
+ * bi_gemm.h -- C ABI of the batch-invariant bf16 linear layer (GB300, sm_103a).
+ *
+ * What the library computes
+ *   GEMM      Y[M,N] = X[M,K] . W[N,K]^T, bf16 storage, fp32 accumulation,
+ *             round-to-nearest-even to bf16 at the end.
+ *   RMSNorm   y_h = bf16_rne((x_h * r) * g_h),  r = 1 / sqrt(mean_h(x_h^2) + eps),
+ *             per row, with fp32 arithmetic.
+ *   Fused     RMSNorm followed by the GEMM, bit for bit equal to the two calls
+ *             made one after the other.
+ *   Glue      the element-wise steps of a Llama-style decode layer (residual
+ *             add, SiLU(gate) * up, and the attention stand-in for a context of
+ *             one token).
+ *
+ * Batch invariance.  Detent (Batch-Invariant LLM Serving and RL Rollouts at
+ * Near-Stock Speed), Sec. 3, Eq. 2, asks that a request's output bits not
+ * depend on the batch it runs in, and gives the sufficient condition (Sec. 1,
+ * Eq. 1) that each kernel is batch-invariant and that kernel selection never
+ * reads the batch.  CoRun (Padding is Simple and Efficient for Deterministic
+ * LLM Inference), Sec. III-B, Def. 1, states the kernel contract:
+ * x_i = x'_j implies F_n(X)_i = F_m(X')_j for all batch sizes n, m and rows
+ * i, j.  This library meets it by construction: every output row's floating
+ * point reduction tree -- the K-tile, the number of K splits and their
+ * boundaries, the order in which the split partials are added, the tensor-core
+ * instruction shape -- is a function of (N, K, pins) only.  M, the row's
+ * position and the other rows' values choose only which SM computes what.
+ *
+ * Pins.  Detent, Sec. 3, calls a value of kernel selection that is replaced by
+ * a constant a pin, and the set of pins fixed before serving a commitment
+ * tuple; an illegal assignment stops the engine before any kernel runs
+ * (Sec. 5).  bi_pins is the GEMM family's slice of such a tuple: callers fix
+ * one bi_pins per (N, K) for a deployment and pass it on every call.
+ * bi_pins_default() gives the library's table entry, which never reads M.
+ *
+ * Conventions for every entry point
+ *   - Pointers are caller-owned DEVICE memory of the current CUDA device, bf16
+ *     tensors row-major and contiguous, 16-byte aligned.  The library keeps no
+ *     reference to them after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return launch-time errors only.  A device-side
+ *     stall (a bounded wait that ran out) is reported by
+ *     bi_last_device_status().
+ *   - Arguments are checked before anything is launched; a call that returns
+ *     an error launched nothing and wrote nothing.
+ *   - M == 0 is a successful no-op.
+ *   - The library allocates no device memory on any call.  The fused call
+ *     takes a caller-provided workspace.
+ *   - Entry points are reentrant; calls on different streams may overlap.
+ */
+#ifndef BI_GEMM_H
+#define BI_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* bi_stream_t;
+
+#define BI_PINS_ABI_VERSION 1
+
+/* bf16 elements per K tile.  The only supported value. */
+#define BI_BK 64
+/* Output features (rows of W) per tensor-core tile: the MMA's M extent. */
+#define BI_TILE_N 128
+/* Largest number of K splits. */
+#define BI_MAX_SPLIT_K 16
+
+/* Schedule flags: speed only.  They choose how the S split chains of a tile
+ * are placed on SMs and never change any output bit.
+ *   AUTO     the library chooses from M (allowed: it changes no bit).
+ *   LOCAL    one persistent CTA per tile computes its S chains one after the
+ *            other into two TMEM accumulators and folds them in registers.
+ *   CLUSTER  a cluster of S CTAs computes one chain each and folds the S
+ *            partials through distributed shared memory (S <= 8 only). */
+#define BI_FLAG_SCHEDULE_AUTO 0x0u
+#define BI_FLAG_SCHEDULE_LOCAL 0x1u
+#define BI_FLAG_SCHEDULE_CLUSTER 0x2u
+#define BI_FLAG_SCHEDULE_MASK 0x3u
+/* Diagnostic only: the load producer withholds its first load so that the
+ * tensor-core warp's bounded wait runs out.  The kernel then abandons the call
+ * (Y is left unspecified), frees its tensor memory and returns, and
+ * bi_last_device_status() reports BI_ERR_DEVICE_TIMEOUT.  Exists to test the
+ * stall detection; never set it otherwise. */
+#define BI_FLAG_DEBUG_STALL_PRODUCER 0x100u
+#define BI_FLAG_KNOWN_MASK (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER)
+
+typedef struct bi_pins {
+  int32_t abi_version; /* BI_PINS_ABI_VERSION */
+  int32_t bk;          /* K-tile width in bf16 elements: BI_BK */
+  int32_t split_k;     /* S, the number of K splits, 1..BI_MAX_SPLIT_K and at most
+                          the number of K tiles.  Split s covers K tiles
+                          [floor(s*KT/S), floor((s+1)*KT/S)), KT = ceil(K/bk); the
+                          partials are added in ascending s. */
+  int32_t tok_tile;    /* T, tokens per tile = the MMA's N extent: 64, 128 or 256 */
+  int32_t stages;      /* shared-memory ring depth; 0 = library default.  Speed
+                          only. */
+  uint32_t flags;      /* BI_FLAG_* */
+} bi_pins;
+
+typedef enum bi_status {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad eps, ... */
+  BI_ERR_ALIGNMENT = 2,         /* a pointer not 16-byte aligned */
+  BI_ERR_UNSUPPORTED_SHAPE = 3, /* e.g. K not a multiple of 8, a dimension too large */
+  BI_ERR_ILLEGAL_PINS = 4,      /* bi_pins_validate() refused the pins */
+  BI_ERR_CUDA = 5,              /* a CUDA runtime call failed (launch, no device, ...) */
+  BI_ERR_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait ran out (see bi_last_device_status) */
+  BI_ERR_WORKSPACE = 7          /* workspace missing or smaller than required */
+} bi_status;
+
+/* Version of this ABI (BI_PINS_ABI_VERSION). */
+int32_t bi_abi_version(void);
+
+/* Human-readable name of a status.  Never NULL; static storage. */
+const char* bi_status_string(bi_status status);
+
+/* The library's pins for a GEMM with N output features and reduction length
+ * K.  There is no M argument: the table is keyed on (N, K) alone (Detent,
+ * Sec. 8.2: the batch reaches neither GEMM selection point).  Fills *out.
+ * Errors: BI_ERR_INVALID_ARG (out NULL, N or K < 1),
+ * BI_ERR_UNSUPPORTED_SHAPE (K % 8 != 0).  Host only; touches no GPU. */
+bi_status bi_pins_default(int64_t N, int64_t K, bi_pins* out);
+
+/* Checks pins for (N, K): version, bk == BI_BK, 1 <= split_k <= min(16, KT),
+ * tok_tile in {64,128,256}, stages 0 or in the legal range for tok_tile, flags
+ * known, CLUSTER only with split_k <= 8.  Returns BI_OK or
+ * BI_ERR_ILLEGAL_PINS (BI_ERR_INVALID_ARG for a NULL pointer).  Host only. */
+bi_status bi_pins_validate(int64_t N, int64_t K, const bi_pins* pins);
+
+/* A description of the launch the GEMM would make, for inspection and tests.
+ * The first group of fields is the reduction tree and depends on (N, K,
+ * pins) only; the second group is the schedule and may depend on M. */
+typedef struct bi_gemm_plan {
+  /* reduction tree: a function of (N, K, pins) */
+  int32_t bk, split_k, tok_tile, mma_m, mma_n, mma_k;
+  int64_t k_tiles;
+  int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* K-tile boundaries, split s = [begin[s], begin[s+1]) */
+  /* schedule: may depend on M */
+  int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL or _CLUSTER */
+  int32_t stages;
+  int64_t n_tiles, m_tiles;
+  int32_t grid_x, grid_y, grid_z, cluster_x, block_threads;
+  int64_t smem_bytes;
+} bi_gemm_plan;
+
+/* Fills *plan for a GEMM of shape (M, N, K) with the given pins (NULL = the
+ * default pins).  `sm_count` sizes the persistent grid (0 = 152, the SM count
+ * of a GB300); it never changes the tree fields.  Host only.
+ * Errors: as bi_gemm_bf16's argument checks. */
+bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi_pins* pins,
+                                int32_t sm_count, bi_gemm_plan* plan);
+
+/* Y[M,N] = bf16_rne(X[M,K] . W[N,K]^T), fp32 accumulation on the tensor cores.
+ *   X  [M,K] bf16 activations (tokens), W [N,K] bf16 weights, Y [M,N] bf16 out.
+ *   pins NULL = bi_pins_default(N, K).
+ * Requirements: K % 8 == 0 (16-byte row pitch for the tensor-memory copies),
+ * X, W, Y 16-byte aligned, M, N, K < 2^31.
+ * Defines: LLM-42 (Enabling Determinism in LLM Inference with Verified
+ * Speculation), Sec. 2.2, Fig. 3: a GEMM whose split-K use follows the shape
+ * changes a token's reduction tree; here S and the split boundaries are pins.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_ILLEGAL_PINS, BI_ERR_CUDA. */
+bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                       const bi_pins* pins, bi_stream_t stream);
+
+/* Y[M,H] = RMSNorm(X[M,H]) with gain g[H], one warp per row: each lane sums
+ * the squares of its 16-byte vectors in ascending order, the 32 lane sums are
+ * combined by a fixed xor-butterfly, r = 1/sqrt(sum/H + eps) (IEEE division
+ * and square root), y = bf16_rne((x * r) * g).  The tree depends on H only.
+ * Defines: LLM-42, Sec. 2.1 (normalisation reduces over the hidden dimension
+ * of each token); CoRun, Fig. 2(a) (RMSNorm among the batch-invariant
+ * operators).
+ * Requirements: H % 8 == 0, 8 <= H <= 65536, eps > 0 and finite, pointers
+ * 16-byte aligned.  X and Y may be the same buffer.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_CUDA. */
+bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
+                          bi_stream_t stream);
+
+/* Bytes of workspace bi_rmsnorm_gemm_bf16 needs for M rows of width K. */
+size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K);
+
+/* Y = bi_gemm_bf16(bi_rmsnorm_bf16(X; g, eps), W), bit for bit.  The
+ * normalised rows are staged in `workspace` (caller-owned device memory of at
+ * least bi_rmsnorm_gemm_workspace_bytes(M, K) bytes, 256-byte aligned; its
+ * contents on return are unspecified).  H of the RMSNorm is K.
+ * Errors: as the two calls, plus BI_ERR_WORKSPACE. */
+bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void* Y, int64_t M,
+                               int64_t N, int64_t K, float eps, const bi_pins* pins,
+                               void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
+/* out[i] = bf16_rne(float(a[i]) + float(b[i])) for i < count (the residual
+ * connection of a decode layer).  count % 8 == 0, pointers 16-byte aligned;
+ * out may alias a or b. */
+bi_status bi_residual_add_bf16(const void* a, const void* b, void* out, int64_t count,
+                               bi_stream_t stream);
+
+/* SwiGLU activation: gu [M, 2I] holds gate (columns 0..I-1) and up (columns
+ * I..2I-1); out[m,i] = bf16_rne(silu(gate) * up) with silu(v) = v / (1 +
+ * exp(-v)) in fp32.  I % 8 == 0, pointers 16-byte aligned. */
+bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I, bi_stream_t stream);
+
+/* Attention at a context of one token: qkv [M, (nq + 2 nkv) D] is
+ * [q | k | v]; with a single key the softmax weight is exactly 1, so query
+ * head j outputs the v vector of group j / (nq / nkv).  out [M, nq D].
+ * nq % nkv == 0, D % 8 == 0, pointers 16-byte aligned. */
+bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
+                                 int64_t D, bi_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's stall
+ * word: BI_OK if no kernel's bounded wait ran out since the last call,
+ * BI_ERR_DEVICE_TIMEOUT otherwise (the affected call's output is
+ * unspecified), BI_ERR_CUDA if the synchronisation itself failed. */
+bi_status bi_last_device_status(bi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_GEMM_H */

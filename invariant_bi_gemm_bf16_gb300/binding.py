@@ -1,0 +1,267 @@
+"""Thin Python binding of the C ABI in ``include/bi_gemm.h``.
+
+Argument marshalling only: every function checks the tensors it is handed,
+passes their device pointers, sizes and the current CUDA stream to the entry
+point of the same name in ``libbi_gemm.so``, and raises ``BiError`` on a
+non-OK status.  All arithmetic runs in the library's kernels.  There is no
+fallback: if the library is missing or cannot be loaded, every call raises.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbi_gemm.so")
+
+BI_OK = 0
+BI_ERR_INVALID_ARG = 1
+BI_ERR_ALIGNMENT = 2
+BI_ERR_UNSUPPORTED_SHAPE = 3
+BI_ERR_ILLEGAL_PINS = 4
+BI_ERR_CUDA = 5
+BI_ERR_DEVICE_TIMEOUT = 6
+BI_ERR_WORKSPACE = 7
+
+BI_PINS_ABI_VERSION = 1
+BI_BK = 64
+BI_TILE_N = 128
+BI_MAX_SPLIT_K = 16
+BI_FLAG_SCHEDULE_AUTO = 0x0
+BI_FLAG_SCHEDULE_LOCAL = 0x1
+BI_FLAG_SCHEDULE_CLUSTER = 0x2
+BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
+
+
+class Pins(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_int32), ("bk", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("tok_tile", ctypes.c_int32), ("stages", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+    def replace(self, **kw) -> "Pins":
+        d = self.as_dict()
+        d.update(kw)
+        return Pins(**d)
+
+    def __repr__(self):
+        return "Pins(%s)" % ", ".join("%s=%s" % kv for kv in self.as_dict().items())
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("bk", ctypes.c_int32), ("split_k", ctypes.c_int32), ("tok_tile", ctypes.c_int32),
+                ("mma_m", ctypes.c_int32), ("mma_n", ctypes.c_int32), ("mma_k", ctypes.c_int32),
+                ("k_tiles", ctypes.c_int64),
+                ("split_begin", ctypes.c_int64 * (BI_MAX_SPLIT_K + 1)),
+                ("schedule", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("n_tiles", ctypes.c_int64), ("m_tiles", ctypes.c_int64),
+                ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
+                ("cluster_x", ctypes.c_int32), ("block_threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64)]
+
+    TREE_FIELDS = ("bk", "split_k", "tok_tile", "mma_m", "mma_n", "mma_k", "k_tiles")
+
+    def tree(self) -> tuple:
+        """The reduction-tree fields: a function of (N, K, pins) only."""
+        return tuple(getattr(self, f) for f in self.TREE_FIELDS) + \
+            tuple(self.split_begin[: self.split_k + 1])
+
+
+class BiError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+# name -> (restype, argtypes); the C ABI of include/bi_gemm.h
+_SIGNATURES = {
+    "bi_abi_version": (ctypes.c_int32, []),
+    "bi_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "bi_pins_default": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(Pins)]),
+    "bi_pins_validate": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(Pins)]),
+    "bi_gemm_plan_describe": (ctypes.c_int, [_i64, _i64, _i64, ctypes.POINTER(Pins), ctypes.c_int32,
+                                             ctypes.POINTER(Plan)]),
+    "bi_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
+    "bi_rmsnorm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
+    "bi_rmsnorm_gemm_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "bi_rmsnorm_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
+                                            ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
+    "bi_residual_add_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
+    "bi_silu_mul_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
+    "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
+    "bi_last_device_status": (ctypes.c_int, [_vp]),
+}
+
+
+def load(path: str | None = None):
+    """Loads libbi_gemm.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError("libbi_gemm.so is not built (%s); run __graft_entry__.build()" % p)
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().bi_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != BI_OK:
+        raise BiError(status, where)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+# ---------------------------------------------------------------------------
+# pins and plans (host only)
+# ---------------------------------------------------------------------------
+
+def bi_pins_default(N: int, K: int) -> Pins:
+    p = Pins()
+    _check(load().bi_pins_default(N, K, ctypes.byref(p)), "bi_pins_default")
+    return p
+
+
+def bi_pins_validate(N: int, K: int, pins: Pins) -> int:
+    return load().bi_pins_validate(N, K, ctypes.byref(pins))
+
+
+def bi_gemm_plan_describe(M: int, N: int, K: int, pins: Pins | None = None, sm_count: int = 0) -> Plan:
+    plan = Plan()
+    _check(load().bi_gemm_plan_describe(M, N, K, ctypes.byref(pins) if pins is not None else None,
+                                        sm_count, ctypes.byref(plan)), "bi_gemm_plan_describe")
+    return plan
+
+
+# ---------------------------------------------------------------------------
+# the layer
+# ---------------------------------------------------------------------------
+
+def bi_gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
+                 pins: Pins | None = None, stream=None) -> torch.Tensor:
+    """Y = X . W^T (bf16, fp32 accumulation).  x [M,K], w [N,K] -> [M,N]."""
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("expected x [M,K] and w [N,K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = load().bi_gemm_bf16(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
+                             ctypes.byref(pins) if pins is not None else None, _stream(stream))
+    _check(st, "bi_gemm_bf16")
+    return out
+
+
+def bi_rmsnorm_bf16(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-5, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """RMSNorm over the last dimension of x [M,H] with gain g [H]."""
+    if x.dim() != 2:
+        raise ValueError("expected x [M,H]")
+    M, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    st = load().bi_rmsnorm_bf16(_dev(x, "x"), _dev(g, "g", (H,)), _dev(out, "out", (M, H)), M, H,
+                                float(eps), _stream(stream))
+    _check(st, "bi_rmsnorm_bf16")
+    return out
+
+
+def bi_rmsnorm_gemm_workspace_bytes(M: int, K: int) -> int:
+    return int(load().bi_rmsnorm_gemm_workspace_bytes(M, K))
+
+
+def bi_rmsnorm_gemm_bf16(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, eps: float = 1e-5,
+                         pins: Pins | None = None, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = RMSNorm(x; g) . W^T, equal bit for bit to the two calls in sequence."""
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("expected x [M,K] and w [N,K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = bi_rmsnorm_gemm_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().bi_rmsnorm_gemm_bf16(_dev(x, "x"), _dev(g, "g", (K,)), _dev(w, "w"),
+                                     _dev(out, "out", (M, N)), M, N, K, float(eps),
+                                     ctypes.byref(pins) if pins is not None else None,
+                                     workspace.data_ptr(), ws_bytes, _stream(stream))
+    _check(st, "bi_rmsnorm_gemm_bf16")
+    return out
+
+
+def bi_residual_add_bf16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    if a.shape != b.shape:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(a)
+    st = load().bi_residual_add_bf16(_dev(a, "a"), _dev(b, "b"), _dev(out, "out", a.shape), a.numel(),
+                                     _stream(stream))
+    _check(st, "bi_residual_add_bf16")
+    return out
+
+
+def bi_silu_mul_bf16(gu: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    M, I2 = gu.shape
+    I = I2 // 2
+    if out is None:
+        out = torch.empty((M, I), dtype=torch.bfloat16, device=gu.device)
+    st = load().bi_silu_mul_bf16(_dev(gu, "gu"), _dev(out, "out", (M, I)), M, I, _stream(stream))
+    _check(st, "bi_silu_mul_bf16")
+    return out
+
+
+def bi_attention_ctx1_bf16(qkv: torch.Tensor, nq: int, nkv: int, D: int, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    M = qkv.shape[0]
+    if out is None:
+        out = torch.empty((M, nq * D), dtype=torch.bfloat16, device=qkv.device)
+    st = load().bi_attention_ctx1_bf16(_dev(qkv, "qkv", (M, (nq + 2 * nkv) * D)),
+                                       _dev(out, "out", (M, nq * D)), M, nq, nkv, D, _stream(stream))
+    _check(st, "bi_attention_ctx1_bf16")
+    return out
+
+
+def bi_last_device_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device's stall status."""
+    return int(load().bi_last_device_status(_stream(stream)))

@@ -1,0 +1,423 @@
+// api.cu -- the C ABI (include/bi_gemm.h): argument checks, the pin table,
+// the launch plan, TMA descriptor encoding, and the launches.
+//
+// Order of work in every entry point: check every argument (no CUDA call),
+// resolve and validate the pins, then touch the device.  A call that returns
+// an error has launched nothing.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+#define BI_API extern "C" __attribute__((visibility("default")))
+
+namespace bi {
+namespace {
+
+// Fixed design constant used by the default pin table to balance split work
+// over a GB300's SMs.  It is never read from the device: the table must not
+// depend on anything but (N, K).
+constexpr int kTableSmCount = 152;
+constexpr int kDefaultSmCount = 152;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The explicit table: the Llama-3.1 projection shapes of the workloads this
+// library is measured on.  (N, K) -> (S, T).
+struct TableEntry {
+  int64_t N, K;
+  int32_t S, T;
+};
+const TableEntry kTable[] = {
+    {128, 256, 2, 128},       // tiny invariance shape: exercises the split fold
+    {4096, 14336, 4, 128},    // Llama-3.1-8B down_proj
+    {6144, 4096, 3, 128},     // Llama-3.1-8B qkv
+    {28672, 4096, 2, 128},    // Llama-3.1-8B gate_up
+    {10240, 8192, 5, 128},    // Llama-3.1-70B qkv
+    {8192, 8192, 2, 128},     // Llama-3.1-70B o_proj
+    {57344, 8192, 1, 128},    // Llama-3.1-70B gate_up
+    {8192, 28672, 2, 128},    // Llama-3.1-70B down_proj
+};
+
+// Rule for shapes outside the table: the split count that best fills
+// kTableSmCount SMs with (N/128) * S equal chains when a whole wave of tiles is
+// one token tile (the decode case), with a small charge per extra split.
+int32_t rule_split(int64_t N, int64_t K) {
+  const int64_t n_tiles = ceil_div(N, kTileN);
+  const int64_t kt = ceil_div(K, kBK);
+  int32_t best = 1;
+  double best_score = -1.0;
+  for (int32_t S = 1; S <= 8 && S <= kt; ++S) {
+    const int64_t units = n_tiles * S;
+    const int64_t waves = ceil_div(units, kTableSmCount);
+    const double eff = (double)units / (double)(waves * kTableSmCount);
+    const double score = eff - 0.03 * (S - 1);
+    if (score > best_score + 1e-12) {
+      best_score = score;
+      best = S;
+    }
+  }
+  return best;
+}
+
+bi_status check_nk(int64_t N, int64_t K) {
+  if (N < 1 || K < 1) return BI_ERR_INVALID_ARG;
+  if (K % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  return BI_OK;
+}
+
+struct Resolved {
+  int32_t S, T, stages;
+  uint32_t flags;
+  int64_t KT;
+};
+
+bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r);
+
+// Which device function pointer encodes tensor maps (driver entry point).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A [rows, K] bf16 row-major matrix, box of 64 x box_rows, 128-byte swizzle,
+// zero fill outside the matrix.
+bool encode_kmajor(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count_current() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kDefaultSmCount;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = kDefaultSmCount;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Schedule choice from M (speed only).  Rounds of chain work per SM:
+// LOCAL runs ceil(tiles / P) tiles of S chains each; CLUSTER runs the
+// tiles * S chains as independent CTAs.  CLUSTER is charged 15% for its
+// un-overlapped epilogue and fold.
+int32_t choose_schedule(const Resolved& r, int64_t tiles, int32_t sm_count) {
+  const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
+  if (r.S == 1) return BI_FLAG_SCHEDULE_LOCAL;
+  if (forced == BI_FLAG_SCHEDULE_LOCAL) return BI_FLAG_SCHEDULE_LOCAL;
+  if (forced == BI_FLAG_SCHEDULE_CLUSTER) return BI_FLAG_SCHEDULE_CLUSTER;
+  if (r.S > 8) return BI_FLAG_SCHEDULE_LOCAL;
+  const double local_rounds = (double)ceil_div(tiles, sm_count) * r.S;
+  const double cluster_rounds = (double)ceil_div(tiles * r.S, sm_count);
+  return cluster_rounds * 1.15 < local_rounds ? BI_FLAG_SCHEDULE_CLUSTER : BI_FLAG_SCHEDULE_LOCAL;
+}
+
+bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& r, int32_t sm_count,
+                    bi_gemm_plan* plan) {
+  std::memset(plan, 0, sizeof(*plan));
+  plan->bk = kBK;
+  plan->split_k = r.S;
+  plan->tok_tile = r.T;
+  plan->mma_m = kTileN;
+  plan->mma_n = r.T;
+  plan->mma_k = kMmaK;
+  plan->k_tiles = r.KT;
+  for (int s = 0; s <= r.S; ++s) plan->split_begin[s] = ((int64_t)s * r.KT) / r.S;
+  plan->stages = r.stages;
+  plan->n_tiles = ceil_div(N, kTileN);
+  plan->m_tiles = M > 0 ? ceil_div(M, r.T) : 0;
+  plan->block_threads = kGemmThreads;
+  const int64_t tiles = plan->n_tiles * plan->m_tiles;
+  plan->schedule = choose_schedule(r, tiles, sm_count);
+  const bool cluster = plan->schedule == BI_FLAG_SCHEDULE_CLUSTER;
+  if (cluster) {
+    if (plan->n_tiles > 65535 || plan->m_tiles > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
+    plan->grid_x = r.S;
+    plan->grid_y = (int32_t)plan->n_tiles;
+    plan->grid_z = (int32_t)plan->m_tiles;
+    plan->cluster_x = r.S;
+  } else {
+    plan->grid_x = (int32_t)(tiles < sm_count ? tiles : sm_count);
+    plan->grid_y = 1;
+    plan->grid_z = 1;
+    plan->cluster_x = 1;
+  }
+  plan->smem_bytes = gemm_smem_bytes(r.T, r.stages, cluster);
+  if (plan->smem_bytes > kMaxDynSmem) return BI_ERR_ILLEGAL_PINS;
+  return BI_OK;
+}
+
+bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
+  if (!p) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  const int64_t kt = ceil_div(K, kBK);
+  if (p->abi_version != BI_PINS_ABI_VERSION) return BI_ERR_ILLEGAL_PINS;
+  if (p->bk != kBK) return BI_ERR_ILLEGAL_PINS;
+  if (p->split_k < 1 || p->split_k > BI_MAX_SPLIT_K || p->split_k > kt) return BI_ERR_ILLEGAL_PINS;
+  if (p->tok_tile != 64 && p->tok_tile != 128 && p->tok_tile != 256) return BI_ERR_ILLEGAL_PINS;
+  if (p->stages != 0 && (p->stages < 2 || p->stages > max_stages(p->tok_tile)))
+    return BI_ERR_ILLEGAL_PINS;
+  if (p->flags & ~BI_FLAG_KNOWN_MASK) return BI_ERR_ILLEGAL_PINS;
+  const uint32_t sched = p->flags & BI_FLAG_SCHEDULE_MASK;
+  if (sched == BI_FLAG_SCHEDULE_MASK) return BI_ERR_ILLEGAL_PINS;
+  if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k > 8) return BI_ERR_ILLEGAL_PINS;
+  return BI_OK;
+}
+
+bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
+  if (!out) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  int32_t S = 0, T = 128;
+  for (const TableEntry& e : kTable) {
+    if (e.N == N && e.K == K) {
+      S = e.S;
+      T = e.T;
+      break;
+    }
+  }
+  if (S == 0) S = rule_split(N, K);
+  const int64_t kt = ceil_div(K, kBK);
+  if (S > kt) S = (int32_t)kt;
+  out->abi_version = BI_PINS_ABI_VERSION;
+  out->bk = kBK;
+  out->split_k = S;
+  out->tok_tile = T;
+  out->stages = 0;
+  out->flags = BI_FLAG_SCHEDULE_AUTO;
+  return BI_OK;
+}
+
+bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r) {
+  bi_pins p;
+  if (pins) {
+    p = *pins;
+  } else {
+    bi_status st = pins_default(N, K, &p);
+    if (st != BI_OK) return st;
+  }
+  bi_status st = validate(N, K, &p);
+  if (st != BI_OK) return st;
+  r->S = p.split_k;
+  r->T = p.tok_tile;
+  r->stages = p.stages ? p.stages : default_stages(p.tok_tile);
+  r->flags = p.flags;
+  r->KT = ceil_div(K, kBK);
+  return BI_OK;
+}
+
+bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M, int64_t N,
+                          int64_t K) {
+  if (M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!X || !W || !Y) return BI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return BI_ERR_ALIGNMENT;
+  return BI_OK;
+}
+
+bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                    const bi_pins* pins, cudaStream_t stream) {
+  bi_status st = check_gemm_args(X, W, Y, M, N, K);
+  if (st != BI_OK) return st;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  bi_gemm_plan plan;
+  st = make_plan(M, N, K, r, sm_count_current(), &plan);
+  if (st != BI_OK) return st;
+  GemmLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  if (!encode_kmajor(&L.tmW, W, N, K, kTileN)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, X, M, K, r.T)) return BI_ERR_CUDA;
+  L.Y = Y;
+  L.M = M;
+  L.N = N;
+  L.K = K;
+  L.n_tiles = (int32_t)plan.n_tiles;
+  L.m_tiles = (int32_t)plan.m_tiles;
+  L.k_tiles = (int32_t)r.KT;
+  L.S = r.S;
+  L.T = r.T;
+  L.stages = r.stages;
+  L.cluster = plan.schedule == BI_FLAG_SCHEDULE_CLUSTER;
+  L.grid_x = plan.grid_x;
+  L.grid_y = plan.grid_y;
+  L.grid_z = plan.grid_z;
+  L.smem = plan.smem_bytes;
+  L.flags = r.flags;
+  L.stream = stream;
+  return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status check_rmsnorm_args(const void* X, const void* g, const void* Y, int64_t M, int64_t H,
+                             float eps) {
+  if (M < 0 || H < 1) return BI_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !(eps < 3.0e38f)) return BI_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > 65536) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!X || !g || !Y) return BI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(g) || !aligned16(Y)) return BI_ERR_ALIGNMENT;
+  return BI_OK;
+}
+
+size_t workspace_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0) return 0;
+  const uint64_t b = (uint64_t)M * (uint64_t)K * 2u;
+  return (size_t)((b + 255u) & ~(uint64_t)255u);
+}
+
+}  // namespace
+}  // namespace bi
+
+using namespace bi;
+
+BI_API int32_t bi_abi_version(void) { return BI_PINS_ABI_VERSION; }
+
+BI_API const char* bi_status_string(bi_status s) {
+  switch (s) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG: invalid argument";
+    case BI_ERR_ALIGNMENT: return "BI_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case BI_ERR_UNSUPPORTED_SHAPE: return "BI_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+    case BI_ERR_ILLEGAL_PINS: return "BI_ERR_ILLEGAL_PINS: pins refused by validation";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA: CUDA runtime error";
+    case BI_ERR_DEVICE_TIMEOUT: return "BI_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    case BI_ERR_WORKSPACE: return "BI_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "BI_ERR_UNKNOWN";
+}
+
+BI_API bi_status bi_pins_default(int64_t N, int64_t K, bi_pins* out) { return pins_default(N, K, out); }
+
+BI_API bi_status bi_pins_validate(int64_t N, int64_t K, const bi_pins* pins) {
+  return validate(N, K, pins);
+}
+
+BI_API bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi_pins* pins,
+                                       int32_t sm_count, bi_gemm_plan* plan) {
+  if (!plan) return BI_ERR_INVALID_ARG;
+  if (M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  return make_plan(M, N, K, r, sm_count > 0 ? sm_count : kDefaultSmCount, plan);
+}
+
+BI_API bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                              const bi_pins* pins, bi_stream_t stream) {
+  return gemm_impl(X, W, Y, M, N, K, pins, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t M, int64_t H,
+                                 float eps, bi_stream_t stream) {
+  bi_status st = check_rmsnorm_args(X, g, Y, M, H, eps);
+  if (st != BI_OK || M == 0) return st;
+  return launch_rmsnorm(X, g, Y, M, H, eps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return workspace_bytes(M, K); }
+
+BI_API bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void* Y,
+                                      int64_t M, int64_t N, int64_t K, float eps,
+                                      const bi_pins* pins, void* workspace, size_t ws_bytes,
+                                      bi_stream_t stream) {
+  bi_status st = check_gemm_args(X, W, Y, M, N, K);
+  if (st != BI_OK) return st;
+  st = check_rmsnorm_args(X, g, workspace ? workspace : Y, M, K, eps);
+  if (st != BI_OK) return st;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  if (!workspace || ws_bytes < workspace_bytes(M, K)) return BI_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_rmsnorm(X, g, workspace, M, K, eps, s) != cudaSuccess) return BI_ERR_CUDA;
+  return gemm_impl(workspace, W, Y, M, N, K, pins, s);
+}
+
+BI_API bi_status bi_residual_add_bf16(const void* a, const void* b, void* out, int64_t count,
+                                      bi_stream_t stream) {
+  if (count < 0) return BI_ERR_INVALID_ARG;
+  if (count % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (count == 0) return BI_OK;
+  if (!a || !b || !out) return BI_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(out)) return BI_ERR_ALIGNMENT;
+  return launch_residual_add(a, b, out, count, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I,
+                                  bi_stream_t stream) {
+  if (M < 0 || I < 1) return BI_ERR_INVALID_ARG;
+  if (I % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!gu || !out) return BI_ERR_INVALID_ARG;
+  if (!aligned16(gu) || !aligned16(out)) return BI_ERR_ALIGNMENT;
+  return launch_silu_mul(gu, out, M, I, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t nq,
+                                        int64_t nkv, int64_t D, bi_stream_t stream) {
+  if (M < 0 || nq < 1 || nkv < 1 || D < 1) return BI_ERR_INVALID_ARG;
+  if (nq % nkv != 0 || D % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!qkv || !out) return BI_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(out)) return BI_ERR_ALIGNMENT;
+  return launch_attention_ctx1(qkv, out, M, nq, nkv, D, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API bi_status bi_last_device_status(bi_stream_t stream) {
+  int v = 0;
+  if (fetch_and_clear_stall(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  return v == 0 ? BI_OK : BI_ERR_DEVICE_TIMEOUT;
+}

@@ -1,0 +1,130 @@
+// rmsnorm.cu -- batch-invariant RMSNorm, one warp per row.
+//
+// y_h = bf16_rne((x_h * r) * g_h),  r = 1 / sqrt(ss / H + eps),  ss = sum_h x_h^2.
+//
+// The reduction tree of a row depends on H only:
+//   * the row is read as 16-byte vectors of 8 bf16; lane l owns vectors
+//     l, l + 32, l + 64, ... and adds their squares in ascending vector order,
+//     element 0..7 within a vector, into one fp32 partial (x*x of a bf16 x is
+//     exact in fp32, so the fused multiply-add rounds only the sum);
+//   * the 32 lane partials are combined by an xor butterfly with offsets
+//     16, 8, 4, 2, 1.  Both operands of every butterfly add are the same two
+//     values in every lane, so all lanes end with the same total;
+//   * ss / H, the square root and 1 / sqrt are IEEE-rounded (no fast math).
+// LLM-42 (Enabling Determinism in LLM Inference with Verified Speculation),
+// Sec. 2.1: normalisation reduces over the hidden dimension of each token; a
+// row is never split across warps, so neither M nor the other rows reach it.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace bi {
+
+constexpr int kRmsWarps = 8;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float sumsq8(const uint4& v, float ss) {
+  ss = __fmaf_rn(bf_lo(v.x), bf_lo(v.x), ss);
+  ss = __fmaf_rn(bf_hi(v.x), bf_hi(v.x), ss);
+  ss = __fmaf_rn(bf_lo(v.y), bf_lo(v.y), ss);
+  ss = __fmaf_rn(bf_hi(v.y), bf_hi(v.y), ss);
+  ss = __fmaf_rn(bf_lo(v.z), bf_lo(v.z), ss);
+  ss = __fmaf_rn(bf_hi(v.z), bf_hi(v.z), ss);
+  ss = __fmaf_rn(bf_lo(v.w), bf_lo(v.w), ss);
+  ss = __fmaf_rn(bf_hi(v.w), bf_hi(v.w), ss);
+  return ss;
+}
+
+__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t g, float r) {
+  const float a = __fmul_rn(__fmul_rn(bf_lo(x), r), bf_lo(g));
+  const float b = __fmul_rn(__fmul_rn(bf_hi(x), r), bf_hi(g));
+  __nv_bfloat162 o = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&o);
+}
+
+__device__ __forceinline__ uint4 norm8(const uint4& x, const uint4& g, float r) {
+  uint4 o;
+  o.x = norm2(x.x, g.x, r);
+  o.y = norm2(x.y, g.y, r);
+  o.z = norm2(x.z, g.z, r);
+  o.w = norm2(x.w, g.w, r);
+  return o;
+}
+
+__device__ __forceinline__ float butterfly_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float inv_rms(float ss, int64_t H, float eps) {
+  const float mean = __fdiv_rn(ss, (float)H);
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+// H = 256 * VPL: each lane holds its VPL vectors in registers.
+template <int VPL>
+__global__ void __launch_bounds__(32 * kRmsWarps)
+    rmsnorm_regs_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M,
+                        float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
+  if (row >= M) return;
+  constexpr int kVecs = VPL * 32;
+  const uint4* x = X + row * kVecs;
+  uint4 v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[i] = __ldcs(x + lane + 32 * i);  // streamed once
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) ss = sumsq8(v[i], ss);
+  ss = butterfly_sum(ss);
+  const float r = inv_rms(ss, (int64_t)kVecs * 8, eps);
+  uint4* y = Y + row * kVecs;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const uint4 gv = __ldg(g + lane + 32 * i);
+    __stcs(y + lane + 32 * i, norm8(v[i], gv, r));
+  }
+}
+
+// Any H with H % 8 == 0: the same lane partition and order, two passes over
+// the row (the second pass re-reads it, typically from L1/L2).
+__global__ void __launch_bounds__(32 * kRmsWarps)
+    rmsnorm_loop_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M,
+                        int64_t H, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int64_t nvec = H / 8;
+  const uint4* x = X + row * nvec;
+  float ss = 0.0f;
+  for (int64_t i = lane; i < nvec; i += 32) ss = sumsq8(x[i], ss);
+  ss = butterfly_sum(ss);
+  const float r = inv_rms(ss, H, eps);
+  uint4* y = Y + row * nvec;
+  for (int64_t i = lane; i < nvec; i += 32) y[i] = norm8(x[i], __ldg(g + i), r);
+}
+
+cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
+                           cudaStream_t stream) {
+  const int64_t blocks = (M + kRmsWarps - 1) / kRmsWarps;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)blocks), block(32 * kRmsWarps);
+  auto x = static_cast<const uint4*>(X);
+  auto gg = static_cast<const uint4*>(g);
+  auto y = static_cast<uint4*>(Y);
+  switch (H) {
+    case 256: rmsnorm_regs_kernel<1><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
+    case 512: rmsnorm_regs_kernel<2><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
+    case 1024: rmsnorm_regs_kernel<4><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
+    case 2048: rmsnorm_regs_kernel<8><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
+    case 4096: rmsnorm_regs_kernel<16><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
+    default: rmsnorm_loop_kernel<<<grid, block, 0, stream>>>(x, gg, y, M, H, eps); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace bi

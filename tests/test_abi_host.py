@@ -1,0 +1,164 @@
+"""Host-side tests of the C ABI: the library loads, exports every entry point
+declared in include/*.h, and its host-only logic (the pin table, validation,
+the launch plan) behaves -- in particular the reduction tree never depends on M.
+No GPU work is done here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bd():
+    from invariant_bi_gemm_bf16_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(bi_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("bi_gemm_bf16", "bi_rmsnorm_bf16", "bi_rmsnorm_gemm_bf16", "bi_pins_default",
+                     "bi_pins_validate", "bi_status_string", "bi_last_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(bd):
+    lib = ctypes.CDLL(bd.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, "not exported: %s" % missing
+    assert set(declared_functions()) <= set(bd._SIGNATURES), "binding lacks a declared entry point"
+
+
+def test_abi_version_and_status_strings(bd):
+    lib = bd.load()
+    assert lib.bi_abi_version() == bd.BI_PINS_ABI_VERSION
+    for s in range(8):
+        assert bd.status_string(s).startswith("BI_")
+    assert bd.status_string(999) == "BI_ERR_UNKNOWN"
+
+
+TABLE_SHAPES = [(128, 256), (4096, 14336), (6144, 4096), (28672, 4096), (10240, 8192), (8192, 8192),
+                (57344, 8192), (8192, 28672)]
+
+
+@pytest.mark.parametrize("N,K", TABLE_SHAPES + [(300, 200), (1000, 8), (64, 65536)])
+def test_default_pins_are_legal(bd, N, K):
+    p = bd.bi_pins_default(N, K)
+    assert p.abi_version == 1 and p.bk == 64
+    assert 1 <= p.split_k <= min(16, -(-K // 64))
+    assert p.tok_tile in (64, 128, 256)
+    assert bd.bi_pins_validate(N, K, p) == bd.BI_OK
+
+
+def test_pins_validation_refuses(bd):
+    N, K = 4096, 14336
+    good = bd.bi_pins_default(N, K)
+    bad = [good.replace(abi_version=2), good.replace(bk=32), good.replace(split_k=0),
+           good.replace(split_k=17), good.replace(tok_tile=96), good.replace(tok_tile=512),
+           good.replace(stages=1), good.replace(stages=99), good.replace(flags=0x8000),
+           good.replace(flags=0x3), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER)]
+    for p in bad:
+        assert bd.bi_pins_validate(N, K, p) == bd.BI_ERR_ILLEGAL_PINS, p
+    # more splits than K tiles
+    assert bd.bi_pins_validate(128, 64, good.replace(split_k=2)) == bd.BI_ERR_ILLEGAL_PINS
+    # bad shapes
+    assert bd.bi_pins_validate(128, 100, good) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert bd.bi_pins_validate(0, 64, good) == bd.BI_ERR_INVALID_ARG
+
+
+def test_null_and_bad_arguments_rejected_before_any_launch(bd):
+    """These return before touching CUDA, so they run without a GPU."""
+    lib = bd.load()
+    p = bd.bi_pins_default(128, 256)
+    # negative M, K not a multiple of 8, null pointers with M > 0
+    assert lib.bi_gemm_bf16(None, None, None, -1, 128, 256, None, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm_bf16(None, None, None, 4, 128, 250, None, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_gemm_bf16(None, None, None, 4, 128, 256, None, None) == bd.BI_ERR_INVALID_ARG
+    # misaligned pointers
+    assert lib.bi_gemm_bf16(16, 18, 32, 4, 128, 256, None, None) == bd.BI_ERR_ALIGNMENT
+    # illegal pins win over a launch
+    assert lib.bi_gemm_bf16(16, 32, 48, 4, 128, 256, ctypes.byref(p.replace(tok_tile=7)), None) == \
+        bd.BI_ERR_ILLEGAL_PINS
+    # M == 0 is a no-op even with null pointers
+    assert lib.bi_gemm_bf16(None, None, None, 0, 128, 256, None, None) == bd.BI_OK
+    assert lib.bi_rmsnorm_bf16(None, None, None, 0, 256, 1e-5, None) == bd.BI_OK
+    assert lib.bi_rmsnorm_bf16(None, None, None, 3, 256, 0.0, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm_bf16(None, None, None, 3, 250, 1e-5, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_rmsnorm_bf16(16, 32, 40, 3, 256, 1e-5, None) == bd.BI_ERR_ALIGNMENT
+    # fused: workspace checks
+    assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, None, 0, None) == \
+        bd.BI_ERR_WORKSPACE
+    ws = bd.bi_rmsnorm_gemm_workspace_bytes(4, 256)
+    assert ws >= 4 * 256 * 2 and ws % 256 == 0
+    assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, 256, ws - 1, None) == \
+        bd.BI_ERR_WORKSPACE
+    # glue
+    assert lib.bi_residual_add_bf16(16, 32, 48, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_silu_mul_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_attention_ctx1_bf16(16, 32, 2, 6, 4, 8, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+
+
+ALL_M = list(range(1, 300)) + [511, 512, 513, 1000, 1023, 1024, 2048, 4095, 4096, 8191, 8192]
+
+
+@pytest.mark.parametrize("N,K", TABLE_SHAPES + [(300, 200), (20000, 1000)])
+def test_reduction_tree_never_depends_on_m(bd, N, K):
+    """Detent Sec. 8.2: the batch reaches no GEMM selection point.  The plan's
+    tree fields (K tile, split count and boundaries, MMA shape) are identical for
+    every M, every SM count and every schedule; only the schedule fields move."""
+    ref = None
+    schedules = set()
+    for M in ALL_M:
+        for sm in (152, 148, 132, 7):
+            plan = bd.bi_gemm_plan_describe(M, N, K, None, sm)
+            if ref is None:
+                ref = plan.tree()
+            assert plan.tree() == ref, (M, sm)
+            schedules.add(plan.schedule)
+    pins = bd.bi_pins_default(N, K)
+    for flags in (bd.BI_FLAG_SCHEDULE_LOCAL, bd.BI_FLAG_SCHEDULE_CLUSTER):
+        if flags == bd.BI_FLAG_SCHEDULE_CLUSTER and pins.split_k > 8:
+            continue
+        for M in (1, 77, 8192):
+            assert bd.bi_gemm_plan_describe(M, N, K, pins.replace(flags=flags)).tree() == ref
+
+
+def test_split_boundaries_partition_k(bd):
+    for N, K in TABLE_SHAPES:
+        for S in range(1, 17):
+            kt = -(-K // 64)
+            if S > kt:
+                continue
+            p = bd.bi_pins_default(N, K).replace(split_k=S)
+            plan = bd.bi_gemm_plan_describe(1, N, K, p)
+            b = list(plan.split_begin[: S + 1])
+            assert b[0] == 0 and b[-1] == kt
+            assert all(b[i] < b[i + 1] for i in range(S))
+            # boundaries are floor(s*KT/S): a fixed function of K and S
+            assert b == [s * kt // S for s in range(S + 1)]
+
+
+def test_plan_schedules(bd):
+    # decode-sized down_proj runs as clusters of S CTAs; prefill-sized as persistent CTAs
+    small = bd.bi_gemm_plan_describe(1, 4096, 14336)
+    assert small.schedule == bd.BI_FLAG_SCHEDULE_CLUSTER and small.cluster_x == small.split_k == 4
+    assert small.grid_x * small.grid_y * small.grid_z == 32 * 4
+    big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
+    assert big.schedule == bd.BI_FLAG_SCHEDULE_LOCAL and big.grid_x == 152
+    for plan in (small, big):
+        assert plan.smem_bytes <= 232448 and plan.block_threads == 320

@@ -1,0 +1,145 @@
+"""GPU parity of bi_gemm_bf16 against the CPU oracle, through the C ABI.
+
+Bar (from the oracle's fp32 result): per element |err| <= 2e-2*sqrt(K/4096)*rms(row)
++ half a bf16 ulp, relative Frobenius error <= 5e-3; bit-exact where every
+summation order is exact (integer inputs, identity / permutation weights)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_bits, check_gemm_parity
+from invariant_bi_gemm_bf16_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run(lib, X, W, pins=None):
+    x = X.cuda()
+    w = W.cuda()
+    y = lib.bi_gemm_bf16(x, w, pins=pins)
+    torch.cuda.synchronize()
+    assert lib.bi_last_device_status() == lib.BI_OK
+    return bf16_bits(y)
+
+
+def pins_for(lib, N, K, **kw):
+    return lib.bi_pins_default(N, K).replace(**kw)
+
+
+@pytest.mark.parametrize("M", [1, 3, 7, 16, 33])
+def test_tiny_config_parity(lib, oracle, M):
+    """X [M,256] ~N(0,1), W [128,256] ~N(0,0.02), seed 0."""
+    X = inputs.normal((M, 256), seed=0, stream=inputs.STREAM_X)
+    W = inputs.normal((128, 256), std=0.02, seed=0, stream=inputs.STREAM_W)
+    yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
+        got = run(lib, X, W, pins_for(lib, 128, 256, flags=flags))
+        check_gemm_parity(got, yf, 256, "tiny M=%d flags=%d" % (M, flags))
+
+
+SHAPES = [
+    # (M, N, K): several tiles and ragged tails in every dimension
+    (200, 300, 200),     # K tail (200 = 3*64 + 8), N tail, M tail
+    (129, 256, 512),
+    (1, 640, 1024),
+    (300, 128, 64),
+    (65, 136, 8),        # a single partial K tile
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("S,T", [(1, 128), (2, 64), (3, 128), (2, 256), (4, 64)])
+def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T):
+    kt = -(-K // 64)
+    if S > kt:
+        pytest.skip("more splits than K tiles")
+    X = inputs.normal((M, K), seed=1, stream=0)
+    W = inputs.normal((N, K), std=0.02, seed=1, stream=1)
+    yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    outs = []
+    for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_AUTO):
+        got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T, flags=flags))
+        check_gemm_parity(got, yf, K, "M=%d N=%d K=%d S=%d T=%d flags=%d" % (M, N, K, S, T, flags))
+        outs.append(got)
+    # the schedule changes which SM computes what, never a bit
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("S,T", [(1, 128), (3, 64), (2, 256)])
+def test_integer_inputs_bit_exact(lib, oracle, S, T):
+    """Integer inputs: every partial sum is an exact integer, so every reduction
+    tree gives the same bits as the oracle."""
+    M, N, K = 77, 260, 704
+    X = inputs.integers((M, K), -8, 8, seed=2, stream=0)
+    W = inputs.integers((N, K), -8, 8, seed=2, stream=1)
+    _, yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T))
+    assert np.array_equal(got, yb)
+
+
+def test_identity_and_permutation_weights(lib):
+    K = 256
+    X = inputs.normal((150, K), seed=3, stream=0)
+    eye = inputs.to_bf16(np.eye(K, dtype=np.float32))
+    assert np.array_equal(run(lib, X, eye), inputs.bits(X))
+    perm = np.random.default_rng(3).permutation(K)
+    P = np.zeros((K, K), dtype=np.float32)
+    P[np.arange(K), perm] = 1.0
+    got = run(lib, X, inputs.to_bf16(P), pins_for(lib, K, K, split_k=2))
+    assert np.array_equal(got, inputs.bits(X)[:, perm])
+
+
+def test_one_hot_rows_exact(lib, oracle):
+    """One non-zero per X row: each output is a single exact product."""
+    M, N, K = 40, 200, 512
+    r = np.random.default_rng(4)
+    Xf = np.zeros((M, K), dtype=np.float32)
+    Xf[np.arange(M), r.integers(0, K, M)] = r.standard_normal(M).astype(np.float32)
+    X = inputs.to_bf16(Xf)
+    W = inputs.normal((N, K), std=0.02, seed=4, stream=1)
+    _, yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    assert np.array_equal(run(lib, X, W, pins_for(lib, N, K, split_k=4)), yb)
+
+
+def test_zero_rows_and_m_zero(lib):
+    x = torch.zeros((5, 128), dtype=torch.bfloat16, device="cuda")
+    w = inputs.normal((64, 128), std=0.02, seed=5, stream=1).cuda()
+    y = lib.bi_gemm_bf16(x, w)
+    assert torch.all(y.float() == 0)
+    empty = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    assert lib.bi_gemm_bf16(empty, w).shape == (0, 64)
+
+
+def test_errors_launch_nothing(lib):
+    w = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((4, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    bad = lib.bi_pins_default(64, 128).replace(split_k=5)
+    with pytest.raises(lib.BiError) as e:
+        lib.bi_gemm_bf16(x, w, out=y, pins=bad)
+    assert e.value.status == lib.BI_ERR_ILLEGAL_PINS
+    torch.cuda.synchronize()
+    assert torch.all(y.float() == 7.0)
+    # a misaligned view (offset of one element = 2 bytes)
+    buf = torch.zeros(4 * 128 + 1, dtype=torch.bfloat16, device="cuda")
+    xm = buf[1:].view(4, 128)
+    with pytest.raises(lib.BiError) as e:
+        lib.bi_gemm_bf16(xm, w, out=y)
+    assert e.value.status == lib.BI_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert torch.all(y.float() == 7.0)
+
+
+def test_stores_stay_inside_y(lib):
+    """Guard bands around Y stay untouched for ragged M and N."""
+    M, N, K = 70, 200, 256
+    X = inputs.normal((M, K), seed=6, stream=0).cuda()
+    W = inputs.normal((N, K), std=0.02, seed=6, stream=1).cuda()
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), 123.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[guard:guard + M * N].view(M, N)
+    for S, T in [(1, 64), (2, 128), (4, 256)]:
+        for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
+            lib.bi_gemm_bf16(X, W, out=y, pins=lib.bi_pins_default(N, K).replace(split_k=S, tok_tile=T, flags=flags))
+            torch.cuda.synchronize()
+            assert torch.all(buf[:guard].float() == 123.0) and torch.all(buf[guard + M * N:].float() == 123.0)

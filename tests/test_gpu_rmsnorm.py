@@ -1,0 +1,58 @@
+"""GPU parity of bi_rmsnorm_bf16 (within one bf16 ulp of the oracle) and of the
+fused bi_rmsnorm_gemm_bf16 (bit-equal to the two calls in sequence)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import EPS, bf16_bits, check_gemm_parity, check_ulp
+from invariant_bi_gemm_bf16_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("H", [256, 4096, 8192, 8, 72, 1000, 2048 + 8])
+@pytest.mark.parametrize("M", [1, 3, 37, 257])
+def test_rmsnorm_parity(lib, oracle, M, H):
+    X = inputs.rows_loguniform(M, H, seed=0, stream=0)
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=0, stream=2)
+    want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
+    got = bf16_bits(lib.bi_rmsnorm_bf16(X.cuda(), g.cuda(), EPS))
+    check_ulp(got, want, 1, "rmsnorm M=%d H=%d" % (M, H))
+
+
+def test_rmsnorm_special_rows(lib):
+    H = 256
+    g1 = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((2, H), dtype=torch.bfloat16, device="cuda")
+    assert torch.all(lib.bi_rmsnorm_bf16(x, g1).float() == 0)
+    sign = torch.where(torch.rand(3, H) < 0.5, -1.0, 1.0).to(torch.bfloat16).cuda()
+    assert torch.equal(lib.bi_rmsnorm_bf16(sign, g1), sign)   # +-1 rows are fixed points
+    nanrow = torch.full((1, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert torch.isnan(lib.bi_rmsnorm_bf16(nanrow, g1).float()).all()
+
+
+def test_rmsnorm_in_place(lib, oracle):
+    X = inputs.rows_loguniform(9, 4096, seed=1, stream=0)
+    g = inputs.normal((4096,), std=0.1, mean=1.0, seed=1, stream=2)
+    want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
+    x = X.cuda()
+    lib.bi_rmsnorm_bf16(x, g.cuda(), EPS, out=x)
+    check_ulp(bf16_bits(x), want, 1, "in place")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 384, 4096), (33, 256, 512), (130, 640, 256)])
+def test_fused_equals_composition_and_oracle(lib, oracle, M, N, K):
+    X = inputs.normal((M, K), seed=2, stream=0)
+    g = inputs.normal((K,), std=0.1, mean=1.0, seed=2, stream=2)
+    W = inputs.normal((N, K), std=0.02, seed=2, stream=1)
+    x, gg, w = X.cuda(), g.cuda(), W.cuda()
+    fused = lib.bi_rmsnorm_gemm_bf16(x, gg, w, EPS)
+    xh = lib.bi_rmsnorm_bf16(x, gg, EPS)
+    comp = lib.bi_gemm_bf16(xh, w)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, comp)
+    # the GEMM part against the oracle, fed the GPU's own normalised rows
+    yf, _ = oracle.gemm(bf16_bits(xh), inputs.bits(W))
+    check_gemm_parity(bf16_bits(fused), yf, K, "fused")
+    # and the normalisation against the oracle's
+    check_ulp(bf16_bits(xh), oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS), 1, "fused norm")
