@@ -1,0 +1,467 @@
+"""Benchmark of the batch-invariant linear layer on GB300.
+
+Default workload (one GPU): the Llama-3.1-8B down_proj GEMM, W [4096, 14336],
+swept over M = 1, 2, 4, ..., 8192 tokens.  One step = one bi_gemm_bf16 call at
+every M of the sweep.  `value` = the sweep's FLOPs / its device time (TFLOPS).
+Per-M times, TFLOPS, GB/s, roofline fractions and the torch.mm (cuBLAS) time on
+the same tensors are in "sweep".
+
+Other workloads (--workload): "stack" (the 4-layer Llama-3.1-70B-shaped decode
+step at 32 tokens, us/step), "fused" (RMSNorm + qkv / gate_up projections),
+"rmsnorm" (the RMSNorm token sweep).
+
+L2 handling: every launch reads a weight copy that was not read by the
+previous launches (enough copies that they exceed the 129 MB L2), and
+activations rotate likewise; no flush writes are issued.
+
+--impl reference times the CPU oracle (the reference arm of this build) on a
+bounded sample of the same workload.  Under torchrun each rank runs the same
+per-GPU workload on its own replica (weak scaling: rows are independent and
+the reduction tree never depends on M, so no collective is needed).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+DOWN_N, DOWN_K = 4096, 14336
+SWEEP_M = [1 << i for i in range(14)]  # 1 .. 8192
+EPS = 1e-5
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def gemm_work(M, N, K):
+    """Algorithmic FLOPs and bytes of one GEMM (W counted once)."""
+    return 2.0 * M * N * K, 2.0 * (N * K + M * K + M * N)
+
+
+def roof_time_us(flops, bytes_, peaks):
+    return max(flops / (peaks["bf16_tflops"] * 1e6), bytes_ / (peaks["hbm_gbs"] * 1e3))
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (torchrun: one rank per GPU)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float) -> float:
+        if not self.pg:
+            return v
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_inputs(max_rows: int):
+    """Host bf16 bit patterns of the down_proj workload (seed 0), cached."""
+    from invariant_bi_gemm_bf16_gb300 import inputs
+    if max_rows not in _ORACLE_INPUTS:
+        W = inputs.bits(inputs.normal((DOWN_N, DOWN_K), std=0.02, seed=0, stream=inputs.STREAM_W))
+        X = inputs.bits(inputs.normal((max_rows, DOWN_K), seed=0, stream=inputs.STREAM_X))
+        _ORACLE_INPUTS[max_rows] = (X, W)
+    return _ORACLE_INPUTS[max_rows]
+
+
+def oracle_gemm_throughput(target_s: float = 12.0, max_rows: int = 2048):
+    """Times the oracle's down_proj GEMM on a sample of rows (all 4096 output
+    features each), grown until it takes about target_s seconds.  Returns
+    (TFLOPS, seconds, rows, threads)."""
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    X, W = oracle_inputs(max_rows)
+    rows = 2
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(X[:rows], W, nthreads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or rows >= max_rows:
+            break
+        rows = min(max_rows, max(rows * 2, int(rows * target_s / max(dt, 1e-3))))
+    flops = 2.0 * rows * DOWN_N * DOWN_K
+    return flops / dt / 1e12, dt, rows, threads
+
+
+def smi_gpu_id(local_rank: int) -> str:
+    """The nvidia-smi -i argument for this process's GPU."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class DownProjSweep:
+    """configs: Llama-3.1-8B down_proj, X [M,14336] ~N(0,1), W [4096,14336] ~N(0,0.02)."""
+    name = "down_proj_m_sweep"
+
+    def __init__(self, bd, dev, seed, sweep=SWEEP_M):
+        from invariant_bi_gemm_bf16_gb300 import inputs
+        self.bd = bd
+        self.dev = dev
+        self.N, self.K = DOWN_N, DOWN_K
+        self.ms = list(sweep)
+        wbytes = self.N * self.K * 2
+        self.nw = max(2, math.ceil(2 * L2_BYTES / wbytes) + 1)
+        self.W = [inputs.device_normal((self.N, self.K), std=0.02, seed=seed, stream=inputs.STREAM_W + 16 * i,
+                                       device=dev) for i in range(self.nw)]
+        self.X = {}
+        for M in self.ms:
+            nx = min(self.nw, max(1, math.ceil(2 * L2_BYTES / (M * self.K * 2))))
+            self.X[M] = [inputs.device_normal((M, self.K), seed=seed, stream=inputs.STREAM_X + 16 * i, device=dev)
+                         for i in range(nx)]
+        self.Y = {M: torch.empty((M, self.N), dtype=torch.bfloat16, device=dev) for M in self.ms}
+        self.pins = bd.bi_pins_default(self.N, self.K)
+        self.it = 0
+
+    def launches_per_step(self):
+        return len(self.ms)
+
+    def step(self, events=None, use_torch=False):
+        for j, M in enumerate(self.ms):
+            xs = self.X[M]
+            x = xs[self.it % len(xs)]
+            w = self.W[self.it % self.nw]
+            if events is not None:
+                events[j][0].record()
+            if use_torch:
+                torch.mm(x, w.t(), out=self.Y[M])
+            else:
+                self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins)
+            if events is not None:
+                events[j][1].record()
+            self.it += 1
+
+    def work(self):
+        f = sum(gemm_work(M, self.N, self.K)[0] for M in self.ms)
+        b = sum(gemm_work(M, self.N, self.K)[1] for M in self.ms)
+        return f, b
+
+    def e2e_step(self, host_x, host_y):
+        """Through the public API with host buffers: H2D of each M's X from
+        pinned memory, the GEMM, D2H of its Y into pinned memory."""
+        h2d = d2h = 0
+        for M in self.ms:
+            x = self.X[M][0]
+            x.copy_(host_x[M], non_blocking=True)
+            self.bd.bi_gemm_bf16(x, self.W[self.it % self.nw], out=self.Y[M], pins=self.pins)
+            host_y[M].copy_(self.Y[M], non_blocking=True)
+            h2d += x.numel() * 2
+            d2h += self.Y[M].numel() * 2
+            self.it += 1
+        return h2d, d2h
+
+
+def time_steps(fn, steps, dist):
+    dist.barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return s.elapsed_time(e) / 1e3  # seconds
+
+
+def run_ours(args, dist):
+    from invariant_bi_gemm_bf16_gb300 import binding as bd
+    bd.load()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    wl = DownProjSweep(bd, dev, seed=dist.rank)
+    L = wl.launches_per_step()
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-launch CUDA events on the launching stream
+    clocks = ClockSampler(smi_gpu_id(dist.local_rank))
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+          for _ in range(args.steps)]
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for k in range(args.steps):
+        wl.step(events=ev[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    status = bd.bi_last_device_status()
+    if status != bd.BI_OK:
+        raise RuntimeError("device stall status: %s" % bd.status_string(status))
+    wall = t_start.elapsed_time(t_end) / 1e3
+    per_launch = np.array([[ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e3 for j in range(L)]
+                           for k in range(args.steps)])  # us
+    wall_max = dist.max(wall)
+    flops, bytes_ = wl.work()
+    total_flops = dist.sum(flops * args.steps)
+    value = total_flops / wall_max / 1e12
+
+    # torch.mm on the same tensors, same protocol (untimed region of ours)
+    for _ in range(args.warmup):
+        wl.step(use_torch=True)
+    tev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        wl.step(events=tev[k], use_torch=True)
+    torch.cuda.synchronize()
+    torch_launch = np.array([[tev[k][j][0].elapsed_time(tev[k][j][1]) * 1e3 for j in range(L)]
+                             for k in range(args.steps)])
+
+    sweep = []
+    sum_roof = 0.0
+    sum_meas = 0.0
+    for j, M in enumerate(wl.ms):
+        us = float(np.median(per_launch[:, j]))
+        tus = float(np.median(torch_launch[:, j]))
+        f, b = gemm_work(M, wl.N, wl.K)
+        tr = roof_time_us(f, b, peaks)
+        sum_roof += tr
+        sum_meas += us
+        bound = "tensor" if f / (peaks["bf16_tflops"] * 1e6) >= b / (peaks["hbm_gbs"] * 1e3) else "hbm"
+        sweep.append({"M": M, "us": round(us, 2), "tflops": round(f / us / 1e6, 1),
+                      "gbs": round(b / us / 1e3, 1), "bound": bound, "roofline_frac": round(tr / us, 3),
+                      "torch_mm_us": round(tus, 2), "vs_torch_mm": round(tus / us, 3)})
+
+    # e2e through the C ABI with host buffers
+    host_x = {M: wl.X[M][0].cpu().pin_memory() for M in wl.ms}
+    host_y = {M: torch.empty((M, wl.N), dtype=torch.bfloat16).pin_memory() for M in wl.ms}
+    for _ in range(max(1, args.warmup // 2)):
+        wl.e2e_step(host_x, host_y)
+    torch.cuda.synchronize()
+    holder = {}
+
+    def e2e():
+        holder["b"] = wl.e2e_step(host_x, host_y)
+    e2e_wall = dist.max(time_steps(e2e, args.steps, dist))
+    e2e_value = dist.sum(flops * args.steps) / e2e_wall / 1e12
+    h2d, d2h = holder["b"]
+
+    launch_sum = float(per_launch.sum()) / 1e6
+    achieved = flops * args.steps / launch_sum / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 3), "traffic": None,
+            "peak_source": peaks["source"] + " (burst bf16)",
+            "sweep_time_weighted_frac": round(sum_roof / sum_meas, 3),
+            "note": "GEMM kernel over the whole M sweep: sweep FLOPs / summed launch time; "
+                    "per-M bound and fraction (max of FLOP/peak, bytes/HBM) in sweep[]"}
+    result = {
+        "metric": "batch-invariant GEMM TFLOPS over the down_proj M sweep (M=1..8192)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(wall_max / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": "Llama-3.1-8B down_proj W[4096,14336], M in 1,2,4..8192, one call per M",
+                   "N": wl.N, "K": wl.K, "M_sweep": wl.ms, "pins": wl.pins.as_dict(),
+                   "l2": "no flush; %d weight copies (%.0f MB) and rotating activations so no launch "
+                         "reads what the previous launch left in L2" % (wl.nw, wl.nw * wl.N * wl.K * 2 / 1e6),
+                   "parallelism": "replicas x%d (rows sharded, no collective)" % dist.world},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": L * args.steps,
+        "clocks": clk,
+        "sweep": sweep,
+        "torch_mm_sweep_tflops": round(flops / (float(torch_launch.sum()) / args.steps / 1e6) / 1e12, 1),
+    }
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                  "sample": "oracle down_proj GEMM on %d rows x all 4096 outputs (K=14336), "
+                                            "%.1f s" % (rows, secs)}
+    return result
+
+
+def run_reference(args, dist):
+    """The reference arm: the CPU oracle on a bounded sample of the same workload."""
+    if dist.rank != 0:
+        return None
+    step_s = min(args.ref_step_seconds, 150.0 / max(1, args.steps))
+    oracle_inputs(2048)
+    for _ in range(args.warmup):
+        oracle_gemm_throughput(target_s=0.05, max_rows=2048)
+    vals = []
+    t0 = time.perf_counter()
+    info = None
+    for _ in range(args.steps):
+        info = oracle_gemm_throughput(target_s=step_s, max_rows=2048)
+        vals.append(info[0])
+    total = time.perf_counter() - t0
+    value = statistics.median(vals)
+    return {"impl": "reference", "metric": "batch-invariant GEMM TFLOPS over the down_proj M sweep (M=1..8192)",
+            "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+            "config": {"workload": "Llama-3.1-8B down_proj W[4096,14336], M in 1,2,4..8192, one call per M",
+                       "N": DOWN_N, "K": DOWN_K},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": info[3], "kind": "oracle",
+                             "sample": "per step: oracle down_proj GEMM on %d rows x 4096 outputs" % info[2]},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        else:
+            res = run_ours(args, dist)
+        if dist.rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()
