@@ -194,6 +194,31 @@ bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void
                                int64_t N, int64_t K, float eps, const bi_pins* pins,
                                void* workspace, size_t workspace_bytes, bi_stream_t stream);
 
+/* Capacity in bytes of the static scratch array used by
+ * bi_rmsnorm_gemm_bf16_noalloc: M * K * 2 must not exceed it. */
+#define BI_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/* The fused layer for callers that cannot allocate device memory -- for
+ * example a plugin inside a host runtime that has reserved the device's memory
+ * and offers no allocator, or a latency-critical path where cudaMalloc /
+ * cudaFree would synchronise the device.  Same arguments, result and bits as
+ * bi_rmsnorm_gemm_bf16, but no workspace: the normalised rows are staged in a
+ * static device array of BI_NOALLOC_SCRATCH_BYTES that the library holds on
+ * every GPU that loads it, until the process exits.  The call allocates
+ * nothing.
+ *   - The first call on a device looks the array's address up (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; calls whose work overlaps on the GPU (e.g. on two streams)
+ *     race on it and must be serialised by the caller.
+ * Errors: as bi_rmsnorm_gemm_bf16; BI_ERR_WORKSPACE when M * K * 2 exceeds
+ * BI_NOALLOC_SCRATCH_BYTES (nothing is launched).
+ * The paper has no counterpart to this entry point. */
+bi_status bi_rmsnorm_gemm_bf16_noalloc(const void* X, const void* g, const void* W, void* Y,
+                                       int64_t M, int64_t N, int64_t K, float eps,
+                                       const bi_pins* pins, bi_stream_t stream);
+
 /* out[i] = bf16_rne(float(a[i]) + float(b[i])) for i < count (the residual
  * connection of a decode layer).  count % 8 == 0, pointers 16-byte aligned;
  * out may alias a or b. */

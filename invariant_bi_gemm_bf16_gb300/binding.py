@@ -98,6 +98,8 @@ _SIGNATURES = {
     "bi_rmsnorm_gemm_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "bi_rmsnorm_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
                                             ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
+    "bi_rmsnorm_gemm_bf16_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
+                                                    ctypes.POINTER(Pins), _vp]),
     "bi_residual_add_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "bi_silu_mul_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
@@ -226,6 +228,27 @@ def bi_rmsnorm_gemm_bf16(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, eps:
                                      ctypes.byref(pins) if pins is not None else None,
                                      workspace.data_ptr(), ws_bytes, _stream(stream))
     _check(st, "bi_rmsnorm_gemm_bf16")
+    return out
+
+
+BI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def bi_rmsnorm_gemm_bf16_noalloc(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
+                                 eps: float = 1e-5, pins: Pins | None = None, stream=None) -> torch.Tensor:
+    """The fused layer for callers that cannot allocate device memory: the
+    caller passes the output, and the normalised rows are staged in the
+    library's static device array (M*K*2 <= BI_NOALLOC_SCRATCH_BYTES).  Calls
+    that overlap on the GPU race on that array."""
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("expected x [M,K] and w [N,K]")
+    M, K = x.shape
+    N = w.shape[0]
+    st = load().bi_rmsnorm_gemm_bf16_noalloc(_dev(x, "x"), _dev(g, "g", (K,)), _dev(w, "w"),
+                                             _dev(out, "out", (M, N)), M, N, K, float(eps),
+                                             ctypes.byref(pins) if pins is not None else None,
+                                             _stream(stream))
+    _check(st, "bi_rmsnorm_gemm_bf16_noalloc")
     return out
 
 
