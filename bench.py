@@ -107,26 +107,35 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def shard_rows(total: int, world: int, rank: int):
+    """Contiguous row range [lo, hi) of `rank` when `total` independent rows are
+    split over `world` ranks (a replica of W on every rank, no exchange)."""
+    return (total * rank // world, total * (rank + 1) // world)
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every 20 ms; only the samples that
+    arrive while the timed region runs (mark_start .. mark_end) are kept."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
             return
@@ -136,11 +145,18 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -150,7 +166,11 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        t0 = self.t0 if self.t0 is not None else -1e30
+        t1 = self.t1 if self.t1 is not None else 1e30
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1 + 0.025:
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -166,7 +186,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": round((t1 - t0), 3) if self.t0 is not None and self.t1 is not None else None}
 
 
 # ---------------------------------------------------------------------------
@@ -261,6 +282,29 @@ class DownProjSweep:
                 events[j][1].record()
             self.it += 1
 
+    def time_m(self, j, reps=20, use_torch=False):
+        """Average device time of one launch at the j-th M, from `reps`
+        back-to-back launches (rotating weight copies) between two events."""
+        M = self.ms[j]
+        xs = self.X[M]
+        for i in range(3):
+            self._launch(M, xs[i % len(xs)], self.W[i % self.nw], use_torch)
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        for i in range(reps):
+            self._launch(M, xs[i % len(xs)], self.W[i % self.nw], use_torch)
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) * 1e3 / reps
+
+    def _launch(self, M, x, w, use_torch):
+        if use_torch:
+            torch.mm(x, w.t(), out=self.Y[M])
+        else:
+            self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins)
+
     def work(self):
         f = sum(gemm_work(M, self.N, self.K)[0] for M in self.ms)
         b = sum(gemm_work(M, self.N, self.K)[1] for M in self.ms)
@@ -279,6 +323,53 @@ class DownProjSweep:
             d2h += self.Y[M].numel() * 2
             self.it += 1
         return h2d, d2h
+
+
+def torch_stack_forward(x, layers, shape):
+    """The same decode-step stack with torch.mm and F.rms_norm (cuBLAS; not
+    batch-invariant): the speed reference for the stack."""
+    import torch.nn.functional as F
+    s = shape
+    M = x.shape[0]
+    for L in layers:
+        xn = F.rms_norm(x, (s.hidden,), L["g_attn"], s.eps)
+        qkv = torch.mm(xn, L["Wqkv"].t())
+        v = qkv[:, (s.n_q + s.n_kv) * s.head_dim:].reshape(M, s.n_kv, 1, s.head_dim)
+        att = v.expand(M, s.n_kv, s.n_q // s.n_kv, s.head_dim).reshape(M, s.n_q * s.head_dim)
+        h = x + torch.mm(att, L["Wo"].t())
+        hn = F.rms_norm(h, (s.hidden,), L["g_mlp"], s.eps)
+        gu = torch.mm(hn, L["Wgu"].t())
+        act = F.silu(gu[:, :s.inter]) * gu[:, s.inter:]
+        x = h + torch.mm(act, L["Wd"].t())
+    return x
+
+
+def run_stack(args, dist, peaks):
+    """Configuration 5: the 4-layer Llama-3.1-70B-shaped decode step at 32 tokens."""
+    from invariant_bi_gemm_bf16_gb300.stack import LLAMA31_70B, DecodeStack, random_layers
+    from invariant_bi_gemm_bf16_gb300 import inputs
+    shape = LLAMA31_70B
+    layers = random_layers(shape, seed=dist.rank)
+    stack = DecodeStack(shape, layers)
+    x = inputs.device_normal((32, shape.hidden), seed=dist.rank, stream=0)
+    for _ in range(args.warmup):
+        stack.forward(x)
+    t = dist.max(time_steps(lambda: stack.forward(x), args.steps, dist))
+    us = t / args.steps * 1e6
+    for _ in range(args.warmup):
+        torch_stack_forward(x, layers, shape)
+    tt = dist.max(time_steps(lambda: torch_stack_forward(x, layers, shape), args.steps, dist))
+    tus = tt / args.steps * 1e6
+    wbytes = sum(v.numel() * 2 for L in layers for v in L.values())
+    roof_us = wbytes / (peaks["hbm_gbs"] * 1e3)
+    res = {"workload": "4-layer Llama-3.1-70B-shaped decode step, 32 tokens, hidden 8192, GQA 64/8 x 128, "
+                       "SwiGLU 28672, RMSNorm before attention and MLP; attention at a context of one token",
+           "us_per_step": round(us, 1), "torch_us_per_step": round(tus, 1), "vs_torch": round(tus / us, 3),
+           "weight_bytes": wbytes, "roofline_us": round(roof_us, 1), "roofline_frac": round(roof_us / us, 3),
+           "bound": "hbm", "launches_per_step": stack.launches_per_step()}
+    del stack, layers
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_steps(fn, steps, dist):
@@ -308,51 +399,44 @@ def run_ours(args, dist):
         wl.step()
     torch.cuda.synchronize()
 
-    # timed region: K steps, per-launch CUDA events on the launching stream
+    # timed region: K whole steps between two CUDA events on the launching
+    # stream (no events between launches, so consecutive kernels overlap their
+    # ramp-up and drain exactly as in a real sweep)
     clocks = ClockSampler(smi_gpu_id(dist.local_rank))
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
-          for _ in range(args.steps)]
     clocks.start()
     dist.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
     t_start.record()
     for k in range(args.steps):
-        wl.step(events=ev[k])
+        wl.step()
     t_end.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     dist.barrier()
     clk = clocks.stop()
     status = bd.bi_last_device_status()
     if status != bd.BI_OK:
         raise RuntimeError("device stall status: %s" % bd.status_string(status))
     wall = t_start.elapsed_time(t_end) / 1e3
-    per_launch = np.array([[ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e3 for j in range(L)]
-                           for k in range(args.steps)])  # us
+    # per-M launch durations: R back-to-back launches of one M between two events
+    per_launch = np.array([[wl.time_m(j, reps=args.per_m_reps)] for j in range(L)]).T  # us
     wall_max = dist.max(wall)
     flops, bytes_ = wl.work()
     total_flops = dist.sum(flops * args.steps)
     value = total_flops / wall_max / 1e12
 
-    # torch.mm on the same tensors, same protocol (untimed region of ours)
-    for _ in range(args.warmup):
-        wl.step(use_torch=True)
-    tev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
-           for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for k in range(args.steps):
-        wl.step(events=tev[k], use_torch=True)
-    torch.cuda.synchronize()
-    torch_launch = np.array([[tev[k][j][0].elapsed_time(tev[k][j][1]) * 1e3 for j in range(L)]
-                             for k in range(args.steps)])
-
+    # torch.mm on the same tensors, same protocol
+    torch_launch = np.array([[wl.time_m(j, reps=args.per_m_reps, use_torch=True)] for j in range(L)]).T
+    torch_wall = time_steps(lambda: wl.step(use_torch=True), args.steps, dist)
     sweep = []
     sum_roof = 0.0
     sum_meas = 0.0
     for j, M in enumerate(wl.ms):
-        us = float(np.median(per_launch[:, j]))
-        tus = float(np.median(torch_launch[:, j]))
+        us = float(per_launch[0, j])
+        tus = float(torch_launch[0, j])
         f, b = gemm_work(M, wl.N, wl.K)
         tr = roof_time_us(f, b, peaks)
         sum_roof += tr
@@ -376,8 +460,8 @@ def run_ours(args, dist):
     e2e_value = dist.sum(flops * args.steps) / e2e_wall / 1e12
     h2d, d2h = holder["b"]
 
-    launch_sum = float(per_launch.sum()) / 1e6
-    achieved = flops * args.steps / launch_sum / 1e12
+    launch_sum = float(per_launch.sum()) / 1e6          # one sweep, seconds
+    achieved = flops / launch_sum / 1e12
     roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(achieved / peaks["bf16_tflops"], 3), "traffic": None,
             "peak_source": peaks["source"] + " (burst bf16)",
@@ -399,10 +483,13 @@ def run_ours(args, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": L * args.steps,
+        "per_m_timing": "per-M times: %d back-to-back launches of that M between two CUDA events" % args.per_m_reps,
         "clocks": clk,
         "sweep": sweep,
-        "torch_mm_sweep_tflops": round(flops / (float(torch_launch.sum()) / args.steps / 1e6) / 1e12, 1),
+        "torch_mm_sweep_tflops": round(flops * args.steps / torch_wall / 1e12, 1),
     }
+    if not args.no_stack:
+        result["stack"] = run_stack(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -442,12 +529,14 @@ def run_reference(args, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--per-m-reps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

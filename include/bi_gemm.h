@@ -97,8 +97,11 @@ typedef struct bi_pins {
                           [floor(s*KT/S), floor((s+1)*KT/S)), KT = ceil(K/bk); the
                           partials are added in ascending s. */
   int32_t tok_tile;    /* T, tokens per tile = the MMA's N extent: 64, 128 or 256 */
-  int32_t stages;      /* shared-memory ring depth; 0 = library default.  Speed
-                          only. */
+  int32_t mma_ctas;    /* 1: tcgen05.mma.cta_group::1, 128 W rows per MMA;
+                          2: tcgen05.mma.cta_group::2 across a CTA pair, 256 W rows
+                          per MMA (each CTA holds 128 W rows and T/2 tokens). */
+  int32_t stages;      /* depth of the W shared-memory ring; 0 = chosen by the
+                          library from the launch.  Speed only. */
   uint32_t flags;      /* BI_FLAG_* */
 } bi_pins;
 
@@ -127,8 +130,8 @@ const char* bi_status_string(bi_status status);
 bi_status bi_pins_default(int64_t N, int64_t K, bi_pins* out);
 
 /* Checks pins for (N, K): version, bk == BI_BK, 1 <= split_k <= min(16, KT),
- * tok_tile in {64,128,256}, stages 0 or in the legal range for tok_tile, flags
- * known, CLUSTER only with split_k <= 8.  Returns BI_OK or
+ * tok_tile in {64,128,256}, mma_ctas in {1,2}, stages 0 or in the legal range,
+ * flags known, CLUSTER only with split_k <= 8.  Returns BI_OK or
  * BI_ERR_ILLEGAL_PINS (BI_ERR_INVALID_ARG for a NULL pointer).  Host only. */
 bi_status bi_pins_validate(int64_t N, int64_t K, const bi_pins* pins);
 
@@ -137,12 +140,13 @@ bi_status bi_pins_validate(int64_t N, int64_t K, const bi_pins* pins);
  * pins) only; the second group is the schedule and may depend on M. */
 typedef struct bi_gemm_plan {
   /* reduction tree: a function of (N, K, pins) */
-  int32_t bk, split_k, tok_tile, mma_m, mma_n, mma_k;
+  int32_t bk, split_k, tok_tile, mma_ctas, mma_m, mma_n, mma_k;
   int64_t k_tiles;
   int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* K-tile boundaries, split s = [begin[s], begin[s+1]) */
   /* schedule: may depend on M */
   int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL or _CLUSTER */
-  int32_t stages;
+  int32_t w_stages, x_stages;              /* depths of the W and X shared-memory rings */
+  int32_t x_box_rows;                      /* token rows per X copy (< tok_tile for small M) */
   int64_t n_tiles, m_tiles;
   int32_t grid_x, grid_y, grid_z, cluster_x, block_threads;
   int64_t smem_bytes;

@@ -40,7 +40,8 @@ BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
 
 class Pins(ctypes.Structure):
     _fields_ = [("abi_version", ctypes.c_int32), ("bk", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("tok_tile", ctypes.c_int32), ("stages", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("tok_tile", ctypes.c_int32), ("mma_ctas", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -56,16 +57,18 @@ class Pins(ctypes.Structure):
 
 class Plan(ctypes.Structure):
     _fields_ = [("bk", ctypes.c_int32), ("split_k", ctypes.c_int32), ("tok_tile", ctypes.c_int32),
-                ("mma_m", ctypes.c_int32), ("mma_n", ctypes.c_int32), ("mma_k", ctypes.c_int32),
+                ("mma_ctas", ctypes.c_int32), ("mma_m", ctypes.c_int32), ("mma_n", ctypes.c_int32),
+                ("mma_k", ctypes.c_int32),
                 ("k_tiles", ctypes.c_int64),
                 ("split_begin", ctypes.c_int64 * (BI_MAX_SPLIT_K + 1)),
-                ("schedule", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("schedule", ctypes.c_int32), ("w_stages", ctypes.c_int32), ("x_stages", ctypes.c_int32),
+                ("x_box_rows", ctypes.c_int32),
                 ("n_tiles", ctypes.c_int64), ("m_tiles", ctypes.c_int64),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("cluster_x", ctypes.c_int32), ("block_threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64)]
 
-    TREE_FIELDS = ("bk", "split_k", "tok_tile", "mma_m", "mma_n", "mma_k", "k_tiles")
+    TREE_FIELDS = ("bk", "split_k", "tok_tile", "mma_ctas", "mma_m", "mma_n", "mma_k", "k_tiles")
 
     def tree(self) -> tuple:
         """The reduction-tree fields: a function of (N, K, pins) only."""

@@ -29,20 +29,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // The explicit table: the Llama-3.1 projection shapes of the workloads this
-// library is measured on.  (N, K) -> (S, T).
+// library is measured on.  (N, K) -> (S, T, mma_ctas).
 struct TableEntry {
   int64_t N, K;
-  int32_t S, T;
+  int32_t S, T, ctas;
 };
 const TableEntry kTable[] = {
-    {128, 256, 2, 128},       // tiny invariance shape: exercises the split fold
-    {4096, 14336, 4, 128},    // Llama-3.1-8B down_proj
-    {6144, 4096, 3, 128},     // Llama-3.1-8B qkv
-    {28672, 4096, 2, 128},    // Llama-3.1-8B gate_up
-    {10240, 8192, 5, 128},    // Llama-3.1-70B qkv
-    {8192, 8192, 2, 128},     // Llama-3.1-70B o_proj
-    {57344, 8192, 1, 128},    // Llama-3.1-70B gate_up
-    {8192, 28672, 2, 128},    // Llama-3.1-70B down_proj
+    {128, 256, 2, 128, 1},       // tiny invariance shape: exercises the split fold
+    {4096, 14336, 4, 256, 1},    // Llama-3.1-8B down_proj: 32 W tiles x 4 = 128 CTAs at decode
+    {6144, 4096, 3, 256, 1},     // Llama-3.1-8B qkv: 48 x 3 = 144
+    {28672, 4096, 2, 256, 1},    // Llama-3.1-8B gate_up: 224 x 2 = 448 (2.95 waves)
+    {10240, 8192, 3, 256, 1},    // Llama-3.1-70B qkv: 80 x 3 = 240
+    {8192, 8192, 2, 256, 1},     // Llama-3.1-70B o_proj: 64 x 2 = 128
+    {57344, 8192, 1, 256, 1},    // Llama-3.1-70B gate_up: 448 tiles, persistent
+    {8192, 28672, 2, 256, 1},    // Llama-3.1-70B down_proj: 64 x 2 = 128
 };
 
 // Rule for shapes outside the table: the split count that best fills
@@ -74,7 +74,7 @@ bi_status check_nk(int64_t N, int64_t K) {
 }
 
 struct Resolved {
-  int32_t S, T, stages;
+  int32_t S, T, ctas, w_pin;
   uint32_t flags;
   int64_t KT;
 };
@@ -128,18 +128,19 @@ int sm_count_current() {
   return n;
 }
 
-// Schedule choice from M (speed only).  Rounds of chain work per SM:
-// LOCAL runs ceil(tiles / P) tiles of S chains each; CLUSTER runs the
-// tiles * S chains as independent CTAs.  CLUSTER is charged 15% for its
-// un-overlapped epilogue and fold.
+// Schedule choice from M (speed only).  Rounds of chain work per unit (a CTA,
+// or a CTA pair when mma_ctas = 2): LOCAL runs ceil(tiles / units) tiles of S
+// chains each; CLUSTER runs the tiles * S chains as independent units.
+// CLUSTER is charged 15% for its un-overlapped epilogue and fold.
 int32_t choose_schedule(const Resolved& r, int64_t tiles, int32_t sm_count) {
   const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
   if (r.S == 1) return BI_FLAG_SCHEDULE_LOCAL;
   if (forced == BI_FLAG_SCHEDULE_LOCAL) return BI_FLAG_SCHEDULE_LOCAL;
   if (forced == BI_FLAG_SCHEDULE_CLUSTER) return BI_FLAG_SCHEDULE_CLUSTER;
-  if (r.S > 8) return BI_FLAG_SCHEDULE_LOCAL;
-  const double local_rounds = (double)ceil_div(tiles, sm_count) * r.S;
-  const double cluster_rounds = (double)ceil_div(tiles * r.S, sm_count);
+  if (r.S * r.ctas > 8) return BI_FLAG_SCHEDULE_LOCAL;  // portable cluster sizes only
+  const int64_t slots = sm_count / r.ctas;
+  const double local_rounds = (double)ceil_div(tiles, slots) * r.S;
+  const double cluster_rounds = (double)ceil_div(tiles * r.S, slots);
   return cluster_rounds * 1.15 < local_rounds ? BI_FLAG_SCHEDULE_CLUSTER : BI_FLAG_SCHEDULE_LOCAL;
 }
 
@@ -149,31 +150,41 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& r, int32_t 
   plan->bk = kBK;
   plan->split_k = r.S;
   plan->tok_tile = r.T;
-  plan->mma_m = kTileN;
+  plan->mma_ctas = r.ctas;
+  plan->mma_m = kTileN * r.ctas;
   plan->mma_n = r.T;
   plan->mma_k = kMmaK;
   plan->k_tiles = r.KT;
   for (int s = 0; s <= r.S; ++s) plan->split_begin[s] = ((int64_t)s * r.KT) / r.S;
-  plan->stages = r.stages;
-  plan->n_tiles = ceil_div(N, kTileN);
+  plan->n_tiles = ceil_div(N, plan->mma_m);
   plan->m_tiles = M > 0 ? ceil_div(M, r.T) : 0;
+  // Token rows each CTA holds per X stage, and how many of them a copy brings
+  // in: a single token tile loads only its valid rows (rounded up to 8); the
+  // rest of each X stage is zeroed once and never rewritten.  Speed only: the
+  // MMA still reads all rows, and rows past M are zero either way.
+  const int32_t x_rows = r.T / r.ctas;
+  plan->x_box_rows = (plan->m_tiles == 1 && M <= x_rows) ? (int32_t)((M + 7) / 8 * 8) : x_rows;
+  if (plan->x_box_rows > x_rows) plan->x_box_rows = x_rows;
+  choose_stages(x_rows, plan->x_box_rows, r.w_pin, &plan->w_stages, &plan->x_stages);
   plan->block_threads = kGemmThreads;
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
   plan->schedule = choose_schedule(r, tiles, sm_count);
   const bool cluster = plan->schedule == BI_FLAG_SCHEDULE_CLUSTER;
   if (cluster) {
     if (plan->n_tiles > 65535 || plan->m_tiles > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
-    plan->grid_x = r.S;
+    plan->grid_x = r.S * r.ctas;
     plan->grid_y = (int32_t)plan->n_tiles;
     plan->grid_z = (int32_t)plan->m_tiles;
-    plan->cluster_x = r.S;
+    plan->cluster_x = r.S * r.ctas;
   } else {
-    plan->grid_x = (int32_t)(tiles < sm_count ? tiles : sm_count);
+    const int64_t slots = sm_count / r.ctas > 0 ? sm_count / r.ctas : 1;
+    plan->grid_x = (int32_t)((tiles < slots ? tiles : slots) * r.ctas);
     plan->grid_y = 1;
     plan->grid_z = 1;
-    plan->cluster_x = 1;
+    plan->cluster_x = r.ctas;
   }
-  plan->smem_bytes = gemm_smem_bytes(r.T, r.stages, cluster);
+  plan->smem_bytes = gemm_smem_bytes(r.T, x_rows, plan->w_stages, plan->x_stages, cluster);
+  if (plan->w_stages < 2 || plan->x_stages < 2) return BI_ERR_ILLEGAL_PINS;
   if (plan->smem_bytes > kMaxDynSmem) return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
 }
@@ -187,11 +198,13 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
   if (p->bk != kBK) return BI_ERR_ILLEGAL_PINS;
   if (p->split_k < 1 || p->split_k > BI_MAX_SPLIT_K || p->split_k > kt) return BI_ERR_ILLEGAL_PINS;
   if (p->tok_tile != 64 && p->tok_tile != 128 && p->tok_tile != 256) return BI_ERR_ILLEGAL_PINS;
-  if (p->stages != 0 && (p->stages < 2 || p->stages > max_stages(p->tok_tile)))
+  if (p->mma_ctas != 1 && p->mma_ctas != 2) return BI_ERR_ILLEGAL_PINS;
+  if (p->stages != 0 && (p->stages < 2 || p->stages > max_w_stages(p->tok_tile / p->mma_ctas, 2)))
     return BI_ERR_ILLEGAL_PINS;
   if (p->flags & ~BI_FLAG_KNOWN_MASK) return BI_ERR_ILLEGAL_PINS;
   const uint32_t sched = p->flags & BI_FLAG_SCHEDULE_MASK;
   if (sched == BI_FLAG_SCHEDULE_MASK) return BI_ERR_ILLEGAL_PINS;
+  if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * p->mma_ctas > 16) return BI_ERR_ILLEGAL_PINS;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k > 8) return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
 }
@@ -200,11 +213,12 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
   if (!out) return BI_ERR_INVALID_ARG;
   bi_status st = check_nk(N, K);
   if (st != BI_OK) return st;
-  int32_t S = 0, T = 128;
+  int32_t S = 0, T = 256, ctas = 1;
   for (const TableEntry& e : kTable) {
     if (e.N == N && e.K == K) {
       S = e.S;
       T = e.T;
+      ctas = e.ctas;
       break;
     }
   }
@@ -215,6 +229,7 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
   out->bk = kBK;
   out->split_k = S;
   out->tok_tile = T;
+  out->mma_ctas = ctas;
   out->stages = 0;
   out->flags = BI_FLAG_SCHEDULE_AUTO;
   return BI_OK;
@@ -232,7 +247,8 @@ bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r) {
   if (st != BI_OK) return st;
   r->S = p.split_k;
   r->T = p.tok_tile;
-  r->stages = p.stages ? p.stages : default_stages(p.tok_tile);
+  r->ctas = p.mma_ctas;
+  r->w_pin = p.stages;
   r->flags = p.flags;
   r->KT = ceil_div(K, kBK);
   return BI_OK;
@@ -264,7 +280,7 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
   if (!encode_kmajor(&L.tmW, W, N, K, kTileN)) return BI_ERR_CUDA;
-  if (!encode_kmajor(&L.tmX, X, M, K, r.T)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows)) return BI_ERR_CUDA;
   L.Y = Y;
   L.M = M;
   L.N = N;
@@ -274,13 +290,18 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.k_tiles = (int32_t)r.KT;
   L.S = r.S;
   L.T = r.T;
-  L.stages = r.stages;
+  L.w_stages = plan.w_stages;
+  L.x_stages = plan.x_stages;
+  L.x_box_rows = plan.x_box_rows;
   L.cluster = plan.schedule == BI_FLAG_SCHEDULE_CLUSTER;
+  L.pair = r.ctas == 2;
   L.grid_x = plan.grid_x;
   L.grid_y = plan.grid_y;
   L.grid_z = plan.grid_z;
   L.smem = plan.smem_bytes;
   L.flags = r.flags;
+  if (plan.x_box_rows < r.T / r.ctas) L.flags |= kFlagZeroX;
+  if (plan.m_tiles == 1) L.flags |= kFlagStreamW;
   L.stream = stream;
   return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }

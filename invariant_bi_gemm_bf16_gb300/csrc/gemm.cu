@@ -6,9 +6,10 @@
 //   * K is cut into K tiles of 64 elements; split s (0 <= s < S) owns K tiles
 //     [floor(s*KT/S), floor((s+1)*KT/S)).
 //   * Inside a split, the partial acc_s is one chain of tcgen05.mma
-//     instructions of shape 128 x T x 16 in ascending k, the first of which
-//     overwrites the accumulator.  W rows sit on the MMA's M side (TMEM lanes),
-//     tokens on its N side (TMEM columns); T is a pin.
+//     instructions of shape (128 * mma_ctas) x T x 16 in ascending k, the first
+//     of which overwrites the accumulator.  W rows sit on the MMA's M side
+//     (TMEM lanes), tokens on its N side (TMEM columns).  T and mma_ctas
+//     (cta_group::1, or cta_group::2 across a CTA pair) are pins.
 //   * The partials are added in ascending s in fp32: (((acc_0 + acc_1) + acc_2) ...).
 // CoRun (Padding is Simple and Efficient for Deterministic LLM Inference),
 // Sec. III-A, Fig. 3(b): a batch-invariant reduction uses one fixed partition
@@ -17,18 +18,27 @@
 // the split count and boundaries are pins in the same spirit.
 //
 // What may depend on M (and changes no bit): the number of token tiles, the
-// grid, which SM runs which tile, and whether the S chains of a tile run on one
-// CTA (LOCAL) or on a cluster of S CTAs (CLUSTER):
-//   LOCAL   a persistent CTA walks its tiles; for each tile it runs the S
+// grid, which SM runs which tile, how many token rows a copy brings in, the
+// ring depths, and whether the S chains of a tile run on one CTA (pair) or on a
+// cluster (LOCAL vs CLUSTER):
+//   LOCAL   a persistent CTA (pair) walks its tiles; for each tile it runs the S
 //           chains one after the other into two ping-pong TMEM accumulators;
 //           the epilogue warps fold them into registers as they complete.
-//   CLUSTER each CTA of an S-CTA cluster runs one chain; the partials go to
-//           shared memory and are folded in ascending rank order through
+//   CLUSTER each CTA (pair) of a cluster runs one chain; the partials go to
+//           shared memory and are folded in ascending split order through
 //           distributed shared memory.  No atomics and no global workspace.
 //
-// Warp roles (320 threads): warp 0 = TMA producer (one lane), warp 1 = MMA
-// issuer (one lane) and TMEM owner, warps 2..9 = epilogue (two warps per TMEM
-// lane quadrant, each owning half of the T accumulator columns).
+// Warp roles (352 threads): warp 0 = W producer (TMA, one lane), warp 1 = MMA
+// issuer (one lane) and TMEM owner, warp 2 = X producer, warps 3..10 =
+// epilogue (two warps per TMEM lane quadrant, each owning half of the T
+// accumulator columns).  W and X have separate shared-memory rings so that
+// the W stream (from HBM) can run further ahead than the X stream.
+//
+// In a CTA pair (mma_ctas = 2) both CTAs load their own W rows and their half
+// of the token rows; the even CTA waits for both halves on its own mbarriers,
+// issues the cta_group::2 MMAs, and its commits free both CTAs' stages
+// (multicast).  Both CTAs' epilogues release an accumulator on the even CTA's
+// barrier.
 //
 // Every wait is bounded (2 s of wall clock).  When one runs out, the kernel
 // records BI_ERR_DEVICE_TIMEOUT in a device status word, every role abandons
@@ -48,13 +58,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct GemmParams {
   __nv_bfloat16* Y;
   int64_t M, N;
-  int32_t n_tiles, m_tiles, k_tiles, S, stages;
-  uint32_t flags;
+  int32_t n_tiles, m_tiles, k_tiles, S;
+  int32_t w_stages, x_stages, x_box_rows;
+  uint32_t flags;  // BI_FLAG_DEBUG_STALL_PRODUCER | kFlagStreamW | kFlagZeroX
 };
 
 struct __align__(8) SmemCtl {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t w_full[kMaxStages];
+  uint64_t w_empty[kMaxStages];
+  uint64_t x_full[kMaxStages];
+  uint64_t x_empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
@@ -105,47 +118,70 @@ __device__ __forceinline__ int64_t split_begin(int32_t s, int32_t S, int32_t KT)
   return ((int64_t)s * KT) / S;
 }
 
-template <int T, bool CLUSTER>
+template <int T, bool CLUSTER, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     bi_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
-  constexpr int kStage = stage_bytes(T);
-  constexpr int kWBytes = kTileN * kBK * 2;
+  constexpr int kXRows = PAIR ? T / 2 : T;          // token rows in this CTA's X stage
+  constexpr int kXStage = kXRows * kBK * 2;
+  constexpr int kMmaM = PAIR ? 2 * kTileN : kTileN;  // W rows per tile
   constexpr uint32_t kTmemCols = CLUSTER ? (uint32_t)T : 2u * (uint32_t)T;
-  constexpr int kHalf = T / 2;  // accumulator columns per epilogue warp
+  constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quadrant
+  constexpr int kHalf = T / kColGroups;      // accumulator columns per epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int stages = p.stages;
-  const int64_t ring_bytes = (int64_t)stages * kStage;
+  const int ws = p.w_stages;
+  const int xs = p.x_stages;
+  const int64_t w_ring = (int64_t)ws * kWStageBytes;
+  const int64_t ring_bytes = w_ring + (int64_t)xs * kXStage;
   const int64_t part_bytes = CLUSTER ? (int64_t)T * kTileN * 4 : 0;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (ring_bytes > part_bytes ? ring_bytes : part_bytes));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
+  const uint32_t w_base = smem_base;                       // W stage i at w_base + i * 16 KB
+  const uint32_t x_base = smem_base + (uint32_t)w_ring;    // X stage i at x_base + i * kXStage
+
+  const uint32_t crank = (PAIR || CLUSTER) ? cluster_ctarank() : 0u;
+  const uint32_t peer = PAIR ? (crank & 1u) : 0u;          // 0 = the pair's MMA-issuing CTA
+  const bool leader = peer == 0;
+  const uint32_t leader_rank = crank & ~1u;
+  const uint16_t pair_mask = (uint16_t)(3u << leader_rank);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    for (int i = 0; i < ws; ++i) {
+      mbar_init(smem_u32(&ctl->w_full[i]), 1);
+      mbar_init(smem_u32(&ctl->w_empty[i]), 1);
+    }
+    for (int i = 0; i < xs; ++i) {
+      mbar_init(smem_u32(&ctl->x_full[i]), 1);
+      mbar_init(smem_u32(&ctl->x_empty[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiWarps);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiWarps * (PAIR ? 2 : 1));
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
+  // In a pair, the peer's barriers must be initialised before anyone signals them.
+  if constexpr (PAIR) cluster_sync();
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmX);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -156,20 +192,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int32_t S = p.S;
   const int32_t KT = p.k_tiles;
   const int64_t num_tiles = (int64_t)p.n_tiles * p.m_tiles;
-  // Work list.  CLUSTER: one tile (blockIdx.y, blockIdx.z), one split (the
-  // cluster rank).  LOCAL: tiles blockIdx.x, blockIdx.x + gridDim.x, ... and
-  // all S splits of each.
-  const int32_t my_split = CLUSTER ? (int32_t)cluster_ctarank() : 0;
-  const int64_t tile_first = CLUSTER ? 0 : blockIdx.x;
-  const int64_t tile_step = CLUSTER ? 1 : gridDim.x;
+  // Work list.  CLUSTER: one tile (blockIdx.y, blockIdx.z) and one split (the
+  // cluster rank, counted in pairs when PAIR).  LOCAL: tiles u, u + U, ... for
+  // unit u of U (a unit is a CTA, or a CTA pair), all S splits of each.
+  const int32_t my_split = CLUSTER ? (int32_t)(PAIR ? (crank >> 1) : crank) : 0;
+  const int64_t unit = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t units = PAIR ? (gridDim.x >> 1) : gridDim.x;
+  const int64_t tile_first = CLUSTER ? 0 : unit;
+  const int64_t tile_step = CLUSTER ? 1 : units;
   const int64_t tile_end = CLUSTER ? 1 : num_tiles;
   const int32_t s_first = CLUSTER ? my_split : 0;
   const int32_t s_end = CLUSTER ? my_split + 1 : S;
+  const bool stream_w = (p.flags & kFlagStreamW) != 0;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------ producers (W: warp 0, X: warp 2)
+    const bool is_w = warp == 0;
+    if (!is_w && (p.flags & kFlagZeroX)) {
+      // The X boxes cover fewer rows than the MMA reads: zero the whole X ring
+      // once; the loads then only ever overwrite the leading rows.
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t off = (int64_t)lane * 16; off < (int64_t)xs * kXStage; off += 32 * 16)
+        *reinterpret_cast<uint4*>(smem + w_ring + off) = z;
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     if (lane == 0) {
-      const bool stall = (p.flags & BI_FLAG_DEBUG_STALL_PRODUCER) != 0;
+      const bool stall = is_w && (p.flags & BI_FLAG_DEBUG_STALL_PRODUCER) != 0;
+      const int nst = is_w ? ws : xs;
+      uint64_t* full_bar = is_w ? ctl->w_full : ctl->x_full;
+      uint64_t* empty_bar = is_w ? ctl->w_empty : ctl->x_empty;
+      const uint32_t ring = is_w ? w_base : x_base;
+      const uint32_t stage_sz = is_w ? (uint32_t)kWStageBytes : (uint32_t)kXStage;
+      // transaction bytes per stage, both CTAs of a pair counted on the even CTA
+      const uint32_t tx = (is_w ? (uint32_t)kWStageBytes : (uint32_t)p.x_box_rows * kBK * 2) *
+                          (PAIR ? 2u : 1u);
+      const CUtensorMap* map = is_w ? &tmW : &tmX;
+      const bool hinted = stream_w;
+      const uint64_t policy = is_w ? policy_evict_first() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -177,43 +237,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
         const int32_t n_tile = CLUSTER ? (int32_t)blockIdx.y : (int32_t)(t % p.n_tiles);
         const int32_t m_tile = CLUSTER ? (int32_t)blockIdx.z : (int32_t)(t / p.n_tiles);
+        const int32_t row = is_w ? n_tile * kMmaM + (int32_t)peer * kTileN
+                                 : m_tile * T + (int32_t)peer * kXRows;
         for (int32_t s = s_first; ok && s < s_end; ++s) {
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
           for (int64_t kt = k0; kt < k1; ++kt) {
-            const uint32_t empty = smem_u32(&ctl->empty[stage]);
-            if (!wait_or_abort(empty, phase ^ 1u, abort)) {
+            if (!wait_or_abort(smem_u32(&empty_bar[stage]), phase ^ 1u, abort)) {
               ok = false;
               break;
             }
             if (!(stall && issued == 0)) {
-              const uint32_t full = smem_u32(&ctl->full[stage]);
-              const uint32_t sw = smem_base + stage * kStage;
-              mbar_arrive_expect_tx(full, (uint32_t)kStage);
-              tma_load_2d(sw, &tmW, full, (int32_t)(kt * kBK), n_tile * kTileN);
-              tma_load_2d(sw + kWBytes, &tmX, full, (int32_t)(kt * kBK), m_tile * T);
+              const uint32_t full = smem_u32(&full_bar[stage]);
+              const uint32_t dst = ring + (uint32_t)stage * stage_sz;
+              const int32_t kx = (int32_t)(kt * kBK);
+              if constexpr (PAIR) {
+                const uint32_t bar = leader ? full : mapa_shared(full, leader_rank);
+                if (leader) mbar_arrive_expect_tx(full, tx);
+                if (hinted)
+                  tma_load_2d_pair_hint(dst, map, bar, kx, row, policy);
+                else
+                  tma_load_2d_pair(dst, map, bar, kx, row);
+              } else {
+                mbar_arrive_expect_tx(full, tx);
+                if (hinted)
+                  tma_load_2d_hint(dst, map, full, kx, row, policy);
+                else
+                  tma_load_2d(dst, map, full, kx, row);
+              }
             }
             ++issued;
-            if (++stage == stages) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
       }
-      // Drain: the copies of the last `stages` loads must have landed before
-      // the CTA may exit (they write into this CTA's shared memory).
-      const int64_t first = issued > stages ? issued - stages : 0;
-      for (int64_t i = first; i < issued; ++i) {
-        if (stall && i == 0) continue;
-        wait_drain(smem_u32(&ctl->full[i % stages]), (uint32_t)((i / stages) & 1));
+      // Drain: the copies of the last `nst` loads must have landed before the
+      // CTA may exit (they write into this CTA's shared memory).  In a pair the
+      // odd CTA's copies complete on the even CTA's barriers, which that CTA
+      // drains; both CTAs meet at a cluster barrier before either exits.
+      if (leader) {
+        const int64_t first = issued > nst ? issued - nst : 0;
+        for (int64_t i = first; i < issued; ++i) {
+          if (stall && i == 0) continue;
+          wait_drain(smem_u32(&full_bar[i % nst]), (uint32_t)((i / nst) & 1));
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(kTileN, T);
-      int stage = 0;
-      uint32_t phase = 0;
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = make_idesc_bf16(kMmaM, T);
+      int wi = 0, xi = 0;
+      uint32_t wph = 0, xph = 0;
       uint32_t acc_iter = 0;
       bool ok = true;
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
@@ -228,41 +305,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t d_tmem = tmem_base + buf * (uint32_t)T;
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
           for (int64_t kt = k0; kt < k1; ++kt) {
-            if (!wait_or_abort(smem_u32(&ctl->full[stage]), phase, abort)) {
+            if (!wait_or_abort(smem_u32(&ctl->w_full[wi]), wph, abort) ||
+                !wait_or_abort(smem_u32(&ctl->x_full[xi]), xph, abort)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sw = smem_base + stage * kStage;
-            const uint64_t a_desc = make_sdesc_sw128(sw);
-            const uint64_t b_desc = make_sdesc_sw128(sw + kWBytes);
+            const uint64_t a_desc = make_sdesc_sw128(w_base + (uint32_t)wi * kWStageBytes);
+            const uint64_t b_desc = make_sdesc_sw128(x_base + (uint32_t)xi * kXStage);
 #pragma unroll
             for (int j = 0; j < kBK / kMmaK; ++j) {
               // +32 bytes per 16 K elements, in the descriptor's 16-byte units
-              mma_bf16(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc,
-                       (kt > k0 || j > 0) ? 1u : 0u);
+              const uint32_t acc = (kt > k0 || j > 0) ? 1u : 0u;
+              if constexpr (PAIR)
+                mma_bf16_pair(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc, acc);
+              else
+                mma_bf16(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc, acc);
             }
-            mma_commit(smem_u32(&ctl->empty[stage]));
-            if (++stage == stages) {
-              stage = 0;
-              phase ^= 1u;
+            if constexpr (PAIR) {
+              mma_commit_pair_mc(smem_u32(&ctl->w_empty[wi]), pair_mask);
+              mma_commit_pair_mc(smem_u32(&ctl->x_empty[xi]), pair_mask);
+            } else {
+              mma_commit(smem_u32(&ctl->w_empty[wi]));
+              mma_commit(smem_u32(&ctl->x_empty[xi]));
+            }
+            if (++wi == ws) {
+              wi = 0;
+              wph ^= 1u;
+            }
+            if (++xi == xs) {
+              xi = 0;
+              xph ^= 1u;
             }
           }
           if (!ok) break;
-          mma_commit(smem_u32(&ctl->acc_full[buf]));
+          if constexpr (PAIR)
+            mma_commit_pair_mc(smem_u32(&ctl->acc_full[buf]), pair_mask);
+          else
+            mma_commit(smem_u32(&ctl->acc_full[buf]));
           ++acc_iter;
         }
       }
       // Every MMA this thread issued must be complete before TMEM is freed.
-      mma_commit(smem_u32(&ctl->mma_done));
+      if constexpr (PAIR)
+        mma_commit_pair(smem_u32(&ctl->mma_done));
+      else
+        mma_commit(smem_u32(&ctl->mma_done));
       wait_drain(smem_u32(&ctl->mma_done), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
+    const int ew = warp - kFirstEpiWarp;
     const int quad = warp & 3;            // TMEM lanes [32*quad, 32*quad + 32)
-    const int half = ew >> 2;             // accumulator columns [half*T/2, half*T/2 + T/2)
-    const int n_local = quad * 32 + lane; // W row within the tile
+    const int half = ew >> 2;             // accumulator columns [half*kHalf, (half+1)*kHalf)
+    const int n_local = quad * 32 + lane; // W row within this CTA's 128 rows
     const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
     uint32_t acc_iter = 0;
     bool ok = true;
@@ -283,34 +379,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t taddr = tmem_base + t_lane + buf * (uint32_t)T + (uint32_t)(half * kHalf);
 #pragma unroll
-          for (int c = 0; c < kHalf; c += 32) {
-            float v[32];
-            tmem_ld32(taddr + (uint32_t)c, v);
+          for (int c = 0; c < kHalf; c += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)c, v);
             if (s == 0) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) R[c + i] = v[i];
+              for (int i = 0; i < 16; ++i) R[c + i] = v[i];
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) R[c + i] = __fadd_rn(R[c + i], v[i]);
+              for (int i = 0; i < 16; ++i) R[c + i] = __fadd_rn(R[c + i], v[i]);
             }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+          if (lane == 0) {
+            const uint32_t ae = smem_u32(&ctl->acc_empty[buf]);
+            if constexpr (PAIR)
+              mbar_arrive_remote(mapa_shared(ae, leader_rank));
+            else
+              mbar_arrive(ae);
+          }
           ++acc_iter;
         }
         if (!ok) break;
-        const int64_t n = (int64_t)n_tile * kTileN + n_local;
+        const int64_t n = (int64_t)n_tile * kMmaM + (int64_t)peer * kTileN + n_local;
         if (n < p.N) {
           const int64_t m0 = (int64_t)m_tile * T + half * kHalf;
           __nv_bfloat16* y = p.Y + m0 * p.N + n;
           const int64_t mrem = p.M - m0;
+          const int mv = mrem < kHalf ? (int)mrem : kHalf;
 #pragma unroll
-          for (int c = 0; c < kHalf; c += 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (c + i < mrem) y[(int64_t)(c + i) * p.N] = __float2bfloat16_rn(R[c + i]);
-            }
+          for (int j = 0; j < kHalf; ++j) {
+            if (j < mv) *y = __float2bfloat16_rn(R[j]);
+            y += p.N;
           }
         }
       }
@@ -338,21 +439,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
+  // In a pair, the even CTA's MMAs write both CTAs' TMEM: nobody frees TMEM
+  // (or exits) until that CTA has drained them.
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
   if constexpr (CLUSTER) {
-    // Fold the S partials of the tile in ascending rank order.  CTA r folds
-    // tokens r, r + S, r + 2S, ...; element pairs are spread over all threads.
+    // Fold the S partials of the tile in ascending split order.  The CTA of
+    // split r folds tokens r, r + S, r + 2S, ... of its own 128 W rows; element
+    // pairs are spread over all threads.
     cluster_sync();
     const int32_t rank = my_split;
     const int64_t m0 = (int64_t)blockIdx.z * T;
-    const int64_t n0 = (int64_t)blockIdx.y * kTileN;
+    const int64_t n0 = (int64_t)blockIdx.y * kMmaM + (int64_t)peer * kTileN;
     const int64_t remm = p.M - m0;
     const int mv = remm < T ? (int)remm : T;
     const int64_t remn = p.N - n0;
-    const int nv = remn < kTileN ? (int)remn : kTileN;
+    const int nv = remn <= 0 ? 0 : (remn < kTileN ? (int)remn : kTileN);
     const int rows_mine = rank < mv ? (mv - rank + S - 1) / S : 0;
     const int items = rows_mine * (kTileN / 2);
     const bool even_n = (p.N & 1) == 0;
@@ -361,9 +469,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int n = 2 * (it % (kTileN / 2));
       if (n >= nv) continue;
       const uint32_t off = smem_base + (uint32_t)((j * kTileN + n) * 4);
-      float2 r = ld_dsmem_f32x2(mapa_shared(off, 0));
+      // split c's partial of these W rows sits in cluster CTA c (or 2c + peer)
+      float2 r = ld_dsmem_f32x2(mapa_shared(off, PAIR ? peer : 0u));
       for (int c = 1; c < S; ++c) {
-        const float2 v = ld_dsmem_f32x2(mapa_shared(off, (uint32_t)c));
+        const uint32_t src = PAIR ? (uint32_t)(2 * c) + peer : (uint32_t)c;
+        const float2 v = ld_dsmem_f32x2(mapa_shared(off, src));
         r.x = __fadd_rn(r.x, v.x);
         r.y = __fadd_rn(r.y, v.y);
       }
@@ -383,29 +493,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-int max_stages(int T) {
-  const int avail = kMaxDynSmem - 1024 - kCtlBytes;
-  int s = avail / stage_bytes(T);
-  return s > kMaxStages ? kMaxStages : s;
+int max_w_stages(int x_rows, int x_stages) {
+  const int left = kRingBytes - x_stages * x_stage_bytes(x_rows);
+  int w = left / kWStageBytes;
+  return w > kMaxStages ? kMaxStages : w;
 }
 
-int default_stages(int T) {
-  const int m = max_stages(T);
-  return m > 6 ? 6 : m;
+void choose_stages(int x_rows, int x_box_rows, int w_pin, int* w_stages, int* x_stages) {
+  const int xb = x_stage_bytes(x_rows);
+  int xs, w;
+  if (x_box_rows <= 64) {
+    // Decode: X is a few rows from L2, W streams from HBM -- put the shared
+    // memory into W bytes in flight.
+    xs = 3;
+    w = max_w_stages(x_rows, xs);
+  } else {
+    // Both operands matter: as many balanced stages as fit, then extra W.
+    int n = kRingBytes / (kWStageBytes + xb);
+    if (n > kMaxStages) n = kMaxStages;
+    xs = n;
+    w = max_w_stages(x_rows, xs);
+  }
+  if (w_pin > 0) {
+    w = w_pin;
+    int xfit = (kRingBytes - w * kWStageBytes) / xb;
+    if (xs > xfit) xs = xfit;
+  }
+  *w_stages = w;
+  *x_stages = xs;
 }
 
-int64_t gemm_smem_bytes(int T, int stages, bool cluster) {
-  int64_t ring = (int64_t)stages * stage_bytes(T);
+int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, bool cluster) {
+  int64_t ring = (int64_t)w_stages * kWStageBytes + (int64_t)x_stages * x_stage_bytes(x_rows);
   int64_t part = cluster ? (int64_t)T * kTileN * 4 : 0;
   return 1024 + (ring > part ? ring : part) + kCtlBytes;
 }
 
-template <int T, bool CLUSTER>
+template <int T, bool CLUSTER, bool PAIR>
 static cudaError_t launch_t(const GemmLaunch& L) {
-  auto kern = bi_gemm_kernel<T, CLUSTER>;
+  auto kern = bi_gemm_kernel<T, CLUSTER, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   if (e != cudaSuccess) return e;
-  if (CLUSTER && L.S > 8) {
+  const int cluster = CLUSTER ? L.S * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
+  if (cluster > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
@@ -417,7 +547,9 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   prm.m_tiles = L.m_tiles;
   prm.k_tiles = L.k_tiles;
   prm.S = L.S;
-  prm.stages = L.stages;
+  prm.w_stages = L.w_stages;
+  prm.x_stages = L.x_stages;
+  prm.x_box_rows = L.x_box_rows;
   prm.flags = L.flags;
 
   cudaLaunchConfig_t cfg = {};
@@ -427,9 +559,9 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
   cfg.numAttrs = 0;
-  if (CLUSTER) {
+  if (cluster > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)L.S;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -438,17 +570,22 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.tmW, L.tmX, prm);
 }
 
-cudaError_t launch_gemm(const GemmLaunch& L) {
+template <bool PAIR>
+static cudaError_t launch_p(const GemmLaunch& L) {
   switch (L.T) {
     case 64:
-      return L.cluster ? launch_t<64, true>(L) : launch_t<64, false>(L);
+      return L.cluster ? launch_t<64, true, PAIR>(L) : launch_t<64, false, PAIR>(L);
     case 128:
-      return L.cluster ? launch_t<128, true>(L) : launch_t<128, false>(L);
+      return L.cluster ? launch_t<128, true, PAIR>(L) : launch_t<128, false, PAIR>(L);
     case 256:
-      return L.cluster ? launch_t<256, true>(L) : launch_t<256, false>(L);
+      return L.cluster ? launch_t<256, true, PAIR>(L) : launch_t<256, false, PAIR>(L);
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L) {
+  return L.pair ? launch_p<true>(L) : launch_p<false>(L);
 }
 
 cudaError_t fetch_and_clear_stall(int* host_dst, cudaStream_t stream) {

@@ -14,27 +14,41 @@ namespace bi {
 constexpr int kTileN = BI_TILE_N;  // W rows per tile: the MMA's M extent
 constexpr int kBK = BI_BK;         // K elements per K tile (one 128-byte swizzle row)
 constexpr int kMmaK = 16;          // K per tcgen05.mma.kind::f16 instruction
-constexpr int kEpiWarps = 8;       // epilogue warps (two per TMEM lane quadrant)
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue
+constexpr int kEpiWarps = 16;      // epilogue warps (four per TMEM lane quadrant)
+constexpr int kFirstEpiWarp = 3;   // warps 0..2: W producer, MMA issuer, X producer
+constexpr int kGemmThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kMaxStages = 16;
 constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 
-// Shared-memory bytes of one ring stage: a W tile [128 x 64] and an X tile [T x 64].
-constexpr int stage_bytes(int T) { return (kTileN + T) * kBK * 2; }
-// Bytes after the ring for mbarriers and bookkeeping.
-constexpr int kCtlBytes = 512;
-int max_stages(int T);
-int default_stages(int T);
+// Internal GEMM flags (above the public BI_FLAG_* bits).
+constexpr uint32_t kFlagStreamW = 1u << 16;  // W read once: evict-first, X evict-last in L2
+constexpr uint32_t kFlagZeroX = 1u << 17;    // X boxes hold fewer rows than T: zero the ring once
+
+// Shared-memory bytes of one W stage [128 x 64] and one X stage [rows x 64]
+// (rows = T, or T/2 per CTA of a pair).
+constexpr int kWStageBytes = kTileN * kBK * 2;
+constexpr int x_stage_bytes(int x_rows) { return x_rows * kBK * 2; }
+// Bytes after the rings for mbarriers and bookkeeping.
+constexpr int kCtlBytes = 1024;
+// Bytes available to the two rings (the rest is alignment slack and control).
+constexpr int kRingBytes = kMaxDynSmem - 1024 - kCtlBytes;
+// Deepest W ring that still leaves `x_stages` X stages of `x_rows` rows.
+int max_w_stages(int x_rows, int x_stages);
+// Ring depths for a launch: deep W and shallow X when the X box is small
+// (decode), balanced otherwise.  `w_pin` (the pins' stages field) overrides the
+// W depth when non-zero.  Speed only.
+void choose_stages(int x_rows, int x_box_rows, int w_pin, int* w_stages, int* x_stages);
 // Dynamic shared memory of one GEMM CTA (includes 1 KB of alignment slack).
-int64_t gemm_smem_bytes(int T, int stages, bool cluster);
+int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, bool cluster);
 
 struct GemmLaunch {
   CUtensorMap tmW;   // W [N,K], box 64 x 128, 128-byte swizzle
-  CUtensorMap tmX;   // X [M,K], box 64 x T, 128-byte swizzle, zero fill past M / K
+  CUtensorMap tmX;   // X [M,K], box 64 x x_box_rows, 128-byte swizzle, zero fill past M / K
   void* Y;
   int64_t M, N, K;
-  int32_t n_tiles, m_tiles, k_tiles, S, T, stages;
-  bool cluster;
+  int32_t n_tiles, m_tiles, k_tiles, S, T, w_stages, x_stages, x_box_rows;
+  bool cluster;      // one chain per CTA (pair), folded through DSMEM
+  bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;
   int64_t smem;
   uint32_t flags;

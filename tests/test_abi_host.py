@@ -61,7 +61,7 @@ def test_default_pins_are_legal(bd, N, K):
     p = bd.bi_pins_default(N, K)
     assert p.abi_version == 1 and p.bk == 64
     assert 1 <= p.split_k <= min(16, -(-K // 64))
-    assert p.tok_tile in (64, 128, 256)
+    assert p.tok_tile in (64, 128, 256) and p.mma_ctas in (1, 2)
     assert bd.bi_pins_validate(N, K, p) == bd.BI_OK
 
 
@@ -71,7 +71,8 @@ def test_pins_validation_refuses(bd):
     bad = [good.replace(abi_version=2), good.replace(bk=32), good.replace(split_k=0),
            good.replace(split_k=17), good.replace(tok_tile=96), good.replace(tok_tile=512),
            good.replace(stages=1), good.replace(stages=99), good.replace(flags=0x8000),
-           good.replace(flags=0x3), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER)]
+           good.replace(flags=0x3), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER),
+           good.replace(mma_ctas=0), good.replace(mma_ctas=4)]
     for p in bad:
         assert bd.bi_pins_validate(N, K, p) == bd.BI_ERR_ILLEGAL_PINS, p
     # more splits than K tiles
@@ -156,9 +157,14 @@ def test_split_boundaries_partition_k(bd):
 def test_plan_schedules(bd):
     # decode-sized down_proj runs as clusters of S CTAs; prefill-sized as persistent CTAs
     small = bd.bi_gemm_plan_describe(1, 4096, 14336)
+    assert small.mma_ctas == 1 and small.mma_m == 128 and small.tok_tile == 256
     assert small.schedule == bd.BI_FLAG_SCHEDULE_CLUSTER and small.cluster_x == small.split_k == 4
     assert small.grid_x * small.grid_y * small.grid_z == 32 * 4
+    assert small.x_box_rows == 8 and small.w_stages > small.x_stages
     big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
-    assert big.schedule == bd.BI_FLAG_SCHEDULE_LOCAL and big.grid_x == 152
-    for plan in (small, big):
-        assert plan.smem_bytes <= 232448 and plan.block_threads == 320
+    assert big.schedule == bd.BI_FLAG_SCHEDULE_LOCAL and big.grid_x == 152 and big.cluster_x == 1
+    assert big.x_box_rows == 256
+    pair = bd.bi_gemm_plan_describe(8192, 4096, 14336, bd.bi_pins_default(4096, 14336).replace(mma_ctas=2))
+    assert pair.mma_m == 256 and pair.cluster_x == 2 and pair.grid_x == 152 and pair.x_box_rows == 128
+    for plan in (small, big, pair):
+        assert plan.smem_bytes <= 232448 and plan.block_threads == 32 * 19

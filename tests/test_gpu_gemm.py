@@ -27,14 +27,18 @@ def pins_for(lib, N, K, **kw):
 
 
 @pytest.mark.parametrize("M", [1, 3, 7, 16, 33])
-def test_tiny_config_parity(lib, oracle, M):
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_tiny_config_parity(lib, oracle, M, ctas):
     """X [M,256] ~N(0,1), W [128,256] ~N(0,0.02), seed 0."""
     X = inputs.normal((M, 256), seed=0, stream=inputs.STREAM_X)
     W = inputs.normal((128, 256), std=0.02, seed=0, stream=inputs.STREAM_W)
     yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    outs = []
     for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
-        got = run(lib, X, W, pins_for(lib, 128, 256, flags=flags))
-        check_gemm_parity(got, yf, 256, "tiny M=%d flags=%d" % (M, flags))
+        got = run(lib, X, W, pins_for(lib, 128, 256, flags=flags, mma_ctas=ctas))
+        check_gemm_parity(got, yf, 256, "tiny M=%d flags=%d ctas=%d" % (M, flags, ctas))
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
 
 
 SHAPES = [
@@ -49,7 +53,8 @@ SHAPES = [
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("S,T", [(1, 128), (2, 64), (3, 128), (2, 256), (4, 64)])
-def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T):
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T, ctas):
     kt = -(-K // 64)
     if S > kt:
         pytest.skip("more splits than K tiles")
@@ -58,23 +63,36 @@ def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T):
     yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
     outs = []
     for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_AUTO):
-        got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T, flags=flags))
-        check_gemm_parity(got, yf, K, "M=%d N=%d K=%d S=%d T=%d flags=%d" % (M, N, K, S, T, flags))
+        got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T, flags=flags, mma_ctas=ctas))
+        check_gemm_parity(got, yf, K, "M=%d N=%d K=%d S=%d T=%d ctas=%d flags=%d" % (M, N, K, S, T, ctas, flags))
         outs.append(got)
     # the schedule changes which SM computes what, never a bit
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
 @pytest.mark.parametrize("S,T", [(1, 128), (3, 64), (2, 256)])
-def test_integer_inputs_bit_exact(lib, oracle, S, T):
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_integer_inputs_bit_exact(lib, oracle, S, T, ctas):
     """Integer inputs: every partial sum is an exact integer, so every reduction
     tree gives the same bits as the oracle."""
     M, N, K = 77, 260, 704
     X = inputs.integers((M, K), -8, 8, seed=2, stream=0)
     W = inputs.integers((N, K), -8, 8, seed=2, stream=1)
     _, yb = oracle.gemm(inputs.bits(X), inputs.bits(W))
-    got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T))
+    got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T, mma_ctas=ctas))
     assert np.array_equal(got, yb)
+
+
+def test_observation_mma_pairing(lib):
+    """Not a requirement (the pairing is a pin, part of the tree): records
+    whether cta_group::1 and cta_group::2 MMAs of the same chain give the same
+    bits on this GPU."""
+    M, N, K = 300, 512, 1024
+    X = inputs.normal((M, K), seed=7, stream=0)
+    W = inputs.normal((N, K), std=0.02, seed=7, stream=1)
+    a = run(lib, X, W, pins_for(lib, N, K, split_k=2, tok_tile=128, mma_ctas=1))
+    b = run(lib, X, W, pins_for(lib, N, K, split_k=2, tok_tile=128, mma_ctas=2))
+    print("cta_group::1 vs ::2: %d of %d elements differ" % (int((a != b).sum()), a.size))
 
 
 def test_identity_and_permutation_weights(lib):
@@ -138,8 +156,9 @@ def test_stores_stay_inside_y(lib):
     guard = 4096
     buf = torch.full((guard + M * N + guard,), 123.0, dtype=torch.bfloat16, device="cuda")
     y = buf[guard:guard + M * N].view(M, N)
-    for S, T in [(1, 64), (2, 128), (4, 256)]:
+    for S, T, ctas in [(1, 64, 1), (2, 128, 1), (4, 256, 1), (1, 64, 2), (2, 128, 2), (4, 256, 2)]:
         for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
-            lib.bi_gemm_bf16(X, W, out=y, pins=lib.bi_pins_default(N, K).replace(split_k=S, tok_tile=T, flags=flags))
+            lib.bi_gemm_bf16(X, W, out=y, pins=lib.bi_pins_default(N, K).replace(
+                split_k=S, tok_tile=T, flags=flags, mma_ctas=ctas))
             torch.cuda.synchronize()
             assert torch.all(buf[:guard].float() == 123.0) and torch.all(buf[guard + M * N:].float() == 123.0)
