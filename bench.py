@@ -261,7 +261,9 @@ class DownProjSweep:
             self.X[M] = [inputs.device_normal((M, self.K), seed=seed, stream=inputs.STREAM_X + 16 * i, device=dev)
                          for i in range(nx)]
         self.Y = {M: torch.empty((M, self.N), dtype=torch.bfloat16, device=dev) for M in self.ms}
+        # the weight copies are never written while the sweep runs
         self.pins = bd.bi_pins_default(self.N, self.K)
+        self.pins = self.pins.replace(flags=self.pins.flags | bd.BI_FLAG_PREFETCH_W)
         self.it = 0
 
     def launches_per_step(self):

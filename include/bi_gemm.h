@@ -87,7 +87,15 @@ typedef struct CUstream_st* bi_stream_t;
  * bi_last_device_status() reports BI_ERR_DEVICE_TIMEOUT.  Exists to test the
  * stall detection; never set it otherwise. */
 #define BI_FLAG_DEBUG_STALL_PRODUCER 0x100u
-#define BI_FLAG_KNOWN_MASK (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER)
+/* Speed only.  Every kernel of this library is launched so that it may start
+ * while the previous kernel in the stream is still finishing; it waits for that
+ * kernel before reading any input or writing any output.  With this flag the
+ * GEMM also starts streaming W before that wait, so a decode step's weight
+ * stream overlaps the small kernels before it.  The caller must then guarantee
+ * that W is not written by any kernel still running in the stream when the
+ * call is made (weights are normally written once, long before). */
+#define BI_FLAG_PREFETCH_W 0x200u
+#define BI_FLAG_KNOWN_MASK (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER | BI_FLAG_PREFETCH_W)
 
 typedef struct bi_pins {
   int32_t abi_version; /* BI_PINS_ABI_VERSION */

@@ -36,6 +36,7 @@ BI_FLAG_SCHEDULE_AUTO = 0x0
 BI_FLAG_SCHEDULE_LOCAL = 0x1
 BI_FLAG_SCHEDULE_CLUSTER = 0x2
 BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
+BI_FLAG_PREFETCH_W = 0x200
 
 
 class Pins(ctypes.Structure):

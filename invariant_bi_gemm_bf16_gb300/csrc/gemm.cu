@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmX);
   }
+  // The next kernel in the stream may be scheduled now; it waits for this
+  // grid before touching memory.
+  if (threadIdx.x == 0) grid_dep_launch_dependents();
   if (warp == 1) {
     if constexpr (PAIR) {
       tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -218,6 +221,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
     }
     if (lane == 0) {
+      // Inputs may come from the previous kernel in the stream: wait for it
+      // before the first copy (W may start earlier when the caller allows).
+      if (!is_w || (p.flags & BI_FLAG_PREFETCH_W) == 0) grid_dep_wait();
       const bool stall = is_w && (p.flags & BI_FLAG_DEBUG_STALL_PRODUCER) != 0;
       const int nst = is_w ? ws : xs;
       uint64_t* full_bar = is_w ? ctl->w_full : ctl->x_full;
@@ -557,16 +563,20 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.smem;
   cfg.stream = L.stream;
-  cudaLaunchAttribute attr[1];
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, L.tmW, L.tmX, prm);
 }
 

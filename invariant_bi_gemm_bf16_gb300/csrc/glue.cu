@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bi {
 
@@ -24,6 +25,8 @@ __device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
 
 // out = bf16_rne(a + b)
 __global__ void residual_add_kernel(const uint4* a, const uint4* b, uint4* out, int64_t nvec) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // inputs may come from the previous kernel in the stream
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
        i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 x = a[i], y = b[i];
@@ -49,6 +52,8 @@ __device__ __forceinline__ uint32_t silu_mul2(uint32_t g, uint32_t u) {
 
 // gu [M, 2I] -> out [M, I]; vectors of 8 along I.
 __global__ void silu_mul_kernel(const uint4* gu, uint4* out, int64_t M, int64_t I) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int64_t vpr = I / 8;  // vectors per output row
   const int64_t nvec = M * vpr;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
@@ -69,6 +74,8 @@ __global__ void silu_mul_kernel(const uint4* gu, uint4* out, int64_t M, int64_t 
 // j / (nq / nkv) (the softmax over a single key is exactly 1).
 __global__ void attention_ctx1_kernel(const uint4* qkv, uint4* out, int64_t M, int64_t nq,
                                       int64_t nkv, int64_t D) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int64_t dv = D / 8;                       // vectors per head
   const int64_t in_row = (nq + 2 * nkv) * dv;     // vectors per qkv row
   const int64_t out_row = nq * dv;
@@ -92,22 +99,20 @@ static dim3 glue_grid(int64_t nvec) {
 cudaError_t launch_residual_add(const void* a, const void* b, void* out, int64_t count,
                                 cudaStream_t stream) {
   const int64_t nvec = count / 8;
-  residual_add_kernel<<<glue_grid(nvec), kGlueThreads, 0, stream>>>(
-      static_cast<const uint4*>(a), static_cast<const uint4*>(b), static_cast<uint4*>(out), nvec);
-  return cudaGetLastError();
+  return launch_overlapped(residual_add_kernel, glue_grid(nvec), dim3(kGlueThreads), stream,
+                           static_cast<const uint4*>(a), static_cast<const uint4*>(b),
+                           static_cast<uint4*>(out), nvec);
 }
 
 cudaError_t launch_silu_mul(const void* gu, void* out, int64_t M, int64_t I, cudaStream_t stream) {
-  silu_mul_kernel<<<glue_grid(M * I / 8), kGlueThreads, 0, stream>>>(
-      static_cast<const uint4*>(gu), static_cast<uint4*>(out), M, I);
-  return cudaGetLastError();
+  return launch_overlapped(silu_mul_kernel, glue_grid(M * I / 8), dim3(kGlueThreads), stream,
+                           static_cast<const uint4*>(gu), static_cast<uint4*>(out), M, I);
 }
 
 cudaError_t launch_attention_ctx1(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
                                   int64_t D, cudaStream_t stream) {
-  attention_ctx1_kernel<<<glue_grid(M * nq * D / 8), kGlueThreads, 0, stream>>>(
-      static_cast<const uint4*>(qkv), static_cast<uint4*>(out), M, nq, nkv, D);
-  return cudaGetLastError();
+  return launch_overlapped(attention_ctx1_kernel, glue_grid(M * nq * D / 8), dim3(kGlueThreads), stream,
+                           static_cast<const uint4*>(qkv), static_cast<uint4*>(out), M, nq, nkv, D);
 }
 
 }  // namespace bi

@@ -27,6 +27,23 @@ __device__ __forceinline__ uint32_t lane_id() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Blocks until the grids this grid depends on (the previous kernels in the
+// stream, when launched with programmatic stream serialization) have completed
+// and their memory is visible.  Returns at once for an ordinary launch.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled before this grid finishes
+// (it still waits in grid_dep_wait() before reading anything).
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 

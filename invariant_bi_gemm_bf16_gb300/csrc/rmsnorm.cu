@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bi {
 
@@ -69,6 +70,8 @@ template <int VPL>
 __global__ void __launch_bounds__(32 * kRmsWarps)
     rmsnorm_regs_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M,
                         float eps) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -95,6 +98,8 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
 __global__ void __launch_bounds__(32 * kRmsWarps)
     rmsnorm_loop_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M,
                         int64_t H, float eps) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -117,14 +122,13 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
   auto gg = static_cast<const uint4*>(g);
   auto y = static_cast<uint4*>(Y);
   switch (H) {
-    case 256: rmsnorm_regs_kernel<1><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
-    case 512: rmsnorm_regs_kernel<2><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
-    case 1024: rmsnorm_regs_kernel<4><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
-    case 2048: rmsnorm_regs_kernel<8><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
-    case 4096: rmsnorm_regs_kernel<16><<<grid, block, 0, stream>>>(x, gg, y, M, eps); break;
-    default: rmsnorm_loop_kernel<<<grid, block, 0, stream>>>(x, gg, y, M, H, eps); break;
+    case 256: return launch_overlapped(rmsnorm_regs_kernel<1>, grid, block, stream, x, gg, y, M, eps);
+    case 512: return launch_overlapped(rmsnorm_regs_kernel<2>, grid, block, stream, x, gg, y, M, eps);
+    case 1024: return launch_overlapped(rmsnorm_regs_kernel<4>, grid, block, stream, x, gg, y, M, eps);
+    case 2048: return launch_overlapped(rmsnorm_regs_kernel<8>, grid, block, stream, x, gg, y, M, eps);
+    case 4096: return launch_overlapped(rmsnorm_regs_kernel<16>, grid, block, stream, x, gg, y, M, eps);
+    default: return launch_overlapped(rmsnorm_loop_kernel, grid, block, stream, x, gg, y, M, H, eps);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace bi

@@ -73,6 +73,10 @@ class DecodeStack:
             "gu": bd.bi_pins_default(2 * s.inter, s.hidden),
             "d": bd.bi_pins_default(s.hidden, s.inter),
         }
+        # The weights are written once, before serving: let each GEMM start
+        # streaming its weights while the small kernels before it finish.
+        for k in self.pins:
+            self.pins[k] = self.pins[k].replace(flags=self.pins[k].flags | bd.BI_FLAG_PREFETCH_W)
         if pins:
             self.pins.update(pins)
         self._bufs = {}
