@@ -43,6 +43,24 @@ SWEEP_M = [1 << i for i in range(14)]  # 1 .. 8192
 EPS = 1e-5
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of single
+# launches, from ncu captures of `python bench.py --single-m M --launches 2`
+# (summaries in profiles/), valid only for the kernel build they were taken on.
+NCU_TRAFFIC = {
+    "1323c7db72ec0c536245d3dcf7b2715f68f1fdc9d8605be06bdc18ddcef9f6eb": {8192: 1123254528 + 138966528,
+                                                                         1: 117500672 + 2701056},
+}
+
+
+def build_fingerprint():
+    p = os.path.join(ROOT, "invariant_bi_gemm_bf16_gb300", "libbi_gemm.so.stamp")
+    try:
+        with open(p) as f:
+            return f.read().strip()
+    except OSError:
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -463,13 +481,29 @@ def run_ours(args, dist):
     h2d, d2h = holder["b"]
 
     launch_sum = float(per_launch.sum()) / 1e6          # one sweep, seconds
-    achieved = flops / launch_sum / 1e12
-    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(achieved / peaks["bf16_tflops"], 3), "traffic": None,
-            "peak_source": peaks["source"] + " (burst bf16)",
-            "sweep_time_weighted_frac": round(sum_roof / sum_meas, 3),
-            "note": "GEMM kernel over the whole M sweep: sweep FLOPs / summed launch time; "
-                    "per-M bound and fraction (max of FLOP/peak, bytes/HBM) in sweep[]"}
+    sweep_tflops = flops / launch_sum / 1e12
+    traffic = NCU_TRAFFIC.get(build_fingerprint() or "", {})
+    # the dominant launch of the step (largest M, the biggest share of its time)
+    j_big = len(wl.ms) - 1
+    M_big = wl.ms[j_big]
+    f_big, b_big = gemm_work(M_big, wl.N, wl.K)
+    ach_big = f_big / (float(per_launch[0, j_big]) * 1e-6) / 1e12
+    roof = {"bound": "tensor", "achieved": round(ach_big, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(ach_big / peaks["bf16_tflops"], 3), "traffic": traffic.get(M_big),
+            "algorithmic_bytes": int(b_big), "launch": "bi_gemm_bf16 at M=%d (%.0f%% of the step's time)" % (
+                M_big, 100.0 * float(per_launch[0, j_big]) / float(per_launch.sum())),
+            "peak_source": peaks["source"] + " (burst bf16; launches timed back to back)"}
+    # the decode end of the sweep: HBM-bound
+    M_small = wl.ms[0]
+    f_s, b_s = gemm_work(M_small, wl.N, wl.K)
+    ach_s = b_s / (float(per_launch[0, 0]) * 1e-6) / 1e9
+    roof_decode = {"bound": "hbm", "achieved": round(ach_s, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(ach_s / peaks["hbm_gbs"], 3), "traffic": traffic.get(M_small),
+                   "algorithmic_bytes": int(b_s), "launch": "bi_gemm_bf16 at M=%d" % M_small,
+                   "peak_source": peaks["source"] + " (copy bandwidth)"}
+    sweep_roof = {"tflops": round(sweep_tflops, 1), "frac_of_bf16_peak": round(sweep_tflops / peaks["bf16_tflops"], 3),
+                  "time_weighted_roofline_frac": round(sum_roof / sum_meas, 3),
+                  "note": "whole sweep: FLOPs / summed per-launch times; per-M bound and fraction in sweep[]"}
     result = {
         "metric": "batch-invariant GEMM TFLOPS over the down_proj M sweep (M=1..8192)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
@@ -482,6 +516,8 @@ def run_ours(args, dist):
                          "reads what the previous launch left in L2" % (wl.nw, wl.nw * wl.N * wl.K * 2 / 1e6),
                    "parallelism": "replicas x%d (rows sharded, no collective)" % dist.world},
         "roofline": roof,
+        "roofline_decode": roof_decode,
+        "sweep_roofline": sweep_roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": L * args.steps,
@@ -498,6 +534,21 @@ def run_ours(args, dist):
                                   "sample": "oracle down_proj GEMM on %d rows x all 4096 outputs (K=14336), "
                                             "%.1f s" % (rows, secs)}
     return result
+
+
+def run_single_m(args, dist):
+    """Launches the sweep's GEMM (same tensors, pins and weight rotation) at one
+    M, --launches times, for an ncu capture of that launch."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    wl = DownProjSweep(bd, torch.device("cuda", dist.local_rank), seed=dist.rank, sweep=[args.single_m])
+    for i in range(args.launches):
+        wl._launch(args.single_m, wl.X[args.single_m][i % len(wl.X[args.single_m])], wl.W[i % wl.nw], False)
+    torch.cuda.synchronize()
+    st = bd.bi_last_device_status()
+    if st != bd.BI_OK:
+        raise RuntimeError(bd.status_string(st))
 
 
 def run_reference(args, dist):
@@ -539,11 +590,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--single-m", type=int, default=0,
+                    help="profiling helper: only launch the sweep's GEMM at this M --launches times")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     dist = Dist()
     try:
+        if args.single_m:
+            run_single_m(args, dist)
+            return
         if args.impl == "reference":
             res = run_reference(args, dist)
         else:
