@@ -95,7 +95,15 @@ typedef struct CUstream_st* bi_stream_t;
  * that W is not written by any kernel still running in the stream when the
  * call is made (weights are normally written once, long before). */
 #define BI_FLAG_PREFETCH_W 0x200u
-#define BI_FLAG_KNOWN_MASK (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER | BI_FLAG_PREFETCH_W)
+/* Speed only.  Copy W and X two K tiles at a time into ring stages of two K
+ * tiles (through 3-D views of the matrices), so that the tensor-core warp
+ * waits and commits once per eight MMAs instead of four.  Honoured when
+ * K % 64 == 0, tok_tile == 256 and the X copies cover the whole token tile;
+ * otherwise one K tile per copy.  The MMAs consume K tiles one by one in the
+ * same order either way, so the flag never changes a bit of Y. */
+#define BI_FLAG_KTILE_PAIRS 0x400u
+#define BI_FLAG_KNOWN_MASK \
+  (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER | BI_FLAG_PREFETCH_W | BI_FLAG_KTILE_PAIRS)
 
 typedef struct bi_pins {
   int32_t abi_version; /* BI_PINS_ABI_VERSION */
@@ -107,8 +115,13 @@ typedef struct bi_pins {
   int32_t tok_tile;    /* T, tokens per tile = the MMA's N extent: 64, 128 or 256 */
   int32_t mma_ctas;    /* 1: tcgen05.mma.cta_group::1, 128 W rows per MMA;
                           2: tcgen05.mma.cta_group::2 across a CTA pair, 256 W rows
-                          per MMA (each CTA holds 128 W rows and T/2 tokens). */
-  int32_t stages;      /* depth of the W shared-memory ring; 0 = chosen by the
+                          per MMA (each CTA holds 128 W rows and T/2 tokens);
+                          0: chosen per launch for speed.  Both groupings give
+                          every output element the same bits (each is one chain
+                          of k16 steps in the same order), which the GPU tests
+                          check; pin 1 or 2 to fix the grouping regardless. */
+  int32_t stages;      /* depth of the W shared-memory ring, in copies (a copy
+                          holds bi_gemm_plan.kps K tiles); 0 = chosen by the
                           library from the launch.  Speed only. */
   uint32_t flags;      /* BI_FLAG_* */
 } bi_pins;
@@ -144,18 +157,28 @@ bi_status bi_pins_default(int64_t N, int64_t K, bi_pins* out);
 bi_status bi_pins_validate(int64_t N, int64_t K, const bi_pins* pins);
 
 /* A description of the launch the GEMM would make, for inspection and tests.
- * The first group of fields is the reduction tree and depends on (N, K,
- * pins) only; the second group is the schedule and may depend on M. */
+ * Reduction tree (bk, split_k, mma_k, k_tiles, split_begin): a function of
+ * (N, K, pins) only.  MMA layout (tok_tile, mma_ctas, mma_m, mma_n): how many
+ * output elements one MMA computes side by side, and on how many SMs; fixed
+ * by the pins when they fix mma_ctas, chosen per launch when mma_ctas = 0.  It
+ * never changes a bit of Y.  Everything else is the schedule and may depend
+ * on M. */
 typedef struct bi_gemm_plan {
-  /* reduction tree: a function of (N, K, pins) */
-  int32_t bk, split_k, tok_tile, mma_ctas, mma_m, mma_n, mma_k;
-  int64_t k_tiles;
-  int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* K-tile boundaries, split s = [begin[s], begin[s+1]) */
+  int32_t bk, split_k;                     /* tree */
+  int32_t tok_tile, mma_ctas, mma_m, mma_n; /* MMA layout */
+  int32_t mma_k;                           /* tree: 16 K elements per MMA step */
+  int64_t k_tiles;                         /* tree */
+  int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* tree: K-tile boundaries, split s = [begin[s], begin[s+1]) */
   /* schedule: may depend on M */
   int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL or _CLUSTER */
   int32_t w_stages, x_stages;              /* depths of the W and X shared-memory rings */
   int32_t x_box_rows;                      /* token rows per X copy (< tok_tile for small M) */
+  int32_t kps;                             /* K tiles per copy and ring stage (1, or 2 with
+                                              BI_FLAG_KTILE_PAIRS and paired MMAs).  The MMAs
+                                              consume the K tiles one by one, in order, either
+                                              way. */
   int64_t n_tiles, m_tiles;
+  int32_t group_n;                         /* LOCAL tile order: W tiles per group (0 for CLUSTER) */
   int32_t grid_x, grid_y, grid_z, cluster_x, block_threads;
   int64_t smem_bytes;
 } bi_gemm_plan;

@@ -37,6 +37,7 @@ BI_FLAG_SCHEDULE_LOCAL = 0x1
 BI_FLAG_SCHEDULE_CLUSTER = 0x2
 BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
 BI_FLAG_PREFETCH_W = 0x200
+BI_FLAG_KTILE_PAIRS = 0x400
 
 
 class Pins(ctypes.Structure):
@@ -63,18 +64,24 @@ class Plan(ctypes.Structure):
                 ("k_tiles", ctypes.c_int64),
                 ("split_begin", ctypes.c_int64 * (BI_MAX_SPLIT_K + 1)),
                 ("schedule", ctypes.c_int32), ("w_stages", ctypes.c_int32), ("x_stages", ctypes.c_int32),
-                ("x_box_rows", ctypes.c_int32),
-                ("n_tiles", ctypes.c_int64), ("m_tiles", ctypes.c_int64),
+                ("x_box_rows", ctypes.c_int32), ("kps", ctypes.c_int32),
+                ("n_tiles", ctypes.c_int64), ("m_tiles", ctypes.c_int64), ("group_n", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("cluster_x", ctypes.c_int32), ("block_threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64)]
 
-    TREE_FIELDS = ("bk", "split_k", "tok_tile", "mma_ctas", "mma_m", "mma_n", "mma_k", "k_tiles")
+    TREE_FIELDS = ("bk", "split_k", "mma_k", "k_tiles")
+    LAYOUT_FIELDS = ("tok_tile", "mma_ctas", "mma_m", "mma_n")
 
     def tree(self) -> tuple:
         """The reduction-tree fields: a function of (N, K, pins) only."""
         return tuple(getattr(self, f) for f in self.TREE_FIELDS) + \
             tuple(self.split_begin[: self.split_k + 1])
+
+    def layout(self) -> tuple:
+        """The MMA layout: fixed by pins that fix mma_ctas, else chosen per
+        launch; it changes no output bit."""
+        return tuple(getattr(self, f) for f in self.LAYOUT_FIELDS)
 
 
 class BiError(RuntimeError):

@@ -29,20 +29,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // The explicit table: the Llama-3.1 projection shapes of the workloads this
-// library is measured on.  (N, K) -> (S, T, mma_ctas).
+// library is measured on.  (N, K) -> (S, T, mma_ctas); mma_ctas 0 leaves the
+// CTA grouping to each launch (it never changes a bit).
 struct TableEntry {
   int64_t N, K;
   int32_t S, T, ctas;
 };
 const TableEntry kTable[] = {
-    {128, 256, 2, 128, 1},       // tiny invariance shape: exercises the split fold
-    {4096, 14336, 4, 256, 1},    // Llama-3.1-8B down_proj: 32 W tiles x 4 = 128 CTAs at decode
-    {6144, 4096, 3, 256, 1},     // Llama-3.1-8B qkv: 48 x 3 = 144
-    {28672, 4096, 2, 256, 1},    // Llama-3.1-8B gate_up: 224 x 2 = 448 (2.95 waves)
-    {10240, 8192, 3, 256, 1},    // Llama-3.1-70B qkv: 80 x 3 = 240
-    {8192, 8192, 2, 256, 1},     // Llama-3.1-70B o_proj: 64 x 2 = 128
-    {57344, 8192, 1, 256, 1},    // Llama-3.1-70B gate_up: 448 tiles, persistent
-    {8192, 28672, 2, 256, 1},    // Llama-3.1-70B down_proj: 64 x 2 = 128
+    {128, 256, 2, 128, 0},       // tiny invariance shape: exercises the split fold
+    {4096, 14336, 4, 256, 0},    // Llama-3.1-8B down_proj: 32 W tiles x 4 = 128 CTAs at decode
+    {6144, 4096, 3, 256, 0},     // Llama-3.1-8B qkv: 48 x 3 = 144
+    {28672, 4096, 2, 256, 0},    // Llama-3.1-8B gate_up: 224 x 2 = 448 (2.95 waves)
+    {10240, 8192, 3, 256, 0},    // Llama-3.1-70B qkv: 80 x 3 = 240
+    {8192, 8192, 2, 256, 0},     // Llama-3.1-70B o_proj: 64 x 2 = 128
+    {57344, 8192, 1, 256, 0},    // Llama-3.1-70B gate_up: 448 tiles, persistent
+    {8192, 28672, 2, 256, 0},    // Llama-3.1-70B down_proj: 64 x 2 = 128
 };
 
 // Rule for shapes outside the table: the split count that best fills
@@ -79,6 +80,16 @@ struct Resolved {
   int64_t KT;
 };
 
+// K tiles per copy for a launch with token tile T and CTA grouping ctas: 2
+// when the flag asks for it and it is possible (K % 64 == 0, T = 256) and the
+// MMAs are paired, else 1.  (A single CTA at T = 256 has a 48 KB K tile; its
+// rings would hold only two X stages of two tiles, which measured slower.)
+// Launches whose X copies cover fewer rows than the token tile use 1
+// (make_plan).
+int pins_kps(int64_t K, int32_t T, int32_t ctas, uint32_t flags) {
+  return ((flags & BI_FLAG_KTILE_PAIRS) && K % kBK == 0 && T == 256 && ctas == 2) ? 2 : 1;
+}
+
 bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r);
 
 // Which device function pointer encodes tensor maps (driver entry point).
@@ -101,18 +112,36 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A [rows, K] bf16 row-major matrix, box of 64 x box_rows, 128-byte swizzle,
-// zero fill outside the matrix.
-bool encode_kmajor(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+// A [rows, K] bf16 row-major matrix, 128-byte swizzle, zero fill outside the
+// matrix.  view3d false: a 2-D map, box 64 x box_rows (one K tile, kps 1).
+// view3d true (K % 64 == 0 only): the same bytes seen as [K/64][rows][64], box
+// 64 x box_rows x kps, so one copy lands kps K tiles one after another in
+// shared memory, each box_rows x 128 bytes.  Without K % 64 == 0 the 3-D view
+// would read a partial last K tile's tail from the next row instead of zeros.
+bool encode_kmajor(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows,
+                   bool view3d, int kps) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (!view3d) {
+    if (kps != 1) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    if (K % kBK != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(K / kBK)};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kBK * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kps};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -144,9 +173,28 @@ int32_t choose_schedule(const Resolved& r, int64_t tiles, int32_t sm_count) {
   return cluster_rounds * 1.15 < local_rounds ? BI_FLAG_SCHEDULE_CLUSTER : BI_FLAG_SCHEDULE_LOCAL;
 }
 
-bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& r, int32_t sm_count,
+// The CTA grouping when the pins leave it open (mma_ctas = 0).  cta_group::1
+// and ::2 MMAs give every output element the same bits (each element is one
+// chain of k16 steps in the same order on either SM of a pair; tested on GPU),
+// so this is speed only.  A pair halves each SM's share of the token tile's
+// operand bytes, which pays where the tensor pipe is the bound: full token
+// tiles run persistently (LOCAL).  Otherwise -- one short token tile, or few
+// enough tiles that the splits run as clusters -- one CTA per MMA, whose
+// S-CTA clusters fit on the GPU all at once (a pair needs clusters of 2S).
+int32_t choose_ctas(int64_t M, int64_t N, const Resolved& r, int32_t sm_count) {
+  if ((r.flags & BI_FLAG_SCHEDULE_MASK) == BI_FLAG_SCHEDULE_CLUSTER) return 1;
+  if (M <= r.T / 2) return 1;  // a single token tile with a short X box
+  Resolved r2 = r;
+  r2.ctas = 2;
+  const int64_t tiles2 = ceil_div(N, 2 * kTileN) * ceil_div(M, r.T);
+  return choose_schedule(r2, tiles2, sm_count) == BI_FLAG_SCHEDULE_LOCAL ? 2 : 1;
+}
+
+bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int32_t sm_count,
                     bi_gemm_plan* plan) {
   std::memset(plan, 0, sizeof(*plan));
+  Resolved r = pinned;
+  if (r.ctas == 0) r.ctas = choose_ctas(M, N, r, sm_count);
   plan->bk = kBK;
   plan->split_k = r.S;
   plan->tok_tile = r.T;
@@ -165,7 +213,10 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& r, int32_t 
   const int32_t x_rows = r.T / r.ctas;
   plan->x_box_rows = (plan->m_tiles == 1 && M <= x_rows) ? (int32_t)((M + 7) / 8 * 8) : x_rows;
   if (plan->x_box_rows > x_rows) plan->x_box_rows = x_rows;
-  choose_stages(x_rows, plan->x_box_rows, r.w_pin, &plan->w_stages, &plan->x_stages);
+  // a short X box keeps one K tile per copy: each K tile of X must start
+  // x_rows rows after the previous one in shared memory
+  plan->kps = plan->x_box_rows == x_rows ? pins_kps(K, r.T, r.ctas, r.flags) : 1;
+  choose_stages(x_rows, plan->x_box_rows, r.w_pin, plan->kps, &plan->w_stages, &plan->x_stages);
   plan->block_threads = kGemmThreads;
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
   plan->schedule = choose_schedule(r, tiles, sm_count);
@@ -178,12 +229,18 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& r, int32_t 
     plan->cluster_x = r.S * r.ctas;
   } else {
     const int64_t slots = sm_count / r.ctas > 0 ? sm_count / r.ctas : 1;
-    plan->grid_x = (int32_t)((tiles < slots ? tiles : slots) * r.ctas);
+    const int64_t units = tiles < slots ? tiles : slots;
+    plan->grid_x = (int32_t)(units * r.ctas);
     plan->grid_y = 1;
     plan->grid_z = 1;
     plan->cluster_x = r.ctas;
+    // about sqrt(units) W tiles per group: the units in flight then cover as
+    // many W tiles as token tiles
+    int64_t g = 1;
+    while ((g + 1) * (g + 1) <= units) ++g;
+    plan->group_n = (int32_t)(g < plan->n_tiles ? g : plan->n_tiles);
   }
-  plan->smem_bytes = gemm_smem_bytes(r.T, x_rows, plan->w_stages, plan->x_stages, cluster);
+  plan->smem_bytes = gemm_smem_bytes(r.T, x_rows, plan->w_stages, plan->x_stages, plan->kps, cluster);
   if (plan->w_stages < 2 || plan->x_stages < 2) return BI_ERR_ILLEGAL_PINS;
   if (plan->smem_bytes > kMaxDynSmem) return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
@@ -198,13 +255,22 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
   if (p->bk != kBK) return BI_ERR_ILLEGAL_PINS;
   if (p->split_k < 1 || p->split_k > BI_MAX_SPLIT_K || p->split_k > kt) return BI_ERR_ILLEGAL_PINS;
   if (p->tok_tile != 64 && p->tok_tile != 128 && p->tok_tile != 256) return BI_ERR_ILLEGAL_PINS;
-  if (p->mma_ctas != 1 && p->mma_ctas != 2) return BI_ERR_ILLEGAL_PINS;
-  if (p->stages != 0 && (p->stages < 2 || p->stages > max_w_stages(p->tok_tile / p->mma_ctas, 2)))
-    return BI_ERR_ILLEGAL_PINS;
+  if (p->mma_ctas < 0 || p->mma_ctas > 2) return BI_ERR_ILLEGAL_PINS;
+  // a W depth must leave two X stages at the largest copies of every CTA
+  // grouping the pins allow
+  if (p->stages != 0) {
+    if (p->stages < 2) return BI_ERR_ILLEGAL_PINS;
+    for (int32_t ctas = 1; ctas <= 2; ++ctas) {
+      if (p->mma_ctas != 0 && p->mma_ctas != ctas) continue;
+      const int kps = pins_kps(K, p->tok_tile, ctas, p->flags);
+      if (p->stages > max_w_stages(p->tok_tile / ctas, 2, kps)) return BI_ERR_ILLEGAL_PINS;
+    }
+  }
   if (p->flags & ~BI_FLAG_KNOWN_MASK) return BI_ERR_ILLEGAL_PINS;
   const uint32_t sched = p->flags & BI_FLAG_SCHEDULE_MASK;
   if (sched == BI_FLAG_SCHEDULE_MASK) return BI_ERR_ILLEGAL_PINS;
-  if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * p->mma_ctas > 16) return BI_ERR_ILLEGAL_PINS;
+  if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * (p->mma_ctas == 2 ? 2 : 1) > 16)
+    return BI_ERR_ILLEGAL_PINS;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k > 8) return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
 }
@@ -213,7 +279,7 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
   if (!out) return BI_ERR_INVALID_ARG;
   bi_status st = check_nk(N, K);
   if (st != BI_OK) return st;
-  int32_t S = 0, T = 256, ctas = 1;
+  int32_t S = 0, T = 256, ctas = 0;
   for (const TableEntry& e : kTable) {
     if (e.N == N && e.K == K) {
       S = e.S;
@@ -231,7 +297,7 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
   out->tok_tile = T;
   out->mma_ctas = ctas;
   out->stages = 0;
-  out->flags = BI_FLAG_SCHEDULE_AUTO;
+  out->flags = BI_FLAG_SCHEDULE_AUTO | BI_FLAG_KTILE_PAIRS;
   return BI_OK;
 }
 
@@ -279,8 +345,9 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   if (st != BI_OK) return st;
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
-  if (!encode_kmajor(&L.tmW, W, N, K, kTileN)) return BI_ERR_CUDA;
-  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows)) return BI_ERR_CUDA;
+  const bool map3d = plan.kps > 1;
+  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, plan.kps)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, plan.kps)) return BI_ERR_CUDA;
   L.Y = Y;
   L.M = M;
   L.N = N;
@@ -293,14 +360,16 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.w_stages = plan.w_stages;
   L.x_stages = plan.x_stages;
   L.x_box_rows = plan.x_box_rows;
+  L.kps = plan.kps;
+  L.group_n = plan.group_n > 0 ? plan.group_n : 1;
   L.cluster = plan.schedule == BI_FLAG_SCHEDULE_CLUSTER;
-  L.pair = r.ctas == 2;
+  L.pair = plan.mma_ctas == 2;
   L.grid_x = plan.grid_x;
   L.grid_y = plan.grid_y;
   L.grid_z = plan.grid_z;
   L.smem = plan.smem_bytes;
   L.flags = r.flags;
-  if (plan.x_box_rows < r.T / r.ctas) L.flags |= kFlagZeroX;
+  if (plan.x_box_rows < r.T / plan.mma_ctas) L.flags |= kFlagZeroX;
   if (plan.m_tiles == 1) L.flags |= kFlagStreamW;
   L.stream = stream;
   return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;

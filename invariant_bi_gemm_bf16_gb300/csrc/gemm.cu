@@ -60,6 +60,7 @@ struct GemmParams {
   int64_t M, N;
   int32_t n_tiles, m_tiles, k_tiles, S;
   int32_t w_stages, x_stages, x_box_rows;
+  int32_t group_n;  // LOCAL tile order: groups of group_n W tiles (speed only)
   uint32_t flags;  // BI_FLAG_DEBUG_STALL_PRODUCER | kFlagStreamW | kFlagZeroX
 };
 
@@ -118,12 +119,39 @@ __device__ __forceinline__ int64_t split_begin(int32_t s, int32_t S, int32_t KT)
   return ((int64_t)s * KT) / S;
 }
 
-template <int T, bool CLUSTER, bool PAIR>
+// LOCAL tile order.  Tiles come in groups of G consecutive W tiles (the last
+// group may be narrower); within a group the token tiles run slowest.  Units
+// working on consecutive tiles then share G W tiles and about units / G token
+// tiles, a working set that stays in L2 even when W does not.  Each tile's
+// result is independent of when it is computed.
+__device__ __forceinline__ void tile_coords(int64_t t, int32_t n_tiles, int32_t m_tiles, int32_t G,
+                                            int32_t* n_tile, int32_t* m_tile) {
+  const int64_t full = (int64_t)(n_tiles / G) * G * m_tiles;  // tiles in full-width groups
+  if (t < full) {
+    const int64_t per = (int64_t)G * m_tiles;
+    const int64_t g = t / per, r = t % per;
+    *n_tile = (int32_t)(g * G + r % G);
+    *m_tile = (int32_t)(r / G);
+  } else {
+    const int32_t w = n_tiles % G;  // width of the last group
+    const int64_t r = t - full;
+    *n_tile = (int32_t)((n_tiles / G) * G + r % w);
+    *m_tile = (int32_t)(r / w);
+  }
+}
+
+// KP: K tiles per copy and per ring stage (1, or 2 through 3-D tensor maps).
+// The MMAs consume the K tiles of a stage one after the other, so KP never
+// changes the reduction; it halves the waits and commits per MMA of the
+// issuing thread, which at T = 256 runs close to the tensor pipe's rate.
+template <int T, bool CLUSTER, bool PAIR, int KP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     bi_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
-  constexpr int kXRows = PAIR ? T / 2 : T;          // token rows in this CTA's X stage
-  constexpr int kXStage = kXRows * kBK * 2;
+  constexpr int kXRows = PAIR ? T / 2 : T;          // token rows in this CTA's X tiles
+  constexpr int kXTile = kXRows * kBK * 2;          // one K tile of X
+  constexpr int kXStage = KP * kXTile;
+  constexpr int kWStage = KP * kWStageBytes;
   constexpr int kMmaM = PAIR ? 2 * kTileN : kTileN;  // W rows per tile
   constexpr uint32_t kTmemCols = CLUSTER ? (uint32_t)T : 2u * (uint32_t)T;
   constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quadrant
@@ -134,7 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int ws = p.w_stages;
   const int xs = p.x_stages;
-  const int64_t w_ring = (int64_t)ws * kWStageBytes;
+  const int64_t w_ring = (int64_t)ws * kWStage;
   const int64_t ring_bytes = w_ring + (int64_t)xs * kXStage;
   const int64_t part_bytes = CLUSTER ? (int64_t)T * kTileN * 4 : 0;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (ring_bytes > part_bytes ? ring_bytes : part_bytes));
@@ -142,7 +170,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t w_base = smem_base;                       // W stage i at w_base + i * 16 KB
+  const uint32_t w_base = smem_base;                       // W stage i at w_base + i * kWStage
   const uint32_t x_base = smem_base + (uint32_t)w_ring;    // X stage i at x_base + i * kXStage
 
   const uint32_t crank = (PAIR || CLUSTER) ? cluster_ctarank() : 0u;
@@ -229,9 +257,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint64_t* full_bar = is_w ? ctl->w_full : ctl->x_full;
       uint64_t* empty_bar = is_w ? ctl->w_empty : ctl->x_empty;
       const uint32_t ring = is_w ? w_base : x_base;
-      const uint32_t stage_sz = is_w ? (uint32_t)kWStageBytes : (uint32_t)kXStage;
-      // transaction bytes per stage, both CTAs of a pair counted on the even CTA
-      const uint32_t tx = (is_w ? (uint32_t)kWStageBytes : (uint32_t)p.x_box_rows * kBK * 2) *
+      const uint32_t stage_sz = is_w ? (uint32_t)kWStage : (uint32_t)kXStage;
+      // transaction bytes per stage (whole boxes, also where one lies past K),
+      // both CTAs of a pair counted on the even CTA
+      const uint32_t tx = (uint32_t)KP * (is_w ? (uint32_t)kWStageBytes : (uint32_t)p.x_box_rows * kBK * 2) *
                           (PAIR ? 2u : 1u);
       const CUtensorMap* map = is_w ? &tmW : &tmX;
       const bool hinted = stream_w;
@@ -241,13 +270,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
-        const int32_t n_tile = CLUSTER ? (int32_t)blockIdx.y : (int32_t)(t % p.n_tiles);
-        const int32_t m_tile = CLUSTER ? (int32_t)blockIdx.z : (int32_t)(t / p.n_tiles);
+        int32_t n_tile, m_tile;
+        if (CLUSTER) {
+          n_tile = (int32_t)blockIdx.y;
+          m_tile = (int32_t)blockIdx.z;
+        } else {
+          tile_coords(t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
+        }
         const int32_t row = is_w ? n_tile * kMmaM + (int32_t)peer * kTileN
                                  : m_tile * T + (int32_t)peer * kXRows;
         for (int32_t s = s_first; ok && s < s_end; ++s) {
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
-          for (int64_t kt = k0; kt < k1; ++kt) {
+          // the last copy of a split may reach one K tile past it (loaded, unused)
+          for (int64_t kt = k0; kt < k1; kt += KP) {
             if (!wait_or_abort(smem_u32(&empty_bar[stage]), phase ^ 1u, abort)) {
               ok = false;
               break;
@@ -255,20 +290,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!(stall && issued == 0)) {
               const uint32_t full = smem_u32(&full_bar[stage]);
               const uint32_t dst = ring + (uint32_t)stage * stage_sz;
-              const int32_t kx = (int32_t)(kt * kBK);
+              const int32_t kx = (int32_t)(kt * kBK);  // 2-D maps: element column
+              const int32_t kz = (int32_t)kt;          // 3-D maps: K tile index
               if constexpr (PAIR) {
                 const uint32_t bar = leader ? full : mapa_shared(full, leader_rank);
                 if (leader) mbar_arrive_expect_tx(full, tx);
-                if (hinted)
-                  tma_load_2d_pair_hint(dst, map, bar, kx, row, policy);
-                else
-                  tma_load_2d_pair(dst, map, bar, kx, row);
+                if constexpr (KP == 1) {
+                  if (hinted)
+                    tma_load_2d_pair_hint(dst, map, bar, kx, row, policy);
+                  else
+                    tma_load_2d_pair(dst, map, bar, kx, row);
+                } else {
+                  if (hinted)
+                    tma_load_3d_pair_hint(dst, map, bar, 0, row, kz, policy);
+                  else
+                    tma_load_3d_pair(dst, map, bar, 0, row, kz);
+                }
               } else {
                 mbar_arrive_expect_tx(full, tx);
-                if (hinted)
-                  tma_load_2d_hint(dst, map, full, kx, row, policy);
-                else
-                  tma_load_2d(dst, map, full, kx, row);
+                if constexpr (KP == 1) {
+                  if (hinted)
+                    tma_load_2d_hint(dst, map, full, kx, row, policy);
+                  else
+                    tma_load_2d(dst, map, full, kx, row);
+                } else {
+                  if (hinted)
+                    tma_load_3d_hint(dst, map, full, 0, row, kz, policy);
+                  else
+                    tma_load_3d(dst, map, full, 0, row, kz);
+                }
               }
             }
             ++issued;
@@ -310,23 +360,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * (uint32_t)T;
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
-          for (int64_t kt = k0; kt < k1; ++kt) {
+          for (int64_t kt = k0; kt < k1; kt += KP) {
             if (!wait_or_abort(smem_u32(&ctl->w_full[wi]), wph, abort) ||
                 !wait_or_abort(smem_u32(&ctl->x_full[xi]), xph, abort)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t a_desc = make_sdesc_sw128(w_base + (uint32_t)wi * kWStageBytes);
+            const uint64_t a_desc = make_sdesc_sw128(w_base + (uint32_t)wi * kWStage);
             const uint64_t b_desc = make_sdesc_sw128(x_base + (uint32_t)xi * kXStage);
 #pragma unroll
-            for (int j = 0; j < kBK / kMmaK; ++j) {
-              // +32 bytes per 16 K elements, in the descriptor's 16-byte units
-              const uint32_t acc = (kt > k0 || j > 0) ? 1u : 0u;
-              if constexpr (PAIR)
-                mma_bf16_pair(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc, acc);
-              else
-                mma_bf16(d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc, acc);
+            for (int sub = 0; sub < KP; ++sub) {
+              // sub-tile sub holds K tile kt + sub (absent past the split's end)
+              if (sub > 0 && kt + sub >= k1) break;
+#pragma unroll
+              for (int j = 0; j < kBK / kMmaK; ++j) {
+                // +32 bytes per 16 K elements, in the descriptor's 16-byte units
+                const uint64_t da = (uint64_t)(sub * (kWStageBytes >> 4) + 2 * j);
+                const uint64_t db = (uint64_t)(sub * (kXTile >> 4) + 2 * j);
+                const uint32_t acc = (kt > k0 || sub > 0 || j > 0) ? 1u : 0u;
+                if constexpr (PAIR)
+                  mma_bf16_pair(d_tmem, a_desc + da, b_desc + db, idesc, acc);
+                else
+                  mma_bf16(d_tmem, a_desc + da, b_desc + db, idesc, acc);
+              }
             }
             if constexpr (PAIR) {
               mma_commit_pair_mc(smem_u32(&ctl->w_empty[wi]), pair_mask);
@@ -370,8 +427,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     if constexpr (!CLUSTER) {
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
-        const int32_t n_tile = (int32_t)(t % p.n_tiles);
-        const int32_t m_tile = (int32_t)(t / p.n_tiles);
+        int32_t n_tile, m_tile;
+        tile_coords(t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
         float R[kHalf];
         for (int32_t s = 0; s < S; ++s) {
           const uint32_t buf = acc_iter & 1u;
@@ -499,45 +556,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-int max_w_stages(int x_rows, int x_stages) {
-  const int left = kRingBytes - x_stages * x_stage_bytes(x_rows);
-  int w = left / kWStageBytes;
+int max_w_stages(int x_rows, int x_stages, int kps) {
+  const int left = kRingBytes - x_stages * kps * x_stage_bytes(x_rows);
+  int w = left / (kps * kWStageBytes);
   return w > kMaxStages ? kMaxStages : w;
 }
 
-void choose_stages(int x_rows, int x_box_rows, int w_pin, int* w_stages, int* x_stages) {
-  const int xb = x_stage_bytes(x_rows);
+void choose_stages(int x_rows, int x_box_rows, int w_pin, int kps, int* w_stages, int* x_stages) {
+  const int xb = kps * x_stage_bytes(x_rows);
+  const int wb = kps * kWStageBytes;
   int xs, w;
   if (x_box_rows <= 64) {
     // Decode: X is a few rows from L2, W streams from HBM -- put the shared
     // memory into W bytes in flight.
     xs = 3;
-    w = max_w_stages(x_rows, xs);
+    w = max_w_stages(x_rows, xs, kps);
   } else {
     // Both operands matter: as many balanced stages as fit, then extra W.
-    int n = kRingBytes / (kWStageBytes + xb);
+    int n = kRingBytes / (wb + xb);
     if (n > kMaxStages) n = kMaxStages;
     xs = n;
-    w = max_w_stages(x_rows, xs);
+    w = max_w_stages(x_rows, xs, kps);
   }
   if (w_pin > 0) {
     w = w_pin;
-    int xfit = (kRingBytes - w * kWStageBytes) / xb;
+    int xfit = (kRingBytes - w * wb) / xb;
     if (xs > xfit) xs = xfit;
   }
   *w_stages = w;
   *x_stages = xs;
 }
 
-int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, bool cluster) {
-  int64_t ring = (int64_t)w_stages * kWStageBytes + (int64_t)x_stages * x_stage_bytes(x_rows);
+int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, int kps, bool cluster) {
+  int64_t ring = (int64_t)kps * ((int64_t)w_stages * kWStageBytes + (int64_t)x_stages * x_stage_bytes(x_rows));
   int64_t part = cluster ? (int64_t)T * kTileN * 4 : 0;
   return 1024 + (ring > part ? ring : part) + kCtlBytes;
 }
 
-template <int T, bool CLUSTER, bool PAIR>
+template <int T, bool CLUSTER, bool PAIR, int KP>
 static cudaError_t launch_t(const GemmLaunch& L) {
-  auto kern = bi_gemm_kernel<T, CLUSTER, PAIR>;
+  auto kern = bi_gemm_kernel<T, CLUSTER, PAIR, KP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   if (e != cudaSuccess) return e;
   const int cluster = CLUSTER ? L.S * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
@@ -556,6 +614,7 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   prm.w_stages = L.w_stages;
   prm.x_stages = L.x_stages;
   prm.x_box_rows = L.x_box_rows;
+  prm.group_n = L.group_n;
   prm.flags = L.flags;
 
   cudaLaunchConfig_t cfg = {};
@@ -584,11 +643,15 @@ template <bool PAIR>
 static cudaError_t launch_p(const GemmLaunch& L) {
   switch (L.T) {
     case 64:
-      return L.cluster ? launch_t<64, true, PAIR>(L) : launch_t<64, false, PAIR>(L);
+      if (L.kps != 1) return cudaErrorInvalidValue;
+      return L.cluster ? launch_t<64, true, PAIR, 1>(L) : launch_t<64, false, PAIR, 1>(L);
     case 128:
-      return L.cluster ? launch_t<128, true, PAIR>(L) : launch_t<128, false, PAIR>(L);
+      if (L.kps != 1) return cudaErrorInvalidValue;
+      return L.cluster ? launch_t<128, true, PAIR, 1>(L) : launch_t<128, false, PAIR, 1>(L);
     case 256:
-      return L.cluster ? launch_t<256, true, PAIR>(L) : launch_t<256, false, PAIR>(L);
+      if (L.kps == 2)
+        return L.cluster ? launch_t<256, true, PAIR, 2>(L) : launch_t<256, false, PAIR, 2>(L);
+      return L.cluster ? launch_t<256, true, PAIR, 1>(L) : launch_t<256, false, PAIR, 1>(L);
     default:
       return cudaErrorInvalidValue;
   }

@@ -32,21 +32,24 @@ constexpr int x_stage_bytes(int x_rows) { return x_rows * kBK * 2; }
 constexpr int kCtlBytes = 1024;
 // Bytes available to the two rings (the rest is alignment slack and control).
 constexpr int kRingBytes = kMaxDynSmem - 1024 - kCtlBytes;
-// Deepest W ring that still leaves `x_stages` X stages of `x_rows` rows.
-int max_w_stages(int x_rows, int x_stages);
+// Deepest W ring that still leaves `x_stages` X stages of `x_rows` rows, with
+// stages of `kps` K tiles.
+int max_w_stages(int x_rows, int x_stages, int kps);
 // Ring depths for a launch: deep W and shallow X when the X box is small
 // (decode), balanced otherwise.  `w_pin` (the pins' stages field) overrides the
 // W depth when non-zero.  Speed only.
-void choose_stages(int x_rows, int x_box_rows, int w_pin, int* w_stages, int* x_stages);
+void choose_stages(int x_rows, int x_box_rows, int w_pin, int kps, int* w_stages, int* x_stages);
 // Dynamic shared memory of one GEMM CTA (includes 1 KB of alignment slack).
-int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, bool cluster);
+int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, int kps, bool cluster);
 
 struct GemmLaunch {
-  CUtensorMap tmW;   // W [N,K], box 64 x 128, 128-byte swizzle
-  CUtensorMap tmX;   // X [M,K], box 64 x x_box_rows, 128-byte swizzle, zero fill past M / K
+  CUtensorMap tmW;   // W [N,K], box 64 x 128 (x kps), 128-byte swizzle
+  CUtensorMap tmX;   // X [M,K], box 64 x x_box_rows (x kps), 128-byte swizzle, zero fill past M / K
   void* Y;
   int64_t M, N, K;
   int32_t n_tiles, m_tiles, k_tiles, S, T, w_stages, x_stages, x_box_rows;
+  int32_t kps;       // K tiles per copy: 1 (2-D maps) or 2 (3-D maps, T = 256 only)
+  int32_t group_n;   // LOCAL tile order: W tiles per group (1 .. n_tiles)
   bool cluster;      // one chain per CTA (pair), folded through DSMEM
   bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;

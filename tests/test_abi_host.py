@@ -61,7 +61,7 @@ def test_default_pins_are_legal(bd, N, K):
     p = bd.bi_pins_default(N, K)
     assert p.abi_version == 1 and p.bk == 64
     assert 1 <= p.split_k <= min(16, -(-K // 64))
-    assert p.tok_tile in (64, 128, 256) and p.mma_ctas in (1, 2)
+    assert p.tok_tile in (64, 128, 256) and p.mma_ctas in (0, 1, 2)
     assert bd.bi_pins_validate(N, K, p) == bd.BI_OK
 
 
@@ -72,7 +72,7 @@ def test_pins_validation_refuses(bd):
            good.replace(split_k=17), good.replace(tok_tile=96), good.replace(tok_tile=512),
            good.replace(stages=1), good.replace(stages=99), good.replace(flags=0x8000),
            good.replace(flags=0x3), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER),
-           good.replace(mma_ctas=0), good.replace(mma_ctas=4)]
+           good.replace(mma_ctas=-1), good.replace(mma_ctas=4)]
     for p in bad:
         assert bd.bi_pins_validate(N, K, p) == bd.BI_ERR_ILLEGAL_PINS, p
     # more splits than K tiles
@@ -139,6 +139,31 @@ def test_reduction_tree_never_depends_on_m(bd, N, K):
             assert bd.bi_gemm_plan_describe(M, N, K, pins.replace(flags=flags)).tree() == ref
 
 
+@pytest.mark.parametrize("N,K", TABLE_SHAPES)
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_pinned_mma_layout_never_depends_on_m(bd, N, K, ctas):
+    """With mma_ctas pinned, the MMA layout is fixed too (only the schedule moves)."""
+    pins = bd.bi_pins_default(N, K).replace(mma_ctas=ctas)
+    layouts = {bd.bi_gemm_plan_describe(M, N, K, pins, sm).layout() for M in ALL_M for sm in (152, 132)}
+    assert len(layouts) == 1
+    (T, c, mm, mn), = layouts
+    assert c == ctas and mm == 128 * ctas and mn == T == pins.tok_tile
+
+
+def test_open_grouping_follows_m(bd):
+    """mma_ctas = 0 (the default): one CTA per MMA while the splits run as
+    clusters or the token tile is short; CTA pairs with two-tile copies for
+    persistent full-tile work."""
+    assert bd.bi_pins_default(4096, 14336).mma_ctas == 0
+    small = bd.bi_gemm_plan_describe(1, 4096, 14336)
+    mid = bd.bi_gemm_plan_describe(512, 4096, 14336)
+    big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
+    assert (small.mma_ctas, small.kps, small.schedule) == (1, 1, bd.BI_FLAG_SCHEDULE_CLUSTER)
+    assert (mid.mma_ctas, mid.schedule) == (1, bd.BI_FLAG_SCHEDULE_CLUSTER)
+    assert (big.mma_ctas, big.kps, big.schedule, big.mma_m) == (2, 2, bd.BI_FLAG_SCHEDULE_LOCAL, 256)
+    assert small.tree() == mid.tree() == big.tree()
+
+
 def test_split_boundaries_partition_k(bd):
     for N, K in TABLE_SHAPES:
         for S in range(1, 17):
@@ -161,10 +186,31 @@ def test_plan_schedules(bd):
     assert small.schedule == bd.BI_FLAG_SCHEDULE_CLUSTER and small.cluster_x == small.split_k == 4
     assert small.grid_x * small.grid_y * small.grid_z == 32 * 4
     assert small.x_box_rows == 8 and small.w_stages > small.x_stages
-    big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
+    one = bd.bi_pins_default(4096, 14336).replace(mma_ctas=1)
+    big = bd.bi_gemm_plan_describe(8192, 4096, 14336, one)
     assert big.schedule == bd.BI_FLAG_SCHEDULE_LOCAL and big.grid_x == 152 and big.cluster_x == 1
-    assert big.x_box_rows == 256
-    pair = bd.bi_gemm_plan_describe(8192, 4096, 14336, bd.bi_pins_default(4096, 14336).replace(mma_ctas=2))
+    assert big.x_box_rows == 256 and big.kps == 1
+    pair = bd.bi_gemm_plan_describe(8192, 4096, 14336, one.replace(mma_ctas=2))
     assert pair.mma_m == 256 and pair.cluster_x == 2 and pair.grid_x == 152 and pair.x_box_rows == 128
+    assert pair.kps == 2
     for plan in (small, big, pair):
         assert plan.smem_bytes <= 232448 and plan.block_threads == 32 * 19
+
+
+def test_plan_ktile_pairs(bd):
+    """Two K tiles per copy only with the flag, K % 64 == 0, T = 256 and full X boxes."""
+    p = bd.bi_pins_default(4096, 14336).replace(mma_ctas=2, flags=bd.BI_FLAG_SCHEDULE_AUTO)
+    pk = p.replace(flags=p.flags | bd.BI_FLAG_KTILE_PAIRS)
+    big = bd.bi_gemm_plan_describe(8192, 4096, 14336, pk)
+    assert big.kps == 2 and big.smem_bytes <= 232448
+    assert bd.bi_gemm_plan_describe(8192, 4096, 14336, p).kps == 1
+    assert big.tree() == bd.bi_gemm_plan_describe(8192, 4096, 14336, p).tree()
+    assert bd.bi_gemm_plan_describe(8192, 4096, 14336, pk.replace(mma_ctas=1)).kps == 1  # one CTA
+    assert bd.bi_gemm_plan_describe(1, 4096, 14336, pk).kps == 1          # short X box
+    assert bd.bi_gemm_plan_describe(8192, 4096, 14336, pk.replace(tok_tile=128)).kps == 1
+    q = bd.bi_pins_default(256, 200).replace(mma_ctas=2)
+    assert bd.bi_gemm_plan_describe(512, 256, 200, q.replace(flags=q.flags | bd.BI_FLAG_KTILE_PAIRS)).kps == 1
+    # a W depth legal with one-tile stages may be too deep for two-tile stages
+    deep = p.replace(stages=6)
+    assert bd.bi_pins_validate(4096, 14336, deep) == bd.BI_OK
+    assert bd.bi_pins_validate(4096, 14336, deep.replace(flags=bd.BI_FLAG_KTILE_PAIRS)) == bd.BI_ERR_ILLEGAL_PINS

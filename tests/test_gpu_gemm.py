@@ -72,6 +72,28 @@ def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T, ctas):
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 256, 1472), (513, 384, 640), (256, 200, 704), (1, 256, 1472)])
+@pytest.mark.parametrize("S", [1, 2, 3])
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_ktile_pairs_change_no_bit(lib, oracle, M, N, K, S, ctas):
+    """Copies of two K tiles (3-D tensor maps) against one-tile copies, with
+    odd K-tile counts per split (the last copy of a split reaches past it) and a
+    short X box at M=1 (which keeps one tile per copy)."""
+    X = inputs.normal((M, K), seed=11, stream=0)
+    W = inputs.normal((N, K), std=0.02, seed=11, stream=1)
+    yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
+    outs = []
+    for extra in (0, lib.BI_FLAG_KTILE_PAIRS):
+        for sched in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
+            pins = pins_for(lib, N, K, split_k=S, tok_tile=256, mma_ctas=ctas, flags=sched | extra)
+            plan = lib.bi_gemm_plan_describe(M, N, K, pins)
+            assert plan.kps == (2 if extra and ctas == 2 and plan.x_box_rows == 128 else 1)
+            got = run(lib, X, W, pins)
+            check_gemm_parity(got, yf, K, "M=%d N=%d K=%d S=%d ctas=%d flags=%d" % (M, N, K, S, ctas, sched | extra))
+            outs.append(got)
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
 @pytest.mark.parametrize("S,T", [(1, 128), (3, 64), (2, 256)])
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_integer_inputs_bit_exact(lib, oracle, S, T, ctas):
