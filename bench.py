@@ -47,8 +47,8 @@ EPS = 1e-5
 # launches, from ncu captures of `python bench.py --single-m M --launches 2`
 # (summaries in profiles/), valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "1323c7db72ec0c536245d3dcf7b2715f68f1fdc9d8605be06bdc18ddcef9f6eb": {8192: 1123254528 + 138966528,
-                                                                         1: 117500672 + 2701056},
+    "8ed1714b7cc4291dc9a4d03caabb397204b51b5aeb2da000b9f160b2c8544702": {8192: 988222208 + 108336896,
+                                                                         1: 117499648 + 2437632},
 }
 
 
