@@ -71,15 +71,22 @@ typedef struct CUstream_st* bi_stream_t;
 #define BI_MAX_SPLIT_K 16
 
 /* Schedule flags: speed only.  They choose how the S split chains of a tile
- * are placed on SMs and never change any output bit.
+ * are placed on SMs and never change any output bit: the partials are always
+ * added in ascending split order, ((P0 + P1) + P2) + ...
  *   AUTO     the library chooses from M (allowed: it changes no bit).
- *   LOCAL    one persistent CTA per tile computes its S chains one after the
- *            other into two TMEM accumulators and folds them in registers.
- *   CLUSTER  a cluster of S CTAs computes one chain each and folds the S
- *            partials through distributed shared memory (S <= 8 only). */
+ *   LOCAL    one persistent CTA (or pair) per tile computes its S chains one
+ *            after the other into two TMEM accumulators and folds them in
+ *            registers.
+ *   CLUSTER  a cluster of S CTAs (or pairs) computes one chain each and folds
+ *            the S partials through distributed shared memory (S <= 8).
+ *   CHAIN    a cluster of ceil(S/2) CTAs (or pairs) per tile; each computes
+ *            two consecutive chains (one for the first when S is odd).  Each
+ *            adds its chains, in order, to the running sum the previous one
+ *            left in shared memory (S >= 3). */
 #define BI_FLAG_SCHEDULE_AUTO 0x0u
 #define BI_FLAG_SCHEDULE_LOCAL 0x1u
 #define BI_FLAG_SCHEDULE_CLUSTER 0x2u
+#define BI_FLAG_SCHEDULE_CHAIN 0x3u
 #define BI_FLAG_SCHEDULE_MASK 0x3u
 /* Diagnostic only: the load producer withholds its first load so that the
  * tensor-core warp's bounded wait runs out.  The kernel then abandons the call
@@ -170,7 +177,8 @@ typedef struct bi_gemm_plan {
   int64_t k_tiles;                         /* tree */
   int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* tree: K-tile boundaries, split s = [begin[s], begin[s+1]) */
   /* schedule: may depend on M */
-  int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL or _CLUSTER */
+  int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL, _CLUSTER or _CHAIN */
+  int32_t units;                           /* cluster schedules: CTAs (or pairs) per tile */
   int32_t w_stages, x_stages;              /* depths of the W and X shared-memory rings */
   int32_t x_box_rows;                      /* token rows per X copy (< tok_tile for small M) */
   int32_t kps;                             /* K tiles per copy and ring stage (1, or 2 with

@@ -35,6 +35,7 @@ BI_MAX_SPLIT_K = 16
 BI_FLAG_SCHEDULE_AUTO = 0x0
 BI_FLAG_SCHEDULE_LOCAL = 0x1
 BI_FLAG_SCHEDULE_CLUSTER = 0x2
+BI_FLAG_SCHEDULE_CHAIN = 0x3
 BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
 BI_FLAG_PREFETCH_W = 0x200
 BI_FLAG_KTILE_PAIRS = 0x400
@@ -63,7 +64,8 @@ class Plan(ctypes.Structure):
                 ("mma_k", ctypes.c_int32),
                 ("k_tiles", ctypes.c_int64),
                 ("split_begin", ctypes.c_int64 * (BI_MAX_SPLIT_K + 1)),
-                ("schedule", ctypes.c_int32), ("w_stages", ctypes.c_int32), ("x_stages", ctypes.c_int32),
+                ("schedule", ctypes.c_int32), ("units", ctypes.c_int32),
+                ("w_stages", ctypes.c_int32), ("x_stages", ctypes.c_int32),
                 ("x_box_rows", ctypes.c_int32), ("kps", ctypes.c_int32),
                 ("n_tiles", ctypes.c_int64), ("m_tiles", ctypes.c_int64), ("group_n", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),

@@ -157,44 +157,86 @@ int sm_count_current() {
   return n;
 }
 
-// Schedule choice from M (speed only).  Rounds of chain work per unit (a CTA,
-// or a CTA pair when mma_ctas = 2): LOCAL runs ceil(tiles / units) tiles of S
-// chains each; CLUSTER runs the tiles * S chains as independent units.
-// CLUSTER is charged 15% for its un-overlapped epilogue and fold.
-int32_t choose_schedule(const Resolved& r, int64_t tiles, int32_t sm_count) {
-  const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
-  if (r.S == 1) return BI_FLAG_SCHEDULE_LOCAL;
-  if (forced == BI_FLAG_SCHEDULE_LOCAL) return BI_FLAG_SCHEDULE_LOCAL;
-  if (forced == BI_FLAG_SCHEDULE_CLUSTER) return BI_FLAG_SCHEDULE_CLUSTER;
-  if (r.S * r.ctas > 8) return BI_FLAG_SCHEDULE_LOCAL;  // portable cluster sizes only
-  const int64_t slots = sm_count / r.ctas;
-  const double local_rounds = (double)ceil_div(tiles, slots) * r.S;
-  const double cluster_rounds = (double)ceil_div(tiles * r.S, slots);
-  return cluster_rounds * 1.15 < local_rounds ? BI_FLAG_SCHEDULE_CLUSTER : BI_FLAG_SCHEDULE_LOCAL;
+// Clusters of `size` CTAs that can be resident at once, at one CTA per SM.
+// Measured on GB300 (152 SMs, about 231 KB of shared memory per CTA): 76 of
+// 2, 36 of 4, 23 of 6, 15 of 8 -- a cluster must fit in one GPC.  Elsewhere
+// an estimate.  Speed only.
+int64_t max_clusters(int32_t size, int32_t sm_count) {
+  if (size <= 1) return sm_count;
+  if (sm_count == kDefaultSmCount) {
+    switch (size) {
+      case 2: return 76;
+      case 4: return 36;
+      case 6: return 23;
+      case 8: return 15;
+      default: break;
+    }
+  }
+  const double est = (double)sm_count / size * (1.0 - size / 40.0);
+  return est < 1.0 ? 1 : (int64_t)est;
 }
 
-// The CTA grouping when the pins leave it open (mma_ctas = 0).  cta_group::1
-// and ::2 MMAs give every output element the same bits (each element is one
-// chain of k16 steps in the same order on either SM of a pair; tested on GPU),
-// so this is speed only.  A pair halves each SM's share of the token tile's
-// operand bytes, which pays where the tensor pipe is the bound: full token
-// tiles run persistently (LOCAL).  Otherwise -- one short token tile, or few
-// enough tiles that the splits run as clusters -- one CTA per MMA, whose
-// S-CTA clusters fit on the GPU all at once (a pair needs clusters of 2S).
-int32_t choose_ctas(int64_t M, int64_t N, const Resolved& r, int32_t sm_count) {
-  if ((r.flags & BI_FLAG_SCHEDULE_MASK) == BI_FLAG_SCHEDULE_CLUSTER) return 1;
-  if (M <= r.T / 2) return 1;  // a single token tile with a short X box
-  Resolved r2 = r;
-  r2.ctas = 2;
-  const int64_t tiles2 = ceil_div(N, 2 * kTileN) * ceil_div(M, r.T);
-  return choose_schedule(r2, tiles2, sm_count) == BI_FLAG_SCHEDULE_LOCAL ? 2 : 1;
+struct LaunchChoice {
+  int32_t ctas, schedule, units;
+  double cost;
+};
+
+// Best schedule for one CTA grouping, with its cost in units of one split
+// chain of a pair tile.  A one-CTA chain covers half the W rows of a pair
+// chain and takes 1.17x its time per SM (measured: its operands are 48 KB per
+// K tile against 32 KB for each CTA of a pair).
+//   LOCAL   ceil(tiles / units) tiles of S chains per persistent unit;
+//   CLUSTER S units per tile, one chain each, + 15% for the un-overlapped
+//           epilogue and the DSMEM fold;
+//   CHAIN   ceil(S/2) units per tile, two chains each, + 10% for the fold
+//           that passes down the units.
+// Cluster schedules run ceil(tiles / resident clusters) waves.
+LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N, int32_t sm_count) {
+  const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
+  const int64_t n_tiles = ceil_div(N, (int64_t)kTileN * ctas);
+  const int64_t m_tiles = ceil_div(M, r.T);
+  const int64_t tiles = n_tiles * m_tiles;
+  const double c = ctas == 2 ? 1.0 : 1.17;
+  const bool grid_ok = n_tiles <= 65535 && m_tiles <= 65535;
+  LaunchChoice local{ctas, BI_FLAG_SCHEDULE_LOCAL, 1, 0.0};
+  const int64_t slots = sm_count / ctas > 0 ? sm_count / ctas : 1;
+  local.cost = (double)ceil_div(tiles, slots) * r.S * c;
+  if (r.S == 1 || forced == BI_FLAG_SCHEDULE_LOCAL || !grid_ok) return local;
+  const int32_t uc = (r.S + 1) / 2;
+  LaunchChoice cl{ctas, BI_FLAG_SCHEDULE_CLUSTER, r.S, 0.0};
+  cl.cost = (double)ceil_div(tiles, max_clusters(r.S * ctas, sm_count)) * c * 1.15;
+  LaunchChoice ch{ctas, BI_FLAG_SCHEDULE_CHAIN, uc, 0.0};
+  ch.cost = (double)ceil_div(tiles, max_clusters(uc * ctas, sm_count)) * 2.0 * c * 1.10;
+  if (forced == BI_FLAG_SCHEDULE_CLUSTER) return cl;
+  if (forced == BI_FLAG_SCHEDULE_CHAIN) return ch;
+  LaunchChoice best = local;
+  if (r.S * ctas <= 8 && cl.cost < best.cost) best = cl;
+  if (r.S >= 3 && uc * ctas <= 8 && ch.cost < best.cost) best = ch;
+  return best;
+}
+
+// The CTA grouping (when the pins leave it open, mma_ctas = 0) and the
+// schedule, from M.  cta_group::1 and ::2 MMAs give every output element the
+// same bits (each element is one chain of k16 steps in the same order on
+// either SM of a pair; tested on GPU), so this is speed only.  A single short
+// token tile (M <= T/2) stays on one CTA per MMA: a pair would hold a
+// half-empty X box, and decode is bound by the W stream, which S-CTA clusters
+// spread over the most SMs.  A forced one-split CLUSTER schedule also keeps
+// one CTA (a pair would need clusters of 2S).
+LaunchChoice choose_launch(int64_t M, int64_t N, const Resolved& r, int32_t sm_count) {
+  if (r.ctas != 0) return best_schedule(r, r.ctas, M, N, sm_count);
+  const LaunchChoice one = best_schedule(r, 1, M, N, sm_count);
+  if (M <= r.T / 2 || (r.flags & BI_FLAG_SCHEDULE_MASK) == BI_FLAG_SCHEDULE_CLUSTER) return one;
+  const LaunchChoice two = best_schedule(r, 2, M, N, sm_count);
+  return two.cost < one.cost ? two : one;
 }
 
 bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int32_t sm_count,
                     bi_gemm_plan* plan) {
   std::memset(plan, 0, sizeof(*plan));
   Resolved r = pinned;
-  if (r.ctas == 0) r.ctas = choose_ctas(M, N, r, sm_count);
+  const LaunchChoice choice = choose_launch(M, N, r, sm_count);
+  r.ctas = choice.ctas;
   plan->bk = kBK;
   plan->split_k = r.S;
   plan->tok_tile = r.T;
@@ -219,14 +261,15 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   choose_stages(x_rows, plan->x_box_rows, r.w_pin, plan->kps, &plan->w_stages, &plan->x_stages);
   plan->block_threads = kGemmThreads;
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
-  plan->schedule = choose_schedule(r, tiles, sm_count);
-  const bool cluster = plan->schedule == BI_FLAG_SCHEDULE_CLUSTER;
+  plan->schedule = choice.schedule;
+  plan->units = choice.units;
+  const bool cluster = plan->schedule != BI_FLAG_SCHEDULE_LOCAL;
   if (cluster) {
     if (plan->n_tiles > 65535 || plan->m_tiles > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
-    plan->grid_x = r.S * r.ctas;
+    plan->grid_x = choice.units * r.ctas;
     plan->grid_y = (int32_t)plan->n_tiles;
     plan->grid_z = (int32_t)plan->m_tiles;
-    plan->cluster_x = r.S * r.ctas;
+    plan->cluster_x = choice.units * r.ctas;
   } else {
     const int64_t slots = sm_count / r.ctas > 0 ? sm_count / r.ctas : 1;
     const int64_t units = tiles < slots ? tiles : slots;
@@ -268,10 +311,13 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
   }
   if (p->flags & ~BI_FLAG_KNOWN_MASK) return BI_ERR_ILLEGAL_PINS;
   const uint32_t sched = p->flags & BI_FLAG_SCHEDULE_MASK;
-  if (sched == BI_FLAG_SCHEDULE_MASK) return BI_ERR_ILLEGAL_PINS;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * (p->mma_ctas == 2 ? 2 : 1) > 16)
     return BI_ERR_ILLEGAL_PINS;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k > 8) return BI_ERR_ILLEGAL_PINS;
+  // CHAIN: ceil(S/2) >= 2 units per tile; an open grouping may choose pairs
+  if (sched == BI_FLAG_SCHEDULE_CHAIN &&
+      (p->split_k < 3 || (p->split_k + 1) / 2 * (p->mma_ctas == 1 ? 1 : 2) > 16))
+    return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
 }
 
@@ -362,7 +408,8 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.x_box_rows = plan.x_box_rows;
   L.kps = plan.kps;
   L.group_n = plan.group_n > 0 ? plan.group_n : 1;
-  L.cluster = plan.schedule == BI_FLAG_SCHEDULE_CLUSTER;
+  L.units = plan.units;
+  L.cluster = plan.schedule != BI_FLAG_SCHEDULE_LOCAL;
   L.pair = plan.mma_ctas == 2;
   L.grid_x = plan.grid_x;
   L.grid_y = plan.grid_y;

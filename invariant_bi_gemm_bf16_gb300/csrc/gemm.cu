@@ -61,6 +61,7 @@ struct GemmParams {
   int32_t n_tiles, m_tiles, k_tiles, S;
   int32_t w_stages, x_stages, x_box_rows;
   int32_t group_n;  // LOCAL tile order: groups of group_n W tiles (speed only)
+  int32_t units;    // CLUSTER: units (CTAs or pairs) per tile; S (one split each) or ceil(S/2)
   uint32_t flags;  // BI_FLAG_DEBUG_STALL_PRODUCER | kFlagStreamW | kFlagZeroX
 };
 
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int kXStage = KP * kXTile;
   constexpr int kWStage = KP * kWStageBytes;
   constexpr int kMmaM = PAIR ? 2 * kTileN : kTileN;  // W rows per tile
-  constexpr uint32_t kTmemCols = CLUSTER ? (uint32_t)T : 2u * (uint32_t)T;
+  constexpr uint32_t kTmemCols = 2u * (uint32_t)T;    // two accumulators
   constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quadrant
   constexpr int kHalf = T / kColGroups;      // accumulator columns per epilogue warp
 
@@ -223,18 +224,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int32_t S = p.S;
   const int32_t KT = p.k_tiles;
   const int64_t num_tiles = (int64_t)p.n_tiles * p.m_tiles;
-  // Work list.  CLUSTER: one tile (blockIdx.y, blockIdx.z) and one split (the
-  // cluster rank, counted in pairs when PAIR).  LOCAL: tiles u, u + U, ... for
-  // unit u of U (a unit is a CTA, or a CTA pair), all S splits of each.
-  const int32_t my_split = CLUSTER ? (int32_t)(PAIR ? (crank >> 1) : crank) : 0;
+  // Work list.  CLUSTER: one tile (blockIdx.y, blockIdx.z); cluster unit u
+  // (the cluster rank, counted in pairs when PAIR) of U runs splits
+  // [floor(u*S/U), floor((u+1)*S/U)): one split each when U = S, one or two
+  // when U = ceil(S/2) (chained).  LOCAL: tiles u, u + U, ... for unit u of U
+  // (a unit is a CTA, or a CTA pair), all S splits of each.
+  const int32_t U = CLUSTER ? p.units : 1;
+  const bool chained = CLUSTER && U != S;
+  const int32_t my_unit = CLUSTER ? (int32_t)(PAIR ? (crank >> 1) : crank) : 0;
   const int64_t unit = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
   const int64_t units = PAIR ? (gridDim.x >> 1) : gridDim.x;
   const int64_t tile_first = CLUSTER ? 0 : unit;
   const int64_t tile_step = CLUSTER ? 1 : units;
   const int64_t tile_end = CLUSTER ? 1 : num_tiles;
-  const int32_t s_first = CLUSTER ? my_split : 0;
-  const int32_t s_end = CLUSTER ? my_split + 1 : S;
+  const int32_t s_first = CLUSTER ? (int32_t)(((int64_t)my_unit * S) / U) : 0;
+  const int32_t s_end = CLUSTER ? (int32_t)(((int64_t)(my_unit + 1) * S) / U) : S;
   const bool stream_w = (p.flags & kFlagStreamW) != 0;
+  bool chain_ok = false;  // epilogue threads of a CLUSTER unit: its chains completed
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------ producers (W: warp 0, X: warp 2)
@@ -351,8 +357,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
         for (int32_t s = s_first; ok && s < s_end; ++s) {
-          const uint32_t buf = CLUSTER ? 0u : (acc_iter & 1u);
-          const uint32_t acc_phase = CLUSTER ? 0u : ((acc_iter >> 1) & 1u);
+          const uint32_t buf = acc_iter & 1u;
+          const uint32_t acc_phase = (acc_iter >> 1) & 1u;
           if (!wait_or_abort(smem_u32(&ctl->acc_empty[buf]), acc_phase ^ 1u, abort)) {
             ok = false;
             break;
@@ -479,10 +485,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     } else {
-      // One chain: move this CTA's partial into shared memory as [token][n].
-      bool got = wait_or_abort(smem_u32(&ctl->acc_full[0]), 0, abort);
+      // This unit's chains, one per TMEM buffer.  Unchained (one split per
+      // unit) and unit 0 of a chain move their partial -- unit 0 the sum of
+      // its splits, in order -- into shared memory as [token][n].  Later units
+      // of a chain keep theirs in TMEM until the running sum reaches them.
+      const int nch = s_end - s_first;
+      bool got = true;
+      for (int b = 0; b < nch; ++b) got = got && wait_or_abort(smem_u32(&ctl->acc_full[b]), 0, abort);
       got = __all_sync(0xffffffffu, got);
-      if (got) {
+      chain_ok = got;
+      if (got && (!chained || my_unit == 0)) {
         tc_fence_after();
         const int64_t m0 = (int64_t)blockIdx.z * T;
         const int64_t rem = p.M - m0;
@@ -492,6 +504,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = half * kHalf; c < c_end; c += 8) {
           float v[8];
           tmem_ld8(tmem_base + t_lane + (uint32_t)c, v);
+          if (nch == 2) {
+            float w[8];
+            tmem_ld8(tmem_base + t_lane + (uint32_t)T + (uint32_t)c, w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], w[i]);
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) P[(c + i) * kTileN + n_local] = v[i];
         }
@@ -502,6 +520,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
+  if (chained) {
+    // The running sum moves down the chain of units: at step u, unit u adds
+    // its splits, in ascending order, to the sum unit u - 1 left in its shared
+    // memory, and leaves the result in its own (the last unit writes Y).
+    // Every thread of the cluster takes part in every barrier.
+    for (int32_t u = 1; u < U; ++u) {
+      cluster_sync();
+      if (my_unit == u && warp >= kFirstEpiWarp && chain_ok) {
+        const int ew = warp - kFirstEpiWarp;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        const int n_local = quad * 32 + lane;
+        const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+        const int nch = s_end - s_first;
+        const int64_t m0 = (int64_t)blockIdx.z * T;
+        const int64_t rem = p.M - m0;
+        const int mv = rem < T ? (int)rem : T;
+        const int c_end = min(half * kHalf + kHalf, (mv + 7) & ~7);
+        const uint32_t prev = (uint32_t)(u - 1) * (PAIR ? 2u : 1u) + peer;  // same W rows, unit u - 1
+        const bool last = u == U - 1;
+        const int64_t n = (int64_t)blockIdx.y * kMmaM + (int64_t)peer * kTileN + n_local;
+        float* P = reinterpret_cast<float*>(smem);
+        tc_fence_after();
+        for (int c = half * kHalf; c < c_end; c += 8) {
+          float v[8], a[8];
+          tmem_ld8(tmem_base + t_lane + (uint32_t)c, a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t off = smem_base + (uint32_t)(((c + i) * kTileN + n_local) * 4);
+            v[i] = __fadd_rn(ld_dsmem_f32(mapa_shared(off, prev)), a[i]);
+          }
+          if (nch == 2) {
+            tmem_ld8(tmem_base + t_lane + (uint32_t)T + (uint32_t)c, a);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], a[i]);
+          }
+          if (last) {
+            if (n < p.N) {
+              __nv_bfloat16* y = p.Y + (m0 + c) * p.N + n;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (c + i < mv) y[(int64_t)i * p.N] = __float2bfloat16_rn(v[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) P[(c + i) * kTileN + n_local] = v[i];
+          }
+        }
+        tc_fence_before();
+      }
+    }
+    cluster_sync();  // no CTA leaves, or frees its tensor memory, while another reads it
+  }
   // In a pair, the even CTA's MMAs write both CTAs' TMEM: nobody frees TMEM
   // (or exits) until that CTA has drained them.
   if constexpr (PAIR) cluster_sync();
@@ -512,12 +583,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     else
       tmem_dealloc(tmem_base, kTmemCols);
   }
-  if constexpr (CLUSTER) {
+  if (CLUSTER && !chained) {
     // Fold the S partials of the tile in ascending split order.  The CTA of
     // split r folds tokens r, r + S, r + 2S, ... of its own 128 W rows; element
     // pairs are spread over all threads.
     cluster_sync();
-    const int32_t rank = my_split;
+    const int32_t rank = my_unit;
     const int64_t m0 = (int64_t)blockIdx.z * T;
     const int64_t n0 = (int64_t)blockIdx.y * kMmaM + (int64_t)peer * kTileN;
     const int64_t remm = p.M - m0;
@@ -598,7 +669,7 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   auto kern = bi_gemm_kernel<T, CLUSTER, PAIR, KP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   if (e != cudaSuccess) return e;
-  const int cluster = CLUSTER ? L.S * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
+  const int cluster = CLUSTER ? L.units * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
   if (cluster > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -615,6 +686,7 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   prm.x_stages = L.x_stages;
   prm.x_box_rows = L.x_box_rows;
   prm.group_n = L.group_n;
+  prm.units = L.units;
   prm.flags = L.flags;
 
   cudaLaunchConfig_t cfg = {};

@@ -50,6 +50,7 @@ struct GemmLaunch {
   int32_t n_tiles, m_tiles, k_tiles, S, T, w_stages, x_stages, x_box_rows;
   int32_t kps;       // K tiles per copy: 1 (2-D maps) or 2 (3-D maps, T = 256 only)
   int32_t group_n;   // LOCAL tile order: W tiles per group (1 .. n_tiles)
+  int32_t units;     // CLUSTER: units (CTAs or pairs) per tile: S, or ceil(S/2) when chained
   bool cluster;      // one chain per CTA (pair), folded through DSMEM
   bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;

@@ -71,7 +71,7 @@ def test_pins_validation_refuses(bd):
     bad = [good.replace(abi_version=2), good.replace(bk=32), good.replace(split_k=0),
            good.replace(split_k=17), good.replace(tok_tile=96), good.replace(tok_tile=512),
            good.replace(stages=1), good.replace(stages=99), good.replace(flags=0x8000),
-           good.replace(flags=0x3), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER),
+           good.replace(split_k=2, flags=bd.BI_FLAG_SCHEDULE_CHAIN), good.replace(split_k=9, flags=bd.BI_FLAG_SCHEDULE_CLUSTER),
            good.replace(mma_ctas=-1), good.replace(mma_ctas=4)]
     for p in bad:
         assert bd.bi_pins_validate(N, K, p) == bd.BI_ERR_ILLEGAL_PINS, p
@@ -159,9 +159,27 @@ def test_open_grouping_follows_m(bd):
     mid = bd.bi_gemm_plan_describe(512, 4096, 14336)
     big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
     assert (small.mma_ctas, small.kps, small.schedule) == (1, 1, bd.BI_FLAG_SCHEDULE_CLUSTER)
-    assert (mid.mma_ctas, mid.schedule) == (1, bd.BI_FLAG_SCHEDULE_CLUSTER)
+    # M=512: 32 pair tiles, each a cluster of 2 pairs running 2 splits each (one wave)
+    assert (mid.mma_ctas, mid.schedule, mid.units, mid.cluster_x) == (2, bd.BI_FLAG_SCHEDULE_CHAIN, 2, 4)
+    assert mid.grid_x * mid.grid_y * mid.grid_z == 4 * 16 * 2
     assert (big.mma_ctas, big.kps, big.schedule, big.mma_m) == (2, 2, bd.BI_FLAG_SCHEDULE_LOCAL, 256)
-    assert small.tree() == mid.tree() == big.tree()
+    m256 = bd.bi_gemm_plan_describe(256, 4096, 14336)
+    m1024 = bd.bi_gemm_plan_describe(1024, 4096, 14336)
+    assert (m256.mma_ctas, m256.schedule) == (1, bd.BI_FLAG_SCHEDULE_CLUSTER)
+    assert (m1024.mma_ctas, m1024.schedule) == (2, bd.BI_FLAG_SCHEDULE_LOCAL)
+    assert small.tree() == mid.tree() == big.tree() == m256.tree() == m1024.tree()
+
+
+@pytest.mark.parametrize("S", [3, 4, 5, 8])
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_chain_schedule_plan(bd, S, ctas):
+    """CHAIN: ceil(S/2) units per tile, each a CTA or a pair; the tree is unchanged."""
+    pins = bd.bi_pins_default(4096, 14336).replace(split_k=S, mma_ctas=ctas, flags=bd.BI_FLAG_SCHEDULE_CHAIN)
+    assert bd.bi_pins_validate(4096, 14336, pins) == bd.BI_OK
+    plan = bd.bi_gemm_plan_describe(700, 4096, 14336, pins)
+    u = (S + 1) // 2
+    assert (plan.schedule, plan.units, plan.cluster_x, plan.grid_x) == (bd.BI_FLAG_SCHEDULE_CHAIN, u, u * ctas, u * ctas)
+    assert plan.tree() == bd.bi_gemm_plan_describe(700, 4096, 14336, pins.replace(flags=0)).tree()
 
 
 def test_split_boundaries_partition_k(bd):

@@ -52,7 +52,7 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-@pytest.mark.parametrize("S,T", [(1, 128), (2, 64), (3, 128), (2, 256), (4, 64)])
+@pytest.mark.parametrize("S,T", [(1, 128), (2, 64), (3, 128), (2, 256), (4, 64), (5, 256)])
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T, ctas):
     kt = -(-K // 64)
@@ -62,8 +62,11 @@ def test_ragged_parity_and_schedules_agree(lib, oracle, M, N, K, S, T, ctas):
     W = inputs.normal((N, K), std=0.02, seed=1, stream=1)
     yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
     outs = []
-    for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_AUTO,
-                  lib.BI_FLAG_SCHEDULE_AUTO | lib.BI_FLAG_PREFETCH_W):
+    scheds = [lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_AUTO,
+              lib.BI_FLAG_SCHEDULE_AUTO | lib.BI_FLAG_PREFETCH_W]
+    if S >= 3:
+        scheds.append(lib.BI_FLAG_SCHEDULE_CHAIN)
+    for flags in scheds:
         got = run(lib, X, W, pins_for(lib, N, K, split_k=S, tok_tile=T, flags=flags, mma_ctas=ctas))
         check_gemm_parity(got, yf, K, "M=%d N=%d K=%d S=%d T=%d ctas=%d flags=%d" % (M, N, K, S, T, ctas, flags))
         outs.append(got)
@@ -84,7 +87,8 @@ def test_ktile_pairs_change_no_bit(lib, oracle, M, N, K, S, ctas):
     yf, _ = oracle.gemm(inputs.bits(X), inputs.bits(W))
     outs = []
     for extra in (0, lib.BI_FLAG_KTILE_PAIRS):
-        for sched in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER):
+        for sched in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER) + \
+                ((lib.BI_FLAG_SCHEDULE_CHAIN,) if S >= 3 else ()):
             pins = pins_for(lib, N, K, split_k=S, tok_tile=256, mma_ctas=ctas, flags=sched | extra)
             plan = lib.bi_gemm_plan_describe(M, N, K, pins)
             assert plan.kps == (2 if extra and ctas == 2 and plan.x_box_rows == 128 else 1)
