@@ -6,9 +6,11 @@ every M of the sweep.  `value` = the sweep's FLOPs / its device time (TFLOPS).
 Per-M times, TFLOPS, GB/s, roofline fractions and the torch.mm (cuBLAS) time on
 the same tensors are in "sweep".
 
-Other workloads (--workload): "stack" (the 4-layer Llama-3.1-70B-shaped decode
-step at 32 tokens, us/step), "fused" (RMSNorm + qkv / gate_up projections),
-"rmsnorm" (the RMSNorm token sweep).
+The same JSON line also carries, unless switched off: "stack" (the 4-layer
+Llama-3.1-70B-shaped decode step at 32 tokens, us/step), "fused" (RMSNorm +
+the Llama-3.1-8B qkv and gate_up projections in one call, per M) and "rmsnorm"
+(the RMSNorm token sweep at H = 4096 and 8192, GB/s), each against torch on
+the same tensors.
 
 L2 handling: every launch reads a weight copy that was not read by the
 previous launches (enough copies that they exceed the 129 MB L2), and
@@ -392,6 +394,102 @@ def run_stack(args, dist, peaks):
     return res
 
 
+def time_reps(fn, reps):
+    """Average device time (us) of one call, from `reps` back-to-back calls
+    (fn(i) rotates its inputs) between two events, after 3 untimed calls."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(reps):
+        fn(i)
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) * 1e3 / reps
+
+
+def copies_for(nbytes: int, cap: int = 64) -> int:
+    """Copies of a tensor so that consecutive calls never find it in L2."""
+    return max(1, min(cap, math.ceil(2 * L2_BYTES / max(nbytes, 1)) + 1))
+
+
+def run_rmsnorm(args, dist, peaks):
+    """Configuration 4: RMSNorm over M tokens at H = 4096 and 8192; row m of X
+    ~ N(0, s_m), s_m log-uniform on [0.1, 10] (drawn on the device from a
+    seeded generator), g ~ N(1, 0.1), eps = 1e-5.  HBM-bound: B = 4MH + 2H."""
+    import torch.nn.functional as F
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    dev = torch.device("cuda", dist.local_rank)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + dist.rank)
+    out = []
+    for H in (4096, 8192):
+        g = inputs.device_normal((H,), std=0.1, mean=1.0, seed=dist.rank, stream=inputs.STREAM_G, device=dev)
+        for M in [1 << i for i in range(15)] + [3, 37, 1001]:
+            n = copies_for(M * H * 2)
+            xs = []
+            for i in range(n):
+                x = inputs.device_normal((M, H), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
+                scale = torch.exp(torch.empty((M, 1), device=dev).uniform_(math.log(0.1), math.log(10.0),
+                                                                         generator=gen))
+                xs.append((x.float() * scale).to(torch.bfloat16))
+            y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+            us = time_reps(lambda i: bd.bi_rmsnorm_bf16(xs[i % n], g, 1e-5, out=y), args.per_m_reps)
+            tus = time_reps(lambda i: F.rms_norm(xs[i % n], (H,), g, 1e-5), args.per_m_reps)
+            b = 4 * M * H + 2 * H
+            out.append({"H": H, "M": M, "us": round(us, 2), "gbs": round(b / us / 1e3, 1),
+                        "roofline_frac": round(b / (peaks["hbm_gbs"] * 1e3) / us, 3),
+                        "torch_rms_norm_us": round(tus, 2), "vs_torch": round(tus / us, 3)})
+            del xs
+    big = [r for r in out if r["M"] == 16384]
+    return {"workload": "RMSNorm, H in {4096, 8192}, M = 1..16384 and 3, 37, 1001; rows ~N(0, s_m), "
+                        "s_m log-uniform on [0.1, 10]", "bound": "hbm",
+            "largest": {("H%d" % r["H"]): {"gbs": r["gbs"], "roofline_frac": r["roofline_frac"],
+                                           "vs_torch": r["vs_torch"]} for r in big},
+            "sweep": out}
+
+
+def run_fused(args, dist, peaks):
+    """Configuration 3: RMSNorm + projection in one call (bi_rmsnorm_gemm_bf16)
+    for the Llama-3.1-8B qkv [6144, 4096] and gate_up [28672, 4096] weights,
+    against F.rms_norm + torch.mm on the same tensors."""
+    import torch.nn.functional as F
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    dev = torch.device("cuda", dist.local_rank)
+    K = 4096
+    g = inputs.device_normal((K,), std=0.1, mean=1.0, seed=dist.rank, stream=inputs.STREAM_G, device=dev)
+    res = []
+    for name, N in (("qkv", 6144), ("gate_up", 28672)):
+        nw = copies_for(N * K * 2, cap=8)
+        W = [inputs.device_normal((N, K), std=0.02, seed=dist.rank, stream=inputs.STREAM_W + 16 * i, device=dev)
+             for i in range(nw)]
+        pins = bd.bi_pins_default(N, K)
+        pins = pins.replace(flags=pins.flags | bd.BI_FLAG_PREFETCH_W)
+        for M in (1, 8, 32, 128, 1024, 4096, 8192):
+            nx = copies_for(M * K * 2, cap=8)
+            xs = [inputs.device_normal((M, K), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
+                  for i in range(nx)]
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(bd.bi_rmsnorm_gemm_workspace_bytes(M, K), 1), dtype=torch.uint8, device=dev)
+            us = time_reps(lambda i: bd.bi_rmsnorm_gemm_bf16(xs[i % nx], g, W[i % nw], 1e-5, pins=pins, out=y,
+                                                             workspace=ws), args.per_m_reps)
+            tus = time_reps(lambda i: torch.mm(F.rms_norm(xs[i % nx], (K,), g, 1e-5), W[i % nw].t(), out=y),
+                            args.per_m_reps)
+            f = 2.0 * M * N * K
+            b = 2.0 * (N * K + M * K + M * N) + 2 * K
+            t_roof = max(f / (peaks["bf16_tflops"] * 1e6), b / (peaks["hbm_gbs"] * 1e3))
+            res.append({"proj": name, "N": N, "K": K, "M": M, "us": round(us, 2), "tflops": round(f / us / 1e6, 1),
+                        "gbs": round(b / us / 1e3, 1), "roofline_frac": round(t_roof / us, 3),
+                        "torch_us": round(tus, 2), "vs_torch": round(tus / us, 3)})
+            del xs
+        del W
+        torch.cuda.empty_cache()
+    return {"workload": "RMSNorm + projection in one call, Llama-3.1-8B qkv [6144,4096] and gate_up [28672,4096], "
+                        "M in 1, 8, 32, 128, 1024, 4096, 8192; against F.rms_norm + torch.mm", "sweep": res}
+
+
 def time_steps(fn, steps, dist):
     dist.barrier()
     torch.cuda.synchronize()
@@ -528,6 +626,10 @@ def run_ours(args, dist):
     }
     if not args.no_stack:
         result["stack"] = run_stack(args, dist, peaks)
+    if not args.no_fused:
+        result["fused"] = run_fused(args, dist, peaks)
+    if not args.no_rmsnorm:
+        result["rmsnorm"] = run_rmsnorm(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -589,6 +691,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-fused", action="store_true")
+    ap.add_argument("--no-rmsnorm", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
     ap.add_argument("--single-m", type=int, default=0,
                     help="profiling helper: only launch the sweep's GEMM at this M --launches times")

@@ -181,34 +181,43 @@ struct LaunchChoice {
   double cost;
 };
 
-// Best schedule for one CTA grouping, with its cost in units of one split
-// chain of a pair tile.  A one-CTA chain covers half the W rows of a pair
-// chain and takes 1.17x its time per SM (measured: its operands are 48 KB per
-// K tile against 32 KB for each CTA of a pair).
+// Best schedule for one CTA grouping, and its cost in units of one K tile of a
+// paired MMA (about 0.33 us on GB300), calibrated on down_proj launches:
+//   - a one-CTA K tile (half the W rows) costs 1.2 pair K tiles: its operands
+//     are 48 KB per K tile against 32 KB for each CTA of a pair;
+//   - a cluster wave adds about 30 K tiles (pipeline fill, the epilogue that
+//     no other chain overlaps, the fold); a persistent launch about 15.
 //   LOCAL   ceil(tiles / units) tiles of S chains per persistent unit;
-//   CLUSTER S units per tile, one chain each, + 15% for the un-overlapped
-//           epilogue and the DSMEM fold;
-//   CHAIN   ceil(S/2) units per tile, two chains each, + 10% for the fold
-//           that passes down the units.
-// Cluster schedules run ceil(tiles / resident clusters) waves.
+//   CLUSTER waves of resident S-unit clusters, one chain per unit;
+//   CHAIN   waves of resident ceil(S/2)-unit clusters, two chains per unit.
+// A single short token tile (decode) streams W from HBM: there the schedule
+// that puts the most CTAs on the W stream wins, which the rounds of LOCAL
+// against those of CLUSTER capture (CHAIN is not used).
 LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N, int32_t sm_count) {
   const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
   const int64_t n_tiles = ceil_div(N, (int64_t)kTileN * ctas);
   const int64_t m_tiles = ceil_div(M, r.T);
   const int64_t tiles = n_tiles * m_tiles;
-  const double c = ctas == 2 ? 1.0 : 1.17;
   const bool grid_ok = n_tiles <= 65535 && m_tiles <= 65535;
-  LaunchChoice local{ctas, BI_FLAG_SCHEDULE_LOCAL, 1, 0.0};
-  const int64_t slots = sm_count / ctas > 0 ? sm_count / ctas : 1;
-  local.cost = (double)ceil_div(tiles, slots) * r.S * c;
-  if (r.S == 1 || forced == BI_FLAG_SCHEDULE_LOCAL || !grid_ok) return local;
   const int32_t uc = (r.S + 1) / 2;
-  LaunchChoice cl{ctas, BI_FLAG_SCHEDULE_CLUSTER, r.S, 0.0};
-  cl.cost = (double)ceil_div(tiles, max_clusters(r.S * ctas, sm_count)) * c * 1.15;
-  LaunchChoice ch{ctas, BI_FLAG_SCHEDULE_CHAIN, uc, 0.0};
-  ch.cost = (double)ceil_div(tiles, max_clusters(uc * ctas, sm_count)) * 2.0 * c * 1.10;
+  const int64_t slots = sm_count / ctas > 0 ? sm_count / ctas : 1;
+  const double k = ctas == 2 ? 1.0 : 1.2;          // cost of one K tile
+  const double chain = (double)r.KT / r.S * k;      // one split chain
+  LaunchChoice local{ctas, BI_FLAG_SCHEDULE_LOCAL, 1,
+                     (double)ceil_div(tiles, slots) * r.S * chain + 15.0};
+  LaunchChoice cl{ctas, BI_FLAG_SCHEDULE_CLUSTER, r.S,
+                  (double)ceil_div(tiles, max_clusters(r.S * ctas, sm_count)) * (chain + 30.0)};
+  LaunchChoice ch{ctas, BI_FLAG_SCHEDULE_CHAIN, uc,
+                  (double)ceil_div(tiles, max_clusters(uc * ctas, sm_count)) * (2.0 * chain + 30.0)};
+  if (r.S == 1 || forced == BI_FLAG_SCHEDULE_LOCAL || !grid_ok) return local;
   if (forced == BI_FLAG_SCHEDULE_CLUSTER) return cl;
   if (forced == BI_FLAG_SCHEDULE_CHAIN) return ch;
+  if (m_tiles == 1 && M <= r.T / 2) {
+    // decode: rounds of chain work per unit; CLUSTER charged 15%
+    const double local_rounds = (double)ceil_div(tiles, slots) * r.S;
+    const double cluster_rounds = (double)ceil_div(tiles * r.S, slots);
+    return (r.S * ctas <= 8 && cluster_rounds * 1.15 < local_rounds) ? cl : local;
+  }
   LaunchChoice best = local;
   if (r.S * ctas <= 8 && cl.cost < best.cost) best = cl;
   if (r.S >= 3 && uc * ctas <= 8 && ch.cost < best.cost) best = ch;

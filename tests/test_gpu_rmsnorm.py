@@ -10,9 +10,11 @@ from invariant_bi_gemm_bf16_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H", [256, 4096, 8192, 8, 72, 1000, 2048 + 8])
-@pytest.mark.parametrize("M", [1, 3, 37, 257])
+@pytest.mark.parametrize("H", [256, 2048, 4096, 8192, 16384, 8, 72, 1000, 2048 + 8])
+@pytest.mark.parametrize("M", [1, 3, 37, 257, 1500])
 def test_rmsnorm_parity(lib, oracle, M, H):
+    """1500 rows exceed the warps of one grid at H >= 2048, so each warp's ring
+    of row buffers wraps around."""
     X = inputs.rows_loguniform(M, H, seed=0, stream=0)
     g = inputs.normal((H,), std=0.1, mean=1.0, seed=0, stream=2)
     want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
@@ -31,13 +33,28 @@ def test_rmsnorm_special_rows(lib):
     assert torch.isnan(lib.bi_rmsnorm_bf16(nanrow, g1).float()).all()
 
 
-def test_rmsnorm_in_place(lib, oracle):
-    X = inputs.rows_loguniform(9, 4096, seed=1, stream=0)
-    g = inputs.normal((4096,), std=0.1, mean=1.0, seed=1, stream=2)
+@pytest.mark.parametrize("M,H", [(9, 4096), (2000, 8192), (700, 16384)])
+def test_rmsnorm_in_place(lib, oracle, M, H):
+    X = inputs.rows_loguniform(M, H, seed=1, stream=0)
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=1, stream=2)
     want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
     x = X.cuda()
     lib.bi_rmsnorm_bf16(x, g.cuda(), EPS, out=x)
     check_ulp(bf16_bits(x), want, 1, "in place")
+
+
+@pytest.mark.parametrize("H", [2048, 8192])
+def test_rmsnorm_rows_independent_of_batch(lib, H):
+    """A row's bits are the same alone, in a batch of 3000 and at another position."""
+    X = inputs.rows_loguniform(3000, H, seed=3, stream=0).cuda()
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=3, stream=2).cuda()
+    full = bf16_bits(lib.bi_rmsnorm_bf16(X, g, EPS))
+    for r in (0, 1234, 2999):
+        alone = bf16_bits(lib.bi_rmsnorm_bf16(X[r:r + 1].contiguous(), g, EPS))
+        assert np.array_equal(alone[0], full[r])
+    perm = torch.randperm(3000, generator=torch.Generator().manual_seed(5))
+    shuffled = bf16_bits(lib.bi_rmsnorm_bf16(X[perm.cuda()].contiguous(), g, EPS))
+    assert np.array_equal(shuffled, full[perm.numpy()])
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 384, 4096), (33, 256, 512), (130, 640, 256)])
