@@ -435,7 +435,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
         int32_t n_tile, m_tile;
         tile_coords(t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
+        // Running sum of the splits.  It starts at -0.0, the identity of
+        // IEEE addition (-0 + x == x for every x, zeros included), so the
+        // first add yields P0 exactly and the sum is ((P0 + P1) + P2) + ...
         float R[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) R[i] = -0.0f;
         for (int32_t s = 0; s < S; ++s) {
           const uint32_t buf = acc_iter & 1u;
           const uint32_t acc_phase = (acc_iter >> 1) & 1u;
@@ -447,17 +452,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem_base + t_lane + buf * (uint32_t)T + (uint32_t)(half * kHalf);
+          // four columns per load: with the 64-float sum live, wider loads
+          // push the epilogue past its register budget (and into local memory)
 #pragma unroll
-          for (int c = 0; c < kHalf; c += 16) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)c, v);
-            if (s == 0) {
+          for (int c = 0; c < kHalf; c += 4) {
+            float v[4];
+            tmem_ld4(taddr + (uint32_t)c, v);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) R[c + i] = v[i];
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) R[c + i] = __fadd_rn(R[c + i], v[i]);
-            }
+            for (int i = 0; i < 4; ++i) R[c + i] = __fadd_rn(R[c + i], v[i]);
           }
           tc_fence_before();
           __syncwarp();
