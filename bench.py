@@ -49,8 +49,8 @@ EPS = 1e-5
 # launches, from ncu captures of `python bench.py --single-m M --launches 2`
 # (summaries in profiles/), valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "8ed1714b7cc4291dc9a4d03caabb397204b51b5aeb2da000b9f160b2c8544702": {8192: 988222208 + 108336896,
-                                                                         1: 117499648 + 2437632},
+    "5accb49fb0461f679cabb3a5fa698ca0c8d0b41cc2d0f89785e05b4eddf36be6": {8192: 965074688 + 63709440,
+                                                                         1: 117513216 + 3063040},
 }
 
 
