@@ -187,6 +187,24 @@ def bi_gemm_plan_describe(M: int, N: int, K: int, pins: Pins | None = None, sm_c
 # the layer
 # ---------------------------------------------------------------------------
 
+# Observers of GEMM calls, fn(M, N, K): the pin tuner's workload recorder.
+# They only count calls; nothing is computed here.
+_call_hooks: list = []
+
+
+def add_call_hook(fn):
+    _call_hooks.append(fn)
+
+
+def remove_call_hook(fn):
+    _call_hooks.remove(fn)
+
+
+def _report(M: int, N: int, K: int):
+    for fn in list(_call_hooks):
+        fn(M, N, K)
+
+
 def bi_gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
                  pins: Pins | None = None, stream=None) -> torch.Tensor:
     """Y = X . W^T (bf16, fp32 accumulation).  x [M,K], w [N,K] -> [M,N]."""
@@ -199,6 +217,8 @@ def bi_gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = No
     st = load().bi_gemm_bf16(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
                              ctypes.byref(pins) if pins is not None else None, _stream(stream))
     _check(st, "bi_gemm_bf16")
+    if _call_hooks:
+        _report(M, N, K)
     return out
 
 
@@ -241,6 +261,8 @@ def bi_rmsnorm_gemm_bf16(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, eps:
                                      ctypes.byref(pins) if pins is not None else None,
                                      workspace.data_ptr(), ws_bytes, _stream(stream))
     _check(st, "bi_rmsnorm_gemm_bf16")
+    if _call_hooks:
+        _report(M, N, K)
     return out
 
 
@@ -262,6 +284,8 @@ def bi_rmsnorm_gemm_bf16_noalloc(x: torch.Tensor, g: torch.Tensor, w: torch.Tens
                                              ctypes.byref(pins) if pins is not None else None,
                                              _stream(stream))
     _check(st, "bi_rmsnorm_gemm_bf16_noalloc")
+    if _call_hooks:
+        _report(M, N, K)
     return out
 
 

@@ -62,7 +62,10 @@ def random_layers(shape: StackShape, seed: int = 0, device="cuda") -> list:
 
 
 class DecodeStack:
-    def __init__(self, shape: StackShape, layers: list, pins: dict | None = None):
+    def __init__(self, shape: StackShape, layers: list, pins: dict | None = None,
+                 pin_table: dict | None = None):
+        """pins: {"qkv"|"o"|"gu"|"d": Pins} overrides; pin_table: {(N, K): Pins}
+        (a tuned table, see tuner.load); both are fixed for every batch size."""
         self.shape = shape
         self.layers = layers
         s = shape
@@ -77,6 +80,13 @@ class DecodeStack:
         # streaming its weights while the small kernels before it finish.
         for k in self.pins:
             self.pins[k] = self.pins[k].replace(flags=self.pins[k].flags | bd.BI_FLAG_PREFETCH_W)
+        if pin_table:
+            shapes = {"qkv": (s.qkv_width, s.hidden), "o": (s.hidden, s.n_q * s.head_dim),
+                      "gu": (2 * s.inter, s.hidden), "d": (s.hidden, s.inter)}
+            for name, nk in shapes.items():
+                if nk in pin_table:
+                    p = pin_table[nk]
+                    self.pins[name] = p.replace(flags=p.flags | bd.BI_FLAG_PREFETCH_W)
         if pins:
             self.pins.update(pins)
         self._bufs = {}
