@@ -8,8 +8,9 @@ the same tensors are in "sweep".
 
 The same JSON line also carries, unless switched off: "stack" (the 4-layer
 Llama-3.1-70B-shaped decode step at 32 tokens, us/step), "fused" (RMSNorm +
-the Llama-3.1-8B qkv and gate_up projections in one call, per M) and "rmsnorm"
-(the RMSNorm token sweep at H = 4096 and 8192, GB/s), each against torch on
+the Llama-3.1-8B qkv and gate_up projections in one call, per M), "rmsnorm"
+(the RMSNorm token sweep at H = 4096 and 8192, GB/s) and "lm_head" (the
+Llama-3.1-8B lm_head with per-token log-probabilities), each against torch on
 the same tensors.
 
 L2 handling: every launch reads a weight copy that was not read by the
@@ -490,6 +491,60 @@ def run_fused(args, dist, peaks):
                         "M in 1, 8, 32, 128, 1024, 4096, 8192; against F.rms_norm + torch.mm", "sweep": res}
 
 
+def run_lm_head(args, dist, peaks):
+    """Llama-3.1-8B lm_head (V = 128256, K = 4096) and the per-token
+    log-probabilities of given ids: bi_gemm_bf16 + bi_token_logprobs_bf16
+    against torch.mm + log_softmax(float) + gather.  Also the full
+    log-softmax kernel alone against its HBM roofline (B = 6 M V)."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    dev = torch.device("cuda", dist.local_rank)
+    V, K = 128256, 4096
+    nw = copies_for(V * K * 2, cap=4)
+    W = [inputs.device_normal((V, K), std=0.02, seed=dist.rank, stream=inputs.STREAM_W + 16 * i, device=dev)
+         for i in range(nw)]
+    pins = bd.bi_pins_default(V, K)
+    pins = pins.replace(flags=pins.flags | bd.BI_FLAG_PREFETCH_W)
+    res = []
+    for M in (1, 32, 256):
+        nx = copies_for(M * K * 2, cap=8)
+        hs = [inputs.device_normal((M, K), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
+              for i in range(nx)]
+        ids = torch.randint(0, V, (M,), dtype=torch.int32, device=dev,
+                            generator=torch.Generator(device=dev).manual_seed(7))
+        ids64 = ids.long().unsqueeze(1)
+        logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+        lp = torch.empty(M, dtype=torch.float32, device=dev)
+
+        def ours(i):
+            bd.bi_gemm_bf16(hs[i % nx], W[i % nw], out=logits, pins=pins)
+            bd.bi_token_logprobs_bf16(logits, ids, out=lp)
+
+        def theirs(i):
+            lg = torch.mm(hs[i % nx], W[i % nw].t())
+            torch.log_softmax(lg.float(), dim=-1).gather(1, ids64)
+
+        us = time_reps(ours, args.per_m_reps)
+        tus = time_reps(theirs, args.per_m_reps)
+        # the log-softmax kernels alone, on resident logits
+        nl = copies_for(M * V * 2, cap=16)
+        ls = [inputs.device_normal((M, V), std=3.0, seed=dist.rank, stream=40 + i, device=dev) for i in range(nl)]
+        yf = torch.empty((M, V), dtype=torch.float32, device=dev)
+        us_tok = time_reps(lambda i: bd.bi_token_logprobs_bf16(ls[i % nl], ids, out=lp), args.per_m_reps)
+        us_full = time_reps(lambda i: bd.bi_log_softmax_bf16(ls[i % nl], out=yf), args.per_m_reps)
+        tus_full = time_reps(lambda i: torch.log_softmax(ls[i % nl].float(), dim=-1), args.per_m_reps)
+        b_full = 6.0 * M * V
+        res.append({"M": M, "us": round(us, 2), "torch_us": round(tus, 2), "vs_torch": round(tus / us, 3),
+                    "token_logprobs_us": round(us_tok, 2), "log_softmax_us": round(us_full, 2),
+                    "log_softmax_gbs": round(b_full / us_full / 1e3, 1),
+                    "log_softmax_roofline_frac": round(b_full / (peaks["hbm_gbs"] * 1e3) / us_full, 3),
+                    "torch_log_softmax_us": round(tus_full, 2)})
+        del hs, ls
+    del W
+    torch.cuda.empty_cache()
+    return {"workload": "Llama-3.1-8B lm_head W[128256,4096] + per-token log-probabilities of given ids, "
+                        "M in 1, 32, 256; against torch.mm + log_softmax + gather", "sweep": res}
+
+
 def time_steps(fn, steps, dist):
     dist.barrier()
     torch.cuda.synchronize()
@@ -630,6 +685,8 @@ def run_ours(args, dist):
         result["fused"] = run_fused(args, dist, peaks)
     if not args.no_rmsnorm:
         result["rmsnorm"] = run_rmsnorm(args, dist, peaks)
+    if not args.no_lm_head:
+        result["lm_head"] = run_lm_head(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -693,6 +750,7 @@ def main():
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-fused", action="store_true")
     ap.add_argument("--no-rmsnorm", action="store_true")
+    ap.add_argument("--no-lm-head", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
     ap.add_argument("--single-m", type=int, default=0,
                     help="profiling helper: only launch the sweep's GEMM at this M --launches times")

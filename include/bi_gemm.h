@@ -280,6 +280,32 @@ bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I, bi_s
 bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
                                  int64_t D, bi_stream_t stream);
 
+/* Log-probabilities of rows of logits (the lm_head output X [M,V] bf16):
+ *   Y[m,v] = x[m,v] - lse_m,  lse_m = max_v x[m,v] + log(sum_v exp(x[m,v] - max)),
+ * in fp32, Y [M,V] fp32.  One CTA per row: thread t folds its 16-byte vectors
+ * t, t + 512, ... in ascending order into a running (max, sum of exp) pair, and
+ * the pairs combine by fixed xor butterflies within and across warps, so the
+ * tree depends on V only.  expf / logf are CUDA's.  A row holding a NaN or a
+ * +Inf, or -Inf everywhere, gives NaN everywhere; otherwise a -Inf logit gives
+ * -Inf.
+ * Defines: Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock
+ * Speed), Sec. 8, Table 6, and CoRun, Sec. IV: per-token log-probabilities
+ * are what batch invariance is checked on.  The formula is the textbook one
+ * (the pages give none).
+ * Requirements: V % 8 == 0, V < 2^31, M < 2^31, X and Y 16-byte aligned; X
+ * and Y must not overlap.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_CUDA. */
+bi_status bi_log_softmax_bf16(const void* X, float* Y, int64_t M, int64_t V, bi_stream_t stream);
+
+/* out[m] = log-probability of token ids[m] in row m of X [M,V] bf16: the same
+ * bits as Y[m, ids[m]] of bi_log_softmax_bf16 (the same kernel arithmetic,
+ * without writing the other V - 1 values).  ids: int32 [M] in device memory;
+ * an id outside [0, V) gives NaN.  out: fp32 [M].  Requirements and errors as
+ * bi_log_softmax_bf16 (ids and out need 4-byte alignment). */
+bi_status bi_token_logprobs_bf16(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
+                                 bi_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's stall
  * word: BI_OK if no kernel's bounded wait ran out since the last call,
  * BI_ERR_DEVICE_TIMEOUT otherwise (the affected call's output is

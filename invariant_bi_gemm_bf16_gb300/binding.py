@@ -117,6 +117,8 @@ _SIGNATURES = {
     "bi_silu_mul_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "bi_last_device_status": (ctypes.c_int, [_vp]),
+    "bi_log_softmax_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
+    "bi_token_logprobs_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp]),
 }
 
 
@@ -298,6 +300,37 @@ def bi_residual_add_bf16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | N
     st = load().bi_residual_add_bf16(_dev(a, "a"), _dev(b, "b"), _dev(out, "out", a.shape), a.numel(),
                                      _stream(stream))
     _check(st, "bi_residual_add_bf16")
+    return out
+
+
+def bi_log_softmax_bf16(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Log-probabilities (fp32 [M,V]) of logits x [M,V] bf16."""
+    if x.dim() != 2:
+        raise ValueError("expected x [M,V]")
+    M, V = x.shape
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.float32, device=x.device)
+    if out.dtype != torch.float32 or not out.is_cuda or not out.is_contiguous() or tuple(out.shape) != (M, V):
+        raise ValueError("out must be a contiguous fp32 CUDA tensor [M,V]")
+    st = load().bi_log_softmax_bf16(_dev(x, "x"), out.data_ptr(), M, V, _stream(stream))
+    _check(st, "bi_log_softmax_bf16")
+    return out
+
+
+def bi_token_logprobs_bf16(x: torch.Tensor, ids: torch.Tensor, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """out[m] = log-probability of token ids[m] in row m of x [M,V] (fp32 [M])."""
+    if x.dim() != 2:
+        raise ValueError("expected x [M,V]")
+    M, V = x.shape
+    if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous() or tuple(ids.shape) != (M,):
+        raise ValueError("ids must be a contiguous int32 CUDA tensor [M]")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=x.device)
+    if out.dtype != torch.float32 or not out.is_cuda or tuple(out.shape) != (M,):
+        raise ValueError("out must be an fp32 CUDA tensor [M]")
+    st = load().bi_token_logprobs_bf16(_dev(x, "x"), ids.data_ptr(), out.data_ptr(), M, V, _stream(stream))
+    _check(st, "bi_token_logprobs_bf16")
     return out
 
 

@@ -536,6 +536,40 @@ BI_API bi_status bi_residual_add_bf16(const void* a, const void* b, void* out, i
              : BI_ERR_CUDA;
 }
 
+namespace bi {
+namespace {
+bi_status check_logits(const void* X, const void* out, int64_t M, int64_t V) {
+  if (M < 0 || V < 1) return BI_ERR_INVALID_ARG;
+  if (V % 8 != 0 || V > 0x7FFFFFFFll || M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!X || !out) return BI_ERR_INVALID_ARG;
+  if (!aligned16(X)) return BI_ERR_ALIGNMENT;
+  return BI_OK;
+}
+}  // namespace
+}  // namespace bi
+
+BI_API bi_status bi_log_softmax_bf16(const void* X, float* Y, int64_t M, int64_t V, bi_stream_t stream) {
+  bi_status st = check_logits(X, Y, M, V);
+  if (st != BI_OK || M == 0) return st;
+  if (!aligned16(Y)) return BI_ERR_ALIGNMENT;
+  return launch_log_softmax(X, Y, M, V, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API bi_status bi_token_logprobs_bf16(const void* X, const int32_t* ids, float* out, int64_t M,
+                                        int64_t V, bi_stream_t stream) {
+  bi_status st = check_logits(X, out, M, V);
+  if (st != BI_OK || M == 0) return st;
+  if (!ids) return BI_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ids) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+    return BI_ERR_ALIGNMENT;
+  return launch_token_logprobs(X, ids, out, M, V, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
 BI_API bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I,
                                   bi_stream_t stream) {
   if (M < 0 || I < 1) return BI_ERR_INVALID_ARG;

@@ -100,6 +100,9 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
 cudaError_t launch_residual_add(const void* a, const void* b, void* out, int64_t count,
                                 cudaStream_t stream);
 cudaError_t launch_silu_mul(const void* gu, void* out, int64_t M, int64_t I, cudaStream_t stream);
+cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cudaStream_t stream);
+cudaError_t launch_token_logprobs(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
+                                  cudaStream_t stream);
 cudaError_t launch_attention_ctx1(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
                                   int64_t D, cudaStream_t stream);
 // Reads and clears the current device's stall word (asynchronously on

@@ -22,6 +22,9 @@ Pins (checks against things other than the oracle itself) live in
   - ``silu_mul``, ``residual_add``, ``attention_ctx1``, ``decode_layer``:
     pinned by closed forms (silu(0)=0, large-|x| limits, zero weights give the
     identity layer, selector weights route v exactly).
+  - ``log_softmax``, ``token_logprobs``: pinned by closed forms (uniform rows
+    give -log V, two-logit rows the stable softplus form), normalisation
+    (sum of exp = 1), shift invariance, -Inf entries and undefined rows.
 """
 from __future__ import annotations
 
@@ -42,6 +45,8 @@ _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _i64 = ctypes.c_int64
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i32p = ctypes.POINTER(ctypes.c_int32)
 
 
 def build(force: bool = False) -> str:
@@ -79,6 +84,8 @@ def _load():
             lib.oracle_decode_layer.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _u16p, _u16p, _u16p,
                                                 _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_float,
                                                 ctypes.c_int]
+            lib.oracle_log_softmax.argtypes = [_u16p, _f64p, _i64, _i64, ctypes.c_int]
+            lib.oracle_token_logprobs.argtypes = [_u16p, _i32p, _f64p, _i64, _i64, ctypes.c_int]
             lib.oracle_bf16_rne_array.argtypes = [_f32p, _u16p, _i64]
             lib.oracle_bf16_to_f32_array.argtypes = [_u16p, _f32p, _i64]
             _lib = lib
@@ -251,3 +258,29 @@ def stack(x, layers, nq: int, nkv: int, D: int, eps: float, nthreads: int | None
     for layer in layers:
         x = decode_layer(x, layer, nq, nkv, D, eps, nthreads)
     return x
+
+
+# --------------------------------------------------------------------------
+# lm_head log-probabilities
+# --------------------------------------------------------------------------
+
+def log_softmax(X, nthreads: int | None = None) -> np.ndarray:
+    """X [M,V] bf16 bits -> [M,V] float64 log-probabilities."""
+    x = _u16(X)
+    M, V = x.shape
+    out = np.empty((M, V), dtype=np.float64)
+    _load().oracle_log_softmax(_p16(x), out.ctypes.data_as(_f64p), M, V, nthreads or default_threads())
+    return out
+
+
+def token_logprobs(X, ids, nthreads: int | None = None) -> np.ndarray:
+    """X [M,V] bf16 bits, ids [M] int -> [M] float64 log-probabilities of the ids."""
+    x = _u16(X)
+    M, V = x.shape
+    i = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    if i.shape != (M,):
+        raise ValueError("ids must have shape [M]")
+    out = np.empty(M, dtype=np.float64)
+    _load().oracle_token_logprobs(_p16(x), i.ctypes.data_as(_i32p), out.ctypes.data_as(_f64p), M, V,
+                                  nthreads or default_threads())
+    return out

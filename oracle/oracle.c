@@ -24,6 +24,8 @@
  *     with one rounding to bf16 at the end.
  *   - The fused layer RMSNorm -> GEMM is the composition through the bf16
  *     normalised activations.
+ *   - Log-softmax of a row of bf16 logits (the lm_head's per-token
+ *     log-probabilities), in fp64: x_v - (max + log sum exp(x - max)).
  *   - One decode layer of a Llama-style stack (for the linear-stack
  *     workload): RMSNorm, qkv projection, an attention stand-in for context
  *     length 1 (softmax over one key is exactly 1, so each query head's output
@@ -330,6 +332,75 @@ int oracle_decode_layer(const uint16_t* x_in, uint16_t* x_out, const uint16_t* g
   }
   free(xn); free(qkv); free(att); free(o); free(h); free(hn); free(gu); free(s); free(d);
   return ok ? 0 : -1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Log-softmax over a row of logits (the lm_head's per-token log-probabilities)*/
+/* ------------------------------------------------------------------------ */
+
+/* One row of V bf16 logits -> V log-probabilities, in fp64:
+ *   m = max_v x_v,  s = sum_v exp(x_v - m) (ascending v),  lse = m + log(s),
+ *   out_v = x_v - lse.
+ * Detent, Sec. 8 (Table 6) and CoRun, Sec. IV compare such per-token
+ * log-probabilities bit for bit across batch sizes; the pages give no formula,
+ * so the definition above is the textbook one, in fp64.  Rows holding a NaN or
+ * a +Inf, and rows that are -Inf everywhere, have no defined distribution:
+ * every output is NaN.  Otherwise a -Inf logit has log-probability -Inf.
+ * Returns lse (NaN for the undefined rows). */
+static double log_softmax_row(const uint16_t* x, int64_t V, double* out) {
+  double m = -INFINITY;
+  int undefined = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    const double xv = (double)oracle_bf16_to_f32(x[v]);
+    if (isnan(xv) || xv == INFINITY) undefined = 1;
+    if (xv > m) m = xv;
+  }
+  if (m == -INFINITY) undefined = 1;
+  double lse = NAN;
+  if (!undefined) {
+    double sum = 0.0;
+    for (int64_t v = 0; v < V; ++v) sum += exp((double)oracle_bf16_to_f32(x[v]) - m);
+    lse = m + log(sum);
+  }
+  if (out) {
+    for (int64_t v = 0; v < V; ++v) out[v] = undefined ? NAN : (double)oracle_bf16_to_f32(x[v]) - lse;
+  }
+  return lse;
+}
+
+typedef struct {
+  const uint16_t* X;
+  const int32_t* ids;
+  double* out;
+  int64_t V;
+} lsm_ctx;
+
+static void lsm_range(void* p, int64_t lo, int64_t hi) {
+  lsm_ctx* c = (lsm_ctx*)p;
+  for (int64_t r = lo; r < hi; ++r) log_softmax_row(c->X + r * c->V, c->V, c->out + r * c->V);
+}
+
+/* X [M,V] bf16 logits -> out [M,V] fp64 log-probabilities. */
+void oracle_log_softmax(const uint16_t* X, double* out, int64_t M, int64_t V, int nthreads) {
+  lsm_ctx c = {X, NULL, out, V};
+  parallel_for(lsm_range, &c, M, nthreads);
+}
+
+static void tok_range(void* p, int64_t lo, int64_t hi) {
+  lsm_ctx* c = (lsm_ctx*)p;
+  for (int64_t r = lo; r < hi; ++r) {
+    const int32_t id = c->ids[r];
+    const double lse = log_softmax_row(c->X + r * c->V, c->V, NULL);
+    c->out[r] = (id < 0 || id >= c->V) ? NAN : (double)oracle_bf16_to_f32(c->X[r * c->V + id]) - lse;
+  }
+}
+
+/* out[r] = log-probability of token ids[r] in row r of X [M,V]; NaN for an id
+ * outside [0, V) (and for the undefined rows). */
+void oracle_token_logprobs(const uint16_t* X, const int32_t* ids, double* out, int64_t M, int64_t V,
+                           int nthreads) {
+  lsm_ctx c = {X, ids, out, V};
+  parallel_for(tok_range, &c, M, nthreads);
 }
 
 /* Array forms of the two conversions, for callers that hold whole tensors. */

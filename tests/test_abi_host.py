@@ -112,6 +112,14 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert lib.bi_residual_add_bf16(16, 32, 48, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_silu_mul_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_attention_ctx1_bf16(16, 32, 2, 6, 4, 8, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    # log-probabilities: V must be a multiple of 8; errors before any launch
+    assert lib.bi_log_softmax_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_log_softmax_bf16(16, 32, -1, 16, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_log_softmax_bf16(None, 32, 2, 16, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_log_softmax_bf16(8, 32, 2, 16, None) == bd.BI_ERR_ALIGNMENT
+    assert lib.bi_log_softmax_bf16(0, 0, 0, 16, None) == bd.BI_OK        # M = 0: nothing to do
+    assert lib.bi_token_logprobs_bf16(16, None, 32, 2, 16, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_token_logprobs_bf16(16, 34, 32, 2, 16, None) == bd.BI_ERR_ALIGNMENT
 
 
 ALL_M = list(range(1, 300)) + [511, 512, 513, 1000, 1023, 1024, 2048, 4095, 4096, 8191, 8192]

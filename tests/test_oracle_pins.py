@@ -440,3 +440,81 @@ def test_rmsnorm_single_final_rounding(oracle):
     g = inputs.bits(inputs.to_bf16(np.full(64, gv, dtype=np.float32)))
     Y = oracle.rmsnorm(X, g, EPS)
     assert np.all(Y == single) and single != double
+
+
+# --------------------------------------------------------------------------
+# log-softmax (lm_head log-probabilities)
+# --------------------------------------------------------------------------
+
+def lsm_rows(values) -> np.ndarray:
+    """Rows of exact bf16 values (given as floats) -> bf16 bits."""
+    a = np.asarray(values, dtype=np.float32)
+    bits = (a.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bf16_val(bits), a, equal_nan=True), "values must be exact in bf16"
+    return bits
+
+
+@pytest.mark.parametrize("V", [1, 2, 8, 1000, 128256])
+def test_log_softmax_uniform_row_is_minus_log_v(oracle, V):
+    for c in (0.0, 3.5, -1024.0):
+        out = oracle.log_softmax(lsm_rows(np.full((1, V), c)))
+        assert np.allclose(out, -math.log(V), rtol=0, atol=1e-15 * (abs(c) + math.log(V) + 1))
+
+
+def test_log_softmax_two_logits_softplus_form(oracle):
+    # log p(a) = -log(1 + e^(b - a)), written with log1p of the smaller
+    # exponential: independent of the max-shift formulation
+    for a, b in [(0.0, 0.0), (1.0, 0.0), (0.0, -7.5), (96.0, 100.0), (-3.25, 2.5)]:
+        out = oracle.log_softmax(lsm_rows([[a, b]]))[0]
+        hi, lo = max(a, b), min(a, b)
+        lse = hi + math.log1p(math.exp(lo - hi))
+        assert abs(out[0] - (a - lse)) <= 1e-14 * (1 + abs(lse))
+        assert abs(out[1] - (b - lse)) <= 1e-14 * (1 + abs(lse))
+
+
+def test_log_softmax_large_logits_do_not_overflow(oracle):
+    # exp(1000) overflows fp64: the max must be taken out before exp
+    out = oracle.log_softmax(lsm_rows([[1000.0, 992.0, -1000.0]]))[0]
+    lse = 1000.0 + math.log1p(math.exp(-8.0))
+    assert np.all(np.isfinite(out[:2]))
+    assert abs(out[0] + (lse - 1000.0)) < 1e-12 and abs(out[1] - (992.0 - lse)) < 1e-12
+
+
+def test_log_softmax_normalised_and_shift_invariant(oracle):
+    rng = np.random.default_rng(11)
+    V = 4096
+    base = np.clip(np.round(rng.normal(0, 6, size=(4, V))), -32, 31)   # integers: exact in bf16
+    out = oracle.log_softmax(lsm_rows(base))
+    assert np.all(np.abs(np.exp(out).sum(axis=1) - 1.0) < 1e-12)
+    shifted = oracle.log_softmax(lsm_rows(base + 32.0))          # integers 0..63: still exact
+    assert np.allclose(shifted, out, rtol=0, atol=1e-12)
+    assert np.all(out <= 0)
+    # monotone in the logit
+    order = np.argsort(base[0], kind="stable")
+    assert np.all(np.diff(out[0][order]) >= 0)
+
+
+def test_log_softmax_infinities_and_nan(oracle):
+    out = oracle.log_softmax(lsm_rows([[0.0, -np.inf, 0.0, -np.inf]]))[0]
+    assert out[1] == -np.inf and out[3] == -np.inf
+    assert abs(out[0] + math.log(2)) < 1e-15 and abs(out[2] + math.log(2)) < 1e-15
+    for row in ([np.nan, 0.0, 1.0, 2.0], [np.inf, 0.0, 1.0, 2.0], [-np.inf] * 4):
+        assert np.all(np.isnan(oracle.log_softmax(lsm_rows([row]))))
+
+
+def test_token_logprobs_pick_the_row_value(oracle):
+    rng = np.random.default_rng(12)
+    x = lsm_rows(np.round(rng.normal(0, 2, size=(5, 300)) * 8) / 8)
+    full = oracle.log_softmax(x)
+    ids = np.array([0, 299, 17, 150, 3])
+    assert np.array_equal(oracle.token_logprobs(x, ids), full[np.arange(5), ids])
+    bad = oracle.token_logprobs(x, np.array([-1, 300, 0, 0, 0]))
+    assert np.isnan(bad[0]) and np.isnan(bad[1]) and not np.isnan(bad[2])
+
+
+def test_log_softmax_rows_are_independent(oracle):
+    rng = np.random.default_rng(13)
+    x = lsm_rows(np.round(rng.normal(0, 2, size=(7, 512)) * 16) / 16)
+    full = oracle.log_softmax(x)
+    for r in range(7):
+        assert np.array_equal(oracle.log_softmax(x[r:r + 1])[0], full[r])
