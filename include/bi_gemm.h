@@ -282,10 +282,11 @@ bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t 
 
 /* Log-probabilities of rows of logits (the lm_head output X [M,V] bf16):
  *   Y[m,v] = x[m,v] - lse_m,  lse_m = max_v x[m,v] + log(sum_v exp(x[m,v] - max)),
- * in fp32, Y [M,V] fp32.  One CTA per row: thread t folds its 16-byte vectors
- * t, t + 512, ... in ascending order into a running (max, sum of exp) pair, and
- * the pairs combine by fixed xor butterflies within and across warps, so the
- * tree depends on V only.  expf / logf are CUDA's.  A row holding a NaN or a
+ * in fp32, Y [M,V] fp32.  A cluster of 8 CTAs of 512 threads per row: thread
+ * g of the cluster folds its 16-byte vectors g, g + 4096, ... in ascending
+ * order into a running (max, sum of exp) pair, and the pairs combine by fixed
+ * xor butterflies within warps, across warps and across the 8 CTAs (through
+ * distributed shared memory), so the tree depends on V only.  expf / logf are CUDA's.  A row holding a NaN or a
  * +Inf, or -Inf everywhere, gives NaN everywhere; otherwise a -Inf logit gives
  * -Inf.
  * Defines: Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock
