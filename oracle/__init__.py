@@ -25,6 +25,10 @@ Pins (checks against things other than the oracle itself) live in
   - ``log_softmax``, ``token_logprobs``: pinned by closed forms (uniform rows
     give -log V, two-logit rows the stable softplus form), normalisation
     (sum of exp = 1), shift invariance, -Inf entries and undefined rows.
+  - ``e4m3_encode``/``e4m3_decode``, ``quantize_rows_e4m3``, ``gemm_e4m3``:
+    pinned by hand-derived codes (1.0, 448, subnormals, ties, saturation,
+    NaN), the decode/encode round trip over all codes, exact scales for
+    power-of-two rows, and integer-exact GEMMs.
 """
 from __future__ import annotations
 
@@ -47,6 +51,7 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _i64 = ctypes.c_int64
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def build(force: bool = False) -> str:
@@ -86,6 +91,13 @@ def _load():
                                                 ctypes.c_int]
             lib.oracle_log_softmax.argtypes = [_u16p, _f64p, _i64, _i64, ctypes.c_int]
             lib.oracle_token_logprobs.argtypes = [_u16p, _i32p, _f64p, _i64, _i64, ctypes.c_int]
+            lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+            lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+            lib.oracle_e4m3_rne_sat.argtypes = [ctypes.c_float]
+            lib.oracle_quantize_rows_e4m3.argtypes = [_u16p, _u8p, _f32p, _i64, _i64, ctypes.c_int]
+            lib.oracle_gemm_e4m3.argtypes = [_u8p, _f32p, _u8p, _f32p, _f32p, _u16p, _i64, _i64, _i64,
+                                             ctypes.c_int]
             lib.oracle_bf16_rne_array.argtypes = [_f32p, _u16p, _i64]
             lib.oracle_bf16_to_f32_array.argtypes = [_u16p, _f32p, _i64]
             _lib = lib
@@ -284,3 +296,45 @@ def token_logprobs(X, ids, nthreads: int | None = None) -> np.ndarray:
     _load().oracle_token_logprobs(_p16(x), i.ctypes.data_as(_i32p), out.ctypes.data_as(_f64p), M, V,
                                   nthreads or default_threads())
     return out
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) with per-row scales
+# --------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    lib = _load()
+    return np.array([lib.oracle_e4m3_to_f32(int(v)) for v in c.ravel()], dtype=np.float32).reshape(c.shape)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    f = np.ascontiguousarray(np.asarray(values, dtype=np.float32))
+    lib = _load()
+    return np.array([lib.oracle_e4m3_rne_sat(float(v)) for v in f.ravel()], dtype=np.uint8).reshape(f.shape)
+
+
+def quantize_rows_e4m3(X, nthreads: int | None = None):
+    """X [M,K] bf16 bits -> (codes [M,K] uint8, scales [M] float32)."""
+    x = _u16(X)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    sc = np.empty(M, dtype=np.float32)
+    _load().oracle_quantize_rows_e4m3(_p16(x), q.ctypes.data_as(_u8p), _pf(sc), M, K,
+                                      nthreads or default_threads())
+    return q, sc
+
+
+def gemm_e4m3(Xq, sx, Wq, sw, nthreads: int | None = None):
+    """(fp32 unscaled sums [M,N], bf16 bits of the scaled result [M,N])."""
+    xq = np.ascontiguousarray(Xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    sxa = np.ascontiguousarray(sx, dtype=np.float32)
+    swa = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = xq.shape
+    N = wq.shape[0]
+    yf = np.empty((M, N), dtype=np.float32)
+    yb = np.empty((M, N), dtype=np.uint16)
+    _load().oracle_gemm_e4m3(xq.ctypes.data_as(_u8p), _pf(sxa), wq.ctypes.data_as(_u8p), _pf(swa), _pf(yf),
+                             _p16(yb), M, N, K, nthreads or default_threads())
+    return yf, yb

@@ -26,6 +26,8 @@
  *     normalised activations.
  *   - Log-softmax of a row of bf16 logits (the lm_head's per-token
  *     log-probabilities), in fp64: x_v - (max + log sum exp(x - max)).
+ *   - FP8 (E4M3) with per-token activation scales and per-channel weight
+ *     scales: per-row quantisation and the scaled GEMM.
  *   - One decode layer of a Llama-style stack (for the linear-stack
  *     workload): RMSNorm, qkv projection, an attention stand-in for context
  *     length 1 (softmax over one key is exactly 1, so each query head's output
@@ -401,6 +403,123 @@ void oracle_token_logprobs(const uint16_t* X, const int32_t* ids, double* out, i
                            int nthreads) {
   lsm_ctx c = {X, ids, out, V};
   parallel_for(tok_range, &c, M, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) with per-token activation scales and per-channel weight scales  */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3, the 8-bit format with 1 sign, 4 exponent (bias 7) and 3 mantissa
+ * bits: no infinities; S.1111.111 is NaN; the largest finite value is 448
+ * (S.1111.110); exponent field 0 holds the subnormals m/8 * 2^-6.  Decoding is
+ * exact in fp32. */
+float oracle_e4m3_to_f32(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const float v = e == 0 ? ldexpf((float)m, -9) : ldexpf(1.0f + (float)m / 8.0f, e - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+/* Round to nearest E4M3, ties to the even code (mantissa LSB 0), saturating
+ * at +-448; NaN gives 0x7F.  The 127 finite non-negative codes 0x00..0x7E
+ * increase with their value, so a binary search finds the two neighbours of
+ * |x| and the nearer one wins. */
+uint8_t oracle_e4m3_rne_sat(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  int lo = 0, hi = 0x7E;  /* value(lo) <= a < value(hi) */
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if ((double)oracle_e4m3_to_f32((uint8_t)mid) <= a) lo = mid; else hi = mid;
+  }
+  const double dl = a - (double)oracle_e4m3_to_f32((uint8_t)lo);
+  const double dh = (double)oracle_e4m3_to_f32((uint8_t)hi) - a;
+  int c;
+  if (dl < dh) c = lo;
+  else if (dh < dl) c = hi;
+  else c = (lo & 1) ? hi : lo;
+  return sign | (uint8_t)c;
+}
+
+/* Per-row (per-token, or per-channel for weights) quantisation of a bf16 row:
+ *   amax = max_k |x_k|;  scale = amax / 448 (fp32 division);
+ *   q_k = e4m3_rne_sat(x_k / scale) (fp32 division).
+ * amax == 0 gives scale 1 (and zero codes); a NaN or an infinity in the row
+ * gives scale NaN and NaN codes.  Detent, Limits: dynamic per-tensor FP8
+ * activation scales span the batch; per-token or static scales keep each
+ * row's bits its own. */
+static void quantize_row(const uint16_t* x, int64_t K, uint8_t* q, float* scale) {
+  float amax = 0.0f;
+  int bad = 0;
+  for (int64_t k = 0; k < K; ++k) {
+    const float v = fabsf(oracle_bf16_to_f32(x[k]));
+    if (!isfinite(v)) bad = 1;
+    else if (v > amax) amax = v;
+  }
+  if (bad) {
+    *scale = NAN;
+    for (int64_t k = 0; k < K; ++k) q[k] = 0x7F;
+    return;
+  }
+  const float s = amax == 0.0f ? 1.0f : amax / 448.0f;
+  *scale = s;
+  for (int64_t k = 0; k < K; ++k) q[k] = oracle_e4m3_rne_sat(oracle_bf16_to_f32(x[k]) / s);
+}
+
+typedef struct {
+  const uint16_t* X;
+  uint8_t* Q;
+  float* S;
+  int64_t K;
+} quant_ctx;
+
+static void quant_range(void* p, int64_t lo, int64_t hi) {
+  quant_ctx* c = (quant_ctx*)p;
+  for (int64_t r = lo; r < hi; ++r) quantize_row(c->X + r * c->K, c->K, c->Q + r * c->K, c->S + r);
+}
+
+/* X [M,K] bf16 -> Q [M,K] E4M3 codes, scale [M] fp32. */
+void oracle_quantize_rows_e4m3(const uint16_t* X, uint8_t* Q, float* scale, int64_t M, int64_t K,
+                               int nthreads) {
+  quant_ctx c = {X, Q, scale, K};
+  parallel_for(quant_range, &c, M, nthreads);
+}
+
+typedef struct {
+  const uint8_t *Xq, *Wq;
+  const float *sx, *sw;
+  float* Yf;
+  uint16_t* Yb;
+  int64_t N, K;
+} gemm8_ctx;
+
+/* One output element: acc = sum_k qx_k * qw_k in ascending k (each product of
+ * two E4M3 values has at most 8 significant bits, so it is exact in fp32;
+ * only the additions round); y = bf16_rne((acc * sx) * sw). */
+static void gemm8_range(void* p, int64_t lo, int64_t hi) {
+  gemm8_ctx* c = (gemm8_ctx*)p;
+  for (int64_t i = lo; i < hi; ++i) {
+    const int64_t m = i / c->N, n = i % c->N;
+    const uint8_t* x = c->Xq + m * c->K;
+    const uint8_t* w = c->Wq + n * c->K;
+    float acc = 0.0f;
+    for (int64_t k = 0; k < c->K; ++k) {
+      const float prod = oracle_e4m3_to_f32(x[k]) * oracle_e4m3_to_f32(w[k]);
+      acc = acc + prod;
+    }
+    if (c->Yf) c->Yf[i] = acc;
+    if (c->Yb) c->Yb[i] = oracle_bf16_rne((acc * c->sx[m]) * c->sw[n]);
+  }
+}
+
+/* Y [M,N] = bf16((Xq . Wq^T) * sx[m] * sw[n]); Yf (may be NULL) gets the
+ * unscaled fp32 sums. */
+void oracle_gemm_e4m3(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, float* Yf,
+                      uint16_t* Yb, int64_t M, int64_t N, int64_t K, int nthreads) {
+  gemm8_ctx c = {Xq, Wq, sx, sw, Yf, Yb, N, K};
+  parallel_for(gemm8_range, &c, M * N, nthreads);
 }
 
 /* Array forms of the two conversions, for callers that hold whole tensors. */

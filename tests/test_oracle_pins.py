@@ -518,3 +518,99 @@ def test_log_softmax_rows_are_independent(oracle):
     full = oracle.log_softmax(x)
     for r in range(7):
         assert np.array_equal(oracle.log_softmax(x[r:r + 1])[0], full[r])
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) with per-row scales
+# --------------------------------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    """Independent decoding from the format's fields (1 sign, 4 exponent bits
+    with bias 7, 3 mantissa bits; S.1111.111 is NaN; exponent 0: subnormal)."""
+    s, e, m = code >> 7, (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return math.nan
+    v = m / 8 * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+    return -v if s else v
+
+
+def test_e4m3_hand_derived_codes(oracle):
+    # (value, code): 1.0 = 1.000 x 2^0 -> 0.0111.000; 448 = 1.110 x 2^8 -> 0.1111.110; ties go to
+    # the even mantissa (1.0625 -> 1.000, 1.1875 -> 1.010); 2^-10 and 3 x 2^-10 are subnormal ties
+    cases = [(1.0, 0x38), (448.0, 0x7E), (500.0, 0x7E), (-448.0, 0xFE), (1e30, 0x7E), (-np.inf, 0xFE),
+             (0.5, 0x30), (2.0 ** -9, 0x01), (2.0 ** -6, 0x08), (1.0625, 0x38), (1.1875, 0x3A), (-0.0, 0x80),
+             (0.0, 0x00), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (240.0, 0x77), (416.0, 0x7D)]
+    got = oracle.e4m3_encode([v for v, _ in cases])
+    assert [int(g) for g in got] == [c for _, c in cases]
+    assert oracle.e4m3_encode([np.nan])[0] == 0x7F
+
+
+def test_e4m3_decode_matches_the_fields_and_round_trips(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    dec = oracle.e4m3_decode(codes)
+    for c in range(256):
+        want = e4m3_value(c)
+        if math.isnan(want):
+            assert math.isnan(dec[c])
+        else:
+            assert dec[c] == want and math.copysign(1, dec[c]) == math.copysign(1, want)
+    finite = [c for c in range(256) if not math.isnan(e4m3_value(c))]
+    assert [int(v) for v in oracle.e4m3_encode(dec[finite])] == finite
+    assert np.all(np.diff(dec[:0x7F]) > 0)          # codes 0..0x7E increase with their value
+    assert dec[0x7E] == 448.0
+
+
+def test_e4m3_rounding_is_nearest_even_by_brute_force(oracle):
+    rng = np.random.default_rng(31)
+    vals = np.concatenate([rng.uniform(-460, 460, 3000), rng.uniform(-0.05, 0.05, 2000)]).astype(np.float32)
+    got = oracle.e4m3_encode(vals)
+    table = [(c, e4m3_value(c)) for c in range(0x7F)]
+    for v, g in zip(vals, got):
+        a = abs(float(v))
+        if a >= 448:
+            want = 0x7E
+        else:
+            best = min(table, key=lambda cv: (abs(cv[1] - a), cv[0] & 1))
+            want = best[0]
+        if math.copysign(1, float(v)) < 0:
+            want |= 0x80
+        assert int(g) == want, (float(v), int(g), want)
+
+
+def test_quantize_rows_exact_scales(oracle):
+    # amax 448 -> scale 1; amax 224 -> scale 0.5 (x / 0.5 is exact); zero row -> scale 1
+    rows = np.zeros((4, 16), dtype=np.float32)
+    rows[0] = np.linspace(-448, 448, 16).round()
+    rows[1] = np.linspace(-224, 224, 16).round()
+    rows[3, 5] = np.inf
+    bits = (rows.view(np.uint32) >> 16).astype(np.uint16)
+    x = bf16_val(bits)
+    q, s = oracle.quantize_rows_e4m3(bits)
+    assert s[0] == 1.0 and s[1] == 0.5 and s[2] == 1.0 and np.isnan(s[3])
+    assert np.array_equal(q[0], oracle.e4m3_encode(x[0]))
+    assert np.array_equal(q[1], oracle.e4m3_encode(x[1] * 2))
+    assert np.all(q[2] == 0) and np.all(q[3] == 0x7F)
+    # the largest magnitude of a row lands on +-448
+    rng = np.random.default_rng(32)
+    X = inputs.normal((8, 300), std=3.0, seed=33, stream=0)
+    q, s = oracle.quantize_rows_e4m3(inputs.bits(X))
+    xv = X.float().numpy()
+    for r in range(8):
+        k = int(np.argmax(np.abs(xv[r])))
+        assert q[r, k] & 0x7F == 0x7E
+        assert s[r] == np.float32(np.float32(np.abs(xv[r]).max()) / np.float32(448.0))
+
+
+def test_gemm_e4m3_integer_exact(oracle):
+    # small-integer codes: every product and partial sum is an exact integer
+    rng = np.random.default_rng(34)
+    vx = rng.integers(-8, 9, size=(5, 96)).astype(np.float32)
+    vw = rng.integers(-8, 9, size=(7, 96)).astype(np.float32)
+    qx, qw = oracle.e4m3_encode(vx), oracle.e4m3_encode(vw)
+    sx = np.array([1.0, 0.5, 2.0, 0.25, 4.0], dtype=np.float32)
+    sw = np.array([1.0, 2.0, 0.5, 1.0, 0.125, 8.0, 1.0], dtype=np.float32)
+    yf, yb = oracle.gemm_e4m3(qx, sx, qw, sw)
+    exact = vx.astype(np.int64) @ vw.astype(np.int64).T
+    assert np.array_equal(yf, exact.astype(np.float32))
+    want = oracle.bf16_rne((exact * sx[:, None] * sw[None, :]).astype(np.float32))
+    assert np.array_equal(yb, want)
