@@ -10,8 +10,9 @@ The same JSON line also carries, unless switched off: "stack" (the 4-layer
 Llama-3.1-70B-shaped decode step at 32 tokens, us/step), "fused" (RMSNorm +
 the Llama-3.1-8B qkv and gate_up projections in one call, per M), "rmsnorm"
 (the RMSNorm token sweep at H = 4096 and 8192, GB/s) and "lm_head" (the
-Llama-3.1-8B lm_head with per-token log-probabilities), each against torch on
-the same tensors.
+Llama-3.1-8B lm_head with per-token log-probabilities) and "fp8" (the
+down_proj shape in E4M3 with per-token scales), each against torch on the
+same tensors.
 
 L2 handling: every launch reads a weight copy that was not read by the
 previous launches (enough copies that they exceed the 129 MB L2), and
@@ -545,6 +546,52 @@ def run_lm_head(args, dist, peaks):
                         "M in 1, 32, 256; against torch.mm + log_softmax + gather", "sweep": res}
 
 
+def run_fp8(args, dist, peaks):
+    """FP8 (E4M3, per-token and per-channel scales) on the down_proj shape:
+    bi_quantize_rows_e4m3 of the activations + bi_gemm_fp8, against torch.mm
+    in bf16 on the unquantised tensors.  Peak: the measured bf16 burst peak x 2,
+    the nominal FP8 / bf16 ratio of dense tensor throughput."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    dev = torch.device("cuda", dist.local_rank)
+    N, K = DOWN_N, DOWN_K
+    nw = copies_for(N * K, cap=6)
+    Ws = [inputs.device_normal((N, K), std=0.02, seed=dist.rank, stream=inputs.STREAM_W + 16 * i, device=dev)
+          for i in range(nw)]
+    wq = [bd.bi_quantize_rows_e4m3(w) for w in Ws]
+    pins = bd.bi_pins_default_fp8(N, K)
+    pins = pins.replace(flags=pins.flags | bd.BI_FLAG_PREFETCH_W)
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    baseline = "torch.mm in bf16 on the unquantised tensors"
+    res = []
+    for M in (1, 128, 512, 2048, 8192):
+        nx = copies_for(M * K * 2, cap=8)
+        xs = [inputs.device_normal((M, K), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
+              for i in range(nx)]
+        xq = [bd.bi_quantize_rows_e4m3(x) for x in xs]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        us_gemm = time_reps(lambda i: bd.bi_gemm_fp8(xq[i % nx][0], xq[i % nx][1], wq[i % nw][0], wq[i % nw][1],
+                                                     out=y, pins=pins), args.per_m_reps)
+        qbuf = (torch.empty((M, K), dtype=torch.uint8, device=dev), torch.empty(M, dtype=torch.float32, device=dev))
+
+        def layer(i):
+            q, sxv = bd.bi_quantize_rows_e4m3(xs[i % nx], q=qbuf[0], scale=qbuf[1])
+            bd.bi_gemm_fp8(q, sxv, wq[i % nw][0], wq[i % nw][1], out=y, pins=pins)
+        us_layer = time_reps(layer, args.per_m_reps)
+        tus = time_reps(lambda i: torch.mm(xs[i % nx], Ws[i % nw].t(), out=y), args.per_m_reps)
+        f = 2.0 * M * N * K
+        b = float(N * K + M * K + 2 * M * N + 4 * (M + N))
+        t_roof = max(f / (peak8 * 1e6), b / (peaks["hbm_gbs"] * 1e3))
+        res.append({"M": M, "gemm_us": round(us_gemm, 2), "tflops": round(f / us_gemm / 1e6, 1),
+                    "roofline_frac": round(t_roof / us_gemm, 3), "quantize_and_gemm_us": round(us_layer, 2),
+                    "baseline_us": round(tus, 2), "vs_baseline": round(tus / us_gemm, 3)})
+        del xs, xq
+    del Ws, wq
+    torch.cuda.empty_cache()
+    return {"workload": "FP8 E4M3 down_proj W[4096,14336], per-token activation and per-channel weight scales",
+            "peak_tflops": peak8, "peak_source": "measured bf16 burst x 2 (nominal FP8 / bf16 ratio)",
+            "baseline": baseline, "sweep": res}
+
+
 def time_steps(fn, steps, dist):
     dist.barrier()
     torch.cuda.synchronize()
@@ -687,6 +734,8 @@ def run_ours(args, dist):
         result["rmsnorm"] = run_rmsnorm(args, dist, peaks)
     if not args.no_lm_head:
         result["lm_head"] = run_lm_head(args, dist, peaks)
+    if not args.no_fp8:
+        result["fp8"] = run_fp8(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -751,6 +800,7 @@ def main():
     ap.add_argument("--no-fused", action="store_true")
     ap.add_argument("--no-rmsnorm", action="store_true")
     ap.add_argument("--no-lm-head", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
     ap.add_argument("--single-m", type=int, default=0,
                     help="profiling helper: only launch the sweep's GEMM at this M --launches times")

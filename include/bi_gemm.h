@@ -280,6 +280,44 @@ bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I, bi_s
 bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
                                  int64_t D, bi_stream_t stream);
 
+/* ---- FP8 (E4M3) with per-token and per-channel scales ---------------------
+ * Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock Speed),
+ * Limits: dynamic per-tensor FP8 activation scales span the batch; per-token
+ * (or static) scales keep each row's bits its own.  The pages give no format:
+ * E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite
+ * value 448, no infinities) with a per-row scale amax / 448. */
+
+/* Per-row quantisation: for each row of X [M,K] bf16, amax = max |x|,
+ * scale[m] = amax / 448 (IEEE division; 1 for a zero row), Q[m,k] =
+ * E4M3(x / scale[m]) rounded to nearest even, saturated at +-448.  A row with
+ * a NaN or an infinity gets scale NaN and NaN codes (0x7F).  Used for the
+ * activations (per token) and, offline, for the weights (per output channel).
+ * Q: uint8 [M,K]; scale: fp32 [M].
+ * Requirements: K % 16 == 0, X and Q 16-byte aligned, scale 4-byte aligned.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_CUDA. */
+bi_status bi_quantize_rows_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                bi_stream_t stream);
+
+/* Pins of the FP8 GEMM: as bi_pins_default / bi_pins_validate with bk = 128
+ * (a K tile is 128 E4M3 values, the same 128 bytes) and tok_tile = 256. */
+bi_status bi_pins_default_fp8(int64_t N, int64_t K, bi_pins* out);
+bi_status bi_pins_validate_fp8(int64_t N, int64_t K, const bi_pins* pins);
+bi_status bi_gemm_plan_describe_fp8(int64_t M, int64_t N, int64_t K, const bi_pins* pins,
+                                    int32_t sm_count, bi_gemm_plan* plan);
+
+/* Y[M,N] = bf16_rne((acc[m,n] * sx[m]) * sw[n]),  acc = Xq . Wq^T with fp32
+ * accumulation on the tensor cores (tcgen05.mma kind::f8f6f4, 32 K values per
+ * step).  Xq [M,K] and Wq [N,K] are E4M3 codes (bi_quantize_rows_e4m3), sx [M]
+ * and sw [N] their scales.  The reduction tree is the bf16 GEMM's -- K tiles,
+ * split count and boundaries, fold order, all fixed by (N, K, pins) -- and the
+ * scales touch only the finished sum of their own row and column.
+ * Requirements: K % 16 == 0, Xq, Wq, Y 16-byte aligned, sx and sw 4-byte
+ * aligned, M, N, K < 2^31.  pins NULL = bi_pins_default_fp8(N, K).
+ * Errors: as bi_gemm_bf16. */
+bi_status bi_gemm_fp8(const void* Xq, const float* sx, const void* Wq, const float* sw, void* Y,
+                      int64_t M, int64_t N, int64_t K, const bi_pins* pins, bi_stream_t stream);
+
 /* Log-probabilities of rows of logits (the lm_head output X [M,V] bf16):
  *   Y[m,v] = x[m,v] - lse_m,  lse_m = max_v x[m,v] + log(sum_v exp(x[m,v] - max)),
  * in fp32, Y [M,V] fp32.  A cluster of 8 CTAs of 512 threads per row: thread

@@ -118,6 +118,12 @@ _SIGNATURES = {
     "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "bi_last_device_status": (ctypes.c_int, [_vp]),
     "bi_log_softmax_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
+    "bi_quantize_rows_e4m3": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp]),
+    "bi_pins_default_fp8": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(Pins)]),
+    "bi_pins_validate_fp8": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(Pins)]),
+    "bi_gemm_plan_describe_fp8": (ctypes.c_int, [_i64, _i64, _i64, ctypes.POINTER(Pins), ctypes.c_int32,
+                                                 ctypes.POINTER(Plan)]),
+    "bi_gemm_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
     "bi_token_logprobs_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp]),
 }
 
@@ -300,6 +306,67 @@ def bi_residual_add_bf16(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | N
     st = load().bi_residual_add_bf16(_dev(a, "a"), _dev(b, "b"), _dev(out, "out", a.shape), a.numel(),
                                      _stream(stream))
     _check(st, "bi_residual_add_bf16")
+    return out
+
+
+def _dev_as(t: torch.Tensor, name: str, dtype, shape) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous %s CUDA tensor" % (name, dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+def bi_quantize_rows_e4m3(x: torch.Tensor, q: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                          stream=None):
+    """Per-row E4M3 codes (uint8 [M,K]) and scales (fp32 [M]) of x [M,K] bf16."""
+    if x.dim() != 2:
+        raise ValueError("expected x [M,K]")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    st = load().bi_quantize_rows_e4m3(_dev(x, "x"), _dev_as(q, "q", torch.uint8, (M, K)),
+                                      _dev_as(scale, "scale", torch.float32, (M,)), M, K, _stream(stream))
+    _check(st, "bi_quantize_rows_e4m3")
+    return q, scale
+
+
+def bi_pins_default_fp8(N: int, K: int) -> Pins:
+    p = Pins()
+    _check(load().bi_pins_default_fp8(N, K, ctypes.byref(p)), "bi_pins_default_fp8")
+    return p
+
+
+def bi_pins_validate_fp8(N: int, K: int, pins: Pins) -> int:
+    return load().bi_pins_validate_fp8(N, K, ctypes.byref(pins))
+
+
+def bi_gemm_plan_describe_fp8(M: int, N: int, K: int, pins: Pins | None = None, sm_count: int = 0) -> Plan:
+    plan = Plan()
+    st = load().bi_gemm_plan_describe_fp8(M, N, K, ctypes.byref(pins) if pins is not None else None, sm_count,
+                                          ctypes.byref(plan))
+    _check(st, "bi_gemm_plan_describe_fp8")
+    return plan
+
+
+def bi_gemm_fp8(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                out: torch.Tensor | None = None, pins: Pins | None = None, stream=None) -> torch.Tensor:
+    """Y = bf16((Xq . Wq^T) * sx[m] * sw[n]); xq [M,K], wq [N,K] uint8 E4M3 codes."""
+    if xq.dim() != 2 or wq.dim() != 2 or xq.shape[1] != wq.shape[1]:
+        raise ValueError("expected xq [M,K] and wq [N,K]")
+    M, K = xq.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    st = load().bi_gemm_fp8(_dev_as(xq, "xq", torch.uint8, (M, K)), _dev_as(sx, "sx", torch.float32, (M,)),
+                            _dev_as(wq, "wq", torch.uint8, (N, K)), _dev_as(sw, "sw", torch.float32, (N,)),
+                            _dev(out, "out", (M, N)), M, N, K,
+                            ctypes.byref(pins) if pins is not None else None, _stream(stream))
+    _check(st, "bi_gemm_fp8")
+    if _call_hooks:
+        _report(M, N, K)
     return out
 
 

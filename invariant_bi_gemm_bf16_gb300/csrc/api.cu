@@ -67,9 +67,16 @@ int32_t rule_split(int64_t N, int64_t K) {
   return best;
 }
 
-bi_status check_nk(int64_t N, int64_t K) {
+// Operand type of a GEMM.  A K tile is 128 bytes of a row either way: 64 bf16
+// or 128 E4M3 values.
+enum class Elem { BF16, E4M3 };
+constexpr int tile_elems(Elem e) { return e == Elem::E4M3 ? 128 : kBK; }
+constexpr int elem_bytes(Elem e) { return e == Elem::E4M3 ? 1 : 2; }
+
+// K must give 16-byte rows (the tensor-memory copies' row pitch).
+bi_status check_nk(int64_t N, int64_t K, Elem e = Elem::BF16) {
   if (N < 1 || K < 1) return BI_ERR_INVALID_ARG;
-  if (K % 8 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
+  if ((K * elem_bytes(e)) % 16 != 0) return BI_ERR_UNSUPPORTED_SHAPE;
   if (N > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
   return BI_OK;
 }
@@ -78,6 +85,7 @@ struct Resolved {
   int32_t S, T, ctas, w_pin;
   uint32_t flags;
   int64_t KT;
+  Elem elem;
 };
 
 // K tiles per copy for a launch with token tile T and CTA grouping ctas: 2
@@ -86,11 +94,11 @@ struct Resolved {
 // rings would hold only two X stages of two tiles, which measured slower.)
 // Launches whose X copies cover fewer rows than the token tile use 1
 // (make_plan).
-int pins_kps(int64_t K, int32_t T, int32_t ctas, uint32_t flags) {
-  return ((flags & BI_FLAG_KTILE_PAIRS) && K % kBK == 0 && T == 256 && ctas == 2) ? 2 : 1;
+int pins_kps(int64_t K, int32_t T, int32_t ctas, uint32_t flags, Elem e = Elem::BF16) {
+  return ((flags & BI_FLAG_KTILE_PAIRS) && K % tile_elems(e) == 0 && T == 256 && ctas == 2) ? 2 : 1;
 }
 
-bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r);
+bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r, Elem e = Elem::BF16);
 
 // Which device function pointer encodes tensor maps (driver entry point).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -119,28 +127,28 @@ EncodeTiledFn encode_fn() {
 // shared memory, each box_rows x 128 bytes.  Without K % 64 == 0 the 3-D view
 // would read a partial last K tile's tail from the next row instead of zeros.
 bool encode_kmajor(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows,
-                   bool view3d, int kps) {
+                   bool view3d, int kps, Elem e = Elem::BF16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const CUtensorMapDataType dt = e == Elem::E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int64_t te = tile_elems(e), eb = elem_bytes(e);
   CUresult r;
   if (!view3d) {
     if (kps != 1) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K * eb)};
+    cuuint32_t box[2] = {(cuuint32_t)te, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    if (K % kBK != 0) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(K / kBK)};
-    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kBK * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kps};
+    if (K % te != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)te, (cuuint64_t)rows, (cuuint64_t)(K / te)};
+    cuuint64_t strides[2] = {(cuuint64_t)(K * eb), (cuuint64_t)(te * eb)};
+    cuuint32_t box[3] = {(cuuint32_t)te, (cuuint32_t)box_rows, (cuuint32_t)kps};
     cuuint32_t estr[3] = {1, 1, 1};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   return r == CUDA_SUCCESS;
 }
@@ -246,13 +254,13 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   Resolved r = pinned;
   const LaunchChoice choice = choose_launch(M, N, r, sm_count);
   r.ctas = choice.ctas;
-  plan->bk = kBK;
+  plan->bk = tile_elems(r.elem);
   plan->split_k = r.S;
   plan->tok_tile = r.T;
   plan->mma_ctas = r.ctas;
   plan->mma_m = kTileN * r.ctas;
   plan->mma_n = r.T;
-  plan->mma_k = kMmaK;
+  plan->mma_k = r.elem == Elem::E4M3 ? 2 * kMmaK : kMmaK;
   plan->k_tiles = r.KT;
   for (int s = 0; s <= r.S; ++s) plan->split_begin[s] = ((int64_t)s * r.KT) / r.S;
   plan->n_tiles = ceil_div(N, plan->mma_m);
@@ -266,7 +274,7 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   if (plan->x_box_rows > x_rows) plan->x_box_rows = x_rows;
   // a short X box keeps one K tile per copy: each K tile of X must start
   // x_rows rows after the previous one in shared memory
-  plan->kps = plan->x_box_rows == x_rows ? pins_kps(K, r.T, r.ctas, r.flags) : 1;
+  plan->kps = plan->x_box_rows == x_rows ? pins_kps(K, r.T, r.ctas, r.flags, r.elem) : 1;
   choose_stages(x_rows, plan->x_box_rows, r.w_pin, plan->kps, &plan->w_stages, &plan->x_stages);
   plan->block_threads = kGemmThreads;
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
@@ -298,13 +306,14 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   return BI_OK;
 }
 
-bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
+bi_status validate(int64_t N, int64_t K, const bi_pins* p, Elem e = Elem::BF16) {
   if (!p) return BI_ERR_INVALID_ARG;
-  bi_status st = check_nk(N, K);
+  bi_status st = check_nk(N, K, e);
   if (st != BI_OK) return st;
-  const int64_t kt = ceil_div(K, kBK);
+  const int64_t kt = ceil_div(K, tile_elems(e));
   if (p->abi_version != BI_PINS_ABI_VERSION) return BI_ERR_ILLEGAL_PINS;
-  if (p->bk != kBK) return BI_ERR_ILLEGAL_PINS;
+  if (p->bk != tile_elems(e)) return BI_ERR_ILLEGAL_PINS;
+  if (e == Elem::E4M3 && p->tok_tile != 256) return BI_ERR_ILLEGAL_PINS;
   if (p->split_k < 1 || p->split_k > BI_MAX_SPLIT_K || p->split_k > kt) return BI_ERR_ILLEGAL_PINS;
   if (p->tok_tile != 64 && p->tok_tile != 128 && p->tok_tile != 256) return BI_ERR_ILLEGAL_PINS;
   if (p->mma_ctas < 0 || p->mma_ctas > 2) return BI_ERR_ILLEGAL_PINS;
@@ -314,7 +323,7 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
     if (p->stages < 2) return BI_ERR_ILLEGAL_PINS;
     for (int32_t ctas = 1; ctas <= 2; ++ctas) {
       if (p->mma_ctas != 0 && p->mma_ctas != ctas) continue;
-      const int kps = pins_kps(K, p->tok_tile, ctas, p->flags);
+      const int kps = pins_kps(K, p->tok_tile, ctas, p->flags, e);
       if (p->stages > max_w_stages(p->tok_tile / ctas, 2, kps)) return BI_ERR_ILLEGAL_PINS;
     }
   }
@@ -330,9 +339,9 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p) {
   return BI_OK;
 }
 
-bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
+bi_status pins_default(int64_t N, int64_t K, bi_pins* out, Elem e = Elem::BF16) {
   if (!out) return BI_ERR_INVALID_ARG;
-  bi_status st = check_nk(N, K);
+  bi_status st = check_nk(N, K, e);
   if (st != BI_OK) return st;
   int32_t S = 0, T = 256, ctas = 0;
   for (const TableEntry& e : kTable) {
@@ -344,10 +353,11 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
     }
   }
   if (S == 0) S = rule_split(N, K);
-  const int64_t kt = ceil_div(K, kBK);
+  const int64_t kt = ceil_div(K, tile_elems(e));
   if (S > kt) S = (int32_t)kt;
+  if (e == Elem::E4M3) T = 256;
   out->abi_version = BI_PINS_ABI_VERSION;
-  out->bk = kBK;
+  out->bk = tile_elems(e);
   out->split_k = S;
   out->tok_tile = T;
   out->mma_ctas = ctas;
@@ -356,29 +366,30 @@ bi_status pins_default(int64_t N, int64_t K, bi_pins* out) {
   return BI_OK;
 }
 
-bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r) {
+bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r, Elem e) {
   bi_pins p;
   if (pins) {
     p = *pins;
   } else {
-    bi_status st = pins_default(N, K, &p);
+    bi_status st = pins_default(N, K, &p, e);
     if (st != BI_OK) return st;
   }
-  bi_status st = validate(N, K, &p);
+  bi_status st = validate(N, K, &p, e);
   if (st != BI_OK) return st;
   r->S = p.split_k;
   r->T = p.tok_tile;
   r->ctas = p.mma_ctas;
   r->w_pin = p.stages;
   r->flags = p.flags;
-  r->KT = ceil_div(K, kBK);
+  r->KT = ceil_div(K, tile_elems(e));
+  r->elem = e;
   return BI_OK;
 }
 
 bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M, int64_t N,
-                          int64_t K) {
+                          int64_t K, Elem e = Elem::BF16) {
   if (M < 0) return BI_ERR_INVALID_ARG;
-  bi_status st = check_nk(N, K);
+  bi_status st = check_nk(N, K, e);
   if (st != BI_OK) return st;
   if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return BI_OK;
@@ -388,11 +399,16 @@ bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M
 }
 
 bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
-                    const bi_pins* pins, cudaStream_t stream) {
-  bi_status st = check_gemm_args(X, W, Y, M, N, K);
+                    const bi_pins* pins, cudaStream_t stream, Elem e = Elem::BF16,
+                    const float* sx = nullptr, const float* sw = nullptr) {
+  bi_status st = check_gemm_args(X, W, Y, M, N, K, e);
   if (st != BI_OK) return st;
+  if (e == Elem::E4M3 && M > 0) {
+    if (!sx || !sw) return BI_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(sx) & 3u) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return BI_ERR_ALIGNMENT;
+  }
   Resolved r;
-  st = resolve_pins(N, K, pins, &r);
+  st = resolve_pins(N, K, pins, &r, e);
   if (st != BI_OK) return st;
   if (M == 0) return BI_OK;
   bi_gemm_plan plan;
@@ -401,8 +417,11 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
   const bool map3d = plan.kps > 1;
-  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, plan.kps)) return BI_ERR_CUDA;
-  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, plan.kps)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, plan.kps, e)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, plan.kps, e)) return BI_ERR_CUDA;
+  L.fp8 = e == Elem::E4M3;
+  L.sx = sx;
+  L.sw = sw;
   L.Y = Y;
   L.M = M;
   L.N = N;
@@ -491,6 +510,43 @@ BI_API bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi
 BI_API bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                               const bi_pins* pins, bi_stream_t stream) {
   return gemm_impl(X, W, Y, M, N, K, pins, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_pins_default_fp8(int64_t N, int64_t K, bi_pins* out) {
+  return pins_default(N, K, out, Elem::E4M3);
+}
+
+BI_API bi_status bi_pins_validate_fp8(int64_t N, int64_t K, const bi_pins* pins) {
+  return validate(N, K, pins, Elem::E4M3);
+}
+
+BI_API bi_status bi_gemm_plan_describe_fp8(int64_t M, int64_t N, int64_t K, const bi_pins* pins,
+                                           int32_t sm_count, bi_gemm_plan* plan) {
+  if (!plan) return BI_ERR_INVALID_ARG;
+  if (M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K, Elem::E4M3);
+  if (st != BI_OK) return st;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r, Elem::E4M3);
+  if (st != BI_OK) return st;
+  return make_plan(M, N, K, r, sm_count > 0 ? sm_count : kDefaultSmCount, plan);
+}
+
+BI_API bi_status bi_gemm_fp8(const void* Xq, const float* sx, const void* Wq, const float* sw, void* Y,
+                             int64_t M, int64_t N, int64_t K, const bi_pins* pins, bi_stream_t stream) {
+  return gemm_impl(Xq, Wq, Y, M, N, K, pins, reinterpret_cast<cudaStream_t>(stream), Elem::E4M3, sx, sw);
+}
+
+BI_API bi_status bi_quantize_rows_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                       bi_stream_t stream) {
+  if (M < 0 || K < 1) return BI_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > 0x7FFFFFFFll || M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!X || !Q || !scale) return BI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q) || (reinterpret_cast<uintptr_t>(scale) & 3u)) return BI_ERR_ALIGNMENT;
+  return launch_quantize_e4m3(X, Q, scale, M, K, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
 }
 
 BI_API bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t M, int64_t H,

@@ -62,6 +62,8 @@ struct GemmParams {
   int32_t w_stages, x_stages, x_box_rows;
   int32_t group_n;  // LOCAL tile order: groups of group_n W tiles (speed only)
   int32_t units;    // CLUSTER: units (CTAs or pairs) per tile; S (one split each) or ceil(S/2)
+  const float* sx;  // FP8: per-token scales [M]
+  const float* sw;  // FP8: per-channel scales [N]
   uint32_t flags;  // BI_FLAG_DEBUG_STALL_PRODUCER | kFlagStreamW | kFlagZeroX
 };
 
@@ -145,7 +147,10 @@ __device__ __forceinline__ void tile_coords(int64_t t, int32_t n_tiles, int32_t 
 // The MMAs consume the K tiles of a stage one after the other, so KP never
 // changes the reduction; it halves the waits and commits per MMA of the
 // issuing thread, which at T = 256 runs close to the tensor pipe's rate.
-template <int T, bool CLUSTER, bool PAIR, int KP>
+// FP8: E4M3 operands (kind::f8f6f4); a K tile is then 128 values (still 128
+// bytes), and the epilogue scales the fp32 result by sx[m] and then sw[n]
+// before rounding to bf16.
+template <int T, bool CLUSTER, bool PAIR, int KP, bool FP8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     bi_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
@@ -153,6 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int kXTile = kXRows * kBK * 2;          // one K tile of X
   constexpr int kXStage = KP * kXTile;
   constexpr int kWStage = KP * kWStageBytes;
+  constexpr int kTileElems = FP8 ? 128 : kBK;       // K values per K tile
   constexpr int kMmaM = PAIR ? 2 * kTileN : kTileN;  // W rows per tile
   constexpr uint32_t kTmemCols = 2u * (uint32_t)T;    // two accumulators
   constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quadrant
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!(stall && issued == 0)) {
               const uint32_t full = smem_u32(&full_bar[stage]);
               const uint32_t dst = ring + (uint32_t)stage * stage_sz;
-              const int32_t kx = (int32_t)(kt * kBK);  // 2-D maps: element column
+              const int32_t kx = (int32_t)(kt * kTileElems);  // 2-D maps: element column
               const int32_t kz = (int32_t)kt;          // 3-D maps: K tile index
               if constexpr (PAIR) {
                 const uint32_t bar = leader ? full : mapa_shared(full, leader_rank);
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = make_idesc_bf16(kMmaM, T);
+      constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(kMmaM, T) : make_idesc_bf16(kMmaM, T);
       int wi = 0, xi = 0;
       uint32_t wph = 0, xph = 0;
       uint32_t acc_iter = 0;
@@ -385,8 +391,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint64_t da = (uint64_t)(sub * (kWStageBytes >> 4) + 2 * j);
                 const uint64_t db = (uint64_t)(sub * (kXTile >> 4) + 2 * j);
                 const uint32_t acc = (kt > k0 || sub > 0 || j > 0) ? 1u : 0u;
-                if constexpr (PAIR)
+                if constexpr (PAIR && FP8)
+                  mma_e4m3_pair(d_tmem, a_desc + da, b_desc + db, idesc, acc);
+                else if constexpr (PAIR)
                   mma_bf16_pair(d_tmem, a_desc + da, b_desc + db, idesc, acc);
+                else if constexpr (FP8)
+                  mma_e4m3(d_tmem, a_desc + da, b_desc + db, idesc, acc);
                 else
                   mma_bf16(d_tmem, a_desc + da, b_desc + db, idesc, acc);
               }
@@ -479,9 +489,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __nv_bfloat16* y = p.Y + m0 * p.N + n;
           const int64_t mrem = p.M - m0;
           const int mv = mrem < kHalf ? (int)mrem : kHalf;
+          const float swn = FP8 ? p.sw[n] : 1.0f;
 #pragma unroll
           for (int j = 0; j < kHalf; ++j) {
-            if (j < mv) *y = __float2bfloat16_rn(R[j]);
+            if (j < mv) *y = __float2bfloat16_rn(FP8 ? __fmul_rn(__fmul_rn(R[j], p.sx[m0 + j]), swn) : R[j]);
             y += p.N;
           }
         }
@@ -561,9 +572,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (last) {
             if (n < p.N) {
               __nv_bfloat16* y = p.Y + (m0 + c) * p.N + n;
+              const float swn = FP8 ? p.sw[n] : 1.0f;
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                if (c + i < mv) y[(int64_t)i * p.N] = __float2bfloat16_rn(v[i]);
+                if (c + i < mv)
+                  y[(int64_t)i * p.N] = __float2bfloat16_rn(
+                      FP8 ? __fmul_rn(__fmul_rn(v[i], p.sx[m0 + c + i]), swn) : v[i]);
             }
           } else {
 #pragma unroll
@@ -614,6 +628,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         r.y = __fadd_rn(r.y, v.y);
       }
       __nv_bfloat16* y = p.Y + (m0 + j) * p.N + n0 + n;
+      if constexpr (FP8) {
+        const float sxm = p.sx[m0 + j];
+        r.x = __fmul_rn(__fmul_rn(r.x, sxm), p.sw[n0 + n]);
+        if (n + 1 < nv) r.y = __fmul_rn(__fmul_rn(r.y, sxm), p.sw[n0 + n + 1]);
+      }
       if (even_n && n + 1 < nv) {
         *reinterpret_cast<__nv_bfloat162*>(y) = __floats2bfloat162_rn(r.x, r.y);
       } else {
@@ -666,9 +685,9 @@ int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, int kps, 
   return 1024 + (ring > part ? ring : part) + kCtlBytes;
 }
 
-template <int T, bool CLUSTER, bool PAIR, int KP>
+template <int T, bool CLUSTER, bool PAIR, int KP, bool FP8 = false>
 static cudaError_t launch_t(const GemmLaunch& L) {
-  auto kern = bi_gemm_kernel<T, CLUSTER, PAIR, KP>;
+  auto kern = bi_gemm_kernel<T, CLUSTER, PAIR, KP, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   if (e != cudaSuccess) return e;
   const int cluster = CLUSTER ? L.units * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
@@ -689,6 +708,8 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   prm.x_box_rows = L.x_box_rows;
   prm.group_n = L.group_n;
   prm.units = L.units;
+  prm.sx = L.sx;
+  prm.sw = L.sw;
   prm.flags = L.flags;
 
   cudaLaunchConfig_t cfg = {};
@@ -715,6 +736,12 @@ static cudaError_t launch_t(const GemmLaunch& L) {
 
 template <bool PAIR>
 static cudaError_t launch_p(const GemmLaunch& L) {
+  if (L.fp8) {  // E4M3 operands: T = 256 only
+    if (L.T != 256) return cudaErrorInvalidValue;
+    if (L.kps == 2)
+      return L.cluster ? launch_t<256, true, PAIR, 2, true>(L) : launch_t<256, false, PAIR, 2, true>(L);
+    return L.cluster ? launch_t<256, true, PAIR, 1, true>(L) : launch_t<256, false, PAIR, 1, true>(L);
+  }
   switch (L.T) {
     case 64:
       if (L.kps != 1) return cudaErrorInvalidValue;

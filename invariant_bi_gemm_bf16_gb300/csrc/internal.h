@@ -51,6 +51,9 @@ struct GemmLaunch {
   int32_t kps;       // K tiles per copy: 1 (2-D maps) or 2 (3-D maps, T = 256 only)
   int32_t group_n;   // LOCAL tile order: W tiles per group (1 .. n_tiles)
   int32_t units;     // CLUSTER: units (CTAs or pairs) per tile: S, or ceil(S/2) when chained
+  bool fp8;          // E4M3 operands (kind::f8f6f4), K tiles of 128 values; Y scaled by sx, sw
+  const float* sx;   // fp8: per-token scales [M]
+  const float* sw;   // fp8: per-channel scales [N]
   bool cluster;      // one chain per CTA (pair), folded through DSMEM
   bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;
@@ -100,6 +103,8 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
 cudaError_t launch_residual_add(const void* a, const void* b, void* out, int64_t count,
                                 cudaStream_t stream);
 cudaError_t launch_silu_mul(const void* gu, void* out, int64_t M, int64_t I, cudaStream_t stream);
+cudaError_t launch_quantize_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                 cudaStream_t stream);
 cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cudaStream_t stream);
 cudaError_t launch_token_logprobs(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
                                   cudaStream_t stream);

@@ -249,6 +249,28 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// The same two MMAs with 8-bit E4M3 operands (kind::f8f6f4: K = 32 elements,
+// still 32 bytes, per instruction; fp32 accumulation).
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on the mbarrier at offset `bar` in every CTA of `cta_mask`
 // when the pair MMAs issued before it have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
@@ -282,6 +304,25 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n) {
          | (0u << 15) | (0u << 16)              // A, B K-major
          | ((uint32_t)(n >> 3) << 17)           // N / 8
          | ((uint32_t)(m >> 4) << 24);          // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0),
+// fp32 D, both operands K-major.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int m, int n) {
+  return (1u << 4)                              // D format: f32
+         | (0u << 7)                            // A format: E4M3
+         | (0u << 10)                           // B format: E4M3
+         | (0u << 15) | (0u << 16)              // A, B K-major
+         | ((uint32_t)(n >> 3) << 17)           // N / 8
+         | ((uint32_t)(m >> 4) << 24);          // M / 16
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating at
+// +-448): `lo` in the low byte, `hi` in the high byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Shared-memory matrix descriptor for a K-major operand laid out by a TMA load

@@ -1,0 +1,82 @@
+// quant.cu -- per-row E4M3 quantisation for the FP8 GEMM.
+//
+// For each row (a token of the activations, or an output channel of the
+// weights): amax = max_k |x_k|, scale = amax / 448 (IEEE division; 1 for a
+// zero row), q_k = E4M3(x_k / scale) rounded to nearest even and saturated at
+// +-448 (cvt.rn.satfinite).  A row holding a NaN or an infinity gets scale NaN
+// and NaN codes (0x7F).  The maximum is exact whatever the order it is taken
+// in, and every code depends on its own row only.  Detent (Batch-Invariant LLM
+// Serving and RL Rollouts at Near-Stock Speed), Limits: dynamic per-tensor FP8
+// activation scales span the batch; per-token scales keep each row's bits its
+// own.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bi {
+
+constexpr int kQuantWarps = 8;
+
+__device__ __forceinline__ float q_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float q_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void amax2(uint32_t w, float& amax, bool& bad) {
+  const float a = q_lo(w), b = q_hi(w);
+  bad = bad || !isfinite(a) || !isfinite(b);
+  amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+}
+
+// Four E4M3 codes of x[0..3] / s, x[0] in the lowest byte.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float s) {
+  const uint32_t lo = cvt_e4m3x2(__fdiv_rn(q_lo(w0), s), __fdiv_rn(q_hi(w0), s));
+  const uint32_t hi = cvt_e4m3x2(__fdiv_rn(q_lo(w1), s), __fdiv_rn(q_hi(w1), s));
+  return lo | (hi << 16);
+}
+
+// X [M,K] bf16 -> Q [M,K] E4M3, scale [M]; one warp per row, vectors of 8.
+__global__ void __launch_bounds__(32 * kQuantWarps)
+    quantize_e4m3_kernel(const uint4* X, uint2* Q, float* scale, int64_t M, int64_t K) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int64_t nvec = K / 8;
+  const uint4* x = X + row * nvec;
+  float amax = 0.0f;
+  bool bad = false;
+  for (int64_t i = lane; i < nvec; i += 32) {
+    const uint4 v = x[i];
+    amax2(v.x, amax, bad);
+    amax2(v.y, amax, bad);
+    amax2(v.z, amax, bad);
+    amax2(v.w, amax, bad);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
+  }
+  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
+  if (lane == 0) scale[row] = s;
+  uint2* q = Q + row * nvec;
+  for (int64_t i = lane; i < nvec; i += 32) {
+    if (bad) {
+      q[i] = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+      const uint4 v = x[i];
+      q[i] = make_uint2(codes4(v.x, v.y, s), codes4(v.z, v.w, s));
+    }
+  }
+}
+
+cudaError_t launch_quantize_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                 cudaStream_t stream) {
+  const int64_t blocks = (M + kQuantWarps - 1) / kQuantWarps;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_overlapped(quantize_e4m3_kernel, dim3((unsigned)blocks), dim3(32 * kQuantWarps), stream,
+                           static_cast<const uint4*>(X), static_cast<uint2*>(Q), scale, M, K);
+}
+
+}  // namespace bi

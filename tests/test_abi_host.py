@@ -112,6 +112,17 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert lib.bi_residual_add_bf16(16, 32, 48, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_silu_mul_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_attention_ctx1_bf16(16, 32, 2, 6, 4, 8, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    # FP8: K must give 16-byte rows of 1-byte codes; pins with bk = 128 and T = 256
+    assert lib.bi_quantize_rows_e4m3(16, 32, 48, 2, 24, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_quantize_rows_e4m3(16, 32, 50, 2, 32, None) == bd.BI_ERR_ALIGNMENT
+    assert lib.bi_gemm_fp8(16, 48, 32, 64, 80, 2, 128, 24, None, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_gemm_fp8(16, None, 32, 64, 80, 2, 128, 32, None, None) == bd.BI_ERR_INVALID_ARG
+    p8 = bd.bi_pins_default_fp8(4096, 14336)
+    assert p8.bk == 128 and p8.tok_tile == 256 and bd.bi_pins_validate_fp8(4096, 14336, p8) == bd.BI_OK
+    assert bd.bi_pins_validate_fp8(4096, 14336, p8.replace(bk=64)) == bd.BI_ERR_ILLEGAL_PINS
+    assert bd.bi_pins_validate_fp8(4096, 14336, p8.replace(tok_tile=128)) == bd.BI_ERR_ILLEGAL_PINS
+    plan8 = bd.bi_gemm_plan_describe_fp8(8192, 4096, 14336)
+    assert (plan8.bk, plan8.k_tiles, plan8.mma_k) == (128, 112, 32)
     # log-probabilities: V must be a multiple of 8; errors before any launch
     assert lib.bi_log_softmax_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_log_softmax_bf16(16, 32, -1, 16, None) == bd.BI_ERR_INVALID_ARG

@@ -1,0 +1,116 @@
+"""FP8 (E4M3) path on the GPU: per-row quantisation bit-exact against the
+oracle, the scaled FP8 GEMM within the GEMM bar (bit-exact on integer codes),
+and batch invariance -- including across schedules and CTA groupings, which
+the open grouping relies on for kind::f8f6f4 MMAs as for bf16 (H1)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_bits, check_gemm_parity
+from invariant_bi_gemm_bf16_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def u8(t):
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (37, 4096), (300, 14336), (5, 1040)])
+def test_quantize_bit_exact(lib, oracle, M, K):
+    X = inputs.rows_loguniform(M, K, lo=1e-3, hi=1e3, seed=40, stream=0)
+    want_q, want_s = oracle.quantize_rows_e4m3(inputs.bits(X))
+    q, s = lib.bi_quantize_rows_e4m3(X.cuda())
+    assert np.array_equal(u8(q), want_q)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), want_s.view(np.uint32))
+
+
+def test_quantize_special_rows(lib, oracle):
+    K = 64
+    rows = np.ones((5, K), dtype=np.float32)
+    rows[0] = 0.0
+    rows[1, 3] = np.nan
+    rows[2, 7] = -np.inf
+    rows[3] = -0.0
+    rows[4] = np.linspace(-1e-30, 1e-30, K)      # bf16 subnormal-range values
+    X = torch.from_numpy(rows).to(torch.bfloat16)
+    want_q, want_s = oracle.quantize_rows_e4m3(inputs.bits(X))
+    q, s = lib.bi_quantize_rows_e4m3(X.cuda())
+    assert np.array_equal(u8(q), want_q)
+    got_s = s.cpu().numpy()
+    assert np.array_equal(np.isnan(got_s), np.isnan(want_s))
+    assert np.array_equal(got_s[~np.isnan(got_s)], want_s[~np.isnan(want_s)])
+
+
+def quantized(lib, M, N, K, seed):
+    X = inputs.normal((M, K), seed=seed, stream=0).cuda()
+    W = inputs.normal((N, K), std=0.02, seed=seed, stream=1).cuda()
+    xq, sx = lib.bi_quantize_rows_e4m3(X)
+    wq, sw = lib.bi_quantize_rows_e4m3(W)
+    return xq, sx, wq, sw
+
+
+SHAPES = [(200, 300, 1024), (1, 640, 4096), (129, 256, 1040), (300, 512, 14336)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_fp8_parity(lib, oracle, M, N, K):
+    xq, sx, wq, sw = quantized(lib, M, N, K, seed=41)
+    yf, _ = oracle.gemm_e4m3(u8(xq), sx.cpu().numpy(), u8(wq), sw.cpu().numpy())
+    ref = (yf.astype(np.float64) * sx.cpu().numpy()[:, None] * sw.cpu().numpy()[None, :]).astype(np.float32)
+    got = bf16_bits(lib.bi_gemm_fp8(xq, sx, wq, sw))
+    check_gemm_parity(got, ref, K, "fp8 M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4])
+def test_gemm_fp8_integer_codes_bit_exact_in_every_schedule(lib, oracle, S):
+    """Codes of small integers: every product and partial sum is an exact
+    integer, so any tree gives the oracle's bits."""
+    M, N, K = 150, 384, 2048
+    rng = np.random.default_rng(42)
+    vx = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    vw = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
+    qx, qw = oracle.e4m3_encode(vx), oracle.e4m3_encode(vw)
+    sx = (2.0 ** rng.integers(-3, 4, size=M)).astype(np.float32)
+    sw = (2.0 ** rng.integers(-3, 4, size=N)).astype(np.float32)
+    _, yb = oracle.gemm_e4m3(qx, sx, qw, sw)
+    d = [torch.from_numpy(a).cuda() for a in (qx, sx, qw, sw)]
+    base = lib.bi_pins_default_fp8(N, K).replace(split_k=S)
+    for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_AUTO):
+        for ctas in (1, 2):
+            p = base.replace(flags=flags | lib.BI_FLAG_KTILE_PAIRS, mma_ctas=ctas)
+            assert np.array_equal(bf16_bits(lib.bi_gemm_fp8(*d, pins=p)), yb), (flags, ctas)
+
+
+def test_gemm_fp8_schedules_groupings_and_copies_agree(lib):
+    M, N, K = 700, 4096, 14336
+    xq, sx, wq, sw = quantized(lib, M, N, K, seed=43)
+    base = lib.bi_pins_default_fp8(N, K)
+    ref = None
+    for flags in (lib.BI_FLAG_SCHEDULE_LOCAL, lib.BI_FLAG_SCHEDULE_CLUSTER, lib.BI_FLAG_SCHEDULE_CHAIN,
+                  lib.BI_FLAG_SCHEDULE_AUTO):
+        for ctas in (0, 1, 2):
+            for kp in (0, lib.BI_FLAG_KTILE_PAIRS):
+                p = base.replace(flags=flags | kp, mma_ctas=ctas)
+                got = bf16_bits(lib.bi_gemm_fp8(xq, sx, wq, sw, pins=p))
+                if ref is None:
+                    ref = got
+                assert np.array_equal(got, ref), (flags, ctas, kp)
+
+
+def test_fp8_rows_independent_of_batch(lib):
+    """Quantisation and GEMM together: a token's output bits are the same alone,
+    in a batch of 1000 and at another position."""
+    N, K = 4096, 14336
+    X = inputs.device_normal((1000, K), seed=44, stream=0)
+    W = inputs.device_normal((N, K), std=0.02, seed=44, stream=1)
+    wq, sw = lib.bi_quantize_rows_e4m3(W)
+
+    def layer(x):
+        xq, sx = lib.bi_quantize_rows_e4m3(x)
+        return bf16_bits(lib.bi_gemm_fp8(xq, sx, wq, sw))
+    full = layer(X)
+    for r in (0, 517, 999):
+        assert np.array_equal(layer(X[r:r + 1].contiguous())[0], full[r])
+    perm = torch.randperm(1000, generator=torch.Generator().manual_seed(8))
+    assert np.array_equal(layer(X[perm.cuda()].contiguous()), full[perm.numpy()])
