@@ -29,6 +29,11 @@ Pins (checks against things other than the oracle itself) live in
     pinned by hand-derived codes (1.0, 448, subnormals, ties, saturation,
     NaN), the decode/encode round trip over all codes, exact scales for
     power-of-two rows, and integer-exact GEMMs.
+  - ``decode_attention``: pinned by closed forms (one position gives its
+    value row; equal keys or scale 0 give the mean of the values; two
+    positions give the logistic form; a dominant key selects its value),
+    the grouped-query head mapping, position-order and page-placement
+    invariance, convexity, and cache rows past the length being ignored.
 """
 from __future__ import annotations
 
@@ -98,6 +103,9 @@ def _load():
             lib.oracle_quantize_rows_e4m3.argtypes = [_u16p, _u8p, _f32p, _i64, _i64, ctypes.c_int]
             lib.oracle_gemm_e4m3.argtypes = [_u8p, _f32p, _u8p, _f32p, _f32p, _u16p, _i64, _i64, _i64,
                                              ctypes.c_int]
+            lib.oracle_decode_attention.argtypes = [_u16p, _u16p, _u16p, _i32p, _i64, _i32p, _i64p, _i64,
+                                                    _f64p, _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                                    ctypes.c_int]
             lib.oracle_bf16_rne_array.argtypes = [_f32p, _u16p, _i64]
             lib.oracle_bf16_to_f32_array.argtypes = [_u16p, _f32p, _i64]
             _lib = lib
@@ -338,3 +346,43 @@ def gemm_e4m3(Xq, sx, Wq, sw, nthreads: int | None = None):
     _load().oracle_gemm_e4m3(xq.ctypes.data_as(_u8p), _pf(sxa), wq.ctypes.data_as(_u8p), _pf(swa), _pf(yf),
                              _p16(yb), M, N, K, nthreads or default_threads())
     return yf, yb
+
+
+# --------------------------------------------------------------------------
+# Decode attention over a paged key/value cache
+# --------------------------------------------------------------------------
+
+def decode_attention(q, k_cache, v_cache, block_table, seq_lens, scale: float, pairs=None,
+                     nthreads: int | None = None) -> np.ndarray:
+    """q [B,Hq,D] bf16 bits; k_cache, v_cache [num_pages, page_size, Hkv, D]
+    bf16 bits; block_table [B, P] int32; seq_lens [B] int32.  Returns fp64
+    [B,Hq,D], or [n,D] for the (b, h) rows listed in ``pairs`` ([n,2])."""
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    B, Hq, D = qa.shape
+    _, page_size, Hkv, Dk = ka.shape
+    if va.shape != ka.shape or Dk != D or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if bt.ndim != 2 or bt.shape[0] != B or sl.shape != (B,):
+        raise ValueError("block_table must be [B, P] and seq_lens [B]")
+    if np.any(sl > bt.shape[1] * page_size) or np.any(sl < 0):
+        raise ValueError("a length exceeds the pages of its block-table row")
+    for b in range(B):
+        used = bt[b, :(int(sl[b]) + page_size - 1) // page_size]
+        if np.any(used < 0) or np.any(used >= ka.shape[0]):
+            raise ValueError("request %d uses a page id outside the cache" % b)
+    lib = _load()
+    nt = nthreads or default_threads()
+    if pairs is None:
+        out = np.empty((B, Hq, D), dtype=np.float64)
+        lib.oracle_decode_attention(_p16(qa), _p16(ka), _p16(va), bt.ctypes.data_as(_i32p), bt.shape[1],
+                                    sl.ctypes.data_as(_i32p), None, 0, out.ctypes.data_as(_f64p), B, Hq,
+                                    Hkv, D, page_size, float(scale), nt)
+        return out
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    out = np.empty((pr.shape[0], D), dtype=np.float64)
+    lib.oracle_decode_attention(_p16(qa), _p16(ka), _p16(va), bt.ctypes.data_as(_i32p), bt.shape[1],
+                                sl.ctypes.data_as(_i32p), pr.ctypes.data_as(_i64p), pr.shape[0],
+                                out.ctypes.data_as(_f64p), B, Hq, Hkv, D, page_size, float(scale), nt)
+    return out

@@ -28,6 +28,9 @@
  *     log-probabilities), in fp64: x_v - (max + log sum exp(x - max)).
  *   - FP8 (E4M3) with per-token activation scales and per-channel weight
  *     scales: per-row quantisation and the scaled GEMM.
+ *   - Decode attention over a paged key/value cache, in fp64: the plain
+ *     softmax(scale * q . k) . v of each query head over its request's
+ *     positions (grouped-query heads), with no split.
  *   - One decode layer of a Llama-style stack (for the linear-stack
  *     workload): RMSNorm, qkv projection, an attention stand-in for context
  *     length 1 (softmax over one key is exactly 1, so each query head's output
@@ -520,6 +523,89 @@ void oracle_gemm_e4m3(const uint8_t* Xq, const float* sx, const uint8_t* Wq, con
                       uint16_t* Yb, int64_t M, int64_t N, int64_t K, int nthreads) {
   gemm8_ctx c = {Xq, Wq, sx, sw, Yf, Yb, N, K};
   parallel_for(gemm8_range, &c, M * N, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention over a paged key/value cache                            */
+/* ------------------------------------------------------------------------ */
+
+/* One query token per request (decode).  Request b attends to its first L_b
+ * cached positions; query head h reads key/value head h / G, G = Hq / Hkv
+ * (grouped-query attention, consecutive query heads share a group).  The plain
+ * definition, in fp64:
+ *     s_p   = scale * sum_d q_d k_{p,d}                 p = 0 .. L_b - 1
+ *     w_p   = exp(s_p - max s) / sum_p' exp(s_p' - max s)
+ *     out_d = sum_p w_p v_{p,d}
+ * (subtracting the maximum changes no value, only the range of the
+ * exponentials).  Position p of request b lives in page block_table[b][p /
+ * page_size], row p % page_size; a page holds page_size rows of Hkv heads of D
+ * values.  Splitting the positions and combining the partial sums, as
+ * FlashDecoding-style kernels do, reaches the same value up to rounding order;
+ * Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock Speed),
+ * Sec. 7, and LLM-42, Sec. 4.4, fix that split only to make the rounding
+ * reproducible.  Here there is no split: the oracle is the definition.
+ * L_b = 0 gives zeros (an empty sum).  NaN or +Inf scores give NaN through
+ * the IEEE arithmetic of the formula. */
+typedef struct {
+  const uint16_t *q, *k, *v;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int64_t* pairs; /* (b, h) pairs to compute, or NULL for all of them */
+  double* out;
+  int64_t Hq, Hkv, D, page_size, bt_stride;
+  double scale;
+} attn_ctx;
+
+static void attention_one(const attn_ctx* c, int64_t b, int64_t h, double* out) {
+  const int64_t G = c->Hq / c->Hkv, kvh = h / G, L = c->seq_lens[b];
+  const uint16_t* q = c->q + (b * c->Hq + h) * c->D;
+  for (int64_t d = 0; d < c->D; ++d) out[d] = 0.0;
+  if (L <= 0) return;
+  double* s = (double*)malloc(sizeof(double) * (size_t)L);
+  int64_t* row = (int64_t*)malloc(sizeof(int64_t) * (size_t)L);
+  double m = -INFINITY;
+  for (int64_t p = 0; p < L; ++p) {
+    const int64_t page = c->block_table[b * c->bt_stride + p / c->page_size];
+    row[p] = ((page * c->page_size + p % c->page_size) * c->Hkv + kvh) * c->D;
+    double dot = 0.0;
+    for (int64_t d = 0; d < c->D; ++d)
+      dot += (double)oracle_bf16_to_f32(q[d]) * (double)oracle_bf16_to_f32(c->k[row[p] + d]);
+    s[p] = c->scale * dot;
+    if (s[p] > m) m = s[p];
+  }
+  double sum = 0.0;
+  for (int64_t p = 0; p < L; ++p) {
+    s[p] = exp(s[p] - m);
+    sum += s[p];
+  }
+  for (int64_t p = 0; p < L; ++p) {
+    const double w = s[p] / sum;
+    for (int64_t d = 0; d < c->D; ++d) out[d] += w * (double)oracle_bf16_to_f32(c->v[row[p] + d]);
+  }
+  free(s);
+  free(row);
+}
+
+static void attn_range(void* p, int64_t lo, int64_t hi) {
+  const attn_ctx* c = (const attn_ctx*)p;
+  for (int64_t i = lo; i < hi; ++i) {
+    const int64_t b = c->pairs ? c->pairs[2 * i] : i / c->Hq;
+    const int64_t h = c->pairs ? c->pairs[2 * i + 1] : i % c->Hq;
+    attention_one(c, b, h, c->out + i * c->D);
+  }
+}
+
+/* q [B,Hq,D] bf16; k_cache, v_cache [num_pages, page_size, Hkv, D] bf16;
+ * block_table [B, bt_stride] int32; seq_lens [B] int32.  With pairs == NULL,
+ * out [B,Hq,D] fp64 gets every head; otherwise out [n_pairs, D] gets the
+ * listed (b, h) pairs. */
+void oracle_decode_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                             const int64_t* pairs, int64_t n_pairs, double* out, int64_t B, int64_t Hq,
+                             int64_t Hkv, int64_t D, int64_t page_size, double scale, int nthreads) {
+  attn_ctx c = {q, k_cache, v_cache, block_table, seq_lens, pairs, out, Hq, Hkv, D, page_size,
+                bt_stride, scale};
+  parallel_for(attn_range, &c, pairs ? n_pairs : B * Hq, nthreads);
 }
 
 /* Array forms of the two conversions, for callers that hold whole tensors. */

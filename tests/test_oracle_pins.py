@@ -614,3 +614,180 @@ def test_gemm_e4m3_integer_exact(oracle):
     assert np.array_equal(yf, exact.astype(np.float32))
     want = oracle.bf16_rne((exact * sx[:, None] * sw[None, :]).astype(np.float32))
     assert np.array_equal(yb, want)
+
+
+# --------------------------------------------------------------------------- decode attention
+
+def exact_bits(a) -> np.ndarray:
+    """bf16 bit patterns of values that bf16 holds exactly (asserted)."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bf16_val(bits), f), "value not exact in bf16"
+    return bits
+
+
+def bf16_round_vals(a) -> np.ndarray:
+    """Values truncated to bf16 (exact by construction)."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    return ((f.view(np.uint32) >> 16) << 16).view(np.float32)
+
+
+def paged(kd, vd, page_size, order=None, pad_pages=0, fill=0.0):
+    """Dense per-request K/V lists ([L_b, Hkv, D] each) -> (k_cache, v_cache,
+    block_table, seq_lens) with the pages laid out in `order` (a permutation of
+    the page slots; identity when None).  Rows past a request's length in its
+    last page, and `pad_pages` unused pages, hold `fill`."""
+    Hkv, D = kd[0].shape[1], kd[0].shape[2]
+    need = [-(-k.shape[0] // page_size) for k in kd]
+    total = sum(need) + pad_pages
+    order = np.arange(total) if order is None else np.asarray(order)
+    kc = np.full((total, page_size, Hkv, D), fill, dtype=np.float32)
+    vc = np.full((total, page_size, Hkv, D), fill, dtype=np.float32)
+    bt = np.full((len(kd), max(max(need), 1)), -1, dtype=np.int32)
+    slot = 0
+    for b, (k, v) in enumerate(zip(kd, vd)):
+        for i in range(need[b]):
+            pg = int(order[slot])
+            slot += 1
+            rows = slice(i * page_size, min((i + 1) * page_size, k.shape[0]))
+            n = rows.stop - rows.start
+            kc[pg, :n], vc[pg, :n] = k[rows], v[rows]
+            bt[b, i] = pg
+    lens = np.array([k.shape[0] for k in kd], dtype=np.int32)
+    return kc, vc, bt, lens
+
+
+def attn(oracle, q, kd, vd, scale, page_size=4, **kw):
+    kc, vc, bt, lens = paged(kd, vd, page_size, **kw)
+    finite = np.isfinite(kc) & np.isfinite(vc)
+    exact_bits(np.where(finite, kc, 0.0))
+    exact_bits(np.where(finite, vc, 0.0))
+    kb = (kc.view(np.uint32) >> 16).astype(np.uint16)
+    vb = (vc.view(np.uint32) >> 16).astype(np.uint16)
+    return oracle.decode_attention(exact_bits(q), kb, vb, bt, lens, scale)
+
+
+def rand_req(rng, L, Hkv, D, lo=-2.0, hi=2.0):
+    return bf16_round_vals(rng.uniform(lo, hi, (L, Hkv, D))), bf16_round_vals(rng.uniform(lo, hi, (L, Hkv, D)))
+
+
+def test_attention_one_position_gives_its_value_row(oracle):
+    rng = np.random.default_rng(50)
+    k, v = rand_req(rng, 1, 2, 16)
+    q = bf16_round_vals(rng.uniform(-3, 3, (1, 4, 16)))
+    out = attn(oracle, q, [k], [v], 0.25)
+    for h in range(4):
+        assert np.array_equal(out[0, h], v[0, h // 2].astype(np.float64))
+
+
+def test_attention_equal_keys_or_zero_scale_give_the_mean(oracle):
+    rng = np.random.default_rng(51)
+    L, D = 7, 8
+    v = np.asarray(rng.integers(-50, 51, (L, 1, D)), dtype=np.float32)
+    krow = bf16_round_vals(rng.uniform(-1, 1, (1, 1, D)))
+    q = bf16_round_vals(rng.uniform(-1, 1, (1, 1, D)))
+    mean = np.array([float(sum(Fraction(int(x)) for x in v[:, 0, d]) / L) for d in range(D)])
+    out = attn(oracle, q, [np.repeat(krow, L, axis=0)], [v], 0.7)
+    assert np.allclose(out[0, 0], mean, rtol=0, atol=1e-12)
+    k, _ = rand_req(rng, L, 1, D)
+    out = attn(oracle, q, [k], [v], 0.0)
+    assert np.allclose(out[0, 0], mean, rtol=0, atol=1e-12)
+
+
+def test_attention_two_positions_follow_the_logistic_form(oracle):
+    # integer q and k make q . k exact; with scale 1/8, s1 - s0 is exact too:
+    # out = v0 + (v1 - v0) / (1 + exp(s0 - s1))
+    rng = np.random.default_rng(52)
+    D = 16
+    for trial in range(6):
+        q = rng.integers(-3, 4, (1, 1, D)).astype(np.float32)
+        k = rng.integers(-3, 4, (2, 1, D)).astype(np.float32)
+        v = bf16_round_vals(rng.uniform(-4, 4, (2, 1, D)))
+        s = [float(q[0, 0] @ k[p, 0]) / 8 for p in range(2)]
+        want = v[0, 0] + (v[1, 0].astype(np.float64) - v[0, 0]) / (1.0 + math.exp(s[0] - s[1]))
+        out = attn(oracle, q, [k], [v], 0.125)
+        assert np.allclose(out[0, 0], want, rtol=0, atol=1e-13), trial
+
+
+def test_attention_a_dominant_key_selects_its_value(oracle):
+    rng = np.random.default_rng(53)
+    L, D = 40, 32
+    k, v = rand_req(rng, L, 1, D, -0.5, 0.5)
+    q = np.zeros((1, 1, D), dtype=np.float32)
+    q[0, 0, 0] = 64.0
+    k[:, 0, 0] = 0.0
+    k[17, 0, 0] = 2.0                      # s_17 - s_p = 128 * scale = 64 for every other p
+    out = attn(oracle, q, [k], [v], 0.5)
+    assert np.allclose(out[0, 0], v[17, 0], rtol=0, atol=1e-20)
+
+
+def test_attention_grouped_query_heads_read_their_group(oracle):
+    # consecutive query heads share a key/value head: head h reads group h // (Hq / Hkv)
+    rng = np.random.default_rng(54)
+    D, L = 8, 5
+    for Hq, Hkv in ((8, 2), (8, 4), (6, 3), (4, 1)):
+        k, _ = rand_req(rng, L, Hkv, D)
+        v = np.zeros((L, Hkv, D), dtype=np.float32)
+        for j in range(Hkv):
+            v[:, j] = j + 1
+        q = bf16_round_vals(rng.uniform(-1, 1, (1, Hq, D)))
+        out = attn(oracle, q, [k], [v], 0.3)
+        G = Hq // Hkv
+        for h in range(Hq):
+            assert np.allclose(out[0, h], h // G + 1, rtol=0, atol=1e-14), (Hq, Hkv, h)
+
+
+def test_attention_page_placement_and_position_order(oracle):
+    rng = np.random.default_rng(55)
+    D, Hkv, Hq = 16, 2, 4
+    lens = [1, 9, 16, 23]
+    kd, vd = zip(*[rand_req(rng, L, Hkv, D) for L in lens])
+    q = bf16_round_vals(rng.uniform(-2, 2, (len(lens), Hq, D)))
+    base = attn(oracle, q, kd, vd, 0.4, page_size=4)
+    # the same rows in shuffled pages of another size: the same positions in the same order
+    for ps in (1, 4, 8):
+        n = sum(-(-L // ps) for L in lens) + 3
+        got = attn(oracle, q, kd, vd, 0.4, page_size=ps, order=rng.permutation(n), pad_pages=3)
+        assert np.array_equal(got, base), ps
+    # permuting a request's positions changes only the rounding order of the sums
+    perm = [rng.permutation(L) for L in lens]
+    got = attn(oracle, q, [k[p] for k, p in zip(kd, perm)], [v[p] for v, p in zip(vd, perm)], 0.4)
+    assert np.allclose(got, base, rtol=0, atol=1e-13)
+    # each request is computed from its own rows: dropping the others changes nothing
+    for b in range(len(lens)):
+        alone = attn(oracle, q[b:b + 1], [kd[b]], [vd[b]], 0.4)
+        assert np.array_equal(alone[0], base[b])
+
+
+def test_attention_is_a_convex_combination(oracle):
+    rng = np.random.default_rng(56)
+    D, L = 32, 50
+    k, v = rand_req(rng, L, 1, D, -3, 3)
+    q = bf16_round_vals(rng.uniform(-3, 3, (1, 1, D)))
+    out = attn(oracle, q, [k], [v], 1.0)[0, 0]
+    assert np.all(out >= v[:, 0].min(axis=0) - 1e-12) and np.all(out <= v[:, 0].max(axis=0) + 1e-12)
+    ones = attn(oracle, q, [k], [np.ones_like(v)], 1.0)[0, 0]   # the weights sum to one
+    assert np.allclose(ones, 1.0, rtol=0, atol=1e-14)
+
+
+def test_attention_ignores_cache_rows_past_the_length(oracle):
+    rng = np.random.default_rng(57)
+    D, Hkv, Hq = 8, 1, 2
+    kd, vd = zip(*[rand_req(rng, L, Hkv, D) for L in (3, 6)])
+    q = bf16_round_vals(rng.uniform(-2, 2, (2, Hq, D)))
+    clean = attn(oracle, q, kd, vd, 0.5, page_size=4)
+    for fill in (np.nan, np.inf, 2.0 ** 100):
+        dirty = attn(oracle, q, kd, vd, 0.5, page_size=4, pad_pages=2, fill=fill)
+        assert np.array_equal(dirty, clean), fill
+
+
+def test_attention_empty_requests_and_nan_rows(oracle):
+    rng = np.random.default_rng(58)
+    D, Hkv, Hq = 8, 2, 4
+    k, v = rand_req(rng, 5, Hkv, D)
+    k[2, 1, 3] = np.nan                                   # a NaN key in group 1 only
+    q = bf16_round_vals(rng.uniform(-2, 2, (2, Hq, D)))
+    empty_k = np.zeros((0, Hkv, D), dtype=np.float32)
+    out = attn(oracle, q, [k, empty_k], [v, empty_k], 0.5)
+    assert np.all(np.isfinite(out[0, :2])) and np.all(np.isnan(out[0, 2:]))
+    assert np.array_equal(out[1], np.zeros((Hq, D)))
