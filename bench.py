@@ -592,6 +592,81 @@ def run_fp8(args, dist, peaks):
             "baseline": baseline, "sweep": res}
 
 
+ATTN_HEADS = (64, 8, 128, 16)   # query heads, key/value heads, head dim, page size
+ATTN_MIXES = [("64 requests, lengths uniform on [512, 8192]", 64, (512, 8192)),
+              ("256 requests, lengths uniform on [64, 2048]", 256, (64, 2048)),
+              ("1 request of 32768", 1, (32768, 32768))]
+
+
+def attention_case(mix, dist, dev):
+    """(name, lengths, (k_cache, v_cache, block_table, seq_lens, q)) of one request mix."""
+    from invariant_bi_gemm_bf16_gb300 import inputs
+    Hq, Hkv, D, P = ATTN_HEADS
+    name, B, (lo, hi) = ATTN_MIXES[mix]
+    rng = np.random.default_rng(70 + dist.rank)
+    lens = [int(x) for x in rng.integers(lo, hi + 1, size=B)]
+    kc, vc, bt, sl = inputs.device_paged_kv(lens, Hkv, D, P, seed=70 + dist.rank, device=dev)
+    q = inputs.device_normal((B, Hq, D), seed=70 + dist.rank, stream=0, device=dev)
+    return name, lens, (kc, vc, bt, sl, q)
+
+
+def run_attention(args, dist, peaks):
+    """Decode attention over a paged cache (Llama-3.1-70B heads: 64 query
+    heads, 8 key/value heads, D = 128; pages of 16 in shuffled order) against
+    its HBM roofline, for three request mixes.  Algorithmic bytes per call:
+    the keys and values of every request's positions, q and the output.  The
+    caches are larger than L2, so consecutive calls find none of them there.
+    Context: torch's scaled_dot_product_attention on the same requests padded
+    to the longest, with a length mask (torch has no paged decode attention)."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    import torch.nn.functional as F
+    dev = torch.device("cuda", dist.local_rank)
+    Hq, Hkv, D, P = ATTN_HEADS
+    res = []
+    for mix in range(len(ATTN_MIXES)):
+        name, lens, (kc, vc, bt, sl, q) = attention_case(mix, dist, dev)
+        B = len(lens)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        max_len = bt.shape[1] * P
+        alg = sum(lens) * Hkv * D * 2 * 2 + 2 * B * Hq * D * 2
+        row = {"mix": name, "kv_bytes": sum(lens) * Hkv * D * 4, "splits": []}
+        for S in (128, 256, 512, 1024):
+            ws = torch.empty(bd.bi_decode_attention_workspace_bytes(B, Hq, Hkv, max_len, S), dtype=torch.uint8,
+                             device=dev)
+            us = time_reps(lambda i: bd.bi_decode_attention_bf16(q, kc, vc, bt, sl, D ** -0.5, max_seq_len=max_len,
+                                                                 split_size=S, out=out, workspace=ws),
+                           args.per_m_reps)
+            row["splits"].append({"split": S, "us": round(us, 2), "gbs": round(alg / us / 1e3, 1),
+                                  "roofline_frac": round(alg / us / 1e3 / peaks["hbm_gbs"], 3)})
+            del ws
+        if bd.bi_last_device_status() != bd.BI_OK:
+            raise RuntimeError("decode attention reported a device-side error")
+        try:
+            Lmax = max(lens)
+            if B * Hkv * Lmax * D * 2 * 2 <= (8 << 30):
+                Kd = torch.zeros((B, Hkv, Lmax, D), dtype=torch.bfloat16, device=dev)
+                Vd = torch.zeros_like(Kd)
+                for b, L in enumerate(lens):
+                    pos = torch.arange(L, device=dev)
+                    pages = bt[b].long()[pos // P]
+                    Kd[b, :, :L] = kc[pages, pos % P].transpose(0, 1)
+                    Vd[b, :, :L] = vc[pages, pos % P].transpose(0, 1)
+                mask = (torch.arange(Lmax, device=dev)[None, :] < sl[:, None]).view(B, 1, 1, Lmax)
+                q4 = q.view(B, Hq, 1, D)
+                tus = time_reps(lambda i: F.scaled_dot_product_attention(q4, Kd, Vd, attn_mask=mask, enable_gqa=True),
+                                args.per_m_reps)
+                row["torch_sdpa_padded_us"] = round(tus, 2)
+                del Kd, Vd
+        except Exception as e:  # noqa: BLE001 - context only
+            row["torch_sdpa_padded_us"] = None
+            row["torch_sdpa_error"] = type(e).__name__
+        res.append(row)
+        del kc, vc, q
+        torch.cuda.empty_cache()
+    return {"workload": "decode attention, Llama-3.1-70B heads (64 q, 8 kv, D 128), paged cache (pages of 16, "
+                        "shuffled), fixed split sizes 128..1024", "mixes": res}
+
+
 def time_steps(fn, steps, dist):
     dist.barrier()
     torch.cuda.synchronize()
@@ -736,6 +811,8 @@ def run_ours(args, dist):
         result["lm_head"] = run_lm_head(args, dist, peaks)
     if not args.no_fp8:
         result["fp8"] = run_fp8(args, dist, peaks)
+    if not args.no_attention:
+        result["attention"] = run_attention(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -753,6 +830,24 @@ def run_single_m(args, dist):
     wl = DownProjSweep(bd, torch.device("cuda", dist.local_rank), seed=dist.rank, sweep=[args.single_m])
     for i in range(args.launches):
         wl._launch(args.single_m, wl.X[args.single_m][i % len(wl.X[args.single_m])], wl.W[i % wl.nw], False)
+    torch.cuda.synchronize()
+    st = bd.bi_last_device_status()
+    if st != bd.BI_OK:
+        raise RuntimeError(bd.status_string(st))
+
+
+def run_single_attention(args, dist):
+    """Launches decode attention on one request mix (MIX:SPLIT), --launches
+    times, for an ncu capture of those launches."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    mix, split = (int(x) for x in args.single_attention.split(":"))
+    _, lens, (kc, vc, bt, sl, q) = attention_case(mix, dist, dev)
+    D, P = ATTN_HEADS[2], ATTN_HEADS[3]
+    for _ in range(args.launches):
+        bd.bi_decode_attention_bf16(q, kc, vc, bt, sl, D ** -0.5, max_seq_len=bt.shape[1] * P, split_size=split)
     torch.cuda.synchronize()
     st = bd.bi_last_device_status()
     if st != bd.BI_OK:
@@ -801,7 +896,10 @@ def main():
     ap.add_argument("--no-rmsnorm", action="store_true")
     ap.add_argument("--no-lm-head", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--single-attention", default="",
+                    help="MIX:SPLIT -- only launch decode attention on that request mix (for ncu)")
     ap.add_argument("--single-m", type=int, default=0,
                     help="profiling helper: only launch the sweep's GEMM at this M --launches times")
     ap.add_argument("--launches", type=int, default=3)
@@ -810,6 +908,9 @@ def main():
         args.warmup = 3
     dist = Dist()
     try:
+        if args.single_attention:
+            run_single_attention(args, dist)
+            return
         if args.single_m:
             run_single_m(args, dist)
             return

@@ -318,6 +318,65 @@ bi_status bi_gemm_plan_describe_fp8(int64_t M, int64_t N, int64_t K, const bi_pi
 bi_status bi_gemm_fp8(const void* Xq, const float* sx, const void* Wq, const float* sw, void* Y,
                       int64_t M, int64_t N, int64_t K, const bi_pins* pins, bi_stream_t stream);
 
+/* ---- Decode attention over a paged key/value cache -----------------------
+ * Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock Speed),
+ * Sec. 7 (Kernels): attention keeps split-KV, but a request's split
+ * boundaries follow a fixed split size, so they never depend on the batch.
+ * LLM-42, Sec. 4.4, and CoRun, Sec. IV-B, name the alternative, no split at
+ * all.  The split size is the pin: fix one per deployment and pass it on
+ * every call, as with bi_pins. */
+#define BI_ATTN_HEAD_DIM 128
+#define BI_ATTN_MAX_SPLIT 4096
+#define BI_ATTN_DEFAULT_SPLIT 256
+
+/* Workspace of bi_decode_attention_bf16, in *bytes:
+ * B * Hkv * n_split * (128 + 2) * GP * 4, n_split = max(1, ceil(max_seq_len /
+ * split_size)), GP = 8 for up to 8 query heads per key/value head, else 16.
+ * split_size 0 = BI_ATTN_DEFAULT_SPLIT.  Errors: as the call's shape checks.
+ * Host only. */
+bi_status bi_decode_attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len,
+                                              int64_t split_size, size_t* bytes);
+
+/* One decode step of attention: for request b (one query token) and query
+ * head h,  out[b,h,:] = sum_p w_p v_p,  w = softmax_p(scale * q[b,h,:] . k_p)
+ * over the request's positions p < seq_lens[b], with k_p, v_p the key/value
+ * head h / (Hq / Hkv) (grouped-query attention).
+ *   q         [B, Hq, D] bf16, D = 128
+ *   k_cache,
+ *   v_cache   [num_pages, page_size, Hkv, D] bf16; position p of request b is
+ *             row p % page_size of page block_table[b * bt_stride + p / page_size]
+ *   block_table [B, bt_stride] int32, seq_lens [B] int32 (device memory)
+ *   out       [B, Hq, D] bf16
+ * The tree: positions split at multiples of split_size; within a split, tiles
+ * of 64 positions, each warp of four owning 16 positions of every tile with a
+ * running (max, sum, output) state in fp32 (scores on the tensor cores with
+ * fp32 accumulation, exp2 of the log2-scaled scores, weights rounded to bf16
+ * before they multiply v and before they are summed); the warps' states fold
+ * in warp order, the splits' in split order; out = bf16_rne(o / l).  It
+ * depends on seq_lens[b], split_size and D only: no other request, batch size
+ * or page placement reaches it.  An empty request (length 0) gives zeros;
+ * NaN / +Inf scores give NaN.
+ * Requirements: D == 128; Hq % Hkv == 0 and Hq / Hkv <= 16; page_size a power
+ * of two >= 8 with num_pages * page_size < 2^31; split_size a multiple of 64,
+ * at most BI_ATTN_MAX_SPLIT (0 = BI_ATTN_DEFAULT_SPLIT); every seq_lens[b] <=
+ * max_seq_len <= bt_stride * page_size; B, Hkv and ceil(max_seq_len /
+ * split_size) <= 65535; q, caches, out and
+ * ws 16-byte aligned, block_table and seq_lens 4-byte aligned; ws_bytes at
+ * least bi_decode_attention_workspace_bytes(...).  Cache rows past a
+ * request's length are never used (they may hold anything).
+ * Device-side checks: a length outside [0, max_seq_len] or a page id outside
+ * [0, num_pages) sets BI_ERR_INVALID_ARG in the status that
+ * bi_last_device_status() reports; that request's output is then
+ * unspecified (NaN for a bad length).
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_WORKSPACE, BI_ERR_CUDA. */
+bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                                   void* out, int64_t B, int64_t Hq, int64_t Hkv, int64_t D,
+                                   int64_t num_pages, int64_t page_size, int64_t max_seq_len,
+                                   int64_t split_size, float scale, void* ws, size_t ws_bytes,
+                                   bi_stream_t stream);
+
 /* Log-probabilities of rows of logits (the lm_head output X [M,V] bf16):
  *   Y[m,v] = x[m,v] - lse_m,  lse_m = max_v x[m,v] + log(sum_v exp(x[m,v] - max)),
  * in fp32, Y [M,V] fp32.  A cluster of 8 CTAs of 512 threads per row: thread
@@ -345,10 +404,12 @@ bi_status bi_log_softmax_bf16(const void* X, float* Y, int64_t M, int64_t V, bi_
 bi_status bi_token_logprobs_bf16(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
                                  bi_stream_t stream);
 
-/* Synchronises `stream`, then returns and clears the current device's stall
- * word: BI_OK if no kernel's bounded wait ran out since the last call,
- * BI_ERR_DEVICE_TIMEOUT otherwise (the affected call's output is
- * unspecified), BI_ERR_CUDA if the synchronisation itself failed. */
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word, which holds the first problem a kernel recorded since the last call:
+ * BI_OK if none; BI_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out;
+ * BI_ERR_INVALID_ARG if decode attention found a device-resident argument
+ * (a length or a page id) out of range.  The affected call's output is
+ * unspecified.  BI_ERR_CUDA if the synchronisation itself failed. */
 bi_status bi_last_device_status(bi_stream_t stream);
 
 #ifdef __cplusplus

@@ -125,6 +125,11 @@ _SIGNATURES = {
                                                  ctypes.POINTER(Plan)]),
     "bi_gemm_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
     "bi_token_logprobs_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp]),
+    "bi_decode_attention_workspace_bytes": (ctypes.c_int, [_i64, _i64, _i64, _i64, _i64,
+                                                           ctypes.POINTER(ctypes.c_size_t)]),
+    "bi_decode_attention_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                _i64, _i64, _i64, _i64, ctypes.c_float, _vp, ctypes.c_size_t,
+                                                _vp]),
 }
 
 
@@ -425,3 +430,62 @@ def bi_attention_ctx1_bf16(qkv: torch.Tensor, nq: int, nkv: int, D: int, out: to
 def bi_last_device_status(stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device's stall status."""
     return int(load().bi_last_device_status(_stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# decode attention over a paged key/value cache
+# ---------------------------------------------------------------------------
+
+BI_ATTN_HEAD_DIM = 128
+BI_ATTN_MAX_SPLIT = 4096
+BI_ATTN_DEFAULT_SPLIT = 256
+
+
+def bi_decode_attention_workspace_bytes(B: int, Hq: int, Hkv: int, max_seq_len: int, split_size: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().bi_decode_attention_workspace_bytes(B, Hq, Hkv, max_seq_len, split_size, ctypes.byref(n)),
+           "bi_decode_attention_workspace_bytes")
+    return int(n.value)
+
+
+def _dev_i32(t: torch.Tensor, name: str, shape=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous int32 CUDA tensor" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+def bi_decode_attention_bf16(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             max_seq_len: int | None = None, split_size: int = 0,
+                             out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """out [B,Hq,D] = softmax(scale * q . k) . v over each request's cached
+    positions.  q [B,Hq,D]; caches [num_pages, page_size, Hkv, D];
+    block_table [B,P] and seq_lens [B] int32 on the device.  max_seq_len
+    (default P * page_size) bounds every length; split_size is the pin
+    (0 = BI_ATTN_DEFAULT_SPLIT)."""
+    if q.dim() != 3 or k_cache.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("expected q [B,Hq,D], caches [pages,page_size,Hkv,D], block_table [B,P]")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("q and the caches disagree on the head dimension")
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * page_size
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    need = bi_decode_attention_workspace_bytes(B, Hq, Hkv, max_seq_len, split_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    st = load().bi_decode_attention_bf16(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache", tuple(k_cache.shape)),
+        _dev_i32(block_table, "block_table", (B, block_table.shape[1])), block_table.shape[1],
+        _dev_i32(seq_lens, "seq_lens", (B,)), _dev(out, "out", (B, Hq, D)), B, Hq, Hkv, D, num_pages,
+        page_size, int(max_seq_len), int(split_size), float(scale), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "bi_decode_attention_bf16")
+    return out

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbi_gemm.so")
-SOURCES = ["api.cu", "gemm.cu", "rmsnorm.cu", "glue.cu", "noalloc.cu", "logsoftmax.cu", "quant.cu"]
+SOURCES = ["api.cu", "gemm.cu", "rmsnorm.cu", "glue.cu", "noalloc.cu", "logsoftmax.cu", "quant.cu", "attention.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -4,6 +4,8 @@
 // Order of work in every entry point: check every argument (no CUDA call),
 // resolve and validate the pins, then touch the device.  A call that returns
 // an error has launched nothing.
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -626,6 +628,99 @@ BI_API bi_status bi_token_logprobs_bf16(const void* X, const int32_t* ids, float
              : BI_ERR_CUDA;
 }
 
+namespace {
+
+bi_status attn_geometry(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len, int64_t* split,
+                        int64_t* n_split, int64_t* gp) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || max_seq_len < 0 || *split < 0) return BI_ERR_INVALID_ARG;
+  if (*split == 0) *split = BI_ATTN_DEFAULT_SPLIT;
+  if (Hq % Hkv != 0 || Hq / Hkv > 16 || *split % 64 != 0 || *split > BI_ATTN_MAX_SPLIT || B > 65535 ||
+      Hkv > 65535 || Hq > (int64_t)1 << 20 || max_seq_len > ((int64_t)1 << 40))
+    return BI_ERR_UNSUPPORTED_SHAPE;
+  *n_split = std::max<int64_t>(1, (max_seq_len + *split - 1) / *split);
+  if (*n_split > 65535) return BI_ERR_UNSUPPORTED_SHAPE;  // the grid's y extent
+  *gp = Hq / Hkv <= 8 ? 8 : 16;
+  return BI_OK;
+}
+
+int64_t attn_ws_bytes(int64_t B, int64_t Hkv, int64_t n_split, int64_t gp) {
+  return B * Hkv * n_split * (BI_ATTN_HEAD_DIM + 2) * gp * 4;
+}
+
+// A paged cache [num_pages, page_size, Hkv, 128] seen as rows of Hkv * 128
+// values; a box is box_rows positions of one 64-value half of one head.
+bool encode_cache(CUtensorMap* map, const void* ptr, int64_t rows, int64_t Hkv, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(Hkv * BI_ATTN_HEAD_DIM), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(Hkv * BI_ATTN_HEAD_DIM * 2)};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+BI_API bi_status bi_decode_attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len,
+                                                     int64_t split_size, size_t* bytes) {
+  if (!bytes) return BI_ERR_INVALID_ARG;
+  int64_t n_split = 0, gp = 0;
+  bi_status st = attn_geometry(B, Hq, Hkv, max_seq_len, &split_size, &n_split, &gp);
+  if (st != BI_OK) return st;
+  *bytes = (size_t)attn_ws_bytes(B, Hkv, n_split, gp);
+  return BI_OK;
+}
+
+BI_API bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                                          void* out, int64_t B, int64_t Hq, int64_t Hkv, int64_t D,
+                                          int64_t num_pages, int64_t page_size, int64_t max_seq_len,
+                                          int64_t split_size, float scale, void* ws, size_t ws_bytes,
+                                          bi_stream_t stream) {
+  int64_t n_split = 0, gp = 0;
+  bi_status st = attn_geometry(B, Hq, Hkv, max_seq_len, &split_size, &n_split, &gp);
+  if (st != BI_OK) return st;
+  if (num_pages < 1 || page_size < 1 || bt_stride < 0 || !std::isfinite(scale)) return BI_ERR_INVALID_ARG;
+  if (D != BI_ATTN_HEAD_DIM || page_size < 8 || (page_size & (page_size - 1)) != 0 ||
+      num_pages > 0x7FFFFFFFll / page_size)
+    return BI_ERR_UNSUPPORTED_SHAPE;
+  if (bt_stride < (max_seq_len + page_size - 1) / page_size) return BI_ERR_INVALID_ARG;
+  if (B == 0) return BI_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !ws) return BI_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return BI_ERR_ALIGNMENT;
+  if (ws_bytes < (size_t)attn_ws_bytes(B, Hkv, n_split, gp)) return BI_ERR_WORKSPACE;
+  AttnLaunch A = {};
+  const int box_rows = (int)std::min<int64_t>(page_size, 64);
+  if (!encode_cache(&A.tmK, k_cache, num_pages * page_size, Hkv, box_rows) ||
+      !encode_cache(&A.tmV, v_cache, num_pages * page_size, Hkv, box_rows))
+    return BI_ERR_CUDA;
+  A.p.q = q;
+  A.p.block_table = block_table;
+  A.p.seq_lens = seq_lens;
+  A.p.part = static_cast<float*>(ws);
+  A.p.bt_stride = bt_stride;
+  A.p.num_pages = num_pages;
+  A.p.max_len = max_seq_len;
+  A.p.Hq = (int32_t)Hq;
+  A.p.Hkv = (int32_t)Hkv;
+  A.p.G = (int32_t)(Hq / Hkv);
+  A.p.page_size = (int32_t)page_size;
+  A.p.box_rows = box_rows;
+  A.p.split_size = (int32_t)split_size;
+  A.p.n_split = (int32_t)n_split;
+  A.p.qk_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+  A.p.status = device_status_word();
+  if (!A.p.status) return BI_ERR_CUDA;
+  A.out = out;
+  A.B = B;
+  A.stream = reinterpret_cast<cudaStream_t>(stream);
+  return launch_decode_attention(A) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
 BI_API bi_status bi_silu_mul_bf16(const void* gu, void* out, int64_t M, int64_t I,
                                   bi_stream_t stream) {
   if (M < 0 || I < 1) return BI_ERR_INVALID_ARG;
@@ -655,5 +750,6 @@ BI_API bi_status bi_last_device_status(bi_stream_t stream) {
   int v = 0;
   if (fetch_and_clear_stall(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return BI_ERR_CUDA;
-  return v == 0 ? BI_OK : BI_ERR_DEVICE_TIMEOUT;
+  // the word holds the first code a kernel recorded since the last read
+  return v == 0 ? BI_OK : (bi_status)v;
 }

@@ -762,6 +762,11 @@ cudaError_t launch_gemm(const GemmLaunch& L) {
   return L.pair ? launch_p<true>(L) : launch_p<false>(L);
 }
 
+int* device_status_word() {
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, g_stall_status) == cudaSuccess ? static_cast<int*>(p) : nullptr;
+}
+
 cudaError_t fetch_and_clear_stall(int* host_dst, cudaStream_t stream) {
   cudaError_t e = cudaMemcpyFromSymbolAsync(host_dst, g_stall_status, sizeof(int), 0,
                                             cudaMemcpyDeviceToHost, stream);

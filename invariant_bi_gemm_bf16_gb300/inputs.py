@@ -116,3 +116,56 @@ def scatter_rows(target: torch.Tensor, batch: int, seed: int = 0, stream: int = 
         full = torch.full((batch, K), float(corunner_fill), dtype=torch.bfloat16)
     full[torch.from_numpy(pos)] = target.to(torch.bfloat16).cpu()
     return full, pos
+
+
+STREAM_KV = 20
+
+
+def paged_kv(lens, Hkv: int, D: int, page_size: int, seed: int = 0, stream: int = STREAM_KV,
+             spare_pages: int = 0, stale: float = float("nan"), std: float = 1.0):
+    """Seeded keys and values for requests of the given lengths, in a paged
+    cache whose pages are handed out in a shuffled order (host tensors):
+    k_cache, v_cache [num_pages, page_size, Hkv, D] bf16; block_table [B, P]
+    int32 (P = the most pages any request needs, unused entries -1); seq_lens
+    [B] int32.  Cache rows past a request's length and the spare pages hold
+    ``stale``.  Layout only: no arithmetic of the method."""
+    lens = [int(x) for x in lens]
+    need = [-(-L // page_size) for L in lens]
+    total = sum(need) + int(spare_pages)
+    r = _rng(seed, stream)
+    order = r.permutation(max(total, 1))
+    k = np.full((max(total, 1), page_size, Hkv, D), stale, dtype=np.float32)
+    v = np.full((max(total, 1), page_size, Hkv, D), stale, dtype=np.float32)
+    bt = np.full((len(lens), max(max(need, default=0), 1)), -1, dtype=np.int32)
+    slot = 0
+    for b, L in enumerate(lens):
+        kd = r.standard_normal(size=(L, Hkv, D), dtype=np.float32) * np.float32(std)
+        vd = r.standard_normal(size=(L, Hkv, D), dtype=np.float32) * np.float32(std)
+        for i in range(need[b]):
+            pg = int(order[slot])
+            slot += 1
+            lo, hi = i * page_size, min((i + 1) * page_size, L)
+            k[pg, :hi - lo], v[pg, :hi - lo] = kd[lo:hi], vd[lo:hi]
+            bt[b, i] = pg
+    return to_bf16(k), to_bf16(v), torch.from_numpy(bt), torch.tensor(lens, dtype=torch.int32)
+
+
+def device_paged_kv(lens, Hkv: int, D: int, page_size: int, seed: int = 0, stream: int = STREAM_KV,
+                    device="cuda"):
+    """The same layout drawn on the device, for caches too large for the host:
+    every cache row is N(0, 1) (no stale marker), pages handed out in a seeded
+    shuffled order.  Returns (k_cache, v_cache, block_table, seq_lens) on the
+    device."""
+    lens = [int(x) for x in lens]
+    need = [-(-L // page_size) for L in lens]
+    total = max(sum(need), 1)
+    k = device_normal((total, page_size, Hkv, D), seed=seed, stream=stream, device=device)
+    v = device_normal((total, page_size, Hkv, D), seed=seed, stream=stream + 1, device=device)
+    order = _rng(seed, stream + 2).permutation(total)
+    bt = np.full((len(lens), max(max(need, default=0), 1)), -1, dtype=np.int32)
+    slot = 0
+    for b in range(len(lens)):
+        bt[b, :need[b]] = order[slot:slot + need[b]]
+        slot += need[b]
+    return (k, v, torch.from_numpy(bt).to(device),
+            torch.tensor(lens, dtype=torch.int32, device=device))

@@ -133,6 +133,38 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert lib.bi_token_logprobs_bf16(16, 34, 32, 2, 16, None) == bd.BI_ERR_ALIGNMENT
 
 
+
+def test_decode_attention_arguments_rejected_before_any_launch(bd):
+    """Decode attention's host checks: shapes, the split-size pin, alignment
+    and the workspace, all before anything touches CUDA."""
+    lib = bd.load()
+
+    def call(q=16, k=32, v=48, bt=64, bts=4, sl=80, out=96, B=2, Hq=8, Hkv=2, D=128, pages=10, P=16,
+             max_len=64, split=0, scale=0.088, ws=112, ws_bytes=1 << 30):
+        return lib.bi_decode_attention_bf16(q, k, v, bt, bts, sl, out, B, Hq, Hkv, D, pages, P, max_len, split,
+                                            scale, ws, ws_bytes, None)
+    assert call(D=64) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert call(Hq=6, Hkv=4) == bd.BI_ERR_UNSUPPORTED_SHAPE      # Hq % Hkv
+    assert call(Hq=34, Hkv=2) == bd.BI_ERR_UNSUPPORTED_SHAPE     # 17 query heads per group
+    assert call(P=12) == bd.BI_ERR_UNSUPPORTED_SHAPE             # not a power of two
+    assert call(P=4) == bd.BI_ERR_UNSUPPORTED_SHAPE              # below 8
+    assert call(split=100) == bd.BI_ERR_UNSUPPORTED_SHAPE        # not a multiple of 64
+    assert call(split=8192) == bd.BI_ERR_UNSUPPORTED_SHAPE       # above BI_ATTN_MAX_SPLIT
+    assert call(split=-64) == bd.BI_ERR_INVALID_ARG
+    assert call(max_len=65, bts=4) == bd.BI_ERR_INVALID_ARG      # the block table is too short
+    assert call(scale=float("nan")) == bd.BI_ERR_INVALID_ARG
+    assert call(q=None) == bd.BI_ERR_INVALID_ARG
+    assert call(q=18) == bd.BI_ERR_ALIGNMENT
+    assert call(sl=82) == bd.BI_ERR_ALIGNMENT
+    assert call(ws_bytes=100) == bd.BI_ERR_WORKSPACE
+    assert call(B=0, q=None, k=None, v=None, bt=None, sl=None, out=None, ws=None) == bd.BI_OK
+    # workspace: B * Hkv * ceil(max_len / split) * (128 + 2) * GP * 4
+    assert bd.bi_decode_attention_workspace_bytes(2, 8, 2, 1000, 256) == 2 * 2 * 4 * 130 * 8 * 4
+    assert bd.bi_decode_attention_workspace_bytes(3, 32, 2, 64, 64) == 3 * 2 * 1 * 130 * 16 * 4
+    assert bd.bi_decode_attention_workspace_bytes(1, 8, 8, 0, 0) == 1 * 8 * 1 * 130 * 8 * 4
+    assert bd.bi_decode_attention_workspace_bytes(1, 8, 8, 1000, 0) == \
+        bd.bi_decode_attention_workspace_bytes(1, 8, 8, 1000, bd.BI_ATTN_DEFAULT_SPLIT)
+
 ALL_M = list(range(1, 300)) + [511, 512, 513, 1000, 1023, 1024, 2048, 4095, 4096, 8191, 8192]
 
 
