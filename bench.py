@@ -577,12 +577,16 @@ def run_fp8(args, dist, peaks):
             q, sxv = bd.bi_quantize_rows_e4m3(xs[i % nx], q=qbuf[0], scale=qbuf[1])
             bd.bi_gemm_fp8(q, sxv, wq[i % nw][0], wq[i % nw][1], out=y, pins=pins)
         us_layer = time_reps(layer, args.per_m_reps)
+        us_q = time_reps(lambda i: bd.bi_quantize_rows_e4m3(xs[i % nx], q=qbuf[0], scale=qbuf[1]), args.per_m_reps)
+        bq = 3.0 * M * K + 4.0 * M   # bf16 in, E4M3 codes and fp32 scales out
         tus = time_reps(lambda i: torch.mm(xs[i % nx], Ws[i % nw].t(), out=y), args.per_m_reps)
         f = 2.0 * M * N * K
         b = float(N * K + M * K + 2 * M * N + 4 * (M + N))
         t_roof = max(f / (peak8 * 1e6), b / (peaks["hbm_gbs"] * 1e3))
         res.append({"M": M, "gemm_us": round(us_gemm, 2), "tflops": round(f / us_gemm / 1e6, 1),
                     "roofline_frac": round(t_roof / us_gemm, 3), "quantize_and_gemm_us": round(us_layer, 2),
+                    "quantize_us": round(us_q, 2),
+                    "quantize_hbm_frac": round(bq / us_q / 1e3 / peaks["hbm_gbs"], 3),
                     "baseline_us": round(tus, 2), "vs_baseline": round(tus / us_gemm, 3)})
         del xs, xq
     del Ws, wq

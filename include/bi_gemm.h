@@ -288,8 +288,10 @@ bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t 
  * value 448, no infinities) with a per-row scale amax / 448. */
 
 /* Per-row quantisation: for each row of X [M,K] bf16, amax = max |x|,
- * scale[m] = amax / 448 (IEEE division; 1 for a zero row), Q[m,k] =
- * E4M3(x / scale[m]) rounded to nearest even, saturated at +-448.  A row with
+ * scale[m] = amax / 448 and inv = 448 / amax (IEEE divisions, once per row;
+ * both 1 for a zero row; inv clamped to the largest finite float when 448 / amax
+ * overflows), Q[m,k] = E4M3(x * inv), the fp32 product rounded to
+ * nearest even, saturated at +-448.  A row with
  * a NaN or an infinity gets scale NaN and NaN codes (0x7F).  Used for the
  * activations (per token) and, offline, for the weights (per output channel).
  * Q: uint8 [M,K]; scale: fp32 [M].

@@ -1,9 +1,11 @@
 // quant.cu -- per-row E4M3 quantisation for the FP8 GEMM.
 //
 // For each row (a token of the activations, or an output channel of the
-// weights): amax = max_k |x_k|, scale = amax / 448 (IEEE division; 1 for a
-// zero row), q_k = E4M3(x_k / scale) rounded to nearest even and saturated at
-// +-448 (cvt.rn.satfinite).  A row holding a NaN or an infinity gets scale NaN
+// weights): amax = max_k |x_k|, scale = amax / 448 and inv = 448 / amax (IEEE
+// divisions once per row; both 1 for a zero row; inv clamped to the largest
+// finite float when 448 / amax overflows), q_k = E4M3(x_k * inv), the
+// fp32 product rounded to nearest even and saturated at +-448
+// (cvt.rn.satfinite).  A row holding a NaN or an infinity gets scale NaN
 // and NaN codes (0x7F).  The maximum is exact whatever the order it is taken
 // in, and every code depends on its own row only.  Detent (Batch-Invariant LLM
 // Serving and RL Rollouts at Near-Stock Speed), Limits: dynamic per-tensor FP8
@@ -27,10 +29,10 @@ __device__ __forceinline__ void amax2(uint32_t w, float& amax, bool& bad) {
   amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
 }
 
-// Four E4M3 codes of x[0..3] / s, x[0] in the lowest byte.
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float s) {
-  const uint32_t lo = cvt_e4m3x2(__fdiv_rn(q_lo(w0), s), __fdiv_rn(q_hi(w0), s));
-  const uint32_t hi = cvt_e4m3x2(__fdiv_rn(q_lo(w1), s), __fdiv_rn(q_hi(w1), s));
+// Four E4M3 codes of x[0..3] * inv, x[0] in the lowest byte.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float inv) {
+  const uint32_t lo = cvt_e4m3x2(__fmul_rn(q_lo(w0), inv), __fmul_rn(q_hi(w0), inv));
+  const uint32_t hi = cvt_e4m3x2(__fmul_rn(q_lo(w1), inv), __fmul_rn(q_hi(w1), inv));
   return lo | (hi << 16);
 }
 
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps)
     bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
   }
   const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
+  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
   if (lane == 0) scale[row] = s;
   uint2* q = Q + row * nvec;
   for (int64_t i = lane; i < nvec; i += 32) {
@@ -66,13 +69,89 @@ __global__ void __launch_bounds__(32 * kQuantWarps)
       q[i] = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
     } else {
       const uint4 v = x[i];
-      q[i] = make_uint2(codes4(v.x, v.y, s), codes4(v.z, v.w, s));
+      q[i] = make_uint2(codes4(v.x, v.y, inv), codes4(v.z, v.w, inv));
     }
   }
 }
 
+// X [M,K] bf16 -> Q, scale; one CTA of kQRowThreads per row, the row held in
+// registers (VPT vectors of 8 per thread), so HBM is read once.  The same
+// arithmetic as quantize_e4m3_kernel: the maximum is exact in any order.
+constexpr int kQRowThreads = 256;
+constexpr int kQRowMaxVpt = 16;
+
+template <int VPT>
+__global__ void __launch_bounds__(kQRowThreads)
+    quantize_e4m3_row_kernel(const uint4* X, uint2* Q, float* scale, int64_t K) {
+  __shared__ float wmax[kQRowThreads / 32];
+  __shared__ int wbad[kQRowThreads / 32];
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int64_t row = blockIdx.x, nvec = K / 8;
+  const uint4* x = X + row * nvec;
+  uint4 v[VPT];
+  float amax = 0.0f;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int64_t j = threadIdx.x + (int64_t)i * kQRowThreads;
+    if (j < nvec) {
+      v[i] = x[j];
+      amax2(v[i].x, amax, bad);
+      amax2(v[i].y, amax, bad);
+      amax2(v[i].z, amax, bad);
+      amax2(v[i].w, amax, bad);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    wmax[warp] = amax;
+    wbad[warp] = bad;
+  }
+  __syncthreads();
+  amax = wmax[0];
+  bad = wbad[0] != 0;
+#pragma unroll
+  for (int w = 1; w < kQRowThreads / 32; ++w) {
+    amax = fmaxf(amax, wmax[w]);
+    bad = bad || wbad[w] != 0;
+  }
+  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
+  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
+  if (threadIdx.x == 0) scale[row] = s;
+  uint2* q = Q + row * nvec;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int64_t j = threadIdx.x + (int64_t)i * kQRowThreads;
+    if (j < nvec)
+      q[j] = bad ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu)
+                 : make_uint2(codes4(v[i].x, v[i].y, inv), codes4(v[i].z, v[i].w, inv));
+  }
+}
+
+template <int VPT>
+static cudaError_t launch_rows_vpt(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                   cudaStream_t stream) {
+  return launch_overlapped(quantize_e4m3_row_kernel<VPT>, dim3((unsigned)M), dim3(kQRowThreads), stream,
+                           static_cast<const uint4*>(X), static_cast<uint2*>(Q), scale, K);
+}
+
 cudaError_t launch_quantize_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
                                  cudaStream_t stream) {
+  const int64_t vpt = (K / 8 + kQRowThreads - 1) / kQRowThreads;
+  if (M <= 0x7FFFFFFF && vpt <= kQRowMaxVpt) {
+    if (vpt <= 1) return launch_rows_vpt<1>(X, Q, scale, M, K, stream);
+    if (vpt <= 2) return launch_rows_vpt<2>(X, Q, scale, M, K, stream);
+    if (vpt <= 4) return launch_rows_vpt<4>(X, Q, scale, M, K, stream);
+    if (vpt <= 8) return launch_rows_vpt<8>(X, Q, scale, M, K, stream);
+    return launch_rows_vpt<16>(X, Q, scale, M, K, stream);
+  }
+  // rows too long for registers: one warp per row, two reads of the row
   const int64_t blocks = (M + kQuantWarps - 1) / kQuantWarps;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   return launch_overlapped(quantize_e4m3_kernel, dim3((unsigned)blocks), dim3(32 * kQuantWarps), stream,

@@ -63,7 +63,11 @@ def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so with gcc (no fused multiply-add)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp.%d" % os.getpid()
-        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+        # -fno-tree-vrp -fno-thread-jumps: gcc 13 at -O2 threaded a branch on
+        # a float range and folded amax / 448 to 0 for a subnormal amax (the
+        # quotient is a nonzero subnormal); the oracle gives up those passes.
+        cmd = ["gcc", "-O2", "-fno-tree-vrp", "-fno-thread-jumps", "-std=c11", "-ffp-contract=off",
+               "-fno-fast-math", "-fPIC",
                "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)

@@ -44,8 +44,11 @@
  * construction).
  *
  * Build with -ffp-contract=off so that no multiply-add is fused: each product
- * and each sum is rounded to fp32 separately, exactly as written.
+ * and each sum is rounded to fp32 separately, exactly as written; and without
+ * gcc's value-range propagation and jump threading, which folded a subnormal
+ * quotient to zero in the quantiser (gcc 13, -O2).
  */
+#include <float.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -447,9 +450,13 @@ uint8_t oracle_e4m3_rne_sat(float x) {
 }
 
 /* Per-row (per-token, or per-channel for weights) quantisation of a bf16 row:
- *   amax = max_k |x_k|;  scale = amax / 448 (fp32 division);
- *   q_k = e4m3_rne_sat(x_k / scale) (fp32 division).
- * amax == 0 gives scale 1 (and zero codes); a NaN or an infinity in the row
+ *   amax = max_k |x_k|;  scale = amax / 448 and inv = 448 / amax (fp32
+ *   divisions, once per row);  q_k = e4m3_rne_sat(x_k * inv) (the product
+ *   rounded to fp32, then to E4M3).
+ * The pages fix no formula; multiplying by the reciprocal scale is the usual
+ * form of per-token quantisation.  scale is what dequantises the GEMM's sum.
+ * amax == 0 gives scale 1 and inv 1 (zero codes); inv is clamped to the largest
+ * finite float when 448 / amax overflows; a NaN or an infinity in the row
  * gives scale NaN and NaN codes.  Detent, Limits: dynamic per-tensor FP8
  * activation scales span the batch; per-token or static scales keep each
  * row's bits its own. */
@@ -467,8 +474,10 @@ static void quantize_row(const uint16_t* x, int64_t K, uint8_t* q, float* scale)
     return;
   }
   const float s = amax == 0.0f ? 1.0f : amax / 448.0f;
+  float inv = amax == 0.0f ? 1.0f : 448.0f / amax;
+  if (inv > FLT_MAX) inv = FLT_MAX; /* amax below about 1.3e-36: keep the product finite */
   *scale = s;
-  for (int64_t k = 0; k < K; ++k) q[k] = oracle_e4m3_rne_sat(oracle_bf16_to_f32(x[k]) / s);
+  for (int64_t k = 0; k < K; ++k) q[k] = oracle_e4m3_rne_sat(oracle_bf16_to_f32(x[k]) * inv);
 }
 
 typedef struct {

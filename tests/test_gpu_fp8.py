@@ -16,7 +16,7 @@ def u8(t):
     return t.cpu().numpy()
 
 
-@pytest.mark.parametrize("M,K", [(1, 16), (37, 4096), (300, 14336), (5, 1040)])
+@pytest.mark.parametrize("M,K", [(1, 16), (37, 4096), (300, 14336), (5, 1040), (3, 28672), (4, 33024)])
 def test_quantize_bit_exact(lib, oracle, M, K):
     X = inputs.rows_loguniform(M, K, lo=1e-3, hi=1e3, seed=40, stream=0)
     want_q, want_s = oracle.quantize_rows_e4m3(inputs.bits(X))
@@ -27,7 +27,8 @@ def test_quantize_bit_exact(lib, oracle, M, K):
 
 def test_quantize_special_rows(lib, oracle):
     K = 64
-    rows = np.ones((5, K), dtype=np.float32)
+    rows = np.ones((6, K), dtype=np.float32)
+    rows[5] = np.linspace(-1e-38, 1e-38, K)      # amax below 448 / FLT_MAX: inv is clamped
     rows[0] = 0.0
     rows[1, 3] = np.nan
     rows[2, 7] = -np.inf

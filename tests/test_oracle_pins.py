@@ -791,3 +791,33 @@ def test_attention_empty_requests_and_nan_rows(oracle):
     out = attn(oracle, q, [k, empty_k], [v, empty_k], 0.5)
     assert np.all(np.isfinite(out[0, :2])) and np.all(np.isnan(out[0, 2:]))
     assert np.array_equal(out[1], np.zeros((Hq, D)))
+
+
+def test_quantize_multiplies_by_the_reciprocal_scale(oracle):
+    # amax = 0.8125 = 13/16 and x = -0.3046875 = -39/128: the exact quotient
+    # x / (amax / 448) is -168, an E4M3 tie between 160 (mantissa 010) and 176
+    # (011).  inv = fl(448 / 0.8125) lies above 551.3846..., so x * inv is just
+    # past -168 and rounds to -176 (code 0xF3); fl(amax / 448) lies above
+    # 13/7168, so x / scale is just short of -168 and would round to the even
+    # -160 (0xF2).  The codes follow the product with the reciprocal.
+    inv = np.float32(448.0) / np.float32(0.8125)
+    assert float(inv) > 448.0 / 0.8125
+    row = np.zeros((1, 16), dtype=np.float32)
+    row[0, 0], row[0, 1] = 0.8125, -0.3046875
+    bits = (row.view(np.uint32) >> 16).astype(np.uint16)
+    q, s = oracle.quantize_rows_e4m3(bits)
+    assert s[0] == np.float32(np.float32(0.8125) / np.float32(448.0))
+    assert q[0, 0] == 0x7E and q[0, 1] == 0xF3
+
+
+def test_quantize_subnormal_rows_keep_their_scale(oracle):
+    # amax = 9.918e-39 (a subnormal binary32): scale = amax / 448 is the
+    # subnormal 2.2139e-41, never 0; inv = 448 / amax overflows and is clamped
+    # to the largest finite float, so amax * inv = 3.377... gives E4M3 3.5 (0x45).
+    r = np.zeros((1, 16), dtype=np.float32)
+    r[0, 0] = 1e-38
+    bits = (r.view(np.uint32) >> 16).astype(np.uint16)
+    amax = bf16_val(bits)[0, 0]
+    q, s = oracle.quantize_rows_e4m3(bits)
+    assert s[0] == np.float32(amax) / np.float32(448.0) and s[0] > 0
+    assert q[0, 0] == 0x45 and np.all(q[0, 1:] == 0)
