@@ -49,20 +49,31 @@ EPS = 1e-5
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of single
 # launches, from ncu captures of `python bench.py --single-m M --launches 2`
-# (summaries in profiles/), valid only for the kernel build they were taken on.
+# (summaries in profiles/), keyed by build_fingerprint() of the GEMM kernel's
+# sources: valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "5accb49fb0461f679cabb3a5fa698ca0c8d0b41cc2d0f89785e05b4eddf36be6": {8192: 965074688 + 63709440,
-                                                                         1: 117513216 + 3063040},
+    "b0dc026b481772df931f264dd6603233ad9eafd580b0080e12cc956b3ec716ad": {8192: 964988928 + 63569152,
+                                                                        1: 117509632 + 2750208},
 }
 
 
-def build_fingerprint():
-    p = os.path.join(ROOT, "invariant_bi_gemm_bf16_gb300", "libbi_gemm.so.stamp")
+def build_fingerprint(kernel_files=("gemm.cu", "ptx.cuh", "internal.h")):
+    """SHA-256 of the sources one kernel is compiled from (default: the GEMM
+    kernel's) and the compiler flags: DRAM counters taken by ncu stay valid
+    while this is unchanged.  The public header is left out: the kernel uses
+    only its ABI constants (tile sizes, flag bits, status codes), which do not
+    change."""
+    import hashlib
+    from invariant_bi_gemm_bf16_gb300 import build as B
+    h = hashlib.sha256()
     try:
-        with open(p) as f:
-            return f.read().strip()
+        for name in kernel_files:
+            with open(os.path.join(B.CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
     except OSError:
         return None
+    h.update(" ".join(B.NVCC_FLAGS).encode())
+    return h.hexdigest()
 
 
 def load_peaks():

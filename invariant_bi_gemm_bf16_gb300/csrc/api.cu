@@ -13,6 +13,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "attention.h"
 #include "internal.h"
 
 #define BI_API extern "C" __attribute__((visibility("default")))

@@ -27,6 +27,7 @@
 // No other request, and no batch size, reaches any of these steps.
 #include <cuda_bf16.h>
 
+#include "attention.h"
 #include "internal.h"
 #include "ptx.cuh"
 

@@ -97,26 +97,6 @@ cudaError_t launch_overlapped_smem(void (*kern)(KArgs...), dim3 grid, dim3 block
 }
 
 
-// Decode attention (attention.cu).
-struct AttnParams {
-  const void* q;               // [B, Hq, 128] bf16
-  const int32_t* block_table;  // [B, bt_stride] page ids
-  const int32_t* seq_lens;     // [B]
-  float* part;                 // per (request, kv head, split): o^T [128][GP], m [GP], l [GP]
-  int64_t bt_stride, num_pages;
-  int64_t max_len;             // every seq_lens[b] must be in [0, max_len]
-  int32_t Hq, Hkv, G, page_size, box_rows, split_size, n_split;
-  float qk_log2;               // scale * log2(e)
-  int* status;                 // the device status word
-};
-struct AttnLaunch {
-  CUtensorMap tmK, tmV;  // caches as [num_pages * page_size, Hkv * 128], box 64 x box_rows, 128-byte swizzle
-  AttnParams p;
-  void* out;             // [B, Hq, 128] bf16
-  int64_t B;
-  cudaStream_t stream;
-};
-cudaError_t launch_decode_attention(const AttnLaunch& A);
 // Device address of the status word that bi_last_device_status() reads.
 int* device_status_word();
 
