@@ -331,11 +331,12 @@ bi_status bi_gemm_fp8(const void* Xq, const float* sx, const void* Wq, const flo
 #define BI_ATTN_MAX_SPLIT 4096
 #define BI_ATTN_DEFAULT_SPLIT 256
 
-/* Workspace of bi_decode_attention_bf16, in *bytes:
- * B * Hkv * n_split * (128 + 2) * GP * 4, n_split = max(1, ceil(max_seq_len /
- * split_size)), GP = 8 for up to 8 query heads per key/value head, else 16.
- * split_size 0 = BI_ATTN_DEFAULT_SPLIT.  Errors: as the call's shape checks.
- * Host only. */
+/* Workspace of bi_decode_attention_bf16, in *bytes: 256 + the item list
+ * (B * n_split * 4, rounded up to 256) + B * Hkv * n_split * (128 + 2) * GP * 4,
+ * n_split = max(1, ceil(max_seq_len / split_size)), GP = 8 for up to 8 query
+ * heads per key/value head, else 16.  split_size 0 = BI_ATTN_DEFAULT_SPLIT.
+ * Every call rewrites the whole workspace it uses: no initial contents are
+ * needed.  Errors: as the call's shape checks.  Host only. */
 bi_status bi_decode_attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len,
                                               int64_t split_size, size_t* bytes);
 
@@ -349,20 +350,20 @@ bi_status bi_decode_attention_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv
  *             row p % page_size of page block_table[b * bt_stride + p / page_size]
  *   block_table [B, bt_stride] int32, seq_lens [B] int32 (device memory)
  *   out       [B, Hq, D] bf16
- * The tree: positions split at multiples of split_size; within a split, tiles
- * of 64 positions, each warp of four owning 16 positions of every tile with a
- * running (max, sum, output) state in fp32 (scores on the tensor cores with
- * fp32 accumulation, exp2 of the log2-scaled scores, weights rounded to bf16
- * before they multiply v and before they are summed); the warps' states fold
- * in warp order, the splits' in split order; out = bf16_rne(o / l).  It
- * depends on seq_lens[b], split_size and D only: no other request, batch size
- * or page placement reaches it.  An empty request (length 0) gives zeros;
+ * The tree: positions split at multiples of split_size; one warp runs a
+ * split over chunks of 16 positions in ascending order with a running (max,
+ * sum, output) state in fp32 (scores on the tensor cores with fp32
+ * accumulation, exp2 of the log2-scaled scores, weights rounded to bf16
+ * before they multiply v and before they are summed); the splits' states
+ * fold in split order; out = bf16_rne(o / l).  It depends on seq_lens[b],
+ * split_size and D only: no other request, batch size or page placement
+ * reaches it, and which warp runs a split, or when, is scheduling only.  An empty request (length 0) gives zeros;
  * NaN / +Inf scores give NaN.
  * Requirements: D == 128; Hq % Hkv == 0 and Hq / Hkv <= 16; page_size a power
  * of two >= 8 with num_pages * page_size < 2^31; split_size a multiple of 64,
  * at most BI_ATTN_MAX_SPLIT (0 = BI_ATTN_DEFAULT_SPLIT); every seq_lens[b] <=
  * max_seq_len <= bt_stride * page_size; B, Hkv and ceil(max_seq_len /
- * split_size) <= 65535; q, caches, out and
+ * split_size) <= 65535 and their product < 2^31; q, caches, out and
  * ws 16-byte aligned, block_table and seq_lens 4-byte aligned; ws_bytes at
  * least bi_decode_attention_workspace_bytes(...).  Cache rows past a
  * request's length are never used (they may hold anything).

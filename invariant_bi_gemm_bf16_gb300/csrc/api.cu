@@ -639,13 +639,19 @@ bi_status attn_geometry(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len,
       Hkv > 65535 || Hq > (int64_t)1 << 20 || max_seq_len > ((int64_t)1 << 40))
     return BI_ERR_UNSUPPORTED_SHAPE;
   *n_split = std::max<int64_t>(1, (max_seq_len + *split - 1) / *split);
-  if (*n_split > 65535) return BI_ERR_UNSUPPORTED_SHAPE;  // the grid's y extent
+  // item entries pack (request, split) into 16 bits each; tickets are 32-bit
+  if (*n_split > 65535 || B * *n_split * Hkv >= ((int64_t)1 << 31)) return BI_ERR_UNSUPPORTED_SHAPE;
   *gp = Hq / Hkv <= 8 ? 8 : 16;
   return BI_OK;
 }
 
+// Workspace: 256 bytes of control words (ticket counter, item count), the
+// item list (one uint32 per (request, split), padded to 256 bytes), then the
+// split records (B * Hkv * n_split of (128 + 2) * GP floats).
+int64_t attn_list_bytes(int64_t B, int64_t n_split) { return (B * n_split * 4 + 255) / 256 * 256; }
+
 int64_t attn_ws_bytes(int64_t B, int64_t Hkv, int64_t n_split, int64_t gp) {
-  return B * Hkv * n_split * (BI_ATTN_HEAD_DIM + 2) * gp * 4;
+  return 256 + attn_list_bytes(B, n_split) + B * Hkv * n_split * (BI_ATTN_HEAD_DIM + 2) * gp * 4;
 }
 
 // A paged cache [num_pages, page_size, Hkv, 128] seen as rows of Hkv * 128
@@ -695,14 +701,16 @@ BI_API bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, co
     return BI_ERR_ALIGNMENT;
   if (ws_bytes < (size_t)attn_ws_bytes(B, Hkv, n_split, gp)) return BI_ERR_WORKSPACE;
   AttnLaunch A = {};
-  const int box_rows = (int)std::min<int64_t>(page_size, 64);
+  const int box_rows = (int)std::min<int64_t>(page_size, 32);
   if (!encode_cache(&A.tmK, k_cache, num_pages * page_size, Hkv, box_rows) ||
       !encode_cache(&A.tmV, v_cache, num_pages * page_size, Hkv, box_rows))
     return BI_ERR_CUDA;
   A.p.q = q;
   A.p.block_table = block_table;
   A.p.seq_lens = seq_lens;
-  A.p.part = static_cast<float*>(ws);
+  A.p.ctl = static_cast<uint32_t*>(ws);
+  A.p.items = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + 256);
+  A.p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + 256 + attn_list_bytes(B, n_split));
   A.p.bt_stride = bt_stride;
   A.p.num_pages = num_pages;
   A.p.max_len = max_seq_len;
@@ -718,6 +726,7 @@ BI_API bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, co
   if (!A.p.status) return BI_ERR_CUDA;
   A.out = out;
   A.B = B;
+  A.grid = sm_count_current();
   A.stream = reinterpret_cast<cudaStream_t>(stream);
   return launch_decode_attention(A) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }

@@ -12,19 +12,29 @@
 // The reduction tree of query head h of request b, a function of the
 // request's length L, the split size and the head dimension only:
 //   * split s covers positions [s*S, min((s+1)*S, L));
-//   * within a split, tiles of 64 positions in ascending order; warp w of the
-//     CTA owns positions 16w .. 16w+15 of every tile and keeps a running
-//     (max m, sum l, unnormalised output o) over them: per tile, the scores
-//     t = (q . k) * scale * log2(e) (fp32 MMA accumulation over d in
-//     ascending 16-wide steps), m' = max(m, max t), then o and l are scaled
-//     by 2^(m - m'), p = 2^(t - m') is rounded to bf16, l gains the sum of
-//     the rounded p, and o gains p . v (fp32 MMA accumulation);
+//   * one warp runs a split alone, over steps of 32 positions in ascending
+//     order, keeping a running (max m, sum l, unnormalised output o): per
+//     step, the scores t = (q . k) * scale * log2(e) (fp32 MMA accumulation
+//     over d in ascending 16-wide steps), m' = max(m, max t), then o and l
+//     are scaled by 2^(m - m'), p = 2^(t - m') (ex2.approx) is rounded to
+//     bf16, l gains the sum of the rounded p (ascending position within a
+//     lane: rows g, g + 8, g + 16, g + 24), and o gains p . v (fp32 MMA
+//     accumulation, the step's two 16-position chunks in order);
 //   * per-lane partial sums of l are added by a fixed xor butterfly;
-//   * the four warps' states fold in warp order, then the splits' states
-//     fold in split order, both with
+//   * the splits' states fold in split order with
 //       m = max(m1, m2), a_i = 2^(m_i - m), l = l1 a1 + l2 a2, o = o1 a1 + o2 a2;
 //   * out = bf16_rne(o / l).
-// No other request, and no batch size, reaches any of these steps.
+// No other request, and no batch size, reaches any of these steps: which
+// warp runs a split, and when, is scheduling only.
+//
+// Three kernels per call, chained by programmatic dependent launch:
+//   plan     one CTA lists the (request, split) items, full splits first,
+//            and resets the ticket counter;
+//   stream   persistent, one CTA per SM; every warp is an independent
+//            stream: it takes items by ticket, stages their 32-position K/V
+//            tiles (and q) through its own ring of TMA copies, runs the
+//            split and writes its record;
+//   combine  folds each request's split records in order.
 #include <cuda_bf16.h>
 
 #include "attention.h"
@@ -33,71 +43,61 @@
 
 namespace bi {
 
-constexpr int kAttnD = 128;                             // head dimension
-constexpr int kAttnTile = 64;                           // positions per staged tile
-constexpr int kAttnCWarps = 4;                          // compute warps (16 positions of a tile each)
-constexpr int kAttnThreads = 32 * (kAttnCWarps + 1);    // + one copy warp
-// Ring depth and resident CTAs per SM, for up to 8 query heads per group
-// (NT = 1) and for 9 to 16 (NT = 2, more registers per thread).  Speed only.
-#ifndef BI_ATTN_STAGES_NT1
-#define BI_ATTN_STAGES_NT1 2
-#endif
-#ifndef BI_ATTN_CTAS_NT1
-#define BI_ATTN_CTAS_NT1 3
-#endif
-#ifndef BI_ATTN_STAGES_NT2
-#define BI_ATTN_STAGES_NT2 3
-#endif
-#ifndef BI_ATTN_CTAS_NT2
-#define BI_ATTN_CTAS_NT2 2
-#endif
-template <int NT> struct AttnCfg;
-template <> struct AttnCfg<1> { static constexpr int stages = BI_ATTN_STAGES_NT1, ctas = BI_ATTN_CTAS_NT1; };
-template <> struct AttnCfg<2> { static constexpr int stages = BI_ATTN_STAGES_NT2, ctas = BI_ATTN_CTAS_NT2; };
-constexpr int kAttnHalfBytes = kAttnTile * 128;         // 64 positions x 64 values
-constexpr int kAttnKVBytes = 2 * kAttnHalfBytes;        // 64 positions x 128 values
-constexpr int kAttnStageBytes = 2 * kAttnKVBytes;       // K tile, then V tile
-template <int NT>
-constexpr int attn_smem_bytes() { return AttnCfg<NT>::stages * kAttnStageBytes + 1024; }
-constexpr int kAttnMaxSplitPages = BI_ATTN_MAX_SPLIT / 8 + 1;
+constexpr int kAttnD = 128;                        // head dimension
+constexpr int kAttnTile = 32;                      // positions per staged tile (two chunks of 16)
+constexpr int kAttnStages = 2;                     // tiles in flight per warp
+constexpr int kAttnHalfBytes = kAttnTile * 128;    // 32 positions x 64 values
+constexpr int kAttnKVBytes = 2 * kAttnHalfBytes;   // 32 positions x 128 values
 constexpr uint64_t kAttnWaitNs = 2000000000ull;
+
+// Stream warps per CTA and stage layout, for up to 8 query heads per group
+// (NT = 1) and for 9 to 16 (NT = 2).  A stage holds the K tile, the V tile
+// and room for the group's q rows (copied with an item's first tile).
+template <int NT>
+struct AttnCfg {
+  static constexpr int warps = NT == 1 ? 6 : 5;
+  static constexpr int q_bytes = 8 * NT * kAttnD * 2;
+  static constexpr int stage_bytes = 2 * kAttnKVBytes + q_bytes;
+  static constexpr int smem = warps * kAttnStages * stage_bytes + 1024;
+};
+static_assert(AttnCfg<1>::stage_bytes % 1024 == 0 && AttnCfg<2>::stage_bytes % 1024 == 0,
+              "stages must keep the 1024-byte alignment of the 128-byte swizzle");
+static_assert(AttnCfg<1>::smem <= kMaxDynSmem && AttnCfg<2>::smem <= kMaxDynSmem, "ring too large");
 
 __device__ __forceinline__ void attn_flag(int* status, int code) { atomicCAS(status, 0, code); }
 
-// Waits for the phase of `parity` on `bar`; false once the CTA gives up (this
-// wait ran 2 s, or another warp gave up).
-__device__ __noinline__ bool attn_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
-                                            int* status) {
+// Waits for the phase of `parity` on `bar`, at most 2 s; false if it ran out
+// (the status word is set).
+__device__ __noinline__ bool attn_wait_slow(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
     if (globaltimer_ns() - t0 > kAttnWaitNs) {
-      *abort = 1;
       attn_flag(status, (int)BI_ERR_DEVICE_TIMEOUT);
       return false;
     }
   }
 }
 
-__device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  return attn_wait_slow(bar, parity, abort, status);
+  return attn_wait_slow(bar, parity, status);
 }
 
-// Bounded wait that ignores the abort flag (for copies still in flight).
-__device__ __noinline__ void attn_drain(uint32_t bar, uint32_t parity, int* status) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kAttnWaitNs) {
-      attn_flag(status, (int)BI_ERR_DEVICE_TIMEOUT);
-      return;
-    }
-  }
+__device__ __forceinline__ void attn_drain(uint32_t bar, uint32_t parity, int* status) {
+  attn_wait(bar, parity, status);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo, __nv_bfloat16 hi) {
   return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+
+// 2^x by the ex2.approx instruction (relative error about 2^-22, far below
+// the bf16 rounding the weights get next); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // The fold of two running states (one column of o).
@@ -107,294 +107,434 @@ __device__ __forceinline__ void attn_scales(float m1, float m2, float& m, float&
   a2 = (m2 == m) ? 1.0f : exp2f(__fsub_rn(m2, m));
 }
 
-// One CTA per (key/value head, split s, request): the running state of the
-// split's positions, written as a partial record.
-template <int NT>
-__global__ void __launch_bounds__(kAttnThreads, AttnCfg<NT>::ctas)
-    decode_attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                             const AttnParams p) {
-  constexpr int GP = 8 * NT;  // query-head columns of the MMAs (G <= GP)
-  constexpr int kAttnStages = AttnCfg<NT>::stages;
-  extern __shared__ uint8_t attn_smem_raw[];
-  __shared__ __align__(8) uint64_t full[kAttnStages];
-  __shared__ __align__(8) uint64_t empty[kAttnStages];
-  __shared__ int32_t pages[kAttnMaxSplitPages];
-  __shared__ int abort_flag;
+// ---------------------------------------------------------------------------
+// plan: the list of (request, split) items and the ticket counter
+// ---------------------------------------------------------------------------
 
-  grid_dep_launch_dependents();
-  grid_dep_wait();  // q and the cache may come from the previous kernel in the stream
+constexpr int kPlanThreads = 1024;
 
-  // The heads of one (request, split) are neighbours in the grid: they run
-  // together and read the same cache rows (each its 256 bytes of a row).
-  const int kvh = blockIdx.x, s = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int64_t L = p.seq_lens[b];
-  if (L < 0 || L > p.max_len) {
-    if (threadIdx.x == 0 && s == 0 && kvh == 0) attn_flag(p.status, (int)BI_ERR_INVALID_ARG);
-    return;
+// Exclusive prefix sum over the CTA (kPlanThreads threads); *total gets the sum.
+__device__ __forceinline__ uint64_t plan_scan(uint64_t v, uint64_t* sh, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  const int64_t p0 = (int64_t)s * p.split_size;
-  if (p0 >= L) return;  // past the request's end: nothing to do
-  const int64_t p1 = min(p0 + (int64_t)p.split_size, L);
-  const int n_tiles = (int)((p1 - p0 + kAttnTile - 1) / kAttnTile);
-  const uint32_t base = (smem_u32(attn_smem_raw) + 1023u) & ~1023u;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort = &abort_flag;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kAttnStages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kAttnCWarps);
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t w = sh[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
     }
-    abort_flag = 0;
-    fence_mbar_init();
+    sh[lane] = w;  // inclusive over warps
   }
   __syncthreads();
+  const uint64_t before = warp > 0 ? sh[warp - 1] : 0;
+  *total = sh[31];
+  __syncthreads();  // sh is reused by the next call
+  return before + x - v;
+}
 
-  if (warp == kAttnCWarps) {
-    // ---------------- copy warp: the split's page ids, then the K/V tiles
-    const int64_t first_page = p0 / p.page_size;
-    const int n_pages = (int)((p1 - 1) / p.page_size - first_page + 1);
-    const int64_t rows = p.num_pages * p.page_size;
-    for (int i = lane; i < n_pages; i += 32) {
-      int32_t pg = p.block_table[b * p.bt_stride + first_page + i];
-      if (pg < 0 || (int64_t)pg >= p.num_pages) {
-        attn_flag(p.status, (int)BI_ERR_INVALID_ARG);
-        pg = -1;  // loaded from past the cache's end: zeros
-      }
-      pages[i] = pg;
+// Items: full splits first (request-major), then the requests' partial last
+// splits.  Entry = (b << 16) | s.  An invalid length gives no items (and is
+// flagged; the combine writes NaN for it).
+__global__ void __launch_bounds__(kPlanThreads) decode_attn_plan_kernel(const AttnParams p, int64_t B) {
+  __shared__ uint64_t sh[32];
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // the lengths may come from the previous kernel in the stream
+  auto length = [&](int64_t b) -> int64_t {
+    const int64_t L = p.seq_lens[b];
+    if (L < 0 || L > p.max_len) {
+      attn_flag(p.status, (int)BI_ERR_INVALID_ARG);
+      return 0;
     }
-    __syncwarp();
-    if (lane == 0) {
-      int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % kAttnStages;
-        if (t >= kAttnStages &&
-            !attn_wait(smem_u32(&empty[st]), ((t / kAttnStages) - 1) & 1, abort, p.status))
-          break;
-        const int64_t tp = p0 + (int64_t)t * kAttnTile;
-        int boxes = 0;
-        for (int r = 0; r < kAttnTile && tp + r < p1; r += p.box_rows) ++boxes;
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(fb, (uint32_t)(boxes * p.box_rows * 128 * 4));
-        const uint32_t kdst = base + (uint32_t)st * kAttnStageBytes;
-        for (int r = 0; r < kAttnTile && tp + r < p1; r += p.box_rows) {
-          const int64_t pos = tp + r;
-          const int32_t pg = pages[pos / p.page_size - first_page];
-          const int32_t y = pg < 0 ? (int32_t)rows : (int32_t)((int64_t)pg * p.page_size + pos % p.page_size);
-          const int32_t x = kvh * kAttnD;
-          const uint32_t off = (uint32_t)r * 128u;
-          tma_load_2d(kdst + off, &tmK, fb, x, y);
-          tma_load_2d(kdst + kAttnHalfBytes + off, &tmK, fb, x + 64, y);
-          tma_load_2d(kdst + kAttnKVBytes + off, &tmV, fb, x, y);
-          tma_load_2d(kdst + kAttnKVBytes + kAttnHalfBytes + off, &tmV, fb, x + 64, y);
-        }
-        ++issued;
-      }
-      // every copy issued has landed before the CTA may end
-      for (int t = issued > kAttnStages ? issued - kAttnStages : 0; t < issued; ++t)
-        attn_drain(smem_u32(&full[t % kAttnStages]), (t / kAttnStages) & 1, p.status);
+    return L;
+  };
+  uint64_t nfull = 0;
+  for (int64_t b = threadIdx.x; b < B; b += kPlanThreads) nfull += (uint64_t)(length(b) / p.split_size);
+  uint64_t ftot = 0;
+  plan_scan(nfull, sh, &ftot);
+  uint64_t carry_f = 0, carry_p = 0;
+  for (int64_t b0 = 0; b0 < B; b0 += kPlanThreads) {
+    const int64_t b = b0 + threadIdx.x;
+    uint64_t f = 0, part = 0;
+    if (b < B) {
+      const int64_t L = length(b);
+      f = (uint64_t)(L / p.split_size);
+      part = (L % p.split_size) != 0 ? 1u : 0u;
     }
-    return;
+    uint64_t tot = 0;
+    const uint64_t ex = plan_scan((f << 32) | part, sh, &tot);
+    if (b < B) {
+      uint32_t* dst = p.items + carry_f + (ex >> 32);
+      for (uint64_t s = 0; s < f; ++s) dst[s] = ((uint32_t)b << 16) | (uint32_t)s;
+      if (part) p.items[ftot + carry_p + (ex & 0xFFFFFFFFu)] = ((uint32_t)b << 16) | (uint32_t)f;
+    }
+    carry_f += tot >> 32;
+    carry_p += tot & 0xFFFFFFFFu;
   }
-
-  // ---------------- compute warps
-  const int g = lane >> 2, c = lane & 3;
-  // q as the MMA's B operand (k = d, n = query head of the group): lane holds
-  // q[head g][d = 16 ks + 2c, +1] and [.. + 8, + 9] for every 16-wide step ks.
-  uint32_t qf[NT][8][2];
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + (b * p.Hq + (int64_t)kvh * p.G) * kAttnD;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int h = j * 8 + g;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t lo = 0, hi = 0;
-      if (h < p.G) {
-        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + (int64_t)h * kAttnD + ks * 16 + 2 * c);
-        lo = qr[0];
-        hi = qr[4];
-      }
-      qf[j][ks][0] = lo;
-      qf[j][ks][1] = hi;
-    }
-  }
-
-  // Running state.  o is o^T [d][head]: o[i][j] covers d = 16 i + g (+ 8) and
-  // heads 8 j + 2c (+ 1); m and l are per head column (2c, 2c + 1).
-  float m[NT][2], l[NT][2], o[8][NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    m[j][0] = m[j][1] = -INFINITY;
-    l[j][0] = l[j][1] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][j][0] = o[i][j][1] = o[i][j][2] = o[i][j][3] = 0.0f;
-  }
-
-  const int row0 = warp * 16;
-  for (int t = 0; t < n_tiles; ++t) {
-    const int st = t % kAttnStages;
-    if (!attn_wait(smem_u32(&full[st]), (t / kAttnStages) & 1, abort, p.status)) break;
-    const uint32_t kb = base + (uint32_t)st * kAttnStageBytes, vb = kb + kAttnKVBytes;
-    const int64_t tp = p0 + (int64_t)t * kAttnTile + row0;  // position of this warp's first row
-    if (tp < p1) {
-      if (tp + 16 > p1) {
-        // The request ends inside these rows: the cache past L is not ours to
-        // read (stale values, Inf, NaN), so its V rows become zeros; its
-        // scores are masked below.
-        const int bad0 = (int)(p1 - tp);
-        for (int i = lane; i < (16 - bad0) * 16; i += 32) {
-          const int rr = row0 + bad0 + i / 16, ch = i % 16;
-          const uint32_t a = vb + (uint32_t)(ch / 8) * kAttnHalfBytes + (uint32_t)rr * 128u + (uint32_t)(ch % 8) * 16u;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-
-      // scores^T [16 positions][GP heads] = K . q^T
-      float acc[NT][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int row = row0 + (lane & 15);
-        const int chunk = ((ks & 3) << 1) + (lane >> 4);
-        uint32_t a[4];
-        ldmatrix_x4(a, kb + (uint32_t)(ks >> 2) * kAttnHalfBytes + (uint32_t)row * 128u +
-                           (uint32_t)((chunk ^ (row & 7)) << 4));
-#pragma unroll
-        for (int j = 0; j < NT; ++j) mma_m16n8k16_bf16(acc[j], a, qf[j][ks][0], qf[j][ks][1]);
-      }
-
-      // online softmax over the 16 positions, then p^T as the B operand of p . v
-      const bool ok0 = tp + g < p1, ok1 = tp + g + 8 < p1;
-      uint32_t pb[NT][2];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        __nv_bfloat16 r[2][2];  // [column][row g, g + 8]
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const float t0 = ok0 ? __fmul_rn(acc[j][cc], p.qk_log2) : -INFINITY;
-          const float t1 = ok1 ? __fmul_rn(acc[j][2 + cc], p.qk_log2) : -INFINITY;
-          float mx = fmaxf(t0, t1);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m[j][cc], mx);
-          const float alpha = (mn == m[j][cc]) ? 1.0f : exp2f(__fsub_rn(m[j][cc], mn));
-          const float e0 = (mn == -INFINITY) ? 0.0f : exp2f(__fsub_rn(t0, mn));
-          const float e1 = (mn == -INFINITY) ? 0.0f : exp2f(__fsub_rn(t1, mn));
-          r[cc][0] = __float2bfloat16_rn(e0);
-          r[cc][1] = __float2bfloat16_rn(e1);
-          l[j][cc] = __fadd_rn(__fmul_rn(l[j][cc], alpha),
-                               __fadd_rn(__bfloat162float(r[cc][0]), __bfloat162float(r[cc][1])));
-          m[j][cc] = mn;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            o[i][j][cc] = __fmul_rn(o[i][j][cc], alpha);
-            o[i][j][2 + cc] = __fmul_rn(o[i][j][2 + cc], alpha);
-          }
-        }
-        pb[j][0] = movmatrix_trans(pack_bf16(r[0][0], r[1][0]));
-        pb[j][1] = movmatrix_trans(pack_bf16(r[0][1], r[1][1]));
-      }
-
-      // o^T [128 d][GP heads] += V^T . p^T
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
-        const int chunk = ((i & 3) << 1) + ((lane >> 3) & 1);
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, vb + (uint32_t)(i >> 2) * kAttnHalfBytes + (uint32_t)row * 128u +
-                                 (uint32_t)((chunk ^ (row & 7)) << 4));
-#pragma unroll
-        for (int j = 0; j < NT; ++j) mma_m16n8k16_bf16(o[i][j], a, pb[j][0], pb[j][1]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-  }
-
-  // l: the eight lanes of a column hold partial sums over their rows
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 4));
-      l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 8));
-      l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 16));
-    }
-
-  // Fold the four warps in order through shared memory (the ring is idle now).
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kAttnCWarps) : "memory");
-  if (*abort) return;  // the call was abandoned: the output is unspecified
-  constexpr int NR = 8 * NT * 4 + 4 * NT;  // floats of state per lane
-  float* scratch = reinterpret_cast<float*>(attn_smem_raw + (base - smem_u32(attn_smem_raw)));
-  if (warp > 0) {
-    float* w = scratch + (warp - 1) * NR * 32 + lane;
-    int r = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[32 * r++] = o[i][j][e];
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        w[32 * r++] = m[j][cc];
-        w[32 * r++] = l[j][cc];
-      }
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kAttnCWarps) : "memory");
-  if (warp > 0) return;
-  for (int src = 0; src < kAttnCWarps - 1; ++src) {
-    const float* w = scratch + src * NR * 32 + lane;
-    float a1[NT][2], a2[NT][2];
-    int r = 8 * NT * 4;
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const float m2 = w[32 * r++], l2 = w[32 * r++];
-        float mm;
-        attn_scales(m[j][cc], m2, mm, a1[j][cc], a2[j][cc]);
-        l[j][cc] = __fadd_rn(__fmul_rn(l[j][cc], a1[j][cc]), __fmul_rn(l2, a2[j][cc]));
-        m[j][cc] = mm;
-      }
-    r = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float o2 = w[32 * r++];
-          o[i][j][e] = __fadd_rn(__fmul_rn(o[i][j][e], a1[j][e & 1]), __fmul_rn(o2, a2[j][e & 1]));
-        }
-  }
-
-  // The split's record: o^T [D][GP], then m [GP], then l [GP].
-  float* rec = p.part + ((b * p.Hkv + kvh) * (int64_t)p.n_split + s) * (int64_t)((kAttnD + 2) * GP);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int d = 16 * i + g, h = 8 * j + 2 * c;
-      *reinterpret_cast<float2*>(rec + d * GP + h) = make_float2(o[i][j][0], o[i][j][1]);
-      *reinterpret_cast<float2*>(rec + (d + 8) * GP + h) = make_float2(o[i][j][2], o[i][j][3]);
-    }
-  if (g == 0) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int h = 8 * j + 2 * c;
-      *reinterpret_cast<float2*>(rec + kAttnD * GP + h) = make_float2(m[j][0], m[j][1]);
-      *reinterpret_cast<float2*>(rec + kAttnD * GP + GP + h) = make_float2(l[j][0], l[j][1]);
-    }
+  if (threadIdx.x == 0) {
+    p.ctl[0] = 0;                             // the ticket counter
+    p.ctl[1] = (uint32_t)(ftot + carry_p);    // items
   }
 }
+
+// ---------------------------------------------------------------------------
+// stream: persistent warps, one split at a time
+// ---------------------------------------------------------------------------
+
+struct AttnItem {
+  int64_t p0, p1;  // positions [p0, p1) of request b
+  int32_t b, s, kvh, ntiles;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
+    decode_attn_stream_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                              const AttnParams p) {
+  constexpr int GP = 8 * NT;  // query-head columns of the MMAs (G <= GP)
+  constexpr int W = AttnCfg<NT>::warps;
+  constexpr int SB = AttnCfg<NT>::stage_bytes;
+  // Items fetched ahead of the one being issued: a fetch starts while fewer
+  // than kAhead are ready and adds one, so the items between the one being
+  // consumed and the last one fetched number at most kAttnStages + kAhead.
+  constexpr int kAhead = 2;
+  constexpr int kQ = kAttnStages + kAhead + 1;
+  extern __shared__ uint8_t attn_smem_raw[];
+  __shared__ __align__(8) uint64_t full[W][kAttnStages];
+  __shared__ AttnItem queue[W][kQ];
+
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // the item list, q and the cache come from earlier kernels
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t ring = ((smem_u32(attn_smem_raw) + 1023u) & ~1023u) + (uint32_t)(warp * kAttnStages * SB);
+  if (lane == 0) {
+    for (int i = 0; i < kAttnStages; ++i) mbar_init(smem_u32(&full[warp][i]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint32_t n_tickets = p.ctl[1] * (uint32_t)p.Hkv;
+  AttnItem* Q = queue[warp];
+  const int64_t rows = p.num_pages * p.page_size;
+
+  // ---- item fetch, one step per loop turn so that each global load has a
+  // whole tile of work to land in: ticket -> list entry -> length -> item.
+  // Tickets run over items x key/value heads, heads fastest, so the heads of
+  // one split are taken together.
+  int fs = 0;            // 0 idle, 1 ticket in flight, 2 entry in flight, 3 length in flight
+  bool fetch_done = false;
+  uint32_t tk = 0, fe = 0, ft = 0;
+  int32_t fL = 0;
+  int nready = 0;        // items fetched into Q (sequence numbers 0 .. nready - 1)
+  auto fetch_step = [&](int pi) {
+    if (fs == 0) {
+      if (fetch_done || nready - pi >= kAhead) return;
+      if (lane == 0) tk = atomicAdd(p.ctl, 1u);
+      fs = 1;
+    } else if (fs == 1) {
+      ft = __shfl_sync(0xffffffffu, tk, 0);
+      if (ft >= n_tickets) {
+        fetch_done = true;
+        fs = 0;
+        return;
+      }
+      if (lane == 0) fe = p.items[ft / (uint32_t)p.Hkv];
+      fs = 2;
+    } else if (fs == 2) {
+      if (lane == 0) fL = p.seq_lens[fe >> 16];
+      fs = 3;
+    } else {
+      if (lane == 0) {
+        AttnItem x;
+        x.b = (int32_t)(fe >> 16);
+        x.s = (int32_t)(fe & 0xFFFFu);
+        x.kvh = (int32_t)(ft % (uint32_t)p.Hkv);
+        x.p0 = (int64_t)x.s * p.split_size;
+        x.p1 = min(x.p0 + (int64_t)p.split_size, (int64_t)fL);
+        x.ntiles = (int32_t)((x.p1 - x.p0 + kAttnTile - 1) / kAttnTile);
+        Q[nready % kQ] = x;
+      }
+      __syncwarp();
+      ++nready;
+      fs = 0;
+    }
+  };
+
+  // ---- page ids of one tile: lane j < nb holds the row of box j.
+  auto tile_rows = [&](const AttnItem& it, int t, int& nb) -> int32_t {
+    const int64_t tp = it.p0 + (int64_t)t * kAttnTile;
+    nb = (int)min((int64_t)(kAttnTile / p.box_rows), (it.p1 - tp + p.box_rows - 1) / p.box_rows);
+    int32_t y = 0;
+    if (lane < nb) {
+      const int64_t pos = tp + (int64_t)lane * p.box_rows;
+      const int32_t pg = p.block_table[(int64_t)it.b * p.bt_stride + pos / p.page_size];
+      if (pg < 0 || (int64_t)pg >= p.num_pages) {
+        attn_flag(p.status, (int)BI_ERR_INVALID_ARG);
+        y = (int32_t)rows;  // past the cache's end: zeros
+      } else {
+        y = (int32_t)((int64_t)pg * p.page_size + pos % p.page_size);
+      }
+    }
+    return y;
+  };
+
+  // Issues tile t of item it into stage st (rows y from tile_rows): the K and
+  // V boxes (one per lane, lanes < nb), and q with the item's first tile.
+  auto issue = [&](const AttnItem& it, int t, int st, int nb, int32_t y) {
+    const uint32_t stage = ring + (uint32_t)(st * SB);
+    const uint32_t fb = smem_u32(&full[warp][st]);
+    if (lane == 0)
+      mbar_arrive_expect_tx(fb, (uint32_t)(nb * p.box_rows * 128 * 4 + (t == 0 ? p.G * kAttnD * 2 : 0)));
+    __syncwarp();
+    if (lane < nb) {
+      const int32_t x = it.kvh * kAttnD;
+      const uint32_t off = (uint32_t)(lane * p.box_rows * 128);
+      tma_load_2d(stage + off, &tmK, fb, x, y);
+      tma_load_2d(stage + kAttnHalfBytes + off, &tmK, fb, x + 64, y);
+      tma_load_2d(stage + kAttnKVBytes + off, &tmV, fb, x, y);
+      tma_load_2d(stage + kAttnKVBytes + kAttnHalfBytes + off, &tmV, fb, x + 64, y);
+    }
+    if (t == 0 && lane == 0) {
+      const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(p.q) +
+                                  ((int64_t)it.b * p.Hq + (int64_t)it.kvh * p.G) * kAttnD;
+      bulk_load(stage + 2 * kAttnKVBytes, qsrc, (uint32_t)(p.G * kAttnD * 2), fb);
+    }
+  };
+
+  uint32_t qf[NT][8][2];
+  float m[NT][2], l[NT][2], o[8][NT][4];
+  int pi = 0, pt = 0, ci = 0, ct = 0, issued = 0, consumed = 0;
+  int pf_item = -1, pf_tile = 0, pf_nb = 0;  // the tile whose rows pf_y holds
+  int32_t pf_y = 0;
+  bool ok = true;
+  while (ok) {
+    fetch_step(pi);
+    // keep kAttnStages tiles in flight
+    while (pi < nready && issued - consumed < kAttnStages) {
+      const AttnItem it = Q[pi % kQ];
+      int nb = pf_nb;
+      int32_t y = pf_y;
+      if (pf_item != pi || pf_tile != pt) y = tile_rows(it, pt, nb);
+      issue(it, pt, issued % kAttnStages, nb, y);
+      ++issued;
+      if (++pt == it.ntiles) {
+        pt = 0;
+        ++pi;
+      }
+      // the next tile's rows load while this one is in flight
+      pf_item = -1;
+      if (pi < nready) {
+        pf_y = tile_rows(Q[pi % kQ], pt, pf_nb);
+        pf_item = pi;
+        pf_tile = pt;
+      }
+    }
+    if (consumed == issued) {
+      if (fetch_done && pi == nready && fs == 0) break;
+      continue;  // waiting for the next item's fetch
+    }
+
+    const int st = consumed % kAttnStages;
+    const bool got = attn_wait(smem_u32(&full[warp][st]), (uint32_t)(consumed / kAttnStages) & 1u, p.status);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    const AttnItem it = Q[ci % kQ];
+    const uint32_t kb = ring + (uint32_t)(st * SB), vb = kb + kAttnKVBytes;
+    if (ct == 0) {
+      // a new split: fresh state, and q as the MMA's B operand (k = d, n =
+      // query head): lane holds q[head g][d = 16 ks + 2c, +1] and [.. + 8, + 9]
+      const uint32_t qs = kb + 2 * kAttnKVBytes;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int h = j * 8 + g;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t lo = 0, hi = 0;
+          if (h < p.G) {
+            const uint32_t a = qs + (uint32_t)(h * kAttnD * 2 + (ks * 16 + 2 * c) * 2);
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lo) : "r"(a));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(a + 16u));
+          }
+          qf[j][ks][0] = lo;
+          qf[j][ks][1] = hi;
+        }
+        m[j][0] = m[j][1] = -INFINITY;
+        l[j][0] = l[j][1] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][j][0] = o[i][j][1] = o[i][j][2] = o[i][j][3] = 0.0f;
+      }
+    }
+    const int64_t tp = it.p0 + (int64_t)ct * kAttnTile;
+    if (tp + kAttnTile > it.p1) {
+      // The request ends inside this tile: the cache past L is not ours to
+      // read (stale values, Inf, NaN), so its V rows become zeros; its scores
+      // are masked below.
+      const int bad0 = (int)(it.p1 - tp);
+      for (int i = lane; i < (kAttnTile - bad0) * 16; i += 32) {
+        const int rr = bad0 + i / 16, ch = i % 16;
+        const uint32_t a = vb + (uint32_t)(ch / 8) * kAttnHalfBytes + (uint32_t)rr * 128u + (uint32_t)(ch % 8) * 16u;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+      }
+      fence_proxy_async_smem();  // before a later copy rewrites this stage
+      __syncwarp();
+    }
+    // scores^T [32 positions][GP heads] = K . q^T, as two 16-position chunks
+    constexpr int NC = kAttnTile / 16;
+    const int nc = (int)min((int64_t)NC, (it.p1 - tp + 15) / 16);  // chunks holding positions
+    float acc[NC][NT][4];
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc[k][j][0] = acc[k][j][1] = acc[k][j][2] = acc[k][j][3] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      if (k >= nc) break;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int row = k * 16 + (lane & 15);
+        const int ch = ((ks & 3) << 1) + (lane >> 4);
+        uint32_t a[4];
+        ldmatrix_x4(a, kb + (uint32_t)(ks >> 2) * kAttnHalfBytes + (uint32_t)row * 128u +
+                           (uint32_t)((ch ^ (row & 7)) << 4));
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_m16n8k16_bf16(acc[k][j], a, qf[j][ks][0], qf[j][ks][1]);
+      }
+    }
+    // online softmax over the tile's 32 positions (one step), then p^T as the
+    // B operand of p . v
+    uint32_t pb[NC][NT][2];
+    bool moved = false;
+    float alpha[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float t[NC][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          const int64_t r = tp + k * 16 + g;
+          t[k][0] = r < it.p1 ? __fmul_rn(acc[k][j][cc], p.qk_log2) : -INFINITY;
+          t[k][1] = r + 8 < it.p1 ? __fmul_rn(acc[k][j][2 + cc], p.qk_log2) : -INFINITY;
+          mx = fmaxf(mx, fmaxf(t[k][0], t[k][1]));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[j][cc], mx);
+        alpha[j][cc] = (mn == m[j][cc]) ? 1.0f : ex2_approx(__fsub_rn(m[j][cc], mn));
+        moved = moved || mn != m[j][cc];
+        float sum = 0.0f;
+        __nv_bfloat16 r[NC][2];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          r[k][0] = __float2bfloat16_rn(mn == -INFINITY ? 0.0f : ex2_approx(__fsub_rn(t[k][0], mn)));
+          r[k][1] = __float2bfloat16_rn(mn == -INFINITY ? 0.0f : ex2_approx(__fsub_rn(t[k][1], mn)));
+          sum = __fadd_rn(sum, __fadd_rn(__bfloat162float(r[k][0]), __bfloat162float(r[k][1])));
+        }
+        l[j][cc] = __fadd_rn(__fmul_rn(l[j][cc], alpha[j][cc]), sum);
+        m[j][cc] = mn;
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          // column cc of rows g and g + 8 of chunk k
+          if (cc == 0) {
+            pb[k][j][0] = (uint32_t)__bfloat16_as_ushort(r[k][0]);
+            pb[k][j][1] = (uint32_t)__bfloat16_as_ushort(r[k][1]);
+          } else {
+            pb[k][j][0] |= (uint32_t)__bfloat16_as_ushort(r[k][0]) << 16;
+            pb[k][j][1] |= (uint32_t)__bfloat16_as_ushort(r[k][1]) << 16;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        pb[k][j][0] = movmatrix_trans(pb[k][j][0]);
+        pb[k][j][1] = movmatrix_trans(pb[k][j][1]);
+      }
+    }
+    // o is rescaled only when some column's maximum moved (x * 1 == x)
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          o[i][j][0] = __fmul_rn(o[i][j][0], alpha[j][0]);
+          o[i][j][1] = __fmul_rn(o[i][j][1], alpha[j][1]);
+          o[i][j][2] = __fmul_rn(o[i][j][2], alpha[j][0]);
+          o[i][j][3] = __fmul_rn(o[i][j][3], alpha[j][1]);
+        }
+    }
+    // o^T [128 d][GP heads] += V^T . p^T, chunk by chunk
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      if (k >= nc) break;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = k * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = ((i & 3) << 1) + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vb + (uint32_t)(i >> 2) * kAttnHalfBytes + (uint32_t)row * 128u +
+                                 (uint32_t)((ch ^ (row & 7)) << 4));
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_m16n8k16_bf16(o[i][j], a, pb[k][j][0], pb[k][j][1]);
+      }
+    }
+    __syncwarp();  // every lane is done with the stage before it is refilled
+    ++consumed;
+    if (++ct == it.ntiles) {
+      // the split's record: o^T [D][GP], then m [GP], then l [GP]
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 4));
+          l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 8));
+          l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 16));
+        }
+      float* rec = p.part + (((int64_t)it.b * p.Hkv + it.kvh) * (int64_t)p.n_split + it.s) *
+                                (int64_t)((kAttnD + 2) * GP);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int d = 16 * i + g, h = 8 * j + 2 * c;
+          *reinterpret_cast<float2*>(rec + d * GP + h) = make_float2(o[i][j][0], o[i][j][1]);
+          *reinterpret_cast<float2*>(rec + (d + 8) * GP + h) = make_float2(o[i][j][2], o[i][j][3]);
+        }
+      if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int h = 8 * j + 2 * c;
+          *reinterpret_cast<float2*>(rec + kAttnD * GP + h) = make_float2(m[j][0], m[j][1]);
+          *reinterpret_cast<float2*>(rec + kAttnD * GP + GP + h) = make_float2(l[j][0], l[j][1]);
+        }
+      }
+      ct = 0;
+      ++ci;
+    }
+  }
+  if (!ok) {
+    // abandoned (a copy did not land in 2 s): every copy still in flight must
+    // land before the CTA ends
+    if (lane == 0)
+      for (int k = consumed; k < issued; ++k)
+        attn_drain(smem_u32(&full[warp][k % kAttnStages]), (uint32_t)(k / kAttnStages) & 1u, p.status);
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine
+// ---------------------------------------------------------------------------
 
 // One CTA per (key/value head, request): folds the request's split records
 // in split order and writes out[b][h][d] for the group's heads.  Thread t owns
@@ -504,20 +644,19 @@ template <int NT>
 static cudaError_t launch_attn_t(const AttnLaunch& A) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_split_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         attn_smem_bytes<NT>());
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnCfg<NT>::smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              comb_smem_bytes<NT>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (A.p.n_split > 0) {
-    cudaError_t e = launch_overlapped_smem(decode_attn_split_kernel<NT>,
-                                           dim3((unsigned)A.p.Hkv, (unsigned)A.p.n_split, (unsigned)A.B),
-                                           dim3(kAttnThreads), attn_smem_bytes<NT>(), A.stream, A.tmK, A.tmV, A.p);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = launch_overlapped(decode_attn_plan_kernel, dim3(1), dim3(kPlanThreads), A.stream, A.p, A.B);
+  if (e != cudaSuccess) return e;
+  e = launch_overlapped_smem(decode_attn_stream_kernel<NT>, dim3((unsigned)A.grid), dim3(32 * AttnCfg<NT>::warps),
+                             AttnCfg<NT>::smem, A.stream, A.tmK, A.tmV, A.p);
+  if (e != cudaSuccess) return e;
   return launch_overlapped_smem(decode_attn_combine_kernel<NT>, dim3((unsigned)A.p.Hkv, (unsigned)A.B),
                                 dim3(kCombThreads), comb_smem_bytes<NT>(), A.stream, A.p, A.out);
 }

@@ -11,6 +11,8 @@ struct AttnParams {
   const void* q;               // [B, Hq, 128] bf16
   const int32_t* block_table;  // [B, bt_stride] page ids
   const int32_t* seq_lens;     // [B]
+  uint32_t* ctl;               // [0] ticket counter, [1] items (both set by the plan kernel)
+  uint32_t* items;             // (b << 16) | s of every (request, split) item
   float* part;                 // per (request, kv head, split): o^T [128][GP], m [GP], l [GP]
   int64_t bt_stride, num_pages;
   int64_t max_len;             // every seq_lens[b] must be in [0, max_len]
@@ -20,9 +22,11 @@ struct AttnParams {
 };
 struct AttnLaunch {
   CUtensorMap tmK, tmV;  // caches as [num_pages * page_size, Hkv * 128], box 64 x box_rows, 128-byte swizzle
+                         // (box_rows = min(page_size, 32))
   AttnParams p;
   void* out;             // [B, Hq, 128] bf16
   int64_t B;
+  int32_t grid;          // stream kernel CTAs (one per SM)
   cudaStream_t stream;
 };
 cudaError_t launch_decode_attention(const AttnLaunch& A);

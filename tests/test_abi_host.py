@@ -158,10 +158,12 @@ def test_decode_attention_arguments_rejected_before_any_launch(bd):
     assert call(sl=82) == bd.BI_ERR_ALIGNMENT
     assert call(ws_bytes=100) == bd.BI_ERR_WORKSPACE
     assert call(B=0, q=None, k=None, v=None, bt=None, sl=None, out=None, ws=None) == bd.BI_OK
-    # workspace: B * Hkv * ceil(max_len / split) * (128 + 2) * GP * 4
-    assert bd.bi_decode_attention_workspace_bytes(2, 8, 2, 1000, 256) == 2 * 2 * 4 * 130 * 8 * 4
-    assert bd.bi_decode_attention_workspace_bytes(3, 32, 2, 64, 64) == 3 * 2 * 1 * 130 * 16 * 4
-    assert bd.bi_decode_attention_workspace_bytes(1, 8, 8, 0, 0) == 1 * 8 * 1 * 130 * 8 * 4
+    # workspace: 256 + list (B * n_split * 4, to 256) + B * Hkv * n_split * (128 + 2) * GP * 4
+    assert bd.bi_decode_attention_workspace_bytes(2, 8, 2, 1000, 256) == 256 + 256 + 2 * 2 * 4 * 130 * 8 * 4
+    assert bd.bi_decode_attention_workspace_bytes(3, 32, 2, 64, 64) == 256 + 256 + 3 * 2 * 1 * 130 * 16 * 4
+    assert bd.bi_decode_attention_workspace_bytes(1, 8, 8, 0, 0) == 256 + 256 + 1 * 8 * 1 * 130 * 8 * 4
+    assert bd.bi_decode_attention_workspace_bytes(100, 8, 8, 4096, 64) == \
+        256 + (100 * 64 * 4 + 255) // 256 * 256 + 100 * 8 * 64 * 130 * 8 * 4
     assert bd.bi_decode_attention_workspace_bytes(1, 8, 8, 1000, 0) == \
         bd.bi_decode_attention_workspace_bytes(1, 8, 8, 1000, bd.BI_ATTN_DEFAULT_SPLIT)
 

@@ -163,6 +163,23 @@ def test_attention_batch_invariance(lib):
             assert np.array_equal(got[p], base[i]), (batch, i)
 
 
+def test_attention_workspace_needs_no_initial_contents(lib):
+    """Each call rewrites its control words, item list and records: a
+    workspace full of garbage, or left over from another shape, gives the
+    same bits."""
+    kc, vc, bt, sl = inputs.paged_kv([300, 1, 700], 2, D, 16, seed=67)
+    q = inputs.normal((3, 8, D), seed=67, stream=0)
+    base = bf16_bits(run(lib, q, kc, vc, bt, sl, 0.0883, split_size=64))
+    need = lib.bi_decode_attention_workspace_bytes(3, 8, 2, bt.shape[1] * 16, 64)
+    for fill in (0xFF, 0x00, 0x7F):
+        ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+        got = bf16_bits(run(lib, q, kc, vc, bt, sl, 0.0883, split_size=64, workspace=ws))
+        assert np.array_equal(got, base), fill
+        # the same workspace again, after a call of another shape
+        run(lib, q[:1], kc, vc, bt[:1], sl[:1], 0.0883, split_size=64, workspace=ws)
+        assert np.array_equal(bf16_bits(run(lib, q, kc, vc, bt, sl, 0.0883, split_size=64, workspace=ws)), base)
+
+
 def test_attention_split_size_is_a_pin(lib, oracle):
     """Another split size is another tree: other bits, each within the bound."""
     lens = [3000, 1025]
