@@ -87,18 +87,19 @@ bi_status check_nk(int64_t N, int64_t K, Elem e = Elem::BF16) {
 struct Resolved {
   int32_t S, T, ctas, w_pin;
   uint32_t flags;
-  int64_t KT;
+  int64_t KT, K;
   Elem elem;
 };
 
 // K tiles per copy for a launch with token tile T and CTA grouping ctas: 2
-// when the flag asks for it and it is possible (K % 64 == 0, T = 256) and the
-// MMAs are paired, else 1.  (A single CTA at T = 256 has a 48 KB K tile; its
+// when the flag asks for it and it is possible (K % 64 == 0, T = 256, or a
+// narrower paired tile of 224, 192 or 160) and the MMAs are paired, else 1.  (A single CTA at T = 256 has a 48 KB K tile; its
 // rings would hold only two X stages of two tiles, which measured slower.)
 // Launches whose X copies cover fewer rows than the token tile use 1
 // (make_plan).
 int pins_kps(int64_t K, int32_t T, int32_t ctas, uint32_t flags, Elem e = Elem::BF16) {
-  return ((flags & BI_FLAG_KTILE_PAIRS) && K % tile_elems(e) == 0 && T == 256 && ctas == 2) ? 2 : 1;
+  const bool wide = T == 256 || T == 224 || T == 192 || T == 160;
+  return ((flags & BI_FLAG_KTILE_PAIRS) && K % tile_elems(e) == 0 && wide && ctas == 2) ? 2 : 1;
 }
 
 bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r, Elem e = Elem::BF16);
@@ -190,6 +191,7 @@ int64_t max_clusters(int32_t size, int32_t sm_count) {
 struct LaunchChoice {
   int32_t ctas, schedule, units;
   double cost;
+  int32_t T = 0;  // token tile of the launch (0: the pinned one)
 };
 
 // Best schedule for one CTA grouping, and its cost in units of one K tile of a
@@ -247,7 +249,25 @@ LaunchChoice choose_launch(int64_t M, int64_t N, const Resolved& r, int32_t sm_c
   if (r.ctas != 0) return best_schedule(r, r.ctas, M, N, sm_count);
   const LaunchChoice one = best_schedule(r, 1, M, N, sm_count);
   if (M <= r.T / 2 || (r.flags & BI_FLAG_SCHEDULE_MASK) == BI_FLAG_SCHEDULE_CLUSTER) return one;
-  const LaunchChoice two = best_schedule(r, 2, M, N, sm_count);
+  LaunchChoice two = best_schedule(r, 2, M, N, sm_count);
+  // A persistent paired launch may also narrow its token tile so that the
+  // tiles fill the last wave (224, 192 or 160 instead of 256).  Its per-K-tile
+  // cost follows the operand bytes each CTA receives: 16 KB of W and T/2 rows
+  // of X, against 32 KB at T = 256 (the MMA itself takes T/2 of its 128
+  // cycles, within that).
+  if (two.schedule == BI_FLAG_SCHEDULE_LOCAL && r.T == 256 && r.elem == Elem::BF16 &&
+      pins_kps(r.K, 256, 2, r.flags) == 2 && M > r.T / 2) {
+    const int64_t n_tiles = ceil_div(N, (int64_t)kTileN * 2);
+    const int64_t slots = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    for (int32_t t : {224, 192, 160}) {
+      const double k = (16.0 + t / 16.0) / 32.0;
+      const double cost = (double)ceil_div(n_tiles * ceil_div(M, (int64_t)t), slots) * (double)r.KT * k + 15.0;
+      if (cost < two.cost * 0.98) {
+        two.cost = cost;
+        two.T = t;
+      }
+    }
+  }
   return two.cost < one.cost ? two : one;
 }
 
@@ -257,6 +277,7 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   Resolved r = pinned;
   const LaunchChoice choice = choose_launch(M, N, r, sm_count);
   r.ctas = choice.ctas;
+  if (choice.T != 0) r.T = choice.T;
   plan->bk = tile_elems(r.elem);
   plan->split_k = r.S;
   plan->tok_tile = r.T;
@@ -385,6 +406,7 @@ bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r, E
   r->w_pin = p.stages;
   r->flags = p.flags;
   r->KT = ceil_div(K, tile_elems(e));
+  r->K = K;
   r->elem = e;
   return BI_OK;
 }
@@ -433,7 +455,7 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.m_tiles = (int32_t)plan.m_tiles;
   L.k_tiles = (int32_t)r.KT;
   L.S = r.S;
-  L.T = r.T;
+  L.T = plan.tok_tile;  // the launch's token tile (may be narrower than the pinned one)
   L.w_stages = plan.w_stages;
   L.x_stages = plan.x_stages;
   L.x_box_rows = plan.x_box_rows;

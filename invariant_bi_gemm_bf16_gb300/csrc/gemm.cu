@@ -160,7 +160,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int kWStage = KP * kWStageBytes;
   constexpr int kTileElems = FP8 ? 128 : kBK;       // K values per K tile
   constexpr int kMmaM = PAIR ? 2 * kTileN : kTileN;  // W rows per tile
-  constexpr uint32_t kTmemCols = 2u * (uint32_t)T;    // two accumulators
+  // two accumulators of T columns; the allocation is a power of two >= 32
+  constexpr uint32_t kTmemCols = 2u * (uint32_t)T <= 128u ? 128u : (2u * (uint32_t)T <= 256u ? 256u : 512u);
+  static_assert(T % 32 == 0 && T >= 64 && T <= 256, "token tile");
   constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quadrant
   constexpr int kHalf = T / kColGroups;      // accumulator columns per epilogue warp
 
@@ -754,7 +756,21 @@ static cudaError_t launch_p(const GemmLaunch& L) {
         return L.cluster ? launch_t<256, true, PAIR, 2>(L) : launch_t<256, false, PAIR, 2>(L);
       return L.cluster ? launch_t<256, true, PAIR, 1>(L) : launch_t<256, false, PAIR, 1>(L);
     default:
-      return cudaErrorInvalidValue;
+      break;
+  }
+  // Narrower token tiles, chosen per launch to fill the last wave of a
+  // persistent paired launch (the MMA's N extent never changes a bit):
+  // LOCAL, CTA pairs, two K tiles per copy only.
+  if constexpr (PAIR) {
+    if (L.cluster || L.kps != 2) return cudaErrorInvalidValue;
+    switch (L.T) {
+      case 224: return launch_t<224, false, true, 2>(L);
+      case 192: return launch_t<192, false, true, 2>(L);
+      case 160: return launch_t<160, false, true, 2>(L);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    return cudaErrorInvalidValue;
   }
 }
 

@@ -61,3 +61,31 @@ def test_mma_shape_and_grouping_leave_bits_unchanged(lib, M, N, K, S):
                         T, ctas, plan.kps, diff, ref.size)
     if K % 64 == 0 and M > 128:
         assert (256, 2, 2) in seen  # the two-tile pair path ran (a short X box keeps one-tile copies)
+
+
+# (M, N, K, S, token tile the open layout narrows to)
+NARROW = [
+    (4096, 4096, 14336, 4, 224),   # down_proj: 19 token tiles fill 4 waves of 76 pairs
+    (1024, 6144, 4096, 3, 192),    # Llama-3.1-8B qkv: 144 tiles in 2 waves
+    (513, 4096, 14336, 4, 160),    # down_proj just past 512
+    (1500, 4096, 4096, 2, 192),
+]
+
+
+@pytest.mark.parametrize("M,N,K,S,T", NARROW)
+def test_narrowed_token_tiles_leave_bits_unchanged(lib, M, N, K, S, T):
+    """Persistent paired launches may narrow their token tile per M (224, 192,
+    160) when the pins leave the layout open.  The bits must equal those of
+    the pinned 256-wide paired layout and of one CTA per MMA."""
+    X = wide_range((M, K), seed=22, stream=0).cuda()
+    W = wide_range((N, K), seed=22, stream=1, std=0.02).cuda()
+    base = lib.bi_pins_default(N, K).replace(split_k=S, flags=lib.BI_FLAG_SCHEDULE_AUTO | lib.BI_FLAG_KTILE_PAIRS)
+    open_pins = base.replace(mma_ctas=0)
+    plan = lib.bi_gemm_plan_describe(M, N, K, open_pins)
+    assert (plan.tok_tile, plan.mma_ctas, plan.kps) == (T, 2, 2), (plan.tok_tile, plan.mma_ctas, plan.kps)
+    got = bf16_bits(lib.bi_gemm_bf16(X, W, pins=open_pins))
+    for ctas in (2, 1):
+        ref = bf16_bits(lib.bi_gemm_bf16(X, W, pins=base.replace(mma_ctas=ctas, tok_tile=256)))
+        assert np.array_equal(got, ref), ctas
+    torch.cuda.synchronize()
+    assert lib.bi_last_device_status() == lib.BI_OK
