@@ -6,9 +6,10 @@
 // tree depends on V only:
 //   * the row is read as 16-byte vectors of 8 bf16; thread g = rank *
 //     kLsmThreads + t of the cluster owns vectors g, g + G, g + 2G, ...
-//     (G = kLsmCtas * kLsmThreads) and folds their elements, in ascending
-//     order, into a running pair (m, s): s is the sum of exp(x - m) for the
-//     elements seen, rescaled by exp(m_old - m_new) whenever the maximum grows;
+//     (G = kLsmCtas * kLsmThreads): it takes the maximum m of their elements,
+//     then s = the sum of exp(x - m) over them, in ascending order, giving the
+//     thread's pair (m, s); its first vectors stay in registers for the
+//     output pass, so a row of up to 131072 logits is read once;
 //   * pairs combine as m = max(m1, m2), s = s1 exp(m1 - m) + s2 exp(m2 - m):
 //     by an xor butterfly (16, 8, 4, 2, 1) within each warp, then the warp
 //     results by the same butterfly in warp 0, then the CTA results (read
@@ -16,7 +17,8 @@
 //     rank 0; lanes past the count hold the identity (-inf, 0).  The two
 //     operands of every combine are the same two pairs in both lanes and IEEE
 //     addition commutes, so every lane ends with the same pair;
-//   * expf and logf are CUDA's (no fast math).
+//   * exp(x - m) is 2^((x - m) log2 e) by the ex2.approx instruction (the
+//     pair combines use CUDA's expf), and logf is CUDA's.
 // Rows holding a NaN or a +Inf, or -Inf everywhere, give NaN everywhere.
 // Detent (Batch-Invariant LLM Serving and RL Rollouts at Near-Stock Speed),
 // Sec. 8, Table 6, and CoRun (Padding is Simple and Efficient for
@@ -37,19 +39,6 @@ constexpr int kLsmStride = kLsmCtas * kLsmThreads;  // vectors between a thread'
 
 __device__ __forceinline__ float lsm_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float lsm_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// One logit into the running pair.  With m = -inf (nothing finite seen yet),
-// s = 0 and a larger x gives s = 0 * exp(-inf) + 1 = 1.  A -inf logit adds
-// exp(-inf) = 0.  A NaN or +Inf logit marks the row undefined.
-__device__ __forceinline__ void ms_add(float& m, float& s, bool& bad, float x) {
-  if (!(x < INFINITY)) bad = true;  // NaN or +Inf
-  if (x > m) {
-    s = __fadd_rn(__fmul_rn(s, expf(m - x)), 1.0f);
-    m = x;
-  } else if (m != -INFINITY) {
-    s = __fadd_rn(s, expf(x - m));
-  }
-}
 
 __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
@@ -80,22 +69,76 @@ struct LsmShared {
   float lse;
 };
 
-// The row's lse (every thread of the cluster returns it).
-__device__ float row_lse(const uint4* x, int64_t nvec, LsmShared& sh) {
+// Vectors a thread keeps in registers between the lse and the output pass
+// (V up to kLsmCache * 8 * kLsmStride = 131072 is read once).
+constexpr int kLsmCache = 4;
+
+__device__ __forceinline__ float max8(const uint4& v) {
+  return fmaxf(fmaxf(fmaxf(lsm_lo(v.x), lsm_hi(v.x)), fmaxf(lsm_lo(v.y), lsm_hi(v.y))),
+               fmaxf(fmaxf(lsm_lo(v.z), lsm_hi(v.z)), fmaxf(lsm_lo(v.w), lsm_hi(v.w))));
+}
+
+__device__ __forceinline__ bool bad8(const uint4& v) {
+  // NaN or +Inf anywhere (-Inf is an ordinary logit)
+  return !(lsm_lo(v.x) < INFINITY) || !(lsm_hi(v.x) < INFINITY) || !(lsm_lo(v.y) < INFINITY) ||
+         !(lsm_hi(v.y) < INFINITY) || !(lsm_lo(v.z) < INFINITY) || !(lsm_hi(v.z) < INFINITY) ||
+         !(lsm_lo(v.w) < INFINITY) || !(lsm_hi(v.w) < INFINITY);
+}
+
+// exp(d) for d = x - m <= 0 as 2^(d * log2(e)) by the ex2.approx
+// instruction: the product rounds once (relative error |d| 2^-24 in the
+// result, and terms with large |d| are tiny), ex2.approx adds about 2^-22.
+__device__ __forceinline__ float exp_le0(float d) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(__fmul_rn(d, 1.4426950408889634f)));
+  return y;
+}
+
+// sum of exp(x - m) over a vector, elements in order (m finite)
+__device__ __forceinline__ float sumexp8(const uint4& v, float m, float s) {
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_lo(v.x), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_hi(v.x), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_lo(v.y), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_hi(v.y), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_lo(v.z), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_hi(v.z), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_lo(v.w), m)));
+  s = __fadd_rn(s, exp_le0(__fsub_rn(lsm_hi(v.w), m)));
+  return s;
+}
+
+// The row's lse (every thread of the cluster returns it).  Thread g of the
+// cluster owns vectors g, g + G, g + 2G, ...: it takes the maximum m of its
+// elements, then s = sum of exp(x - m) over them in ascending order; the
+// per-thread pairs (m, s) then combine by the fixed butterflies.  The first
+// kLsmCache vectors stay in v[] for the output pass.
+__device__ float row_lse(const uint4* x, int64_t nvec, LsmShared& sh, uint4 (&v)[kLsmCache]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
+  const int64_t g0 = (int64_t)rank * kLsmThreads + tid;
   float m = -INFINITY, s = 0.0f;
   bool bad = false;
-  for (int64_t i = (int64_t)rank * kLsmThreads + tid; i < nvec; i += kLsmStride) {
-    const uint4 v = x[i];
-    ms_add(m, s, bad, lsm_lo(v.x));
-    ms_add(m, s, bad, lsm_hi(v.x));
-    ms_add(m, s, bad, lsm_lo(v.y));
-    ms_add(m, s, bad, lsm_hi(v.y));
-    ms_add(m, s, bad, lsm_lo(v.z));
-    ms_add(m, s, bad, lsm_hi(v.z));
-    ms_add(m, s, bad, lsm_lo(v.w));
-    ms_add(m, s, bad, lsm_hi(v.w));
+#pragma unroll
+  for (int i = 0; i < kLsmCache; ++i) {
+    const int64_t k = g0 + (int64_t)i * kLsmStride;
+    if (k < nvec) {
+      v[i] = x[k];
+      m = fmaxf(m, max8(v[i]));
+      bad = bad || bad8(v[i]);
+    }
+  }
+  for (int64_t k = g0 + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) {
+    const uint4 w = x[k];
+    m = fmaxf(m, max8(w));
+    bad = bad || bad8(w);
+  }
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < kLsmCache; ++i) {
+      const int64_t k = g0 + (int64_t)i * kLsmStride;
+      if (k < nvec) s = sumexp8(v[i], m, s);
+    }
+    for (int64_t k = g0 + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) s = sumexp8(x[k], m, s);
   }
   ms_butterfly(m, s, bad);
   if (lane == 0) {
@@ -134,6 +177,11 @@ __device__ float row_lse(const uint4* x, int64_t nvec, LsmShared& sh) {
   return lse;
 }
 
+__device__ __forceinline__ void write_out(float4* y, int64_t k, const uint4& v, float lse) {
+  y[2 * k] = make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse);
+  y[2 * k + 1] = make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse);
+}
+
 // X [M,V] bf16 -> Y [M,V] fp32 log-probabilities; cluster r of the grid is row r.
 __global__ void __launch_bounds__(kLsmThreads)
     log_softmax_kernel(const uint4* X, float4* Y, int64_t nvec) {
@@ -142,13 +190,16 @@ __global__ void __launch_bounds__(kLsmThreads)
   grid_dep_wait();  // the logits may come from the previous kernel in the stream
   const int64_t row = blockIdx.x / kLsmCtas;
   const uint4* x = X + row * nvec;
-  const float lse = row_lse(x, nvec, sh);
+  uint4 v[kLsmCache];
+  const float lse = row_lse(x, nvec, sh, v);
   float4* y = Y + row * nvec * 2;
-  for (int64_t i = (int64_t)cluster_ctarank() * kLsmThreads + threadIdx.x; i < nvec; i += kLsmStride) {
-    const uint4 v = x[i];
-    y[2 * i] = make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse);
-    y[2 * i + 1] = make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse);
+  const int64_t g0 = (int64_t)cluster_ctarank() * kLsmThreads + threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < kLsmCache; ++i) {
+    const int64_t k = g0 + (int64_t)i * kLsmStride;
+    if (k < nvec) write_out(y, k, v[i], lse);
   }
+  for (int64_t k = g0 + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) write_out(y, k, x[k], lse);
 }
 
 // out[row] = log-probability of ids[row] in row `row`; NaN for an id outside [0, V).
@@ -159,8 +210,128 @@ __global__ void __launch_bounds__(kLsmThreads)
   grid_dep_wait();
   const int64_t row = blockIdx.x / kLsmCtas;
   const uint4* x = X + row * nvec;
-  const float lse = row_lse(x, nvec, sh);
+  uint4 v[kLsmCache];
+  const float lse = row_lse(x, nvec, sh, v);
   if (cluster_ctarank() == 0 && threadIdx.x == 0) {
+    const int32_t id = ids[row];
+    const int64_t V = nvec * 8;
+    float r = __int_as_float(0x7fc00000);
+    if (id >= 0 && id < V) {
+      const uint16_t b = reinterpret_cast<const uint16_t*>(x)[id];
+      r = __uint_as_float((uint32_t)b << 16) - lse;
+    }
+    out[row] = r;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The same tree on one CTA per row, for many rows
+// ---------------------------------------------------------------------------
+// A cluster spreads a row over kLsmCtas SMs, which keeps a single row fast;
+// with many rows the cluster barriers and the waves of 8-CTA clusters cost
+// more than they save.  This variant runs the identical arithmetic on one CTA
+// of kLsmCtaThreads threads: thread t plays the cluster's threads t + 1024 j
+// (j < kLsmVirt), whose lanes and warps are its own lane and warp (mod 16),
+// and every butterfly combines the same pairs in the same order.  Both
+// variants give the same bits for every row; which one runs is speed only.
+constexpr int kLsmCtaThreads = 1024;
+constexpr int kLsmVirt = kLsmCtas * kLsmThreads / kLsmCtaThreads;  // cluster threads per thread
+#ifndef BI_LSM_CTA_MIN_ROWS
+#define BI_LSM_CTA_MIN_ROWS 64
+#endif
+
+struct LsmCtaShared {
+  float m[kLsmCtas][kLsmWarps], s[kLsmCtas][kLsmWarps];
+  int bad[kLsmCtas][kLsmWarps];
+  float cm[kLsmCtas], cs[kLsmCtas];
+  int cb[kLsmCtas];
+  float lse;
+};
+
+__device__ float row_lse_cta(const uint4* x, int64_t nvec, LsmCtaShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll 1
+  for (int j = 0; j < kLsmVirt; ++j) {
+    const int g = tid + j * kLsmCtaThreads;   // the cluster thread played
+    const int vr = g / kLsmThreads;           // its CTA rank
+    const int vw = (g % kLsmThreads) >> 5;    // its warp
+    uint4 v[kLsmCache];
+    float m = -INFINITY, s = 0.0f;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kLsmCache; ++i) {
+      const int64_t k = g + (int64_t)i * kLsmStride;
+      if (k < nvec) {
+        v[i] = x[k];
+        m = fmaxf(m, max8(v[i]));
+        bad = bad || bad8(v[i]);
+      }
+    }
+    for (int64_t k = g + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) {
+      const uint4 w = x[k];
+      m = fmaxf(m, max8(w));
+      bad = bad || bad8(w);
+    }
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < kLsmCache; ++i) {
+        const int64_t k = g + (int64_t)i * kLsmStride;
+        if (k < nvec) s = sumexp8(v[i], m, s);
+      }
+      for (int64_t k = g + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) s = sumexp8(x[k], m, s);
+    }
+    ms_butterfly(m, s, bad);
+    if (lane == 0) {
+      sh.m[vr][vw] = m;
+      sh.s[vr][vw] = s;
+      sh.bad[vr][vw] = bad;
+    }
+  }
+  __syncthreads();
+  if (warp < kLsmCtas) {  // warp r plays warp 0 of cluster CTA r
+    float m = lane < kLsmWarps ? sh.m[warp][lane] : -INFINITY;
+    float s = lane < kLsmWarps ? sh.s[warp][lane] : 0.0f;
+    bool bad = lane < kLsmWarps ? sh.bad[warp][lane] != 0 : false;
+    ms_butterfly(m, s, bad);
+    if (lane == 0) {
+      sh.cm[warp] = m;
+      sh.cs[warp] = s;
+      sh.cb[warp] = bad;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // warp 0 of cluster CTA 0
+    float m = lane < kLsmCtas ? sh.cm[lane] : -INFINITY;
+    float s = lane < kLsmCtas ? sh.cs[lane] : 0.0f;
+    bool bad = lane < kLsmCtas ? sh.cb[lane] != 0 : false;
+    ms_butterfly(m, s, bad);
+    if (lane == 0) sh.lse = (bad || m == -INFINITY) ? __int_as_float(0x7fc00000) : m + logf(s);
+  }
+  __syncthreads();
+  return sh.lse;
+}
+
+__global__ void __launch_bounds__(kLsmCtaThreads)
+    log_softmax_cta_kernel(const uint4* X, float4* Y, int64_t nvec) {
+  __shared__ LsmCtaShared sh;
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  const int64_t row = blockIdx.x;
+  const uint4* x = X + row * nvec;
+  const float lse = row_lse_cta(x, nvec, sh);
+  float4* y = Y + row * nvec * 2;
+  for (int64_t k = threadIdx.x; k < nvec; k += kLsmCtaThreads) write_out(y, k, x[k], lse);
+}
+
+__global__ void __launch_bounds__(kLsmCtaThreads)
+    token_logprobs_cta_kernel(const uint4* X, const int32_t* ids, float* out, int64_t nvec) {
+  __shared__ LsmCtaShared sh;
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  const int64_t row = blockIdx.x;
+  const uint4* x = X + row * nvec;
+  const float lse = row_lse_cta(x, nvec, sh);
+  if (threadIdx.x == 0) {
     const int32_t id = ids[row];
     const int64_t V = nvec * 8;
     float r = __int_as_float(0x7fc00000);
@@ -191,6 +362,9 @@ static cudaError_t launch_rows(void (*kern)(KArgs...), int64_t M, cudaStream_t s
 }
 
 cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cudaStream_t stream) {
+  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll)
+    return launch_overlapped(log_softmax_cta_kernel, dim3((unsigned)M), dim3(kLsmCtaThreads), stream,
+                             static_cast<const uint4*>(X), static_cast<float4*>(Y), V / 8);
   if (M > 0x7FFFFFFFll / kLsmCtas) return cudaErrorInvalidValue;
   return launch_rows(log_softmax_kernel, M, stream, static_cast<const uint4*>(X), static_cast<float4*>(Y),
                      V / 8);
@@ -198,6 +372,9 @@ cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cud
 
 cudaError_t launch_token_logprobs(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
                                   cudaStream_t stream) {
+  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll)
+    return launch_overlapped(token_logprobs_cta_kernel, dim3((unsigned)M), dim3(kLsmCtaThreads), stream,
+                             static_cast<const uint4*>(X), ids, out, V / 8);
   if (M > 0x7FFFFFFFll / kLsmCtas) return cudaErrorInvalidValue;
   return launch_rows(token_logprobs_kernel, M, stream, static_cast<const uint4*>(X), ids, out, V / 8);
 }

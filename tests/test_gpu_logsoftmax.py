@@ -2,9 +2,11 @@
 the fp64 oracle, special rows, and batch invariance (bit-exact rows across M,
 positions and permutations).
 
-Tolerance, from the arithmetic: each thread folds n = 8*ceil(V/32768) terms
-into its running sum, then three 5-level butterflies combine the pairs; every
-step rounds once (2^-24) and expf adds at most about one more ulp, so the sum's
+Tolerance, from the arithmetic: each thread sums n = 8*ceil(V/32768) terms
+exp(x - m) (m its own maximum), then three 5-level butterflies combine the
+pairs; every step rounds once (2^-24); a term exp(d) = 2^(d log2 e) by
+ex2.approx is off by about 2^-22 relative plus |d| 2^-24 from the rounded
+product, and since d e^d <= 1/e that adds below n 2^-25 to the sum, so the sum's
 relative error is below (n + 20) * 2^-23 and lse moves by at most that plus
 the rounding of logf and of m + log(s); the final x - lse rounds once more:
     |gpu - ref| <= (n + 30) * 2^-23 + 2^-22 * (|lse| + |ref|)."""
@@ -48,7 +50,7 @@ def f64(X):
 
 
 @pytest.mark.parametrize("V", [8, 1000, 4104, 128256])
-@pytest.mark.parametrize("M,std", [(1, 1.0), (3, 4.0), (37, 8.0)])
+@pytest.mark.parametrize("M,std", [(1, 1.0), (3, 4.0), (37, 8.0), (100, 2.0)])
 def test_log_softmax_parity(lib, oracle, V, M, std):
     X = inputs.normal((M, V), std=std, seed=20, stream=0)
     ref = oracle.log_softmax(inputs.bits(X))
@@ -82,6 +84,26 @@ def test_rows_independent_of_batch_and_position(lib):
     perm = torch.randperm(300, generator=torch.Generator().manual_seed(6))
     shuffled = lib.bi_log_softmax_bf16(X[perm.cuda()].contiguous()).cpu().numpy().view(np.uint32)
     assert np.array_equal(shuffled, full[perm.numpy()])
+
+
+@pytest.mark.parametrize("V", [8, 1000, 128256, 140008])
+def test_cluster_and_cta_variants_give_the_same_bits(lib, V):
+    """Rows of a batch of 70 run one CTA per row; a row alone runs on an
+    8-CTA cluster.  Both follow the same tree: identical bits, including rows
+    longer than the register cache (V > 131072) and special rows."""
+    X = inputs.normal((70, V), std=5.0, seed=24, stream=0)
+    X[5, :] = float("-inf")
+    X[6, V // 2] = float("nan")
+    X[7, V - 1] = float("-inf")
+    X = X.cuda()
+    full = lib.bi_log_softmax_bf16(X).cpu().numpy().view(np.uint32)
+    ids = torch.arange(70, dtype=torch.int32, device="cuda") % V
+    tok = lib.bi_token_logprobs_bf16(X, ids).cpu().numpy().view(np.uint32)
+    for r in (0, 5, 6, 7, 69):
+        alone = lib.bi_log_softmax_bf16(X[r:r + 1].contiguous()).cpu().numpy().view(np.uint32)
+        assert np.array_equal(alone[0], full[r]), r
+        t1 = lib.bi_token_logprobs_bf16(X[r:r + 1].contiguous(), ids[r:r + 1]).cpu().numpy().view(np.uint32)
+        assert t1[0] == tok[r], r
 
 
 def test_token_logprobs_are_the_same_bits(lib, oracle):
