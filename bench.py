@@ -869,6 +869,23 @@ def run_single_attention(args, dist):
         raise RuntimeError(bd.status_string(st))
 
 
+def run_single_rmsnorm(args, dist):
+    """Launches RMSNorm on one shape (H:M), --launches times on rotating
+    inputs, for an ncu capture of those launches."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    H, M = (int(x) for x in args.single_rmsnorm.split(":"))
+    n = copies_for(M * H * 2, cap=8)
+    xs = [inputs.device_normal((M, H), seed=dist.rank, stream=60 + i, device=dev) for i in range(n)]
+    g = inputs.device_normal((H,), std=0.1, mean=1.0, seed=dist.rank, stream=inputs.STREAM_G, device=dev)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    for i in range(args.launches):
+        bd.bi_rmsnorm_bf16(xs[i % n], g, EPS, out=y)
+    torch.cuda.synchronize()
+
+
 def run_reference(args, dist):
     """The reference arm: the CPU oracle on a bounded sample of the same workload."""
     if dist.rank != 0:
@@ -913,6 +930,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--single-rmsnorm", default="",
+                    help="H:M -- only launch RMSNorm on that shape (for ncu)")
     ap.add_argument("--single-attention", default="",
                     help="MIX:SPLIT -- only launch decode attention on that request mix (for ncu)")
     ap.add_argument("--single-m", type=int, default=0,
@@ -925,6 +944,9 @@ def main():
     try:
         if args.single_attention:
             run_single_attention(args, dist)
+            return
+        if args.single_rmsnorm:
+            run_single_rmsnorm(args, dist)
             return
         if args.single_m:
             run_single_m(args, dist)

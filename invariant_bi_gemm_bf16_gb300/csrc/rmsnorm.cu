@@ -93,100 +93,8 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   }
 }
 
-// H = 256 * VPL, wide rows: each warp streams its rows (row w, w + W, ...,
-// W warps in the grid) through a ring of kRmsStages row buffers in shared
-// memory, filled by 16-byte asynchronous copies.  Lane l copies exactly the
-// vectors it later reads (l, l + 32, ...), so its own wait_group makes them
-// visible and no lane waits for another.  The arithmetic is that of
-// rmsnorm_regs_kernel, vector for vector; the copies only keep kRmsStages rows
-// of every warp in flight without holding them in registers.
-constexpr int kRmsStages = 3;
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-template <int VPL>
-__global__ void __launch_bounds__(256)
-    rmsnorm_async_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M, float eps) {
-  extern __shared__ uint4 rms_ring[];
-  grid_dep_launch_dependents();
-  grid_dep_wait();  // X may come from the previous kernel in the stream
-  constexpr int kVecs = VPL * 32;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  uint4* ring = rms_ring + (size_t)warp * kRmsStages * kVecs;
-  // prologue: the warp's first kRmsStages rows (one commit group per row,
-  // empty groups past M keep the count uniform)
-#pragma unroll
-  for (int st = 0; st < kRmsStages; ++st) {
-    const int64_t row = first + st * nwarps;
-    if (row < M) {
-      const uint4* x = X + row * kVecs;
-#pragma unroll 8
-      for (int i = 0; i < VPL; ++i) cp_async16(ring + st * kVecs + lane + 32 * i, x + lane + 32 * i);
-    }
-    cp_async_commit();
-  }
-  // Software pipeline: the serial sum-of-squares chain of the next row runs
-  // interleaved with the (independent) normalisation and stores of the
-  // current one.  Commit groups go one per row in row order, so before the
-  // step for the k-th row k + 3 groups exist and waiting down to one pending
-  // group means rows k and k + 1 have landed.
-  int st = 0;
-  float r = 0.0f;
-  if (first < M) {
-    cp_async_wait<kRmsStages - 1>();
-    const uint4* v = ring;
-    float ss = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < VPL; ++i) ss = sumsq8(v[lane + 32 * i], ss);
-    r = inv_rms(butterfly_sum(ss), (int64_t)kVecs * 8, eps);
-  }
-  for (int64_t row = first; row < M; row += nwarps) {
-    const int64_t nxt = row + nwarps;
-    const bool has_next = nxt < M;  // the same in every lane
-    const int st_next = st + 1 == kRmsStages ? 0 : st + 1;
-    cp_async_wait<1>();
-    const uint4* v = ring + st * kVecs;
-    const uint4* vn = ring + st_next * kVecs;
-    uint4* y = Y + row * kVecs;
-    float ss = 0.0f;
-    if (has_next) {
-#pragma unroll 8
-      for (int i = 0; i < VPL; ++i) {
-        ss = sumsq8(vn[lane + 32 * i], ss);
-        __stcs(y + lane + 32 * i, norm8(v[lane + 32 * i], __ldg(g + lane + 32 * i), r));
-      }
-    } else {
-#pragma unroll 8
-      for (int i = 0; i < VPL; ++i) __stcs(y + lane + 32 * i, norm8(v[lane + 32 * i], __ldg(g + lane + 32 * i), r));
-    }
-    // refill this stage with the row kRmsStages ahead
-    const int64_t ahead = row + (int64_t)kRmsStages * nwarps;
-    if (ahead < M) {
-      const uint4* x = X + ahead * kVecs;
-#pragma unroll 8
-      for (int i = 0; i < VPL; ++i) cp_async16(ring + st * kVecs + lane + 32 * i, x + lane + 32 * i);
-    }
-    cp_async_commit();
-    if (has_next) r = inv_rms(butterfly_sum(ss), (int64_t)kVecs * 8, eps);
-    st = st_next;
-  }
-  cp_async_wait<0>();
-}
-
-// H = 256 * VPL, VPL a multiple of 8, rows too wide to stage per warp at
-// high occupancy: two passes over the row, each issuing 8 vector loads per
-// lane before using them.  The first pass caches the row in L2 only, and the
+// H = 256 * VPL, VPL a multiple of 8: two passes over the row, each issuing 8
+// vector loads per lane before using them.  The first pass caches the row in L2 only, and the
 // second reads it back from there; the arithmetic is vector for vector that
 // of rmsnorm_regs_kernel.  About 40 registers, so many warps per SM hide the
 // serial sum-of-squares chain of each row.
@@ -240,29 +148,10 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   for (int64_t i = lane; i < nvec; i += 32) y[i] = norm8(x[i], __ldg(g + i), r);
 }
 
-// Wide rows through rmsnorm_async_kernel: warps per block so that the rings
-// fill about 192 KB of shared memory, and one block per SM (grid-stride rows).
-template <int VPL>
-static cudaError_t launch_async(const uint4* x, const uint4* g, uint4* y, int64_t M, float eps,
-                                cudaStream_t stream) {
-  constexpr int64_t kRowBytes = (int64_t)VPL * 32 * 16;
-  int warps = (int)((192 * 1024) / (kRmsStages * kRowBytes));
-  if (warps > 8) warps = 8;
-  if (warps < 1) warps = 1;
-  const int smem = warps * kRmsStages * (int)kRowBytes;
-  auto kern = rmsnorm_async_kernel<VPL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  int64_t blocks = (M + warps - 1) / warps;
-  if (blocks > sms) blocks = sms;
-  if (blocks < 1) blocks = 1;
-  return launch_overlapped_smem(kern, dim3((unsigned)blocks), dim3(32 * warps), (size_t)smem, stream, x, g, y,
-                                M, eps);
-}
-
+// Kernel per width, measured on GB300 (M = 16384, fraction of the copy
+// bandwidth): registers for H <= 2048 (2048: 1.00) and 8192 (0.83), two
+// passes for 4096 (0.90) and 16384.  All run the same lane partition and
+// order, so the choice never changes a bit.
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
                            cudaStream_t stream) {
   const int64_t blocks = (M + kRmsWarps - 1) / kRmsWarps;
@@ -275,9 +164,9 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
     case 256: return launch_overlapped(rmsnorm_regs_kernel<1>, grid, block, stream, x, gg, y, M, eps);
     case 512: return launch_overlapped(rmsnorm_regs_kernel<2>, grid, block, stream, x, gg, y, M, eps);
     case 1024: return launch_overlapped(rmsnorm_regs_kernel<4>, grid, block, stream, x, gg, y, M, eps);
-    case 2048: return launch_async<8>(x, gg, y, M, eps, stream);
-    case 4096: return launch_async<16>(x, gg, y, M, eps, stream);
-    case 8192: return launch_overlapped(rmsnorm_wide_kernel<32>, grid, block, stream, x, gg, y, M, eps);
+    case 2048: return launch_overlapped(rmsnorm_regs_kernel<8>, grid, block, stream, x, gg, y, M, eps);
+    case 4096: return launch_overlapped(rmsnorm_wide_kernel<16>, grid, block, stream, x, gg, y, M, eps);
+    case 8192: return launch_overlapped(rmsnorm_regs_kernel<32>, grid, block, stream, x, gg, y, M, eps);
     case 16384: return launch_overlapped(rmsnorm_wide_kernel<64>, grid, block, stream, x, gg, y, M, eps);
     default: return launch_overlapped(rmsnorm_loop_kernel, grid, block, stream, x, gg, y, M, H, eps);
   }
