@@ -52,8 +52,8 @@ EPS = 1e-5
 # (summaries in profiles/), keyed by build_fingerprint() of the GEMM kernel's
 # sources: valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "b0dc026b481772df931f264dd6603233ad9eafd580b0080e12cc956b3ec716ad": {8192: 964988928 + 63569152,
-                                                                        1: 117509632 + 2750208},
+    "700d3dd54d575c18a624fb720a891656b0a21fb605baa2996ad7dd932f078a9a": {8192: 965532416 + 63633408,
+                                                                        1: 117508864 + 2688000},
 }
 
 
