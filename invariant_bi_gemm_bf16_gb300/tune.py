@@ -8,6 +8,11 @@ Workloads (synthetic inputs, random-init weights of the named shapes):
                       1, 2, 4, 2, 1, 1 (recorded by running the stack);
   llama31-8b-prefill  the Llama-3.1-8B qkv, gate_up and down_proj projections at
                       M = 1, 8, 32, 128, 1024, 4096, 8192, one call each.
+  decode-attention-70b  decode attention with Llama-3.1-70B heads (64 query, 8
+                      key/value, pages of 16) over three decode steps, one each:
+                      64 requests with lengths uniform on [512, 8192], 256 on
+                      [64, 2048], and one request of 32768; the split size is
+                      the tuned pin.
 The tuned table is one pin tuple per (N, K), for every batch size.  For the
 decode workload, the additivity error delta is measured on the whole step
 (default tuple against tuned tuple) and reported with its bound.
@@ -98,9 +103,25 @@ def run_prefill(args):
     return entries, meta
 
 
+ATTN_STEPS = ((64, 512, 8192), (256, 64, 2048), (1, 32768, 32768))
+
+
+def run_attention(args):
+    import numpy as np
+    rng = np.random.default_rng(70)
+    calls = [([int(x) for x in rng.integers(lo, hi + 1, size=B)], 1) for B, lo, hi in ATTN_STEPS]
+    e = tuner.tune_attention(64, 8, 16, calls)
+    print(json.dumps(e["attention"]["measured"]), file=sys.stderr, flush=True)
+    meta = {"workload": "decode-attention-70b: 64 query / 8 key-value heads, pages of 16; steps (B, lo, hi) = %s"
+                        % (ATTN_STEPS,),
+            "device": torch.cuda.get_device_name(), "sm_count": torch.cuda.get_device_properties(0).multi_processor_count}
+    return [e], meta
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", choices=["llama31-70b-decode", "llama31-8b-prefill"], required=True)
+    ap.add_argument("--workload", choices=["llama31-70b-decode", "llama31-8b-prefill", "decode-attention-70b"],
+                    required=True)
     ap.add_argument("--mode", choices=["search", "exhaustive"], default="search")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--out", required=True)
@@ -108,8 +129,10 @@ def main(argv=None):
     bd.load()
     if args.workload == "llama31-70b-decode":
         entries, meta = run_decode(args)
-    else:
+    elif args.workload == "llama31-8b-prefill":
         entries, meta = run_prefill(args)
+    else:
+        entries, meta = run_attention(args)
     tuner.dump(entries, args.out, **meta)
     tuner.load(args.out)   # the written table must validate
     print(json.dumps({k: v for k, v in meta.items()}), flush=True)

@@ -20,6 +20,12 @@ Sec. 6 (Tuner) and Eq. 3, restated for this library:
 * Search: coordinate descent from the default pins over the grid's axes,
   measuring a part of the grid (``search``); ``exhaustive`` measures all of it.
 
+Decode attention's split size is tuned the same way (Detent, Sec. 7: the tuner
+also picks FA3's split stride like a pin).  A family is one head layout (query
+heads, key/value heads, page size); its calls are decode steps, each a list of
+request lengths with a count; the split size is the argmin of the family's
+summed time over the legal sizes (multiples of 64 up to 4096), all measured.
+
 Timing: each (candidate, M) is timed as back-to-back calls between two CUDA
 events on rotating weight copies (more bytes than L2), after warm-up calls,
 and a candidate's cost takes the fastest of a few repeats (the SM clock drifts
@@ -251,15 +257,26 @@ def dump(entries: Sequence[dict], path: str, **meta):
         f.write("\n")
 
 
-def load(path: str) -> Dict[Tuple[int, int], bd.Pins]:
-    """{(N, K): Pins} from a tuned table; every entry must pass
-    bi_pins_validate for its shape (an illegal table is refused whole)."""
+def load(path: str) -> Dict[tuple, object]:
+    """{(N, K): Pins, ("attention", Hq, Hkv, page_size): split_size} from a
+    tuned table; every GEMM entry must pass bi_pins_validate for its shape and
+    every split size must be legal (an illegal table is refused whole)."""
     with open(path) as f:
         doc = json.load(f)
     if doc.get("format") != FORMAT:
         raise ValueError("not a %s file: %r" % (FORMAT, doc.get("format")))
     table = {}
     for fam in doc["families"]:
+        if "attention" in fam:
+            att = fam["attention"]
+            key = ("attention", int(att["Hq"]), int(att["Hkv"]), int(att["page_size"]))
+            split = int(att["split_size"])
+            if split % 64 or not 64 <= split <= bd.BI_ATTN_MAX_SPLIT:
+                raise ValueError("split size %d for %r is illegal" % (split, key))
+            if key in table:
+                raise ValueError("two entries for %r" % (key,))
+            table[key] = split
+            continue
         N, K = int(fam["N"]), int(fam["K"])
         p = bd.Pins(**{k: int(v) for k, v in fam["pins"].items()})
         st = bd.bi_pins_validate(N, K, p)
@@ -269,3 +286,91 @@ def load(path: str) -> Dict[Tuple[int, int], bd.Pins]:
             raise ValueError("two entries for (N=%d, K=%d)" % (N, K))
         table[(N, K)] = p
     return table
+
+
+# --------------------------------------------------------------------------- decode attention
+
+ATTN_SPLITS = (64, 128, 256, 512, 1024, 2048, 4096)
+
+
+def attn_legal_splits(splits: Sequence[int] = ATTN_SPLITS) -> List[int]:
+    """The legal split sizes among `splits`: multiples of 64 up to BI_ATTN_MAX_SPLIT."""
+    return [S for S in splits if S % 64 == 0 and 64 <= S <= bd.BI_ATTN_MAX_SPLIT]
+
+
+class AttnTimer:
+    """t(split) of one recorded decode-attention workload on the current CUDA
+    device: `calls` is a list of (request lengths, count); each call is timed
+    as back-to-back decode steps over a paged cache (pages of `page_size`,
+    shuffled) larger than L2."""
+
+    def __init__(self, Hq: int, Hkv: int, page_size: int, calls, reps: int = 10, seed: int = 0):
+        import torch
+        from . import inputs
+        self.calls = [(list(map(int, lens)), int(n)) for lens, n in calls]
+        self.Hq, self.Hkv, self.P = Hq, Hkv, page_size
+        self.data = []
+        for i, (lens, _) in enumerate(self.calls):
+            kc, vc, bt, sl = inputs.device_paged_kv(lens, Hkv, bd.BI_ATTN_HEAD_DIM, page_size, seed=seed + i)
+            q = inputs.device_normal((len(lens), Hq, bd.BI_ATTN_HEAD_DIM), seed=seed + i, stream=0)
+            out = torch.empty_like(q)
+            self.data.append((q, kc, vc, bt, sl, out))
+        self.reps = reps
+
+    def call_time(self, i: int, split: int) -> float:
+        import torch
+        q, kc, vc, bt, sl, out = self.data[i]
+        ml = bt.shape[1] * self.P
+        ws = torch.empty(bd.bi_decode_attention_workspace_bytes(q.shape[0], self.Hq, self.Hkv, ml, split),
+                         dtype=torch.uint8, device=q.device)
+        run = lambda: bd.bi_decode_attention_bf16(q, kc, vc, bt, sl, bd.BI_ATTN_HEAD_DIM ** -0.5, max_seq_len=ml,
+                                                  split_size=split, out=out, workspace=ws)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(self.reps):
+            run()
+        e.record()
+        torch.cuda.synchronize()
+        if bd.bi_last_device_status() != bd.BI_OK:
+            raise bd.BiError(bd.bi_last_device_status(), "tuner timing")
+        return s.elapsed_time(e) * 1e3 / self.reps
+
+    def __call__(self, split: int) -> float:
+        return float(sum(n * self.call_time(i, split) for i, (_, n) in enumerate(self.calls)))
+
+
+def tune_attention(Hq: int, Hkv: int, page_size: int, calls, splits: Sequence[int] = ATTN_SPLITS,
+                   timer=None, repeats: int = 2, margin: float = 0.01) -> dict:
+    """Picks the split size of one attention family: every legal size is
+    measured (the best of `repeats`), then the winner must beat the library
+    default by `margin` in interleaved re-measurements (else the default is
+    kept).  Returns the table entry."""
+    import statistics
+    legal = attn_legal_splits(splits)
+    if not legal:
+        raise ValueError("no legal split size")
+    timer = timer or AttnTimer(Hq, Hkv, page_size, calls)
+    cost = {S: min(timer(S) for _ in range(repeats)) for S in legal}
+    best = min(legal, key=lambda S: (cost[S], S))
+    default = bd.BI_ATTN_DEFAULT_SPLIT
+    chosen, t_default, t_best = default, None, None
+    if best == default:
+        t_default = t_best = cost[best]
+    else:
+        cd, cb = [], []
+        for _ in range(3):
+            cd.append(timer(default))
+            cb.append(timer(best))
+        t_default, t_best = statistics.median(cd), statistics.median(cb)
+        if t_best < t_default * (1.0 - margin):
+            chosen = best
+    return {"attention": {"Hq": Hq, "Hkv": Hkv, "page_size": page_size,
+                          "calls": [{"lengths": len(lens), "max": max(lens), "total": sum(lens), "n": n}
+                                    for lens, n in [(list(c[0]), c[1]) for c in calls]],
+                          "split_size": chosen, "T_us": round(t_best if chosen == best else t_default, 2),
+                          "default_split": default, "T_default_us": round(t_default, 2),
+                          "measured": {str(S): round(c, 2) for S, c in cost.items()}}}

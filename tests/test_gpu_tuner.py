@@ -37,3 +37,17 @@ def test_search_measures_part_of_the_grid(lib):
     e = tuner.tune_family(N, K, [(1, 1), (256, 1)], mode="search", reps=3)
     assert e["measured"] < e["legal"]
     assert e["T_us"] <= e["T_default_us"] * 1.05
+
+
+def test_tune_attention_on_the_gpu(lib, tmp_path):
+    """A small decode-attention family tuned on the GPU: every legal split
+    size measured, a legal choice, and a table that loads."""
+    from invariant_bi_gemm_bf16_gb300 import tuner
+    calls = [([300, 1000, 77], 2), ([2000], 1)]
+    e = tuner.tune_attention(16, 2, 16, calls, splits=(128, 256, 512))
+    att = e["attention"]
+    assert att["split_size"] in (128, 256, 512)
+    assert set(att["measured"]) == {"128", "256", "512"} and all(v > 0 for v in att["measured"].values())
+    path = str(tmp_path / "a.json")
+    tuner.dump([e], path)
+    assert tuner.load(path) == {("attention", 16, 2, 16): att["split_size"]}

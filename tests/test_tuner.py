@@ -109,3 +109,40 @@ def test_json_round_trip_and_refusals(lib, tmp_path):
         json.dump({"format": "something else", "families": []}, f)
     with pytest.raises(ValueError):
         tuner.load(path)
+
+
+def test_attention_split_grid_is_the_legal_sizes(lib):
+    assert tuner.attn_legal_splits((32, 64, 100, 128, 4096, 8192)) == [64, 128, 4096]
+    assert tuner.attn_legal_splits() == list(tuner.ATTN_SPLITS)
+
+
+def test_tune_attention_takes_the_argmin_and_keeps_the_default_within_the_margin(lib):
+    # Detent, Sec. 7: the split stride is tuned like a pin.  A made-up cost per split size.
+    costs = {64: 10.0, 128: 8.0, 256: 9.0, 512: 5.0, 1024: 6.0, 2048: 7.0, 4096: 12.0}
+    e = tuner.tune_attention(64, 8, 16, [([100, 200], 1)], timer=costs.__getitem__, repeats=1)
+    att = e["attention"]
+    assert att["split_size"] == 512 and att["T_us"] == 5.0 and att["T_default_us"] == 9.0
+    assert sorted(int(k) for k in att["measured"]) == list(tuner.ATTN_SPLITS)
+    near = {S: 10.0 for S in costs}
+    near[256], near[512] = 9.0, 8.95   # the best beats the default by less than 1%
+    e = tuner.tune_attention(64, 8, 16, [([100], 1)], timer=near.__getitem__, repeats=1)
+    assert e["attention"]["split_size"] == bd.BI_ATTN_DEFAULT_SPLIT
+    with pytest.raises(ValueError):
+        tuner.tune_attention(64, 8, 16, [([100], 1)], splits=(100,), timer=costs.get)
+
+
+def test_json_round_trip_with_an_attention_entry(lib, tmp_path):
+    p = bd.bi_pins_default(4096, 14336)
+    gemm = {"N": 4096, "K": 14336, "calls": [{"M": 1, "n": 1}], "pins": p.as_dict()}
+    att = {"attention": {"Hq": 64, "Hkv": 8, "page_size": 16, "split_size": 512}}
+    path = str(tmp_path / "t.json")
+    tuner.dump([gemm, att], path)
+    table = tuner.load(path)
+    assert table[("attention", 64, 8, 16)] == 512 and table[(4096, 14336)].as_dict() == p.as_dict()
+    for bad in (100, 8192, 0):
+        tuner.dump([{"attention": dict(att["attention"], split_size=bad)}], path)
+        with pytest.raises(ValueError):
+            tuner.load(path)
+    tuner.dump([att, att], path)
+    with pytest.raises(ValueError):
+        tuner.load(path)
