@@ -260,6 +260,36 @@ def oracle_gemm_throughput(target_s: float = 12.0, max_rows: int = 2048):
     return flops / dt / 1e12, dt, rows, threads
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_gemm_1thread(rows: int = 16):
+    """The oracle's down_proj GEMM on `rows` rows with one thread: (TFLOPS, seconds)."""
+    import oracle
+    X, W = oracle_inputs(max(rows, 2))
+    t0 = time.perf_counter()
+    oracle.gemm(X[:rows], W, nthreads=1)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * DOWN_N * DOWN_K / dt / 1e12, dt
+
+
 def smi_gpu_id(local_rank: int) -> str:
     """The nvidia-smi -i argument for this process's GPU."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -333,6 +363,23 @@ class DownProjSweep:
         e.record()
         torch.cuda.synchronize()
         return s.elapsed_time(e) * 1e3 / reps
+
+    def median_m(self, j, reps=50, use_torch=False):
+        """Median device time of one launch at the j-th M over `reps` launches,
+        each between its own pair of events (rotating weight copies), after
+        10 untimed launches."""
+        M = self.ms[j]
+        xs = self.X[M]
+        for i in range(10):
+            self._launch(M, xs[i % len(xs)], self.W[i % self.nw], use_torch)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            ev[i][0].record()
+            self._launch(M, xs[i % len(xs)], self.W[i % self.nw], use_torch)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) * 1e3 for a, b in ev]))
 
     def _launch(self, M, x, w, use_torch):
         if use_torch:
@@ -740,6 +787,8 @@ def run_ours(args, dist):
 
     # torch.mm on the same tensors, same protocol
     torch_launch = np.array([[wl.time_m(j, reps=args.per_m_reps, use_torch=True)] for j in range(L)]).T
+    med = [wl.median_m(j) for j in range(L)]
+    torch_med = [wl.median_m(j, use_torch=True) for j in range(L)]
     torch_wall = time_steps(lambda: wl.step(use_torch=True), args.steps, dist)
     sweep = []
     sum_roof = 0.0
@@ -754,7 +803,8 @@ def run_ours(args, dist):
         bound = "tensor" if f / (peaks["bf16_tflops"] * 1e6) >= b / (peaks["hbm_gbs"] * 1e3) else "hbm"
         sweep.append({"M": M, "us": round(us, 2), "tflops": round(f / us / 1e6, 1),
                       "gbs": round(b / us / 1e3, 1), "bound": bound, "roofline_frac": round(tr / us, 3),
-                      "torch_mm_us": round(tus, 2), "vs_torch_mm": round(tus / us, 3)})
+                      "torch_mm_us": round(tus, 2), "vs_torch_mm": round(tus / us, 3),
+                      "us_median50": round(med[j], 2), "torch_mm_us_median50": round(torch_med[j], 2)})
 
     # e2e through the C ABI with host buffers
     host_x = {M: wl.X[M][0].cpu().pin_memory() for M in wl.ms}
@@ -811,7 +861,9 @@ def run_ours(args, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": L * args.steps,
-        "per_m_timing": "per-M times: %d back-to-back launches of that M between two CUDA events" % args.per_m_reps,
+        "per_m_timing": ("us: %d back-to-back launches of that M between two CUDA events (mean); us_median50: "
+                         "median of 50 launches, each between its own events, after 10 warm-up launches"
+                         % args.per_m_reps),
         "clocks": clk,
         "sweep": sweep,
         "torch_mm_sweep_tflops": round(flops * args.steps / torch_wall / 1e12, 1),
@@ -830,9 +882,11 @@ def run_ours(args, dist):
         result["attention"] = run_attention(args, dist, peaks)
     if dist.rank == 0 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_gemm_throughput(target_s=args.cpu_seconds)
+        tf1, dt1 = oracle_gemm_1thread(16)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                   "sample": "oracle down_proj GEMM on %d rows x all 4096 outputs (K=14336), "
-                                            "%.1f s" % (rows, secs)}
+                                            "%.1f s" % (rows, secs), "model": cpu_model(),
+                                  "value_1thread": round(tf1, 6), "sample_1thread": "%d rows, %.1f s" % (16, dt1)}
     return result
 
 
