@@ -35,6 +35,8 @@
 //            tiles (and q) through its own ring of TMA copies, runs the
 //            split and writes its record;
 //   combine  folds each request's split records in order.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "attention.h"
@@ -642,15 +644,20 @@ __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const
 
 template <int NT>
 static cudaError_t launch_attn_t(const AttnLaunch& A) {
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory limits are per device: set them once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(decode_attn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          AttnCfg<NT>::smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              comb_smem_bytes<NT>());
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured.fetch_or(bit);
   }
   cudaError_t e = launch_overlapped(decode_attn_plan_kernel, dim3(1), dim3(kPlanThreads), A.stream, A.p, A.B);
   if (e != cudaSuccess) return e;
