@@ -44,6 +44,8 @@
 // records BI_ERR_DEVICE_TIMEOUT in a device status word, every role abandons
 // its work, in-flight copies and MMAs are drained (again with bounded waits),
 // tensor memory is freed and the CTA returns normally.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -690,13 +692,25 @@ int64_t gemm_smem_bytes(int T, int x_rows, int w_stages, int x_stages, int kps, 
 template <int T, bool CLUSTER, bool PAIR, int KP, bool FP8 = false>
 static cudaError_t launch_t(const GemmLaunch& L) {
   auto kern = bi_gemm_kernel<T, CLUSTER, PAIR, KP, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
+  // Kernel attributes are per device: raise this instance's shared-memory
+  // limit to the largest ring (and allow clusters above 8) once per device,
+  // not on every launch.
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int cluster = CLUSTER ? L.units * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
-  if (cluster > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    if (CLUSTER) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    configured.fetch_or(bit);
   }
+  if (L.smem > kMaxDynSmem) return cudaErrorInvalidValue;
+  const int cluster = CLUSTER ? L.units * (PAIR ? 2 : 1) : (PAIR ? 2 : 1);
   GemmParams prm;
   prm.Y = static_cast<__nv_bfloat16*>(L.Y);
   prm.M = L.M;
