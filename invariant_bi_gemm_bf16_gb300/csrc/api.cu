@@ -41,7 +41,7 @@ struct TableEntry {
 const TableEntry kTable[] = {
     {128, 256, 2, 128, 0},       // tiny invariance shape: exercises the split fold
     {4096, 14336, 4, 256, 0},    // Llama-3.1-8B down_proj: 32 W tiles x 4 = 128 CTAs at decode
-    {6144, 4096, 3, 256, 0},     // Llama-3.1-8B qkv: 48 x 3 = 144
+    {6144, 4096, 2, 256, 0},     // Llama-3.1-8B qkv: 48 clusters of 2 fit at once (48 of 3 do not)
     {28672, 4096, 2, 256, 0},    // Llama-3.1-8B gate_up: 224 x 2 = 448 (2.95 waves)
     {10240, 8192, 3, 256, 0},    // Llama-3.1-70B qkv: 80 x 3 = 240
     {8192, 8192, 2, 256, 0},     // Llama-3.1-70B o_proj: 64 x 2 = 128
