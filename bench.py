@@ -818,6 +818,12 @@ def run_ours(args, dist):
     torch_launch = np.array([[wl.time_m(j, reps=args.per_m_reps, use_torch=True)] for j in range(L)]).T
     med = [wl.median_m(j) for j in range(L)]
     torch_med = [wl.median_m(j, use_torch=True) for j in range(L)]
+    def graph_m(j, use_torch):
+        M = wl.ms[j]
+        xs = wl.X[M]
+        return time_graph(lambda i: wl._launch(M, xs[i % len(xs)], wl.W[i % wl.nw], use_torch), args.per_m_reps)
+    gr = [graph_m(j, False) for j in range(L)]
+    torch_gr = [graph_m(j, True) for j in range(L)]
     torch_wall = time_steps(lambda: wl.step(use_torch=True), args.steps, dist)
     sweep = []
     sum_roof = 0.0
@@ -833,7 +839,8 @@ def run_ours(args, dist):
         sweep.append({"M": M, "us": round(us, 2), "tflops": round(f / us / 1e6, 1),
                       "gbs": round(b / us / 1e3, 1), "bound": bound, "roofline_frac": round(tr / us, 3),
                       "torch_mm_us": round(tus, 2), "vs_torch_mm": round(tus / us, 3),
-                      "us_median50": round(med[j], 2), "torch_mm_us_median50": round(torch_med[j], 2)})
+                      "us_median50": round(med[j], 2), "torch_mm_us_median50": round(torch_med[j], 2),
+                      "us_graph": round(gr[j], 2), "torch_mm_us_graph": round(torch_gr[j], 2)})
 
     # e2e through the C ABI with host buffers
     host_x = {M: wl.X[M][0].cpu().pin_memory() for M in wl.ms}
@@ -891,8 +898,9 @@ def run_ours(args, dist):
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": L * args.steps,
         "per_m_timing": ("us: %d back-to-back launches of that M between two CUDA events (mean); us_median50: "
-                         "median of 50 launches, each between its own events, after 10 warm-up launches"
-                         % args.per_m_reps),
+                         "median of 50 launches, each between its own events, after 10 warm-up launches; "
+                         "us_graph: %d launches captured in one CUDA graph and replayed (device time only, no "
+                         "host overhead)" % (args.per_m_reps, args.per_m_reps)),
         "clocks": clk,
         "sweep": sweep,
         "torch_mm_sweep_tflops": round(flops * args.steps / torch_wall / 1e12, 1),
