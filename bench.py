@@ -52,8 +52,8 @@ EPS = 1e-5
 # (summaries in profiles/), keyed by build_fingerprint() of the GEMM kernel's
 # sources: valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "700d3dd54d575c18a624fb720a891656b0a21fb605baa2996ad7dd932f078a9a": {8192: 965532416 + 63633408,
-                                                                        1: 117508864 + 2688000},
+    "933127d6c4cd5c4b61580cd1ff1c974e38bfd68c08a9b16198f6541580d74f26": {8192: 965138432 + 63582464,
+                                                                        1: 117509632 + 2737920},
 }
 
 
