@@ -34,7 +34,9 @@
 //            stream: it takes items by ticket, stages their 32-position K/V
 //            tiles (and q) through its own ring of TMA copies, runs the
 //            split and writes its record;
-//   combine  folds each request's split records in order.
+//   combine  folds each request's split records in order, one CTA per
+//            (key/value head, request), or per (key/value head, slice of
+//            d, request) when there are few requests.
 #include <atomic>
 
 #include <cuda_bf16.h>
@@ -538,35 +540,48 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
 // combine
 // ---------------------------------------------------------------------------
 
-// One CTA per (key/value head, request): folds the request's split records
-// in split order and writes out[b][h][d] for the group's heads.  Thread t owns
-// head h = t % GP and the values d = t / GP + (256 / GP) i; the records come
-// into shared memory kCombChunk at a time by bulk copy, double-buffered, so
-// the fold runs at shared-memory speed.
+// One CTA per (key/value head, slice of 128 / SL d, request): folds the
+// request's split records in split order and writes out[b][h][d] for the
+// group's heads and the slice's d.  Thread t owns head h = t % GP and the
+// values d = t / GP + (256 / GP) i of the slice.  The records come into shared
+// memory a chunk at a time by bulk copy, double-buffered: whole records (one
+// copy per chunk) when SL = 1, else each record's o slice and its m and l (two
+// copies per record).  SL changes no operation: every (h, d) folds the same
+// records in the same order.  Slicing only pays when there are few (request,
+// head) pairs, so the host takes SL = 4 when there are fewer pairs than SMs.
 constexpr int kCombThreads = 256;
-constexpr int kCombChunk = 8;
 
-template <int NT>
+template <int SL>
+struct CombCfg {
+  static constexpr int slice_d = kAttnD / SL;
+  static constexpr int chunk = SL == 1 ? 8 : 32;  // records per staged chunk
+};
+
+template <int NT, int SL>
 constexpr int comb_smem_bytes() {
-  return 2 * kCombChunk * (kAttnD + 2) * 8 * NT * 4 + 16;
+  return 2 * CombCfg<SL>::chunk * (CombCfg<SL>::slice_d + 2) * 8 * NT * 4 + 16;
 }
 
-template <int NT>
+template <int NT, int SL>
 __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const AttnParams p, __nv_bfloat16* out) {
   constexpr int GP = 8 * NT;
+  constexpr int SD = CombCfg<SL>::slice_d;
+  constexpr int kCombChunk = CombCfg<SL>::chunk;
   constexpr int RS = (kAttnD + 2) * GP;            // floats per record
+  constexpr int CS = (SD + 2) * GP;                // floats per staged record slice (o slice, m, l)
   constexpr int DSTEP = kCombThreads / GP;         // distance between a thread's d values
-  constexpr int DPT = kAttnD / DSTEP;              // d values per thread
+  constexpr int DPT = SD / DSTEP;                  // d values per thread
   extern __shared__ __align__(16) float comb_smem[];
   __shared__ __align__(8) uint64_t bars[2];
   grid_dep_launch_dependents();
   grid_dep_wait();  // the split records come from the previous kernel
-  const int kvh = blockIdx.x, t = threadIdx.x, h = t % GP, d0 = t / GP;
+  const int kvh = blockIdx.x / SL, slice = blockIdx.x % SL;
+  const int t = threadIdx.x, h = t % GP, d0 = t / GP;
   const int64_t b = blockIdx.y;
   const int64_t L = p.seq_lens[b];
-  __nv_bfloat16* ob = out + (b * p.Hq + (int64_t)kvh * p.G + h) * kAttnD;
+  __nv_bfloat16* ob = out + (b * p.Hq + (int64_t)kvh * p.G + h) * kAttnD + slice * SD;
   if (L <= 0 || L > p.max_len) {
-    // an empty request gives zeros; an invalid length (flagged by the split
+    // an empty request gives zeros; an invalid length (flagged by the plan
     // kernel) gives NaN
     if (h < p.G) {
       const __nv_bfloat16 v = __float2bfloat16_rn(L == 0 ? 0.0f : __int_as_float(0x7fc00000));
@@ -584,14 +599,27 @@ __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const
     fence_mbar_init();
   }
   __syncthreads();
+  // warp 0 stages a chunk: lane 0 announces the bytes, then the copies go out
+  // (one for the chunk when SL = 1; else lane r copies records r, r + 32, ...)
   auto issue = [&](int c) {
     const int n = min(kCombChunk, ns - c * kCombChunk);
     const uint32_t bar = smem_u32(&bars[c & 1]);
-    mbar_arrive_expect_tx(bar, (uint32_t)(n * RS * 4));
-    bulk_load(smem_u32(comb_smem + (c & 1) * kCombChunk * RS), rec0 + (int64_t)c * kCombChunk * RS,
-              (uint32_t)(n * RS * 4), bar);
+    if (t == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * CS * 4));
+    __syncwarp();
+    if constexpr (SL == 1) {
+      if (t == 0)
+        bulk_load(smem_u32(comb_smem + (c & 1) * kCombChunk * RS), rec0 + (int64_t)c * kCombChunk * RS,
+                  (uint32_t)(n * RS * 4), bar);
+    } else {
+      for (int r = t; r < n; r += 32) {
+        const float* rec = rec0 + (int64_t)(c * kCombChunk + r) * RS;
+        const uint32_t dst = smem_u32(comb_smem + ((c & 1) * kCombChunk + r) * CS);
+        bulk_load(dst, rec + slice * SD * GP, (uint32_t)(SD * GP * 4), bar);
+        bulk_load(dst + SD * GP * 4, rec + kAttnD * GP, (uint32_t)(2 * GP * 4), bar);
+      }
+    }
   };
-  if (t == 0) {
+  if (t < 32) {
     issue(0);
     if (nchunks > 1) issue(1);
   }
@@ -610,15 +638,15 @@ __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const
     }
     if (!__syncthreads_and(ok)) {
       if (t == 0) attn_flag(p.status, (int)BI_ERR_DEVICE_TIMEOUT);
-      // the other buffer's copy, if one was issued, must land before the CTA ends
+      // the other buffer's copies, if issued, must land before the CTA ends
       if (t == 0 && c + 1 < nchunks) attn_drain(smem_u32(&bars[(c + 1) & 1]), ((c + 1) >> 1) & 1, p.status);
       return;
     }
-    const float* buf = comb_smem + (c & 1) * kCombChunk * RS;
+    const float* buf = comb_smem + (c & 1) * kCombChunk * CS;
     const int n = min(kCombChunk, ns - c * kCombChunk);
     for (int r = 0; r < n; ++r) {
-      const float* rec = buf + r * RS;
-      const float m2 = rec[kAttnD * GP + h], l2 = rec[kAttnD * GP + GP + h];
+      const float* rec = buf + r * CS;
+      const float m2 = rec[SD * GP + h], l2 = rec[SD * GP + GP + h];
       if (c == 0 && r == 0) {
         m = m2;
         l = l2;
@@ -634,7 +662,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const
       }
     }
     __syncthreads();  // the buffer is read by everyone before it is refilled
-    if (t == 0 && c + 2 < nchunks) issue(c + 2);
+    if (t < 32 && c + 2 < nchunks) issue(c + 2);
   }
   if (h < p.G) {
 #pragma unroll
@@ -654,8 +682,11 @@ static cudaError_t launch_attn_t(const AttnLaunch& A) {
     cudaError_t e = cudaFuncSetAttribute(decode_attn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          AttnCfg<NT>::smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             comb_smem_bytes<NT>());
+    e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             comb_smem_bytes<NT, 1>());
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             comb_smem_bytes<NT, 4>());
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -664,8 +695,11 @@ static cudaError_t launch_attn_t(const AttnLaunch& A) {
   e = launch_overlapped_smem(decode_attn_stream_kernel<NT>, dim3((unsigned)A.grid), dim3(32 * AttnCfg<NT>::warps),
                              AttnCfg<NT>::smem, A.stream, A.tmK, A.tmV, A.p);
   if (e != cudaSuccess) return e;
-  return launch_overlapped_smem(decode_attn_combine_kernel<NT>, dim3((unsigned)A.p.Hkv, (unsigned)A.B),
-                                dim3(kCombThreads), comb_smem_bytes<NT>(), A.stream, A.p, A.out);
+  if ((int64_t)A.B * A.p.Hkv < A.grid)
+    return launch_overlapped_smem(decode_attn_combine_kernel<NT, 4>, dim3((unsigned)(A.p.Hkv * 4), (unsigned)A.B),
+                                  dim3(kCombThreads), comb_smem_bytes<NT, 4>(), A.stream, A.p, A.out);
+  return launch_overlapped_smem(decode_attn_combine_kernel<NT, 1>, dim3((unsigned)A.p.Hkv, (unsigned)A.B),
+                                dim3(kCombThreads), comb_smem_bytes<NT, 1>(), A.stream, A.p, A.out);
 }
 
 cudaError_t launch_decode_attention(const AttnLaunch& A) {

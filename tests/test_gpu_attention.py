@@ -101,6 +101,8 @@ CASES = [
     ([33, 4097], 16, 2, 16, 4096, 1.0),                               # the largest split
     ([513, 2000], 16, 2, 16, 256, 6.0),                               # peaked softmax
     ([1, 2, 3], 16, 2, 256, 256, 1.0),                                # tiny contexts, big pages
+    # more (request, head) pairs than SMs: the combine takes whole records
+    ([(37 * i) % 401 for i in range(100)], 32, 2, 16, 64, 1.0),      # groups of 16, 100 requests
 ]
 
 
