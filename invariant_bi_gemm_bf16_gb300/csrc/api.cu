@@ -93,9 +93,11 @@ struct Resolved {
 
 // K tiles per copy for a launch with token tile T and CTA grouping ctas: 2
 // when the flag asks for it and it is possible (K % 64 == 0, T = 256, or a
-// narrower paired tile of 224, 192 or 160) and the MMAs are paired, else 1.  (A single CTA at T = 256 has a 48 KB K tile; its
-// rings would hold only two X stages of two tiles, which measured slower.)
-// Launches whose X copies cover fewer rows than the token tile use 1
+// narrower paired tile of 224, 192 or 160) and the MMAs are paired, else 1.
+// (A single CTA at T = 256 has a 48 KB K tile; its rings would hold only two
+// X stages of two tiles, which measured slower.)  Otherwise, launches whose X
+// copies cover fewer rows than the token tile use 1, except decode tiles on
+// single-CTA MMAs, which take two K tiles per stage by 2-D copies
 // (make_plan).
 int pins_kps(int64_t K, int32_t T, int32_t ctas, uint32_t flags, Elem e = Elem::BF16) {
   const bool wide = T == 256 || T == 224 || T == 192 || T == 160;
@@ -278,6 +280,16 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   const LaunchChoice choice = choose_launch(M, N, r, sm_count);
   r.ctas = choice.ctas;
   if (choice.T != 0) r.T = choice.T;
+  // Decode (bf16, M <= 128 on single-CTA MMAs, the CTA grouping and the W
+  // depth left open by the pins): the
+  // token tile narrows to 64 or 128, whichever holds M (the MMA's N extent
+  // changes no bit), and W and X come two K tiles per stage by two 2-D
+  // copies each.  W streams from HBM faster in stages of 256 bytes per row
+  // than of 128 (5.5 against 4.1 TB/s measured for the down_proj pattern),
+  // and the narrower X stages leave the shared memory to them.
+  const bool decode2 = pinned.ctas == 0 && r.ctas == 1 && r.elem == Elem::BF16 && M > 0 && M <= 128 && M <= r.T && r.w_pin == 0 &&
+                       (r.flags & BI_FLAG_KTILE_PAIRS) != 0;
+  if (decode2) r.T = M <= 64 ? 64 : 128;
   plan->bk = tile_elems(r.elem);
   plan->split_k = r.S;
   plan->tok_tile = r.T;
@@ -298,7 +310,7 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   if (plan->x_box_rows > x_rows) plan->x_box_rows = x_rows;
   // a short X box keeps one K tile per copy: each K tile of X must start
   // x_rows rows after the previous one in shared memory
-  plan->kps = plan->x_box_rows == x_rows ? pins_kps(K, r.T, r.ctas, r.flags, r.elem) : 1;
+  plan->kps = decode2 ? 2 : (plan->x_box_rows == x_rows ? pins_kps(K, r.T, r.ctas, r.flags, r.elem) : 1);
   choose_stages(x_rows, plan->x_box_rows, r.w_pin, plan->kps, &plan->w_stages, &plan->x_stages);
   plan->block_threads = kGemmThreads;
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
@@ -441,9 +453,12 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   if (st != BI_OK) return st;
   GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
-  const bool map3d = plan.kps > 1;
-  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, plan.kps, e)) return BI_ERR_CUDA;
-  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, plan.kps, e)) return BI_ERR_CUDA;
+  // two K tiles per copy (3-D maps) on paired MMAs; single-CTA MMAs with two
+  // K tiles per stage take them as two 2-D copies
+  const bool copy2d = plan.kps > 1 && plan.mma_ctas == 1;
+  const bool map3d = plan.kps > 1 && !copy2d;
+  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, map3d ? plan.kps : 1, e)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, map3d ? plan.kps : 1, e)) return BI_ERR_CUDA;
   L.fp8 = e == Elem::E4M3;
   L.sx = sx;
   L.sw = sw;
@@ -469,7 +484,8 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.grid_z = plan.grid_z;
   L.smem = plan.smem_bytes;
   L.flags = r.flags;
-  if (plan.x_box_rows < r.T / plan.mma_ctas) L.flags |= kFlagZeroX;
+  if (plan.x_box_rows < plan.tok_tile / plan.mma_ctas) L.flags |= kFlagZeroX;
+  if (copy2d) L.flags |= kFlagCopy2D;
   if (plan.m_tiles == 1) L.flags |= kFlagStreamW;
   L.stream = stream;
   return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;

@@ -145,10 +145,14 @@ __device__ __forceinline__ void tile_coords(int64_t t, int32_t n_tiles, int32_t 
   }
 }
 
-// KP: K tiles per copy and per ring stage (1, or 2 through 3-D tensor maps).
-// The MMAs consume the K tiles of a stage one after the other, so KP never
-// changes the reduction; it halves the waits and commits per MMA of the
-// issuing thread, which at T = 256 runs close to the tensor pipe's rate.
+// KP: K tiles per ring stage (1 or 2).  With KP = 2 a stage is one copy of a
+// 3-D box (the [K/64][rows][64] view), or, with kFlagCopy2D, two copies of
+// 2-D boxes landing one K tile apart (any K, and X boxes shorter than the
+// stage's rows).  The MMAs consume the K tiles of a stage one after the
+// other, so KP never changes the reduction; it halves the waits and commits
+// per MMA of the issuing thread, which at T = 256 runs close to the tensor
+// pipe's rate, and a W stage then covers 256 contiguous bytes of each of its
+// 128 rows, which HBM serves faster than 128.
 // FP8: E4M3 operands (kind::f8f6f4); a K tile is then 128 values (still 128
 // bytes), and the epilogue scales the fp32 result by sx[m] and then sw[n]
 // before rounding to bf16.
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                           (PAIR ? 2u : 1u);
       const CUtensorMap* map = is_w ? &tmW : &tmX;
       const bool hinted = stream_w;
+      const bool copy2d = (p.flags & kFlagCopy2D) != 0;
       const uint64_t policy = is_w ? policy_evict_first() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -329,6 +334,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tma_load_2d_hint(dst, map, full, kx, row, policy);
                   else
                     tma_load_2d(dst, map, full, kx, row);
+                } else if (copy2d) {
+                  // K tiles kt and kt + 1, one tile of this operand apart
+                  const uint32_t sub = is_w ? (uint32_t)kWStageBytes : (uint32_t)kXTile;
+                  for (int j = 0; j < KP; ++j) {
+                    if (hinted)
+                      tma_load_2d_hint(dst + j * sub, map, full, kx + j * kTileElems, row, policy);
+                    else
+                      tma_load_2d(dst + j * sub, map, full, kx + j * kTileElems, row);
+                  }
                 } else {
                   if (hinted)
                     tma_load_3d_hint(dst, map, full, 0, row, kz, policy);
@@ -760,10 +774,19 @@ static cudaError_t launch_p(const GemmLaunch& L) {
   }
   switch (L.T) {
     case 64:
-      if (L.kps != 1) return cudaErrorInvalidValue;
-      return L.cluster ? launch_t<64, true, PAIR, 1>(L) : launch_t<64, false, PAIR, 1>(L);
     case 128:
+      if (L.kps == 2) {
+        // decode tiles: two K tiles per stage by 2-D copies, single-CTA MMAs
+        if constexpr (PAIR) {
+          return cudaErrorInvalidValue;
+        } else {
+          if (!(L.flags & kFlagCopy2D)) return cudaErrorInvalidValue;
+          if (L.T == 64) return L.cluster ? launch_t<64, true, false, 2>(L) : launch_t<64, false, false, 2>(L);
+          return L.cluster ? launch_t<128, true, false, 2>(L) : launch_t<128, false, false, 2>(L);
+        }
+      }
       if (L.kps != 1) return cudaErrorInvalidValue;
+      if (L.T == 64) return L.cluster ? launch_t<64, true, PAIR, 1>(L) : launch_t<64, false, PAIR, 1>(L);
       return L.cluster ? launch_t<128, true, PAIR, 1>(L) : launch_t<128, false, PAIR, 1>(L);
     case 256:
       if (L.kps == 2)

@@ -211,7 +211,7 @@ def test_open_grouping_follows_m(bd):
     small = bd.bi_gemm_plan_describe(1, 4096, 14336)
     mid = bd.bi_gemm_plan_describe(512, 4096, 14336)
     big = bd.bi_gemm_plan_describe(8192, 4096, 14336)
-    assert (small.mma_ctas, small.kps, small.schedule) == (1, 1, bd.BI_FLAG_SCHEDULE_CLUSTER)
+    assert (small.mma_ctas, small.kps, small.schedule) == (1, 2, bd.BI_FLAG_SCHEDULE_CLUSTER)
     # M=512: 32 pair tiles, each a cluster of 2 pairs running 2 splits each (one wave)
     assert (mid.mma_ctas, mid.schedule, mid.units, mid.cluster_x) == (2, bd.BI_FLAG_SCHEDULE_CHAIN, 2, 4)
     assert mid.grid_x * mid.grid_y * mid.grid_z == 4 * 16 * 2
@@ -253,7 +253,7 @@ def test_split_boundaries_partition_k(bd):
 def test_plan_schedules(bd):
     # decode-sized down_proj runs as clusters of S CTAs; prefill-sized as persistent CTAs
     small = bd.bi_gemm_plan_describe(1, 4096, 14336)
-    assert small.mma_ctas == 1 and small.mma_m == 128 and small.tok_tile == 256
+    assert small.mma_ctas == 1 and small.mma_m == 128 and small.tok_tile == 64 and small.kps == 2
     assert small.schedule == bd.BI_FLAG_SCHEDULE_CLUSTER and small.cluster_x == small.split_k == 4
     assert small.grid_x * small.grid_y * small.grid_z == 32 * 4
     assert small.x_box_rows == 8 and small.w_stages > small.x_stages
@@ -266,6 +266,29 @@ def test_plan_schedules(bd):
     assert pair.kps == 2
     for plan in (small, big, pair):
         assert plan.smem_bytes <= 232448 and plan.block_threads == 32 * 19
+
+
+def test_decode_plan_narrows_the_token_tile(bd):
+    """A single short token tile on single-CTA MMAs, with the grouping and the
+    W depth left open, runs at T = 64 (M <= 64) or 128 (M <= 128) with two K
+    tiles per stage; the tree stays the pinned one."""
+    for N, K in TABLE_SHAPES:
+        ref = bd.bi_gemm_plan_describe(4096, N, K).tree()
+        for M, T in ((1, 64), (8, 64), (33, 64), (64, 64), (65, 128), (128, 128)):
+            plan = bd.bi_gemm_plan_describe(M, N, K)
+            if plan.mma_ctas != 1:
+                continue
+            assert (plan.tok_tile, plan.mma_n, plan.kps, plan.m_tiles) == (T, T, 2, 1), (N, K, M)
+            assert plan.x_stages >= 2 and plan.w_stages >= 4 and plan.smem_bytes <= 232448
+            assert plan.tree() == ref
+    pins = bd.bi_pins_default(4096, 14336)
+    # pinned grouping, pinned W depth, or no two-tile flag: the pinned tile and one tile per stage
+    for p in (pins.replace(mma_ctas=1), pins.replace(stages=4),
+              pins.replace(flags=pins.flags & ~bd.BI_FLAG_KTILE_PAIRS)):
+        plan = bd.bi_gemm_plan_describe(1, 4096, 14336, p)
+        assert (plan.tok_tile, plan.kps) == (256, 1)
+    # above 128 tokens the tile is the pinned one
+    assert bd.bi_gemm_plan_describe(129, 4096, 14336).tok_tile == 256
 
 
 def test_plan_ktile_pairs(bd):
