@@ -766,7 +766,17 @@ static cudaError_t launch_t(const GemmLaunch& L) {
 
 template <bool PAIR>
 static cudaError_t launch_p(const GemmLaunch& L) {
-  if (L.fp8) {  // E4M3 operands: T = 256 only
+  if (L.fp8) {  // E4M3 operands: T = 256, or a decode tile of 64 or 128
+    if (L.T == 64 || L.T == 128) {
+      if constexpr (PAIR) {
+        return cudaErrorInvalidValue;
+      } else {
+        if (L.kps != 2 || !(L.flags & kFlagCopy2D)) return cudaErrorInvalidValue;
+        if (L.T == 64)
+          return L.cluster ? launch_t<64, true, false, 2, true>(L) : launch_t<64, false, false, 2, true>(L);
+        return L.cluster ? launch_t<128, true, false, 2, true>(L) : launch_t<128, false, false, 2, true>(L);
+      }
+    }
     if (L.T != 256) return cudaErrorInvalidValue;
     if (L.kps == 2)
       return L.cluster ? launch_t<256, true, PAIR, 2, true>(L) : launch_t<256, false, PAIR, 2, true>(L);

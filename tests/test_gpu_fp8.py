@@ -113,5 +113,8 @@ def test_fp8_rows_independent_of_batch(lib):
     full = layer(X)
     for r in (0, 517, 999):
         assert np.array_equal(layer(X[r:r + 1].contiguous())[0], full[r])
+    # batches on either side of the decode tiles (64 and 128 tokens)
+    for m in (8, 64, 65, 128, 129):
+        assert np.array_equal(layer(X[:m].contiguous()), full[:m]), m
     perm = torch.randperm(1000, generator=torch.Generator().manual_seed(8))
     assert np.array_equal(layer(X[perm.cuda()].contiguous()), full[perm.numpy()])
