@@ -25,6 +25,8 @@
 // Deterministic LLM Inference), Sec. IV: per-token log-probabilities are
 // what batch invariance is judged on; a row never leaves its cluster, so
 // neither M nor the other rows reach its tree.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -73,17 +75,25 @@ struct LsmShared {
 // (V up to kLsmCache * 8 * kLsmStride = 131072 is read once).
 constexpr int kLsmCache = 4;
 
+// NaN-propagating maxima (exact in any order): a row holding a NaN or a +Inf
+// shows it in its maximum, so no separate test of the elements is needed.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
 __device__ __forceinline__ float max8(const uint4& v) {
-  return fmaxf(fmaxf(fmaxf(lsm_lo(v.x), lsm_hi(v.x)), fmaxf(lsm_lo(v.y), lsm_hi(v.y))),
-               fmaxf(fmaxf(lsm_lo(v.z), lsm_hi(v.z)), fmaxf(lsm_lo(v.w), lsm_hi(v.w))));
+  const uint32_t w = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+  return fmax_nan(lsm_lo(w), lsm_hi(w));
 }
-
-__device__ __forceinline__ bool bad8(const uint4& v) {
-  // NaN or +Inf anywhere (-Inf is an ordinary logit)
-  return !(lsm_lo(v.x) < INFINITY) || !(lsm_hi(v.x) < INFINITY) || !(lsm_lo(v.y) < INFINITY) ||
-         !(lsm_hi(v.y) < INFINITY) || !(lsm_lo(v.z) < INFINITY) || !(lsm_hi(v.z) < INFINITY) ||
-         !(lsm_lo(v.w) < INFINITY) || !(lsm_hi(v.w) < INFINITY);
-}
+// a maximum from max8 / fmax_nan that marks the row undefined (NaN or +Inf;
+// -Inf is an ordinary logit)
+__device__ __forceinline__ bool bad_max(float m) { return !(m < INFINITY) && m != -INFINITY; }
 
 // exp(d) for d = x - m <= 0 as 2^(d * log2(e)) by the ex2.approx
 // instruction: the product rounds once (relative error |d| 2^-24 in the
@@ -123,15 +133,11 @@ __device__ float row_lse(const uint4* x, int64_t nvec, LsmShared& sh, uint4 (&v)
     const int64_t k = g0 + (int64_t)i * kLsmStride;
     if (k < nvec) {
       v[i] = x[k];
-      m = fmaxf(m, max8(v[i]));
-      bad = bad || bad8(v[i]);
+      m = fmax_nan(m, max8(v[i]));
     }
   }
-  for (int64_t k = g0 + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) {
-    const uint4 w = x[k];
-    m = fmaxf(m, max8(w));
-    bad = bad || bad8(w);
-  }
+  for (int64_t k = g0 + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) m = fmax_nan(m, max8(x[k]));
+  bad = bad_max(m);
   if (m != -INFINITY) {
 #pragma unroll
     for (int i = 0; i < kLsmCache; ++i) {
@@ -225,70 +231,105 @@ __global__ void __launch_bounds__(kLsmThreads)
 }
 
 // ---------------------------------------------------------------------------
-// The same tree on one CTA per row, for many rows
+// The same tree on a pair of CTAs per row, for many rows
 // ---------------------------------------------------------------------------
-// A cluster spreads a row over kLsmCtas SMs, which keeps a single row fast;
-// with many rows the cluster barriers and the waves of 8-CTA clusters cost
-// more than they save.  This variant runs the identical arithmetic on one CTA
-// of kLsmCtaThreads threads: thread t plays the cluster's threads t + 1024 j
-// (j < kLsmVirt), whose lanes and warps are its own lane and warp (mod 16),
-// and every butterfly combines the same pairs in the same order.  Both
-// variants give the same bits for every row; which one runs is speed only.
-constexpr int kLsmCtaThreads = 1024;
-constexpr int kLsmVirt = kLsmCtas * kLsmThreads / kLsmCtaThreads;  // cluster threads per thread
+// A cluster of kLsmCtas CTAs per row keeps a single row fast; with many rows
+// its barriers and waves cost more than they save.  This variant runs the
+// identical arithmetic on a cluster of two CTAs of kLsmCtaThreads threads:
+// thread t of rank r plays the cluster threads g = r * kLsmHalf + t +
+// kLsmCtaThreads j (j < kLsmVirt), whose lanes and warps are its own, and
+// every butterfly combines the same pairs in the same order (the last one
+// reads the other CTA's four results through distributed shared memory).
+// Both variants give the same bits for every row; which one runs is speed
+// only.
+//
+// The half row is read from HBM once and kept on chip: cluster thread g's
+// vectors g + kLsmStride i for i < 3 in shared memory (96 KB, staged by
+// 16-byte asynchronous copies) and its vector i = 3 in a register.  Rows
+// longer than kLsmCache * 8 * kLsmStride logits read their further vectors
+// from global memory in each pass.  Two CTAs share an SM, so one's loads
+// overlap the other's arithmetic and stores.
+constexpr int kLsmCtaThreads = 512;
+constexpr int kLsmHalf = kLsmCtas * kLsmThreads / 2;                 // cluster threads per CTA
+constexpr int kLsmVirt = kLsmHalf / kLsmCtaThreads;                   // cluster threads per thread
+constexpr int kLsmSmemVec = (kLsmCache - 1) * kLsmHalf;              // vectors i < 3 of the CTA's threads
+constexpr int kLsmSmemBytes = kLsmSmemVec * 16;
+static_assert(kLsmVirt * 2 == kLsmCtas && kLsmThreads == kLsmCtaThreads, "rank j of the cluster is played as 4r + j");
 #ifndef BI_LSM_CTA_MIN_ROWS
 #define BI_LSM_CTA_MIN_ROWS 64
 #endif
 
-struct LsmCtaShared {
-  float m[kLsmCtas][kLsmWarps], s[kLsmCtas][kLsmWarps];
-  int bad[kLsmCtas][kLsmWarps];
-  float cm[kLsmCtas], cs[kLsmCtas];
-  int cb[kLsmCtas];
+struct LsmPairShared {
+  float m[kLsmVirt][kLsmWarps], s[kLsmVirt][kLsmWarps];
+  int bad[kLsmVirt][kLsmWarps];
+  float cm[kLsmVirt], cs[kLsmVirt], cb[kLsmVirt];  // cb: 1.0f if that cluster CTA saw a NaN or +Inf
   float lse;
 };
 
-__device__ float row_lse_cta(const uint4* x, int64_t nvec, LsmCtaShared& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll 1
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Vector i of this CTA's cluster thread h (row vector k = g + kLsmStride i):
+// shared memory, the register r, or global memory.
+__device__ __forceinline__ uint4 lsm_vec(const uint4* __restrict__ x, const uint4* row_s, const uint4& r, int h,
+                                         int64_t g, int i) {
+  if (i < kLsmCache - 1) return row_s[i * kLsmHalf + h];
+  if (i == kLsmCache - 1) return r;
+  return __ldg(x + g + (int64_t)i * kLsmStride);
+}
+
+template <bool FULL>
+__global__ void __launch_bounds__(kLsmCtaThreads, 2)
+    lsm_rows_kernel(const uint4* __restrict__ X, float4* __restrict__ Y, const int32_t* ids, float* out,
+                    int64_t nvec) {
+  extern __shared__ __align__(16) uint4 lsm_row[];
+  __shared__ LsmPairShared sh;
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // the logits may come from the previous kernel in the stream
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = blockIdx.x >> 1;
+  const uint4* x = X + row * nvec;
+  const int64_t g0 = (int64_t)rank * kLsmHalf;  // this CTA's first cluster thread
+  // stage vectors i < 3 (shared memory) and i = 3 (registers)
+#pragma unroll
+  for (int i = 0; i < kLsmCache - 1; ++i)
+#pragma unroll
+    for (int j = 0; j < kLsmVirt; ++j) {
+      const int h = t + j * kLsmCtaThreads;
+      const int64_t k = g0 + h + (int64_t)i * kLsmStride;
+      if (k < nvec) cp_async16(smem_u32(lsm_row + i * kLsmHalf + h), x + k);
+    }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  uint4 r[kLsmVirt];
+#pragma unroll
   for (int j = 0; j < kLsmVirt; ++j) {
-    const int g = tid + j * kLsmCtaThreads;   // the cluster thread played
-    const int vr = g / kLsmThreads;           // its CTA rank
-    const int vw = (g % kLsmThreads) >> 5;    // its warp
-    uint4 v[kLsmCache];
+    const int64_t k = g0 + t + j * kLsmCtaThreads + (int64_t)(kLsmCache - 1) * kLsmStride;
+    r[j] = k < nvec ? __ldg(x + k) : make_uint4(0, 0, 0, 0);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  const int64_t per = (nvec + kLsmStride - 1) / kLsmStride;  // vectors of cluster thread 0
+#pragma unroll
+  for (int j = 0; j < kLsmVirt; ++j) {
+    const int h = t + j * kLsmCtaThreads;
+    const int64_t g = g0 + h;
+    const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
     float m = -INFINITY, s = 0.0f;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < kLsmCache; ++i) {
-      const int64_t k = g + (int64_t)i * kLsmStride;
-      if (k < nvec) {
-        v[i] = x[k];
-        m = fmaxf(m, max8(v[i]));
-        bad = bad || bad8(v[i]);
-      }
-    }
-    for (int64_t k = g + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) {
-      const uint4 w = x[k];
-      m = fmaxf(m, max8(w));
-      bad = bad || bad8(w);
-    }
-    if (m != -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < kLsmCache; ++i) {
-        const int64_t k = g + (int64_t)i * kLsmStride;
-        if (k < nvec) s = sumexp8(v[i], m, s);
-      }
-      for (int64_t k = g + (int64_t)kLsmCache * kLsmStride; k < nvec; k += kLsmStride) s = sumexp8(x[k], m, s);
-    }
+    for (int i = 0; i < nv; ++i) m = fmax_nan(m, max8(lsm_vec(x, lsm_row, r[j], h, g, i)));
+    bool bad = bad_max(m);
+    if (m != -INFINITY)
+      for (int i = 0; i < nv; ++i) s = sumexp8(lsm_vec(x, lsm_row, r[j], h, g, i), m, s);
     ms_butterfly(m, s, bad);
-    if (lane == 0) {
-      sh.m[vr][vw] = m;
-      sh.s[vr][vw] = s;
-      sh.bad[vr][vw] = bad;
+    if (lane == 0) {  // cluster CTA 4 rank + j, warp `warp`
+      sh.m[j][warp] = m;
+      sh.s[j][warp] = s;
+      sh.bad[j][warp] = bad;
     }
   }
   __syncthreads();
-  if (warp < kLsmCtas) {  // warp r plays warp 0 of cluster CTA r
+  if (warp < kLsmVirt) {  // warp j plays warp 0 of cluster CTA 4 rank + j
     float m = lane < kLsmWarps ? sh.m[warp][lane] : -INFINITY;
     float s = lane < kLsmWarps ? sh.s[warp][lane] : 0.0f;
     bool bad = lane < kLsmWarps ? sh.bad[warp][lane] != 0 : false;
@@ -296,51 +337,82 @@ __device__ float row_lse_cta(const uint4* x, int64_t nvec, LsmCtaShared& sh) {
     if (lane == 0) {
       sh.cm[warp] = m;
       sh.cs[warp] = s;
-      sh.cb[warp] = bad;
+      sh.cb[warp] = bad ? 1.0f : 0.0f;
     }
   }
-  __syncthreads();
-  if (warp == 0) {  // warp 0 of cluster CTA 0
-    float m = lane < kLsmCtas ? sh.cm[lane] : -INFINITY;
-    float s = lane < kLsmCtas ? sh.cs[lane] : 0.0f;
-    bool bad = lane < kLsmCtas ? sh.cb[lane] != 0 : false;
+  cluster_sync();  // both CTAs' results are in their shared memory
+  if (rank == 0 && warp == 0) {  // warp 0 of cluster CTA 0
+    float m = -INFINITY, s = 0.0f;
+    bool bad = false;
+    if (lane < kLsmCtas) {
+      const uint32_t src = (uint32_t)(lane / kLsmVirt), w = (uint32_t)(lane % kLsmVirt);
+      m = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cm[w]), src));
+      s = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cs[w]), src));
+      bad = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cb[w]), src)) != 0.0f;
+    }
     ms_butterfly(m, s, bad);
     if (lane == 0) sh.lse = (bad || m == -INFINITY) ? __int_as_float(0x7fc00000) : m + logf(s);
   }
-  __syncthreads();
-  return sh.lse;
-}
-
-__global__ void __launch_bounds__(kLsmCtaThreads)
-    log_softmax_cta_kernel(const uint4* X, float4* Y, int64_t nvec) {
-  __shared__ LsmCtaShared sh;
-  grid_dep_launch_dependents();
-  grid_dep_wait();
-  const int64_t row = blockIdx.x;
-  const uint4* x = X + row * nvec;
-  const float lse = row_lse_cta(x, nvec, sh);
-  float4* y = Y + row * nvec * 2;
-  for (int64_t k = threadIdx.x; k < nvec; k += kLsmCtaThreads) write_out(y, k, x[k], lse);
-}
-
-__global__ void __launch_bounds__(kLsmCtaThreads)
-    token_logprobs_cta_kernel(const uint4* X, const int32_t* ids, float* out, int64_t nvec) {
-  __shared__ LsmCtaShared sh;
-  grid_dep_launch_dependents();
-  grid_dep_wait();
-  const int64_t row = blockIdx.x;
-  const uint4* x = X + row * nvec;
-  const float lse = row_lse_cta(x, nvec, sh);
-  if (threadIdx.x == 0) {
+  cluster_sync();  // rank 0 has the lse
+  const float lse = ld_dsmem_f32(mapa_shared(smem_u32(&sh.lse), 0u));
+  cluster_sync();  // nobody leaves while its shared memory may still be read
+  if constexpr (FULL) {
+    float4* y = Y + row * nvec * 2;
+#pragma unroll
+    for (int j = 0; j < kLsmVirt; ++j) {
+      const int h = t + j * kLsmCtaThreads;
+      const int64_t g = g0 + h;
+      const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
+      for (int i = 0; i < nv; ++i) {
+        const uint4 v = lsm_vec(x, lsm_row, r[j], h, g, i);
+        const int64_t k = g + (int64_t)i * kLsmStride;
+        __stcs(y + 2 * k, make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse));
+        __stcs(y + 2 * k + 1,
+               make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse));
+      }
+    }
+  } else if (rank == 0 && t == 0) {
     const int32_t id = ids[row];
     const int64_t V = nvec * 8;
-    float r = __int_as_float(0x7fc00000);
+    float res = __int_as_float(0x7fc00000);
     if (id >= 0 && id < V) {
       const uint16_t b = reinterpret_cast<const uint16_t*>(x)[id];
-      r = __uint_as_float((uint32_t)b << 16) - lse;
+      res = __uint_as_float((uint32_t)b << 16) - lse;
     }
-    out[row] = r;
+    out[row] = res;
   }
+}
+
+template <bool FULL>
+static cudaError_t launch_lsm_rows(const void* X, void* Y, const int32_t* ids, float* out, int64_t M, int64_t V,
+                                   cudaStream_t stream) {
+  // the shared-memory limit is per device: set it once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(lsm_rows_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLsmSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * M));
+  cfg.blockDim = dim3(kLsmCtaThreads);
+  cfg.dynamicSmemBytes = kLsmSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, lsm_rows_kernel<FULL>, static_cast<const uint4*>(X), static_cast<float4*>(Y), ids,
+                            out, V / 8);
 }
 
 template <typename... KArgs, typename... Args>
@@ -362,9 +434,8 @@ static cudaError_t launch_rows(void (*kern)(KArgs...), int64_t M, cudaStream_t s
 }
 
 cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cudaStream_t stream) {
-  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll)
-    return launch_overlapped(log_softmax_cta_kernel, dim3((unsigned)M), dim3(kLsmCtaThreads), stream,
-                             static_cast<const uint4*>(X), static_cast<float4*>(Y), V / 8);
+  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll / 2)
+    return launch_lsm_rows<true>(X, Y, nullptr, nullptr, M, V, stream);
   if (M > 0x7FFFFFFFll / kLsmCtas) return cudaErrorInvalidValue;
   return launch_rows(log_softmax_kernel, M, stream, static_cast<const uint4*>(X), static_cast<float4*>(Y),
                      V / 8);
@@ -372,9 +443,8 @@ cudaError_t launch_log_softmax(const void* X, void* Y, int64_t M, int64_t V, cud
 
 cudaError_t launch_token_logprobs(const void* X, const int32_t* ids, float* out, int64_t M, int64_t V,
                                   cudaStream_t stream) {
-  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll)
-    return launch_overlapped(token_logprobs_cta_kernel, dim3((unsigned)M), dim3(kLsmCtaThreads), stream,
-                             static_cast<const uint4*>(X), ids, out, V / 8);
+  if (M >= BI_LSM_CTA_MIN_ROWS && M <= 0x7FFFFFFFll / 2)
+    return launch_lsm_rows<false>(X, nullptr, ids, out, M, V, stream);
   if (M > 0x7FFFFFFFll / kLsmCtas) return cudaErrorInvalidValue;
   return launch_rows(token_logprobs_kernel, M, stream, static_cast<const uint4*>(X), ids, out, V / 8);
 }
