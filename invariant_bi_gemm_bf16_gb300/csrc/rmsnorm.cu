@@ -22,6 +22,12 @@
 namespace bi {
 
 constexpr int kRmsWarps = 8;
+constexpr int64_t kRmsSmCount = 152;  // spreads small batches; any value gives the same bits
+#ifndef BI_RMS_WIDE_MIN_ROWS_4096
+#define BI_RMS_WIDE_MIN_ROWS_4096 4096  // H = 4096: registers below, two passes from here
+#endif
+constexpr int kRmsSmemWarps = 2;                                 // rows per block of the shared-memory kernel
+constexpr int64_t kRmsSmemMinRows = kRmsWarps * kRmsSmCount;     // H = 8192: from full blocks on every SM
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   grid_dep_launch_dependents();
   grid_dep_wait();  // X may come from the previous kernel in the stream
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
   constexpr int kVecs = VPL * 32;
   const uint4* x = X + row * kVecs;
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   grid_dep_wait();
   constexpr int kVecs = VPL * 32;
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
   const uint4* x = X + row * kVecs;
   float ss = 0.0f;
@@ -128,6 +134,40 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   }
 }
 
+// H = 256 * VPL: each warp stages its row in shared memory (VPL * 512 bytes)
+// by 16-byte asynchronous copies, then runs the arithmetic of
+// rmsnorm_regs_kernel vector for vector from there.  Few registers and small
+// blocks, so more rows per SM are in flight than with the row in registers.
+template <int VPL>
+__global__ void __launch_bounds__(32 * kRmsSmemWarps)
+    rmsnorm_smem_kernel(const uint4* X, const uint4* __restrict__ g, uint4* Y, int64_t M, float eps) {
+  extern __shared__ __align__(16) uint4 rms_rows[];
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  constexpr int kVecs = VPL * 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * kRmsSmemWarps + warp;
+  if (row >= M) return;
+  const uint4* x = X + row * kVecs;
+  uint4* buf = rms_rows + warp * kVecs;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + lane + 32 * i)),
+                 "l"(x + lane + 32 * i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  // each lane reads back only the vectors it copied
+  float ss = 0.0f;
+#pragma unroll 8
+  for (int i = 0; i < VPL; ++i) ss = sumsq8(buf[lane + 32 * i], ss);
+  ss = butterfly_sum(ss);
+  const float r = inv_rms(ss, (int64_t)kVecs * 8, eps);
+  uint4* y = Y + row * kVecs;
+#pragma unroll 8
+  for (int i = 0; i < VPL; ++i) __stcs(y + lane + 32 * i, norm8(buf[lane + 32 * i], __ldg(g + lane + 32 * i), r));
+}
+
 // Any H with H % 8 == 0: the same lane partition and order, two passes over
 // the row (the second pass re-reads it, typically from L1/L2).
 __global__ void __launch_bounds__(32 * kRmsWarps)
@@ -136,7 +176,7 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   grid_dep_launch_dependents();
   grid_dep_wait();
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kRmsWarps + (threadIdx.x >> 5);
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
   const int64_t nvec = H / 8;
   const uint4* x = X + row * nvec;
@@ -148,15 +188,22 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   for (int64_t i = lane; i < nvec; i += 32) y[i] = norm8(x[i], __ldg(g + i), r);
 }
 
-// Kernel per width, measured on GB300 (M = 16384, fraction of the copy
-// bandwidth): registers for H <= 2048 (2048: 1.00) and 8192 (0.83), two
-// passes for 4096 (0.90) and 16384.  All run the same lane partition and
-// order, so the choice never changes a bit.
+// Kernel per width and batch size, measured on GB300 as fractions of the
+// copy bandwidth at M = 16384: registers for H <= 2048 (2048: 1.00); for
+// H = 4096 two passes from M = 4096 (0.89) and registers below (2.3 us at
+// M <= 64, 1.2-1.7x F.rms_norm up to M = 512); for H = 8192 the row in
+// shared memory from full blocks on every SM, registers below; two passes for
+// 16384.  All run the same lane partition and order, so the choice never
+// changes a bit.
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
                            cudaStream_t stream) {
-  const int64_t blocks = (M + kRmsWarps - 1) / kRmsWarps;
+  // rows (warps) per block: ceil(M / SMs) up to kRmsWarps, so a small batch
+  // puts at most one block, of as few rows as possible, on each SM
+  int64_t wpb = (M + kRmsSmCount - 1) / kRmsSmCount;
+  wpb = wpb < 1 ? 1 : (wpb > kRmsWarps ? kRmsWarps : wpb);
+  const int64_t blocks = (M + wpb - 1) / wpb;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)blocks), block(32 * kRmsWarps);
+  const dim3 grid((unsigned)blocks), block((unsigned)(32 * wpb));
   auto x = static_cast<const uint4*>(X);
   auto gg = static_cast<const uint4*>(g);
   auto y = static_cast<uint4*>(Y);
@@ -165,8 +212,18 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
     case 512: return launch_overlapped(rmsnorm_regs_kernel<2>, grid, block, stream, x, gg, y, M, eps);
     case 1024: return launch_overlapped(rmsnorm_regs_kernel<4>, grid, block, stream, x, gg, y, M, eps);
     case 2048: return launch_overlapped(rmsnorm_regs_kernel<8>, grid, block, stream, x, gg, y, M, eps);
-    case 4096: return launch_overlapped(rmsnorm_wide_kernel<16>, grid, block, stream, x, gg, y, M, eps);
-    case 8192: return launch_overlapped(rmsnorm_regs_kernel<32>, grid, block, stream, x, gg, y, M, eps);
+    case 4096:
+      if (M < BI_RMS_WIDE_MIN_ROWS_4096)
+        return launch_overlapped(rmsnorm_regs_kernel<16>, grid, block, stream, x, gg, y, M, eps);
+      return launch_overlapped(rmsnorm_wide_kernel<16>, grid, block, stream, x, gg, y, M, eps);
+    case 8192:
+      if (M >= kRmsSmemMinRows) {
+        const int64_t b2 = (M + kRmsSmemWarps - 1) / kRmsSmemWarps;
+        if (b2 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        return launch_overlapped_smem(rmsnorm_smem_kernel<32>, dim3((unsigned)b2), dim3(32 * kRmsSmemWarps),
+                                      (size_t)kRmsSmemWarps * 32 * 512, stream, x, gg, y, M, eps);
+      }
+      return launch_overlapped(rmsnorm_regs_kernel<32>, grid, block, stream, x, gg, y, M, eps);
     case 16384: return launch_overlapped(rmsnorm_wide_kernel<64>, grid, block, stream, x, gg, y, M, eps);
     default: return launch_overlapped(rmsnorm_loop_kernel, grid, block, stream, x, gg, y, M, H, eps);
   }

@@ -43,18 +43,32 @@ def test_rmsnorm_in_place(lib, oracle, M, H):
     check_ulp(bf16_bits(x), want, 1, "in place")
 
 
-@pytest.mark.parametrize("H", [2048, 8192])
-def test_rmsnorm_rows_independent_of_batch(lib, H):
-    """A row's bits are the same alone, in a batch of 3000 and at another position."""
-    X = inputs.rows_loguniform(3000, H, seed=3, stream=0).cuda()
+@pytest.mark.parametrize("H,M", [(2048, 3000), (4096, 5000), (8192, 3000)])
+def test_rmsnorm_rows_independent_of_batch(lib, H, M):
+    """A row's bits are the same alone, in a batch of M and at another position.
+    The batch and the single row run different kernels at H = 4096 (two passes
+    against registers) and H = 8192 (shared memory against registers)."""
+    X = inputs.rows_loguniform(M, H, seed=3, stream=0).cuda()
     g = inputs.normal((H,), std=0.1, mean=1.0, seed=3, stream=2).cuda()
     full = bf16_bits(lib.bi_rmsnorm_bf16(X, g, EPS))
-    for r in (0, 1234, 2999):
+    for r in (0, 1234, M - 1):
         alone = bf16_bits(lib.bi_rmsnorm_bf16(X[r:r + 1].contiguous(), g, EPS))
         assert np.array_equal(alone[0], full[r])
-    perm = torch.randperm(3000, generator=torch.Generator().manual_seed(5))
+    for m in (37, 1215, 1216, 4095):  # the block-size and kernel switches
+        assert np.array_equal(bf16_bits(lib.bi_rmsnorm_bf16(X[:m].contiguous(), g, EPS)), full[:m]), m
+    perm = torch.randperm(M, generator=torch.Generator().manual_seed(5))
     shuffled = bf16_bits(lib.bi_rmsnorm_bf16(X[perm.cuda()].contiguous(), g, EPS))
     assert np.array_equal(shuffled, full[perm.numpy()])
+
+
+@pytest.mark.parametrize("M,H", [(4100, 4096), (1300, 8192)])
+def test_rmsnorm_parity_large_batches(lib, oracle, M, H):
+    """The kernels of large batches (two passes at H = 4096, the row in shared
+    memory at H = 8192) against the oracle."""
+    X = inputs.rows_loguniform(M, H, seed=4, stream=0)
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=4, stream=2)
+    want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
+    check_ulp(bf16_bits(lib.bi_rmsnorm_bf16(X.cuda(), g.cuda(), EPS)), want, 1, "rmsnorm M=%d H=%d" % (M, H))
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 384, 4096), (33, 256, 512), (130, 640, 256)])
