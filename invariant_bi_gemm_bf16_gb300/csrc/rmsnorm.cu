@@ -23,11 +23,8 @@ namespace bi {
 
 constexpr int kRmsWarps = 8;
 constexpr int64_t kRmsSmCount = 152;  // spreads small batches; any value gives the same bits
-#ifndef BI_RMS_WIDE_MIN_ROWS_4096
-#define BI_RMS_WIDE_MIN_ROWS_4096 4096  // H = 4096: registers below, two passes from here
-#endif
 constexpr int kRmsSmemWarps = 2;                                 // rows per block of the shared-memory kernel
-constexpr int64_t kRmsSmemMinRows = kRmsWarps * kRmsSmCount;     // H = 8192: from full blocks on every SM
+constexpr int64_t kRmsSmemMinRows = kRmsWarps * kRmsSmCount;     // H = 4096, 8192: from full blocks on every SM
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -190,11 +187,10 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
 
 // Kernel per width and batch size, measured on GB300 as fractions of the
 // copy bandwidth at M = 16384: registers for H <= 2048 (2048: 1.00); for
-// H = 4096 two passes from M = 4096 (0.89) and registers below (2.3 us at
-// M <= 64, 1.2-1.7x F.rms_norm up to M = 512); for H = 8192 the row in
-// shared memory from full blocks on every SM, registers below; two passes for
-// 16384.  All run the same lane partition and order, so the choice never
-// changes a bit.
+// H = 4096 and 8192 the row in shared memory from full blocks on every SM
+// (0.94 and 0.96; two passes gave 0.89 and 0.79) and registers below (2.3 us
+// at M <= 64 for H = 4096, 1.1-1.8x F.rms_norm); two passes for 16384.  All
+// run the same lane partition and order, so the choice never changes a bit.
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
                            cudaStream_t stream) {
   // rows (warps) per block: ceil(M / SMs) up to kRmsWarps, so a small batch
@@ -213,9 +209,13 @@ cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int
     case 1024: return launch_overlapped(rmsnorm_regs_kernel<4>, grid, block, stream, x, gg, y, M, eps);
     case 2048: return launch_overlapped(rmsnorm_regs_kernel<8>, grid, block, stream, x, gg, y, M, eps);
     case 4096:
-      if (M < BI_RMS_WIDE_MIN_ROWS_4096)
-        return launch_overlapped(rmsnorm_regs_kernel<16>, grid, block, stream, x, gg, y, M, eps);
-      return launch_overlapped(rmsnorm_wide_kernel<16>, grid, block, stream, x, gg, y, M, eps);
+      if (M >= kRmsSmemMinRows) {
+        const int64_t b2 = (M + kRmsSmemWarps - 1) / kRmsSmemWarps;
+        if (b2 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        return launch_overlapped_smem(rmsnorm_smem_kernel<16>, dim3((unsigned)b2), dim3(32 * kRmsSmemWarps),
+                                      (size_t)kRmsSmemWarps * 16 * 512, stream, x, gg, y, M, eps);
+      }
+      return launch_overlapped(rmsnorm_regs_kernel<16>, grid, block, stream, x, gg, y, M, eps);
     case 8192:
       if (M >= kRmsSmemMinRows) {
         const int64_t b2 = (M + kRmsSmemWarps - 1) / kRmsSmemWarps;

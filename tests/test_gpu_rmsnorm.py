@@ -46,8 +46,8 @@ def test_rmsnorm_in_place(lib, oracle, M, H):
 @pytest.mark.parametrize("H,M", [(2048, 3000), (4096, 5000), (8192, 3000)])
 def test_rmsnorm_rows_independent_of_batch(lib, H, M):
     """A row's bits are the same alone, in a batch of M and at another position.
-    The batch and the single row run different kernels at H = 4096 (two passes
-    against registers) and H = 8192 (shared memory against registers)."""
+    The batch and the single row run different kernels at H = 4096 and 8192
+    (the row in shared memory against registers)."""
     X = inputs.rows_loguniform(M, H, seed=3, stream=0).cuda()
     g = inputs.normal((H,), std=0.1, mean=1.0, seed=3, stream=2).cuda()
     full = bf16_bits(lib.bi_rmsnorm_bf16(X, g, EPS))
@@ -63,8 +63,8 @@ def test_rmsnorm_rows_independent_of_batch(lib, H, M):
 
 @pytest.mark.parametrize("M,H", [(4100, 4096), (1300, 8192)])
 def test_rmsnorm_parity_large_batches(lib, oracle, M, H):
-    """The kernels of large batches (two passes at H = 4096, the row in shared
-    memory at H = 8192) against the oracle."""
+    """The kernel of large batches (the row in shared memory) against the
+    oracle."""
     X = inputs.rows_loguniform(M, H, seed=4, stream=0)
     g = inputs.normal((H,), std=0.1, mean=1.0, seed=4, stream=2)
     want = oracle.rmsnorm(inputs.bits(X), inputs.bits(g), EPS)
