@@ -52,8 +52,8 @@ EPS = 1e-5
 # (summaries in profiles/), keyed by build_fingerprint() of the GEMM kernel's
 # sources: valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "085be14a53b0c07c55556b32e4b4d7b599242b80491c0773de9867f5f0de20b5": {8192: 965144320 + 63613184,
-                                                                        1: 117512704 + 2776320},
+    "f7bf86b71357c45995abf076d048fc0408fc349e71b191afc8cf003c605012b4": {8192: 965384960 + 63719424,
+                                                                        1: 117513472 + 2791168},
 }
 
 
@@ -977,6 +977,25 @@ def run_single_rmsnorm(args, dist):
     torch.cuda.synchronize()
 
 
+def run_single_logsoftmax(args, dist):
+    """Launches the full log-softmax and the token log-probabilities on M rows
+    of Llama-3.1-8B logits (V = 128256), --launches times each on rotating
+    inputs, for an ncu capture of those launches."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    M, V = int(args.single_logsoftmax), 128256
+    n = copies_for(M * V * 2, cap=8)
+    xs = [inputs.device_normal((M, V), std=3.0, seed=dist.rank, stream=70 + i, device=dev) for i in range(n)]
+    ids = torch.arange(M, dtype=torch.int32, device=dev) * 97 % V
+    y = torch.empty((M, V), dtype=torch.float32, device=dev)
+    for i in range(args.launches):
+        bd.bi_log_softmax_bf16(xs[i % n], out=y)
+        bd.bi_token_logprobs_bf16(xs[i % n], ids)
+    torch.cuda.synchronize()
+
+
 def run_reference(args, dist):
     """The reference arm: the CPU oracle on a bounded sample of the same workload."""
     if dist.rank != 0:
@@ -1021,6 +1040,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--single-logsoftmax", default="",
+                    help="M: only launch the log-softmax kernels on M rows of V = 128256 logits (for ncu)")
     ap.add_argument("--single-rmsnorm", default="",
                     help="H:M -- only launch RMSNorm on that shape (for ncu)")
     ap.add_argument("--single-attention", default="",
@@ -1035,6 +1056,9 @@ def main():
     try:
         if args.single_attention:
             run_single_attention(args, dist)
+            return
+        if args.single_logsoftmax:
+            run_single_logsoftmax(args, dist)
             return
         if args.single_rmsnorm:
             run_single_rmsnorm(args, dist)
