@@ -11,6 +11,8 @@
 // Serving and RL Rollouts at Near-Stock Speed), Limits: dynamic per-tensor FP8
 // activation scales span the batch; per-token scales keep each row's bits its
 // own.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -134,6 +136,81 @@ __global__ void __launch_bounds__(kQRowThreads)
   }
 }
 
+// The same arithmetic with the row staged in shared memory (16-byte
+// asynchronous copies; each thread reads back only the vectors it copied), so
+// few registers are held and more rows per SM are in flight than with the
+// row in registers.  For rows of up to kQSmemMaxVec vectors.
+constexpr int kQSmemMaxVec = 6144;  // 96 KB
+__global__ void __launch_bounds__(kQRowThreads)
+    quantize_e4m3_smem_kernel(const uint4* X, uint2* Q, float* scale, int64_t K) {
+  extern __shared__ __align__(16) uint4 qrow[];
+  __shared__ float wmax[kQRowThreads / 32];
+  __shared__ int wbad[kQRowThreads / 32];
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int64_t row = blockIdx.x;
+  const int nvec = (int)(K / 8);
+  const uint4* x = X + row * nvec;
+  for (int j = threadIdx.x; j < nvec; j += kQRowThreads)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(qrow + j)), "l"(x + j) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  float amax = 0.0f;
+  bool bad = false;
+  for (int j = threadIdx.x; j < nvec; j += kQRowThreads) {
+    const uint4 v = qrow[j];
+    amax2(v.x, amax, bad);
+    amax2(v.y, amax, bad);
+    amax2(v.z, amax, bad);
+    amax2(v.w, amax, bad);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    wmax[warp] = amax;
+    wbad[warp] = bad;
+  }
+  __syncthreads();
+  amax = wmax[0];
+  bad = wbad[0] != 0;
+#pragma unroll
+  for (int w = 1; w < kQRowThreads / 32; ++w) {
+    amax = fmaxf(amax, wmax[w]);
+    bad = bad || wbad[w] != 0;
+  }
+  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
+  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
+  if (threadIdx.x == 0) scale[row] = s;
+  uint2* q = Q + row * nvec;
+  for (int j = threadIdx.x; j < nvec; j += kQRowThreads) {
+    const uint4 v = qrow[j];
+    q[j] = bad ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : make_uint2(codes4(v.x, v.y, inv), codes4(v.z, v.w, inv));
+  }
+}
+
+static cudaError_t launch_rows_smem(const void* X, void* Q, float* scale, int64_t M, int64_t K,
+                                    cudaStream_t stream) {
+  // the shared-memory limit is per device: set it once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(quantize_e4m3_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kQSmemMaxVec * 16);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  return launch_overlapped_smem(quantize_e4m3_smem_kernel, dim3((unsigned)M), dim3(kQRowThreads),
+                                (size_t)(K / 8) * 16, stream, static_cast<const uint4*>(X), static_cast<uint2*>(Q),
+                                scale, K);
+}
+
 template <int VPT>
 static cudaError_t launch_rows_vpt(const void* X, void* Q, float* scale, int64_t M, int64_t K,
                                    cudaStream_t stream) {
@@ -144,6 +221,7 @@ static cudaError_t launch_rows_vpt(const void* X, void* Q, float* scale, int64_t
 cudaError_t launch_quantize_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
                                  cudaStream_t stream) {
   const int64_t vpt = (K / 8 + kQRowThreads - 1) / kQRowThreads;
+  if (M <= 0x7FFFFFFF && vpt >= 4 && K / 8 <= kQSmemMaxVec) return launch_rows_smem(X, Q, scale, M, K, stream);
   if (M <= 0x7FFFFFFF && vpt <= kQRowMaxVpt) {
     if (vpt <= 1) return launch_rows_vpt<1>(X, Q, scale, M, K, stream);
     if (vpt <= 2) return launch_rows_vpt<2>(X, Q, scale, M, K, stream);
