@@ -211,6 +211,32 @@ bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi_pins* 
 bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                        const bi_pins* pins, bi_stream_t stream);
 
+/* Bytes of device workspace bi_gemm_bf16_host needs for M rows (0 for M = 0). */
+size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Y_host[M,N] = bf16(X_host[M,K] . W[N,K]^T) with X and Y in host memory and W
+ * on the device: the same bits as bi_gemm_bf16 on device copies of X and Y.
+ * The rows travel in chunks of about 16 MB of X through a ring of two
+ * buffers in `workspace`: a chunk is copied in on a library stream, multiplied
+ * on `stream` and copied out on a second library stream, so copies and GEMMs
+ * of consecutive chunks overlap.  Chunking is free because the tree of a row
+ * never depends on M (Detent, Sec. 3: a batch-invariant operator gives each
+ * row the same bits whatever batch it is computed in).
+ * Ownership: X_host and Y_host are caller-owned host memory (page-locked for
+ * the copies to overlap; pageable memory works, with synchronous copies);
+ * W and `workspace` are caller-owned device memory, `workspace` at least
+ * bi_gemm_bf16_host_workspace_bytes(M, N, K) bytes and 256-byte aligned, not
+ * used by work that is not ordered before this call on `stream`.  The library
+ * keeps two streams and a few events per device, created on first use.
+ * Asynchrony: the call enqueues its work after everything already on
+ * `stream`, and `stream` waits for the last rows to reach Y_host; synchronize
+ * `stream` before reading Y_host.
+ * Requirements: as bi_gemm_bf16 (W 16-byte aligned; X_host and Y_host need no
+ * alignment).
+ * Errors: as bi_gemm_bf16, plus BI_ERR_WORKSPACE. */
+bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_host, int64_t M, int64_t N, int64_t K,
+                            const bi_pins* pins, void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
 /* Y[M,H] = RMSNorm(X[M,H]) with gain g[H], one warp per row: each lane sums
  * the squares of its 16-byte vectors in ascending order, the 32 lane sums are
  * combined by a fixed xor-butterfly, r = 1/sqrt(sum/H + eps) (IEEE division

@@ -108,6 +108,9 @@ _SIGNATURES = {
                                              ctypes.POINTER(Plan)]),
     "bi_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
     "bi_rmsnorm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
+    "bi_gemm_bf16_host_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "bi_gemm_bf16_host": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp,
+                                         ctypes.c_size_t, _vp]),
     "bi_rmsnorm_gemm_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "bi_rmsnorm_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
                                             ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
@@ -230,6 +233,46 @@ def bi_gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = No
     st = load().bi_gemm_bf16(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
                              ctypes.byref(pins) if pins is not None else None, _stream(stream))
     _check(st, "bi_gemm_bf16")
+    if _call_hooks:
+        _report(M, N, K)
+    return out
+
+
+def _host(t: torch.Tensor, name: str, shape) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous bf16 host tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+def bi_gemm_bf16_host_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().bi_gemm_bf16_host_workspace_bytes(M, N, K))
+
+
+def bi_gemm_bf16_host(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
+                      pins: Pins | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """Y = X . W^T with x [M,K] and the result [M,N] in host memory (page-locked
+    for overlapped copies) and w [N,K] on the device.  Asynchronous on
+    `stream`: synchronize it before reading the result."""
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("expected x [M,K] and w [N,K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    need = bi_gemm_bf16_host_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=w.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    st = load().bi_gemm_bf16_host(_host(x, "x", (M, K)), _dev(w, "w"), _host(out, "out", (M, N)), M, N, K,
+                                  ctypes.byref(pins) if pins is not None else None, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "bi_gemm_bf16_host")
     if _call_hooks:
         _report(M, N, K)
     return out

@@ -509,6 +509,62 @@ size_t workspace_bytes(int64_t M, int64_t K) {
   return (size_t)((b + 255u) & ~(uint64_t)255u);
 }
 
+// ---- the GEMM on host buffers: rows in chunks through a ring of device buffers
+//
+// Chunk c's rows are copied in on one stream, multiplied on the caller's
+// stream and copied out on another, so the copies of one chunk overlap the
+// GEMM of the next.  Batch invariance makes this free: a row's bits do not
+// depend on the chunk (the M of the launch) it travels in.
+constexpr int kHostSlots = 2;
+
+int64_t host_chunk_rows(int64_t M, int64_t K) {
+  int64_t r = (int64_t{16} << 20) / (2 * K);  // about 16 MB of X per chunk
+  r = r / 128 * 128;
+  r = r < 128 ? 128 : (r > 8192 ? 8192 : r);
+  return r < M ? r : M;
+}
+
+uint64_t round256(uint64_t b) { return (b + 255u) & ~(uint64_t)255u; }
+
+// bytes of one ring slot: the chunk's X, then its Y
+uint64_t host_slot_bytes(int64_t R, int64_t N, int64_t K) {
+  return round256((uint64_t)R * (uint64_t)K * 2u) + round256((uint64_t)R * (uint64_t)N * 2u);
+}
+
+size_t host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const int64_t R = host_chunk_rows(M, K);
+  const int64_t chunks = (M + R - 1) / R;
+  return (size_t)((chunks < kHostSlots ? chunks : kHostSlots) * host_slot_bytes(R, N, K));
+}
+
+// Per-device streams and events, created once and reused by every call; a
+// per-device mutex keeps one call's enqueue sequence whole.
+struct HostCtx {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t copied_in[kHostSlots] = {}, multiplied[kHostSlots] = {}, copied_out[kHostSlots] = {};
+  bool ready = false;
+};
+HostCtx g_host_ctx[64];
+std::mutex g_host_mu[64];
+
+bool host_ctx_init(HostCtx& c) {
+  if (c.ready) return true;
+  const unsigned ef = cudaEventDisableTiming;
+  if (cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&c.start, ef) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&c.end, ef) != cudaSuccess) return false;
+  for (int i = 0; i < kHostSlots; ++i) {
+    if (cudaEventCreateWithFlags(&c.copied_in[i], ef) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&c.multiplied[i], ef) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&c.copied_out[i], ef) != cudaSuccess) return false;
+  }
+  c.ready = true;
+  return true;
+}
+
 }  // namespace
 }  // namespace bi
 
@@ -597,6 +653,63 @@ BI_API bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t 
   return launch_rmsnorm(X, g, Y, M, H, eps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? BI_OK
              : BI_ERR_CUDA;
+}
+
+BI_API size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return host_workspace_bytes(M, N, K);
+}
+
+BI_API bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_host, int64_t M, int64_t N,
+                                   int64_t K, const bi_pins* pins, void* workspace, size_t ws_bytes,
+                                   bi_stream_t stream) {
+  if (M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  if (!X_host || !W || !Y_host) return BI_ERR_INVALID_ARG;
+  if (!aligned16(W)) return BI_ERR_ALIGNMENT;
+  if (!workspace || ws_bytes < host_workspace_bytes(M, N, K)) return BI_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mu[dev]);
+  HostCtx& c = g_host_ctx[dev];
+  if (!host_ctx_init(c)) return BI_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t R = host_chunk_rows(M, K);
+  const int64_t chunks = (M + R - 1) / R;
+  const uint64_t slot = host_slot_bytes(R, N, K), xoff = round256((uint64_t)R * (uint64_t)K * 2u);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // everything before this call on `stream` (W, the workspace's last users) comes first
+  if (!ok(cudaEventRecord(c.start, s)) || !ok(cudaStreamWaitEvent(c.in, c.start, 0)) ||
+      !ok(cudaStreamWaitEvent(c.out, c.start, 0)))
+    return BI_ERR_CUDA;
+  for (int64_t ch = 0; ch < chunks; ++ch) {
+    const int i = (int)(ch % kHostSlots);
+    const int64_t rows = M - ch * R < R ? M - ch * R : R;
+    char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
+    char* yd = xd + xoff;
+    // the slot's previous chunk has been copied out (so also multiplied)
+    if (ch >= kHostSlots && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) return BI_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(X_host) + (uint64_t)ch * R * K * 2, (size_t)rows * K * 2,
+                            cudaMemcpyHostToDevice, c.in)) ||
+        !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0)))
+      return BI_ERR_CUDA;
+    st = gemm_impl(xd, W, yd, rows, N, K, pins, s);
+    if (st != BI_OK) return st;
+    if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(Y_host) + (uint64_t)ch * R * N * 2, yd, (size_t)rows * N * 2,
+                            cudaMemcpyDeviceToHost, c.out)) ||
+        !ok(cudaEventRecord(c.copied_out[i], c.out)))
+      return BI_ERR_CUDA;
+  }
+  // the caller's stream resumes once the last rows are back on the host
+  if (!ok(cudaEventRecord(c.end, c.out)) || !ok(cudaStreamWaitEvent(s, c.end, 0))) return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return workspace_bytes(M, K); }

@@ -108,6 +108,18 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert ws >= 4 * 256 * 2 and ws % 256 == 0
     assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, 256, ws - 1, None) == \
         bd.BI_ERR_WORKSPACE
+    # GEMM on host buffers: argument, pin and workspace checks before any CUDA call
+    assert lib.bi_gemm_bf16_host(None, None, None, 0, 128, 256, None, None, 0, None) == bd.BI_OK
+    assert lib.bi_gemm_bf16_host(None, None, None, -1, 128, 256, None, None, 0, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm_bf16_host(None, None, None, 4, 128, 250, None, None, 0, None) == \
+        bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_gemm_bf16_host(16, None, 48, 4, 128, 256, None, 256, 1 << 20, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm_bf16_host(16, 40, 48, 4, 128, 256, None, 256, 1 << 20, None) == bd.BI_ERR_ALIGNMENT
+    assert lib.bi_gemm_bf16_host(16, 32, 48, 4, 128, 256, ctypes.byref(p.replace(tok_tile=7)), 256, 1 << 20,
+                                 None) == bd.BI_ERR_ILLEGAL_PINS
+    hws = bd.bi_gemm_bf16_host_workspace_bytes(4, 128, 256)
+    assert lib.bi_gemm_bf16_host(16, 32, 48, 4, 128, 256, None, 256, hws - 1, None) == bd.BI_ERR_WORKSPACE
+    assert lib.bi_gemm_bf16_host(16, 32, 48, 4, 128, 256, None, 512 + 16, hws, None) == bd.BI_ERR_ALIGNMENT
     # glue
     assert lib.bi_residual_add_bf16(16, 32, 48, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_silu_mul_bf16(16, 32, 2, 12, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
@@ -169,6 +181,25 @@ def test_decode_attention_arguments_rejected_before_any_launch(bd):
 
 ALL_M = list(range(1, 300)) + [511, 512, 513, 1000, 1023, 1024, 2048, 4095, 4096, 8191, 8192]
 
+
+
+def test_host_gemm_workspace_is_two_chunk_slots(bd):
+    """Rows travel in chunks of about 16 MB of X (a multiple of 128 rows,
+    128..8192); the workspace holds two slots of a chunk's X and Y, each
+    rounded to 256 bytes, or one slot when one chunk holds every row."""
+    def r256(b):
+        return (b + 255) // 256 * 256
+
+    def slot(R, N, K):
+        return r256(R * K * 2) + r256(R * N * 2)
+    assert bd.bi_gemm_bf16_host_workspace_bytes(0, 4096, 14336) == 0
+    # down_proj: 16 MB / 28 KB per row = 585 rows -> 512-row chunks
+    assert bd.bi_gemm_bf16_host_workspace_bytes(8192, 4096, 14336) == 2 * slot(512, 4096, 14336)
+    assert bd.bi_gemm_bf16_host_workspace_bytes(512, 4096, 14336) == slot(512, 4096, 14336)
+    assert bd.bi_gemm_bf16_host_workspace_bytes(3, 4096, 14336) == slot(3, 4096, 14336)
+    # K = 4096: 2048-row chunks; tiny K: at most 8192 rows
+    assert bd.bi_gemm_bf16_host_workspace_bytes(5000, 6144, 4096) == 2 * slot(2048, 6144, 4096)
+    assert bd.bi_gemm_bf16_host_workspace_bytes(100000, 128, 256) == 2 * slot(8192, 128, 256)
 
 @pytest.mark.parametrize("N,K", TABLE_SHAPES + [(300, 200), (20000, 1000)])
 def test_reduction_tree_never_depends_on_m(bd, N, K):

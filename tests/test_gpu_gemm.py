@@ -190,3 +190,35 @@ def test_stores_stay_inside_y(lib):
                 split_k=S, tok_tile=T, flags=flags, mma_ctas=ctas))
             torch.cuda.synchronize()
             assert torch.all(buf[:guard].float() == 123.0) and torch.all(buf[guard + M * N:].float() == 123.0)
+
+
+@pytest.mark.parametrize("M", [1, 300, 2500])
+def test_host_buffers_give_the_device_bits(lib, M):
+    """bi_gemm_bf16_host (X and Y in host memory, rows in 512-row chunks for
+    down_proj: 2500 rows are 5 chunks, the last one partial) gives the bits of
+    bi_gemm_bf16 on device copies, from page-locked and from pageable memory."""
+    N, K = 4096, 14336
+    X = inputs.normal((M, K), seed=30, stream=0)
+    W = inputs.device_normal((N, K), std=0.02, seed=30, stream=1)
+    want = bf16_bits(lib.bi_gemm_bf16(X.cuda(), W))
+    y = lib.bi_gemm_bf16_host(X.contiguous().pin_memory(), W)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(y), want)
+    y2 = torch.empty((M, N), dtype=torch.bfloat16)
+    lib.bi_gemm_bf16_host(X.contiguous(), W, out=y2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(y2), want)
+
+
+def test_host_buffer_calls_back_to_back(lib):
+    """Consecutive calls on one stream and one workspace, with no
+    synchronisation between them, each give their own bits."""
+    N, K = 6144, 4096
+    W = inputs.device_normal((N, K), std=0.02, seed=31, stream=1)
+    Ms = (5000, 1, 2049, 700)
+    xs = [inputs.normal((M, K), seed=31, stream=10 + i).pin_memory() for i, M in enumerate(Ms)]
+    ws = torch.empty(lib.bi_gemm_bf16_host_workspace_bytes(max(Ms), N, K), dtype=torch.uint8, device="cuda")
+    outs = [lib.bi_gemm_bf16_host(x, W, workspace=ws) for x in xs]
+    torch.cuda.synchronize()
+    for x, y in zip(xs, outs):
+        assert np.array_equal(bf16_bits(y), bf16_bits(lib.bi_gemm_bf16(x.cuda(), W)))
