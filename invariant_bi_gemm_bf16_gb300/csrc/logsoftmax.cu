@@ -256,7 +256,7 @@ constexpr int kLsmSmemVec = (kLsmCache - 1) * kLsmHalf;              // vectors 
 constexpr int kLsmSmemBytes = kLsmSmemVec * 16;
 static_assert(kLsmVirt * 2 == kLsmCtas && kLsmThreads == kLsmCtaThreads, "rank j of the cluster is played as 4r + j");
 #ifndef BI_LSM_CTA_MIN_ROWS
-#define BI_LSM_CTA_MIN_ROWS 64
+#define BI_LSM_CTA_MIN_ROWS 128  // measured: 8-CTA clusters win below (M = 96: 28 against 31 us)
 #endif
 
 struct LsmPairShared {

@@ -50,7 +50,7 @@ def f64(X):
 
 
 @pytest.mark.parametrize("V", [8, 1000, 4104, 128256])
-@pytest.mark.parametrize("M,std", [(1, 1.0), (3, 4.0), (37, 8.0), (100, 2.0)])
+@pytest.mark.parametrize("M,std", [(1, 1.0), (3, 4.0), (37, 8.0), (100, 2.0), (130, 3.0)])
 def test_log_softmax_parity(lib, oracle, V, M, std):
     X = inputs.normal((M, V), std=std, seed=20, stream=0)
     ref = oracle.log_softmax(inputs.bits(X))
@@ -88,18 +88,18 @@ def test_rows_independent_of_batch_and_position(lib):
 
 @pytest.mark.parametrize("V", [8, 1000, 128256, 140008])
 def test_cluster_and_cta_variants_give_the_same_bits(lib, V):
-    """Rows of a batch of 70 run one CTA per row; a row alone runs on an
-    8-CTA cluster.  Both follow the same tree: identical bits, including rows
-    longer than the register cache (V > 131072) and special rows."""
-    X = inputs.normal((70, V), std=5.0, seed=24, stream=0)
+    """Rows of a batch of 130 run on a CTA pair per row; a row alone runs on
+    an 8-CTA cluster.  Both follow the same tree: identical bits, including
+    rows longer than the on-chip cache (V > 131072) and special rows."""
+    X = inputs.normal((130, V), std=5.0, seed=24, stream=0)
     X[5, :] = float("-inf")
     X[6, V // 2] = float("nan")
     X[7, V - 1] = float("-inf")
     X = X.cuda()
     full = lib.bi_log_softmax_bf16(X).cpu().numpy().view(np.uint32)
-    ids = torch.arange(70, dtype=torch.int32, device="cuda") % V
+    ids = torch.arange(130, dtype=torch.int32, device="cuda") % V
     tok = lib.bi_token_logprobs_bf16(X, ids).cpu().numpy().view(np.uint32)
-    for r in (0, 5, 6, 7, 69):
+    for r in (0, 5, 6, 7, 129):
         alone = lib.bi_log_softmax_bf16(X[r:r + 1].contiguous()).cpu().numpy().view(np.uint32)
         assert np.array_equal(alone[0], full[r]), r
         t1 = lib.bi_token_logprobs_bf16(X[r:r + 1].contiguous(), ids[r:r + 1]).cpu().numpy().view(np.uint32)
