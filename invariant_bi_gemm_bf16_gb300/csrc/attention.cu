@@ -543,36 +543,24 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
 // One CTA per (key/value head, slice of 128 / SL d, request): folds the
 // request's split records in split order and writes out[b][h][d] for the
 // group's heads and the slice's d.  Thread t owns head h = t % GP and the
-// values d = t / GP + (256 / GP) i of the slice.  The records come into shared
-// memory a chunk at a time by bulk copy, double-buffered: whole records (one
-// copy per chunk) when SL = 1, else each record's o slice and its m and l (two
-// copies per record).  SL changes no operation: every (h, d) folds the same
-// records in the same order.  Slicing only pays when there are few (request,
-// head) pairs, so the host takes SL = 4 when there are fewer pairs than SMs.
+// values d = t / GP + (256 / GP) i of the slice; a record holds o[d][h], then
+// m[h] and l[h], so the CTA's loads of one record are contiguous.  The records
+// are read straight from L2 (the previous kernel just wrote them), several
+// records' loads at a time.  SL changes no operation: every (h, d) folds the
+// same records in the same order.  Slicing only pays when there are few
+// (request, head) pairs, so the host takes SL = 4 when there are fewer pairs
+// than SMs.
 constexpr int kCombThreads = 256;
-
-template <int SL>
-struct CombCfg {
-  static constexpr int slice_d = kAttnD / SL;
-  static constexpr int chunk = SL == 1 ? 8 : 32;  // records per staged chunk
-};
-
-template <int NT, int SL>
-constexpr int comb_smem_bytes() {
-  return 2 * CombCfg<SL>::chunk * (CombCfg<SL>::slice_d + 2) * 8 * NT * 4 + 16;
-}
 
 template <int NT, int SL>
 __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const AttnParams p, __nv_bfloat16* out) {
   constexpr int GP = 8 * NT;
-  constexpr int SD = CombCfg<SL>::slice_d;
-  constexpr int kCombChunk = CombCfg<SL>::chunk;
+  constexpr int SD = kAttnD / SL;                  // d values of the slice
   constexpr int RS = (kAttnD + 2) * GP;            // floats per record
-  constexpr int CS = (SD + 2) * GP;                // floats per staged record slice (o slice, m, l)
   constexpr int DSTEP = kCombThreads / GP;         // distance between a thread's d values
   constexpr int DPT = SD / DSTEP;                  // d values per thread
-  extern __shared__ __align__(16) float comb_smem[];
-  __shared__ __align__(8) uint64_t bars[2];
+  // records whose loads are in flight together (about 32 values per thread)
+  constexpr int kCombAhead = 32 / DPT < 4 ? 4 : (32 / DPT > 16 ? 16 : 32 / DPT);
   grid_dep_launch_dependents();
   grid_dep_wait();  // the split records come from the previous kernel
   const int kvh = blockIdx.x / SL, slice = blockIdx.x % SL;
@@ -591,78 +579,37 @@ __global__ void __launch_bounds__(kCombThreads) decode_attn_combine_kernel(const
     return;
   }
   const int ns = (int)((L + p.split_size - 1) / p.split_size);
-  const int nchunks = (ns + kCombChunk - 1) / kCombChunk;
   const float* rec0 = p.part + (b * p.Hkv + kvh) * (int64_t)p.n_split * RS;
-  if (t == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // warp 0 stages a chunk: lane 0 announces the bytes, then the copies go out
-  // (one for the chunk when SL = 1; else lane r copies records r, r + 32, ...)
-  auto issue = [&](int c) {
-    const int n = min(kCombChunk, ns - c * kCombChunk);
-    const uint32_t bar = smem_u32(&bars[c & 1]);
-    if (t == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * CS * 4));
-    __syncwarp();
-    if constexpr (SL == 1) {
-      if (t == 0)
-        bulk_load(smem_u32(comb_smem + (c & 1) * kCombChunk * RS), rec0 + (int64_t)c * kCombChunk * RS,
-                  (uint32_t)(n * RS * 4), bar);
-    } else {
-      for (int r = t; r < n; r += 32) {
-        const float* rec = rec0 + (int64_t)(c * kCombChunk + r) * RS;
-        const uint32_t dst = smem_u32(comb_smem + ((c & 1) * kCombChunk + r) * CS);
-        bulk_load(dst, rec + slice * SD * GP, (uint32_t)(SD * GP * 4), bar);
-        bulk_load(dst + SD * GP * 4, rec + kAttnD * GP, (uint32_t)(2 * GP * 4), bar);
-      }
-    }
-  };
-  if (t < 32) {
-    issue(0);
-    if (nchunks > 1) issue(1);
-  }
   float m = 0.0f, l = 0.0f, o[DPT];
-  bool ok = true;
-  for (int c = 0; c < nchunks; ++c) {
-    const uint32_t bar = smem_u32(&bars[c & 1]);
-    if (!mbar_try_wait(bar, (c >> 1) & 1)) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar, (c >> 1) & 1)) {
-        if (globaltimer_ns() - t0 > kAttnWaitNs) {
-          ok = false;
-          break;
-        }
+  for (int r0 = 0; r0 < ns; r0 += kCombAhead) {
+    float mv[kCombAhead], lv[kCombAhead], ov[kCombAhead][DPT];
+#pragma unroll
+    for (int u = 0; u < kCombAhead; ++u) {
+      if (r0 + u < ns) {
+        const float* rec = rec0 + (int64_t)(r0 + u) * RS;
+        mv[u] = __ldcg(rec + kAttnD * GP + h);
+        lv[u] = __ldcg(rec + (kAttnD + 1) * GP + h);
+#pragma unroll
+        for (int i = 0; i < DPT; ++i) ov[u][i] = __ldcg(rec + slice * SD * GP + t + kCombThreads * i);
       }
     }
-    if (!__syncthreads_and(ok)) {
-      if (t == 0) attn_flag(p.status, (int)BI_ERR_DEVICE_TIMEOUT);
-      // the other buffer's copies, if issued, must land before the CTA ends
-      if (t == 0 && c + 1 < nchunks) attn_drain(smem_u32(&bars[(c + 1) & 1]), ((c + 1) >> 1) & 1, p.status);
-      return;
-    }
-    const float* buf = comb_smem + (c & 1) * kCombChunk * CS;
-    const int n = min(kCombChunk, ns - c * kCombChunk);
-    for (int r = 0; r < n; ++r) {
-      const float* rec = buf + r * CS;
-      const float m2 = rec[SD * GP + h], l2 = rec[SD * GP + GP + h];
-      if (c == 0 && r == 0) {
-        m = m2;
-        l = l2;
 #pragma unroll
-        for (int i = 0; i < DPT; ++i) o[i] = rec[t + kCombThreads * i];
+    for (int u = 0; u < kCombAhead; ++u) {
+      if (r0 + u >= ns) break;
+      if (r0 + u == 0) {
+        m = mv[u];
+        l = lv[u];
+#pragma unroll
+        for (int i = 0; i < DPT; ++i) o[i] = ov[u][i];
       } else {
         float mm, a1, a2;
-        attn_scales(m, m2, mm, a1, a2);
-        l = __fadd_rn(__fmul_rn(l, a1), __fmul_rn(l2, a2));
+        attn_scales(m, mv[u], mm, a1, a2);
+        l = __fadd_rn(__fmul_rn(l, a1), __fmul_rn(lv[u], a2));
 #pragma unroll
-        for (int i = 0; i < DPT; ++i) o[i] = __fadd_rn(__fmul_rn(o[i], a1), __fmul_rn(rec[t + kCombThreads * i], a2));
+        for (int i = 0; i < DPT; ++i) o[i] = __fadd_rn(__fmul_rn(o[i], a1), __fmul_rn(ov[u][i], a2));
         m = mm;
       }
     }
-    __syncthreads();  // the buffer is read by everyone before it is refilled
-    if (t < 32 && c + 2 < nchunks) issue(c + 2);
   }
   if (h < p.G) {
 #pragma unroll
@@ -682,12 +629,6 @@ static cudaError_t launch_attn_t(const AttnLaunch& A) {
     cudaError_t e = cudaFuncSetAttribute(decode_attn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          AttnCfg<NT>::smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             comb_smem_bytes<NT, 1>());
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_attn_combine_kernel<NT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             comb_smem_bytes<NT, 4>());
-    if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
   cudaError_t e = launch_overlapped(decode_attn_plan_kernel, dim3(1), dim3(kPlanThreads), A.stream, A.p, A.B);
@@ -696,10 +637,10 @@ static cudaError_t launch_attn_t(const AttnLaunch& A) {
                              AttnCfg<NT>::smem, A.stream, A.tmK, A.tmV, A.p);
   if (e != cudaSuccess) return e;
   if ((int64_t)A.B * A.p.Hkv < A.grid)
-    return launch_overlapped_smem(decode_attn_combine_kernel<NT, 4>, dim3((unsigned)(A.p.Hkv * 4), (unsigned)A.B),
-                                  dim3(kCombThreads), comb_smem_bytes<NT, 4>(), A.stream, A.p, A.out);
-  return launch_overlapped_smem(decode_attn_combine_kernel<NT, 1>, dim3((unsigned)A.p.Hkv, (unsigned)A.B),
-                                dim3(kCombThreads), comb_smem_bytes<NT, 1>(), A.stream, A.p, A.out);
+    return launch_overlapped(decode_attn_combine_kernel<NT, 4>, dim3((unsigned)(A.p.Hkv * 4), (unsigned)A.B),
+                             dim3(kCombThreads), A.stream, A.p, A.out);
+  return launch_overlapped(decode_attn_combine_kernel<NT, 1>, dim3((unsigned)A.p.Hkv, (unsigned)A.B),
+                           dim3(kCombThreads), A.stream, A.p, A.out);
 }
 
 cudaError_t launch_decode_attention(const AttnLaunch& A) {
