@@ -270,14 +270,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Vector i of this CTA's cluster thread h (row vector k = g + kLsmStride i):
-// shared memory, the register r, or global memory.
-__device__ __forceinline__ uint4 lsm_vec(const uint4* __restrict__ x, const uint4* row_s, const uint4& r, int h,
-                                         int64_t g, int i) {
-  if (i < kLsmCache - 1) return row_s[i * kLsmHalf + h];
-  if (i == kLsmCache - 1) return r;
-  return __ldg(x + g + (int64_t)i * kLsmStride);
-}
 
 template <bool FULL>
 __global__ void __launch_bounds__(kLsmCtaThreads, 2)
@@ -316,11 +308,21 @@ __global__ void __launch_bounds__(kLsmCtaThreads, 2)
     const int h = t + j * kLsmCtaThreads;
     const int64_t g = g0 + h;
     const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
+    // vectors i < 3 (shared memory), i = 3 (register), i >= 4 (global), in order
     float m = -INFINITY, s = 0.0f;
-    for (int i = 0; i < nv; ++i) m = fmax_nan(m, max8(lsm_vec(x, lsm_row, r[j], h, g, i)));
+#pragma unroll
+    for (int i = 0; i < kLsmCache - 1; ++i)
+      if (i < nv) m = fmax_nan(m, max8(lsm_row[i * kLsmHalf + h]));
+    if (nv >= kLsmCache) m = fmax_nan(m, max8(r[j]));
+    for (int i = kLsmCache; i < nv; ++i) m = fmax_nan(m, max8(__ldg(x + g + (int64_t)i * kLsmStride)));
     bool bad = bad_max(m);
-    if (m != -INFINITY)
-      for (int i = 0; i < nv; ++i) s = sumexp8(lsm_vec(x, lsm_row, r[j], h, g, i), m, s);
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < kLsmCache - 1; ++i)
+        if (i < nv) s = sumexp8(lsm_row[i * kLsmHalf + h], m, s);
+      if (nv >= kLsmCache) s = sumexp8(r[j], m, s);
+      for (int i = kLsmCache; i < nv; ++i) s = sumexp8(__ldg(x + g + (int64_t)i * kLsmStride), m, s);
+    }
     ms_butterfly(m, s, bad);
     if (lane == 0) {  // cluster CTA 4 rank + j, warp `warp`
       sh.m[j][warp] = m;
@@ -363,13 +365,17 @@ __global__ void __launch_bounds__(kLsmCtaThreads, 2)
       const int h = t + j * kLsmCtaThreads;
       const int64_t g = g0 + h;
       const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
-      for (int i = 0; i < nv; ++i) {
-        const uint4 v = lsm_vec(x, lsm_row, r[j], h, g, i);
+      auto put = [&](const uint4& v, int i) {
         const int64_t k = g + (int64_t)i * kLsmStride;
         __stcs(y + 2 * k, make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse));
         __stcs(y + 2 * k + 1,
                make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse));
-      }
+      };
+#pragma unroll
+      for (int i = 0; i < kLsmCache - 1; ++i)
+        if (i < nv) put(lsm_row[i * kLsmHalf + h], i);
+      if (nv >= kLsmCache) put(r[j], kLsmCache - 1);
+      for (int i = kLsmCache; i < nv; ++i) put(__ldg(x + g + (int64_t)i * kLsmStride), i);
     }
   } else if (rank == 0 && t == 0) {
     const int32_t id = ids[row];
