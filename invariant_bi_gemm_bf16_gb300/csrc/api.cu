@@ -281,12 +281,14 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   r.ctas = choice.ctas;
   if (choice.T != 0) r.T = choice.T;
   // Decode (M <= 128 on single-CTA MMAs, the CTA grouping and the W depth
-  // left open by the pins; bf16 or E4M3): the
-  // token tile narrows to 64 or 128, whichever holds M (the MMA's N extent
-  // changes no bit), and W and X come two K tiles per stage by two 2-D
-  // copies each.  W streams from HBM faster in stages of 256 bytes per row
-  // than of 128 (5.5 against 4.1 TB/s measured for the down_proj pattern),
-  // and the narrower X stages leave the shared memory to them.
+  // left open by the pins; bf16 or E4M3): the token tile narrows to 64 or
+  // 128, whichever holds M (the MMA's N extent changes no bit), and W and X
+  // come two K tiles per stage by two 2-D copies each.  W streams from HBM
+  // faster in stages of 256 bytes per row than of 128 (5.5 against 4.1 TB/s
+  // measured for the down_proj pattern), and the narrower X stages leave the
+  // shared memory to them.  (At T = 256 the same stages leave room for only
+  // 3 W and 2 X stages, which measured slower: 34.3 against 30.9 us for
+  // down_proj at M = 256.)
   const bool decode2 = pinned.ctas == 0 && r.ctas == 1 && M > 0 && M <= 128 && M <= r.T && r.w_pin == 0 &&
                        (r.flags & BI_FLAG_KTILE_PAIRS) != 0;
   if (decode2) r.T = M <= 64 ? 64 : 128;

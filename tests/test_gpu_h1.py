@@ -94,14 +94,15 @@ def test_narrowed_token_tiles_leave_bits_unchanged(lib, M, N, K, S, T):
 @pytest.mark.parametrize("N,K", [(4096, 14336), (6144, 4096), (640, 704)])
 def test_decode_tiles_leave_bits_unchanged(lib, N, K):
     """With the grouping left open, a single token tile of up to 128 tokens
-    runs at T = 64 or 128 with two K tiles per stage (2-D copies); pinning one
-    CTA per MMA keeps the pinned T = 256 and one K tile per stage.  Both give
-    the same bits, in bf16 and in FP8 (K = 704 has a partial last K tile)."""
-    X = wide_range((129, K), seed=14, stream=0)
+    on single-CTA MMAs runs at T = 64 or 128 with two K tiles per stage (2-D
+    copies); pinning one CTA per MMA keeps the pinned T = 256 and one K tile
+    per stage.  Both give the same bits, in bf16 and in FP8 (K = 704 has a
+    partial last K tile); larger M cross into the pinned plans."""
+    X = wide_range((256, K), seed=14, stream=0)
     W = wide_range((N, K), seed=14, stream=1, std=0.05)
     x, w = X.cuda(), W.cuda()
     base = lib.bi_pins_default(N, K)
-    for M in (1, 7, 64, 65, 128, 129):
+    for M in (1, 7, 64, 65, 128, 129, 192, 256):
         open_ = lib.bi_gemm_plan_describe(M, N, K, base)
         pinned = base.replace(mma_ctas=1)
         assert lib.bi_gemm_plan_describe(M, N, K, pinned).tok_tile == 256
@@ -112,7 +113,7 @@ def test_decode_tiles_leave_bits_unchanged(lib, N, K):
         wq, sw = lib.bi_quantize_rows_e4m3(w)
         xq, sx = lib.bi_quantize_rows_e4m3(x)
         fb = lib.bi_pins_default_fp8(N, K)
-        for M in (1, 64, 65, 128):
+        for M in (1, 64, 65, 128, 200):
             got = bf16_bits(lib.bi_gemm_fp8(xq[:M].contiguous(), sx[:M].contiguous(), wq, sw, pins=fb))
             ref = bf16_bits(lib.bi_gemm_fp8(xq[:M].contiguous(), sx[:M].contiguous(), wq, sw,
                                             pins=fb.replace(mma_ctas=1)))
