@@ -981,6 +981,23 @@ def run_single_rmsnorm(args, dist):
     torch.cuda.synchronize()
 
 
+def run_single_quantize(args, dist):
+    """Launches the per-row E4M3 quantisation on one shape (M:K), --launches
+    times on rotating inputs, for an ncu capture of those launches."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    M, K = (int(x) for x in args.single_quantize.split(":"))
+    n = copies_for(M * K * 2, cap=8)
+    xs = [inputs.device_normal((M, K), seed=dist.rank, stream=80 + i, device=dev) for i in range(n)]
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sc = torch.empty((M,), dtype=torch.float32, device=dev)
+    for i in range(args.launches):
+        bd.bi_quantize_rows_e4m3(xs[i % n], q=q, scale=sc)
+    torch.cuda.synchronize()
+
+
 def run_single_logsoftmax(args, dist):
     """Launches the full log-softmax and the token log-probabilities on M rows
     of Llama-3.1-8B logits (V = 128256), --launches times each on rotating
@@ -1044,6 +1061,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--single-quantize", default="",
+                    help="M:K: only launch the E4M3 quantisation on that shape (for ncu)")
     ap.add_argument("--single-logsoftmax", default="",
                     help="M: only launch the log-softmax kernels on M rows of V = 128256 logits (for ncu)")
     ap.add_argument("--single-rmsnorm", default="",
@@ -1060,6 +1079,9 @@ def main():
     try:
         if args.single_attention:
             run_single_attention(args, dist)
+            return
+        if args.single_quantize:
+            run_single_quantize(args, dist)
             return
         if args.single_logsoftmax:
             run_single_logsoftmax(args, dist)
