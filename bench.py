@@ -681,9 +681,34 @@ def run_fp8(args, dist, peaks):
         del xs, xq
     del Ws, wq
     torch.cuda.empty_cache()
+    # the FP8 RMSNorm prologue (Llama-3.1-8B hidden 4096): one pass against
+    # bi_rmsnorm_bf16 followed by bi_quantize_rows_e4m3
+    H = 4096
+    g = inputs.device_normal((H,), std=0.1, mean=1.0, seed=dist.rank, stream=inputs.STREAM_G, device=dev)
+    pro = []
+    for M in (1, 128, 2048, 8192):
+        nx = copies_for(M * H * 2, cap=8)
+        xs = [inputs.device_normal((M, H), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
+              for i in range(nx)]
+        q = torch.empty((M, H), dtype=torch.uint8, device=dev)
+        sc = torch.empty(M, dtype=torch.float32, device=dev)
+        yb = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        us_f = time_graph(lambda i: bd.bi_rmsnorm_quantize_e4m3(xs[i % nx], g, EPS, q=q, scale=sc), args.per_m_reps)
+
+        def two(i):
+            bd.bi_rmsnorm_bf16(xs[i % nx], g, EPS, out=yb)
+            bd.bi_quantize_rows_e4m3(yb, q=q, scale=sc)
+        us_2 = time_graph(two, args.per_m_reps)
+        bf = 3.0 * M * H + 4.0 * M + 2.0 * H   # bf16 in, codes and scales out, the gain
+        pro.append({"M": M, "fused_us": round(us_f, 2), "fused_hbm_frac": round(bf / us_f / 1e3 / peaks["hbm_gbs"], 3),
+                    "rmsnorm_then_quantize_us": round(us_2, 2), "speedup": round(us_2 / us_f, 3)})
+        del xs
+    torch.cuda.empty_cache()
     return {"timing": GRAPH_TIMING, "workload": "FP8 E4M3 down_proj W[4096,14336], per-token activation and per-channel weight scales",
             "peak_tflops": peak8, "peak_source": "measured bf16 burst x 2 (nominal FP8 / bf16 ratio)",
-            "baseline": baseline, "sweep": res}
+            "baseline": baseline, "sweep": res,
+            "rmsnorm_quantize": {"workload": "bi_rmsnorm_quantize_e4m3, H = 4096, against bi_rmsnorm_bf16 + "
+                                             "bi_quantize_rows_e4m3", "sweep": pro}}
 
 
 ATTN_HEADS = (64, 8, 128, 16)   # query heads, key/value heads, head dim, page size

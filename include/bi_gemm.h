@@ -327,6 +327,20 @@ bi_status bi_attention_ctx1_bf16(const void* qkv, void* out, int64_t M, int64_t 
 bi_status bi_quantize_rows_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,
                                 bi_stream_t stream);
 
+/* RMSNorm and per-row quantisation in one call: Q and scale are those of
+ * bi_quantize_rows_e4m3 applied to Y = bi_rmsnorm_bf16(X; g, eps), bit for
+ * bit (the same RMSNorm tree and rounding, the same amax, scale and codes),
+ * but X is read once and Y never reaches memory.  The FP8 form of the RMSNorm
+ * prologue.  Defines: LLM-42, Sec. 2.1 (the per-token normalisation) and
+ * Detent, Limits (per-token scales).
+ * X [M,H] bf16, g [H] bf16; Q: uint8 [M,H]; scale: fp32 [M].
+ * Requirements: H % 16 == 0, 16 <= H <= 16384, eps > 0 and finite, X, g and Q
+ * 16-byte aligned, scale 4-byte aligned.
+ * Errors: BI_ERR_INVALID_ARG, BI_ERR_ALIGNMENT, BI_ERR_UNSUPPORTED_SHAPE,
+ * BI_ERR_CUDA. */
+bi_status bi_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, float* scale, int64_t M, int64_t H,
+                                   float eps, bi_stream_t stream);
+
 /* Pins of the FP8 GEMM: as bi_pins_default / bi_pins_validate with bk = 128
  * (a K tile is 128 E4M3 values, the same 128 bytes) and tok_tile = 256. */
 bi_status bi_pins_default_fp8(int64_t N, int64_t K, bi_pins* out);

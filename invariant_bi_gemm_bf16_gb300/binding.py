@@ -108,6 +108,7 @@ _SIGNATURES = {
                                              ctypes.POINTER(Plan)]),
     "bi_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
     "bi_rmsnorm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
+    "bi_rmsnorm_quantize_e4m3": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
     "bi_gemm_bf16_host_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "bi_gemm_bf16_host": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp,
                                          ctypes.c_size_t, _vp]),
@@ -378,6 +379,24 @@ def bi_quantize_rows_e4m3(x: torch.Tensor, q: torch.Tensor | None = None, scale:
     st = load().bi_quantize_rows_e4m3(_dev(x, "x"), _dev_as(q, "q", torch.uint8, (M, K)),
                                       _dev_as(scale, "scale", torch.float32, (M,)), M, K, _stream(stream))
     _check(st, "bi_quantize_rows_e4m3")
+    return q, scale
+
+
+def bi_rmsnorm_quantize_e4m3(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-5, q: torch.Tensor | None = None,
+                             scale: torch.Tensor | None = None, stream=None):
+    """E4M3 codes (uint8 [M,H]) and per-row scales (fp32 [M]) of RMSNorm(x; g),
+    bit for bit those of bi_quantize_rows_e4m3(bi_rmsnorm_bf16(x, g, eps))."""
+    if x.dim() != 2:
+        raise ValueError("expected x [M,H]")
+    M, H = x.shape
+    if q is None:
+        q = torch.empty((M, H), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    st = load().bi_rmsnorm_quantize_e4m3(_dev(x, "x"), _dev(g, "g", (H,)), _dev_as(q, "q", torch.uint8, (M, H)),
+                                         _dev_as(scale, "scale", torch.float32, (M,)), M, H, float(eps),
+                                         _stream(stream))
+    _check(st, "bi_rmsnorm_quantize_e4m3")
     return q, scale
 
 

@@ -15,6 +15,7 @@
 
 #include "attention.h"
 #include "internal.h"
+#include "rowmath.cuh"
 
 #define BI_API extern "C" __attribute__((visibility("default")))
 
@@ -644,6 +645,20 @@ BI_API bi_status bi_quantize_rows_e4m3(const void* X, void* Q, float* scale, int
   if (!X || !Q || !scale) return BI_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(Q) || (reinterpret_cast<uintptr_t>(scale) & 3u)) return BI_ERR_ALIGNMENT;
   return launch_quantize_e4m3(X, Q, scale, M, K, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? BI_OK
+             : BI_ERR_CUDA;
+}
+
+BI_API bi_status bi_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, float* scale, int64_t M,
+                                          int64_t H, float eps, bi_stream_t stream) {
+  bi_status st = check_rmsnorm_args(X, g, Q, M, H, eps);
+  if (st != BI_OK) return st;
+  if (H % 16 != 0 || H > kRqMaxH) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!scale) return BI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(scale) & 3u) return BI_ERR_ALIGNMENT;
+  return launch_rmsnorm_quantize_e4m3(X, g, Q, scale, M, H, eps, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? BI_OK
              : BI_ERR_CUDA;
 }

@@ -17,26 +17,11 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rowmath.cuh"
 
 namespace bi {
 
 constexpr int kQuantWarps = 8;
-
-__device__ __forceinline__ float q_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float q_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void amax2(uint32_t w, float& amax, bool& bad) {
-  const float a = q_lo(w), b = q_hi(w);
-  bad = bad || !isfinite(a) || !isfinite(b);
-  amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
-}
-
-// Four E4M3 codes of x[0..3] * inv, x[0] in the lowest byte.
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float inv) {
-  const uint32_t lo = cvt_e4m3x2(__fmul_rn(q_lo(w0), inv), __fmul_rn(q_hi(w0), inv));
-  const uint32_t hi = cvt_e4m3x2(__fmul_rn(q_lo(w1), inv), __fmul_rn(q_hi(w1), inv));
-  return lo | (hi << 16);
-}
 
 // X [M,K] bf16 -> Q [M,K] E4M3, scale [M]; one warp per row, vectors of 8.
 __global__ void __launch_bounds__(32 * kQuantWarps)
@@ -62,8 +47,8 @@ __global__ void __launch_bounds__(32 * kQuantWarps)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
   }
-  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
-  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
   if (lane == 0) scale[row] = s;
   uint2* q = Q + row * nvec;
   for (int64_t i = lane; i < nvec; i += 32) {
@@ -123,8 +108,8 @@ __global__ void __launch_bounds__(kQRowThreads)
     amax = fmaxf(amax, wmax[w]);
     bad = bad || wbad[w] != 0;
   }
-  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
-  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
   if (threadIdx.x == 0) scale[row] = s;
   uint2* q = Q + row * nvec;
 #pragma unroll
@@ -182,8 +167,8 @@ __global__ void __launch_bounds__(kQRowThreads)
     amax = fmaxf(amax, wmax[w]);
     bad = bad || wbad[w] != 0;
   }
-  const float s = bad ? __int_as_float(0x7fc00000) : (amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f));
-  const float inv = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 3.40282347e38f);
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
   if (threadIdx.x == 0) scale[row] = s;
   uint2* q = Q + row * nvec;
   for (int j = threadIdx.x; j < nvec; j += kQRowThreads) {
@@ -216,6 +201,144 @@ static cudaError_t launch_rows_vpt(const void* X, void* Q, float* scale, int64_t
                                    cudaStream_t stream) {
   return launch_overlapped(quantize_e4m3_row_kernel<VPT>, dim3((unsigned)M), dim3(kQRowThreads), stream,
                            static_cast<const uint4*>(X), static_cast<uint2*>(Q), scale, K);
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm and quantisation in one pass over X
+// ---------------------------------------------------------------------------
+// Row m: y = bf16_rne((x * r) * g) with the RMSNorm tree of bi_rmsnorm_bf16
+// (lane l of the row's warp sums the squares of vectors l, l + 32, ... in
+// order; the xor butterfly combines the lanes), then the E4M3 codes of y with
+// the row's scale, as bi_quantize_rows_e4m3 takes them from y.  Each warp
+// stages its row in shared memory by 16-byte asynchronous copies (and reads
+// back only its own vectors), so X is read once and y never leaves the chip;
+// y is recomputed, with the same bits, for the amax and for the codes.
+constexpr int kRqWarps = 2;  // rows per block
+
+__global__ void __launch_bounds__(32 * kRqWarps)
+    rmsnorm_quantize_kernel(const uint4* X, const uint4* __restrict__ g, uint2* Q, float* scale, int64_t M,
+                            int64_t H, float eps) {
+  extern __shared__ __align__(16) uint4 rq_rows[];
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * kRqWarps + warp;
+  if (row >= M) return;
+  const int nvec = (int)(H / 8);
+  const uint4* x = X + row * nvec;
+  uint4* buf = rq_rows + (int64_t)warp * nvec;
+  for (int i = lane; i < nvec; i += 32)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + i)), "l"(x + i) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  float ss = 0.0f;
+  for (int i = lane; i < nvec; i += 32) ss = sumsq8(buf[i], ss);
+  ss = butterfly_sum(ss);
+  const float r = inv_rms(ss, H, eps);
+  float amax = 0.0f;
+  bool bad = false;
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 y = norm8(buf[i], __ldg(g + i), r);
+    amax2(y.x, amax, bad);
+    amax2(y.y, amax, bad);
+    amax2(y.z, amax, bad);
+    amax2(y.w, amax, bad);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
+  }
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
+  if (lane == 0) scale[row] = s;
+  uint2* q = Q + row * nvec;
+  for (int i = lane; i < nvec; i += 32) {
+    if (bad) {
+      q[i] = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+      const uint4 y = norm8(buf[i], __ldg(g + i), r);
+      q[i] = make_uint2(codes4(y.x, y.y, inv), codes4(y.z, y.w, inv));
+    }
+  }
+}
+
+// The same with the row in registers (H = 256 * VPL): every vector of a
+// lane is loaded at once, normalised in place, and quantised from there.
+template <int VPL>
+__global__ void __launch_bounds__(256)
+    rmsnorm_quantize_regs_kernel(const uint4* X, const uint4* __restrict__ g, uint2* Q, float* scale, int64_t M,
+                                 float eps) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  constexpr int kVecs = VPL * 32;
+  const uint4* x = X + row * kVecs;
+  uint4 v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[i] = __ldcs(x + lane + 32 * i);
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) ss = sumsq8(v[i], ss);
+  ss = butterfly_sum(ss);
+  const float r = inv_rms(ss, (int64_t)kVecs * 8, eps);
+  float amax = 0.0f;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    v[i] = norm8(v[i], __ldg(g + lane + 32 * i), r);
+    amax2(v[i].x, amax, bad);
+    amax2(v[i].y, amax, bad);
+    amax2(v[i].z, amax, bad);
+    amax2(v[i].w, amax, bad);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
+  }
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
+  if (lane == 0) scale[row] = s;
+  uint2* q = Q + row * kVecs;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    q[lane + 32 * i] = bad ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu)
+                           : make_uint2(codes4(v[i].x, v[i].y, inv), codes4(v[i].z, v[i].w, inv));
+}
+
+cudaError_t launch_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, float* scale, int64_t M, int64_t H,
+                                         float eps, cudaStream_t stream) {
+  // the shared-memory limit is per device: set it once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(rmsnorm_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRqWarps * kRqMaxH * 2);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  if (H == 2048 || H == 4096) {
+    // rows (warps) per block: ceil(M / 152) up to 8, as for the RMSNorm
+    int64_t wpb = (M + 151) / 152;
+    wpb = wpb < 1 ? 1 : (wpb > 8 ? 8 : wpb);
+    const int64_t b2 = (M + wpb - 1) / wpb;
+    if (b2 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    auto kern = H == 2048 ? rmsnorm_quantize_regs_kernel<8> : rmsnorm_quantize_regs_kernel<16>;
+    return launch_overlapped(kern, dim3((unsigned)b2), dim3((unsigned)(32 * wpb)), stream,
+                             static_cast<const uint4*>(X), static_cast<const uint4*>(g), static_cast<uint2*>(Q),
+                             scale, M, eps);
+  }
+  const int64_t blocks = (M + kRqWarps - 1) / kRqWarps;
+  if (blocks > 0x7FFFFFFF || H > kRqMaxH) return cudaErrorInvalidValue;
+  return launch_overlapped_smem(rmsnorm_quantize_kernel, dim3((unsigned)blocks), dim3(32 * kRqWarps),
+                                (size_t)kRqWarps * H * 2, stream, static_cast<const uint4*>(X),
+                                static_cast<const uint4*>(g), static_cast<uint2*>(Q), scale, M, H, eps);
 }
 
 cudaError_t launch_quantize_e4m3(const void* X, void* Q, float* scale, int64_t M, int64_t K,

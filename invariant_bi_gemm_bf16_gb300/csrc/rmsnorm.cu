@@ -18,6 +18,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rowmath.cuh"
 
 namespace bi {
 
@@ -25,48 +26,6 @@ constexpr int kRmsWarps = 8;
 constexpr int64_t kRmsSmCount = 152;  // spreads small batches; any value gives the same bits
 constexpr int kRmsSmemWarps = 2;                                 // rows per block of the shared-memory kernel
 constexpr int64_t kRmsSmemMinRows = kRmsWarps * kRmsSmCount;     // H = 4096, 8192: from full blocks on every SM
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float sumsq8(const uint4& v, float ss) {
-  ss = __fmaf_rn(bf_lo(v.x), bf_lo(v.x), ss);
-  ss = __fmaf_rn(bf_hi(v.x), bf_hi(v.x), ss);
-  ss = __fmaf_rn(bf_lo(v.y), bf_lo(v.y), ss);
-  ss = __fmaf_rn(bf_hi(v.y), bf_hi(v.y), ss);
-  ss = __fmaf_rn(bf_lo(v.z), bf_lo(v.z), ss);
-  ss = __fmaf_rn(bf_hi(v.z), bf_hi(v.z), ss);
-  ss = __fmaf_rn(bf_lo(v.w), bf_lo(v.w), ss);
-  ss = __fmaf_rn(bf_hi(v.w), bf_hi(v.w), ss);
-  return ss;
-}
-
-__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t g, float r) {
-  const float a = __fmul_rn(__fmul_rn(bf_lo(x), r), bf_lo(g));
-  const float b = __fmul_rn(__fmul_rn(bf_hi(x), r), bf_hi(g));
-  __nv_bfloat162 o = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&o);
-}
-
-__device__ __forceinline__ uint4 norm8(const uint4& x, const uint4& g, float r) {
-  uint4 o;
-  o.x = norm2(x.x, g.x, r);
-  o.y = norm2(x.y, g.y, r);
-  o.z = norm2(x.z, g.z, r);
-  o.w = norm2(x.w, g.w, r);
-  return o;
-}
-
-__device__ __forceinline__ float butterfly_sum(float v) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
-__device__ __forceinline__ float inv_rms(float ss, int64_t H, float eps) {
-  const float mean = __fdiv_rn(ss, (float)H);
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-}
 
 // H = 256 * VPL: each lane holds its VPL vectors in registers.
 template <int VPL>

@@ -108,6 +108,14 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert ws >= 4 * 256 * 2 and ws % 256 == 0
     assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, 256, ws - 1, None) == \
         bd.BI_ERR_WORKSPACE
+    # RMSNorm fused with the quantisation: H % 16 == 0 and at most 16384
+    assert lib.bi_rmsnorm_quantize_e4m3(None, None, None, None, 0, 4096, 1e-5, None) == bd.BI_OK
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 48, 64, 2, 4104, 1e-5, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 48, 64, 2, 16384 + 16, 1e-5, None) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 48, 64, 2, 4096, 0.0, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 48, None, 2, 4096, 1e-5, None) == bd.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 48, 66, 2, 4096, 1e-5, None) == bd.BI_ERR_ALIGNMENT
+    assert lib.bi_rmsnorm_quantize_e4m3(16, 32, 40, 64, 2, 4096, 1e-5, None) == bd.BI_ERR_ALIGNMENT
     # GEMM on host buffers: argument, pin and workspace checks before any CUDA call
     assert lib.bi_gemm_bf16_host(None, None, None, 0, 128, 256, None, None, 0, None) == bd.BI_OK
     assert lib.bi_gemm_bf16_host(None, None, None, -1, 128, 256, None, None, 0, None) == bd.BI_ERR_INVALID_ARG

@@ -118,3 +118,27 @@ def test_fp8_rows_independent_of_batch(lib):
         assert np.array_equal(layer(X[:m].contiguous()), full[:m]), m
     perm = torch.randperm(1000, generator=torch.Generator().manual_seed(8))
     assert np.array_equal(layer(X[perm.cuda()].contiguous()), full[perm.numpy()])
+
+
+@pytest.mark.parametrize("M,H", [(1, 4096), (37, 8192), (300, 4096), (5, 16384), (3, 1040), (2000, 2048)])
+def test_rmsnorm_quantize_is_the_composition(lib, oracle, M, H):
+    """One pass gives the codes and scales of bi_quantize_rows_e4m3 applied to
+    bi_rmsnorm_bf16's output, bit for bit, and those are the oracle's
+    quantisation of that output; zero and NaN rows included."""
+    X = inputs.rows_loguniform(M, H, lo=1e-3, hi=1e3, seed=45, stream=0)
+    if M >= 3:
+        X[1] = 0
+        X[2, H // 3] = float("nan")
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=45, stream=2)
+    x, gg = X.cuda(), g.cuda()
+    q, sc = lib.bi_rmsnorm_quantize_e4m3(x, gg, 1e-5)
+    y = lib.bi_rmsnorm_bf16(x, gg, 1e-5)
+    q2, sc2 = lib.bi_quantize_rows_e4m3(y)
+    assert np.array_equal(u8(q), u8(q2))
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), sc2.cpu().numpy().view(np.uint32))
+    want_q, want_s = oracle.quantize_rows_e4m3(bf16_bits(y))
+    assert np.array_equal(u8(q), want_q)
+    got_s, want_s = sc.cpu().numpy(), np.asarray(want_s, dtype=np.float32)
+    assert np.array_equal(np.isnan(got_s), np.isnan(want_s))
+    ok = ~np.isnan(want_s)
+    assert np.array_equal(got_s[ok].view(np.uint32), want_s[ok].view(np.uint32))
