@@ -120,7 +120,8 @@ def test_fp8_rows_independent_of_batch(lib):
     assert np.array_equal(layer(X[perm.cuda()].contiguous()), full[perm.numpy()])
 
 
-@pytest.mark.parametrize("M,H", [(1, 4096), (37, 8192), (300, 4096), (5, 16384), (3, 1040), (2000, 2048)])
+@pytest.mark.parametrize("M,H", [(1, 4096), (37, 8192), (300, 4096), (5, 16384), (3, 1040), (2000, 2048),
+                                 (4100, 4096)])
 def test_rmsnorm_quantize_is_the_composition(lib, oracle, M, H):
     """One pass gives the codes and scales of bi_quantize_rows_e4m3 applied to
     bi_rmsnorm_bf16's output, bit for bit, and those are the oracle's
