@@ -330,6 +330,21 @@ def test_decode_plan_narrows_the_token_tile(bd):
     assert bd.bi_gemm_plan_describe(129, 4096, 14336).tok_tile == 256
 
 
+def test_fp8_decode_plan_narrows_the_token_tile(bd):
+    """The FP8 pins fix T = 256, but with the grouping left open a decode tile
+    runs at T = 64 or 128 with two 128-value K tiles per stage; the tree (K
+    tiles of 128 values, the splits) is the pinned one."""
+    for N, K in ((4096, 14336), (6144, 4096)):
+        ref = bd.bi_gemm_plan_describe_fp8(4096, N, K).tree()
+        for M, T in ((1, 64), (64, 64), (65, 128), (128, 128)):
+            plan = bd.bi_gemm_plan_describe_fp8(M, N, K)
+            if plan.mma_ctas != 1:
+                continue
+            assert (plan.tok_tile, plan.kps, plan.bk) == (T, 2, 128), (N, K, M)
+            assert plan.tree() == ref
+        assert bd.bi_gemm_plan_describe_fp8(129, N, K).tok_tile == 256
+
+
 def test_plan_ktile_pairs(bd):
     """Two K tiles per copy only with the flag, K % 64 == 0, T = 256 and full X boxes."""
     p = bd.bi_pins_default(4096, 14336).replace(mma_ctas=2, flags=bd.BI_FLAG_SCHEDULE_AUTO)
