@@ -705,28 +705,38 @@ BI_API bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_ho
   if (!ok(cudaEventRecord(c.start, s)) || !ok(cudaStreamWaitEvent(c.in, c.start, 0)) ||
       !ok(cudaStreamWaitEvent(c.out, c.start, 0)))
     return BI_ERR_CUDA;
-  for (int64_t ch = 0; ch < chunks; ++ch) {
+  bi_status result = BI_OK;
+  for (int64_t ch = 0; ch < chunks && result == BI_OK; ++ch) {
     const int i = (int)(ch % kHostSlots);
     const int64_t rows = M - ch * R < R ? M - ch * R : R;
     char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
     char* yd = xd + xoff;
     // the slot's previous chunk has been copied out (so also multiplied)
-    if (ch >= kHostSlots && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) return BI_ERR_CUDA;
+    if (ch >= kHostSlots && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) {
+      result = BI_ERR_CUDA;
+      break;
+    }
     if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(X_host) + (uint64_t)ch * R * K * 2, (size_t)rows * K * 2,
                             cudaMemcpyHostToDevice, c.in)) ||
-        !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0)))
-      return BI_ERR_CUDA;
-    st = gemm_impl(xd, W, yd, rows, N, K, pins, s);
-    if (st != BI_OK) return st;
+        !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0))) {
+      result = BI_ERR_CUDA;
+      break;
+    }
+    result = gemm_impl(xd, W, yd, rows, N, K, pins, s);
+    if (result != BI_OK) break;
     if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
         !ok(cudaMemcpyAsync(static_cast<char*>(Y_host) + (uint64_t)ch * R * N * 2, yd, (size_t)rows * N * 2,
                             cudaMemcpyDeviceToHost, c.out)) ||
         !ok(cudaEventRecord(c.copied_out[i], c.out)))
-      return BI_ERR_CUDA;
+      result = BI_ERR_CUDA;
   }
-  // the caller's stream resumes once the last rows are back on the host
-  if (!ok(cudaEventRecord(c.end, c.out)) || !ok(cudaStreamWaitEvent(s, c.end, 0))) return BI_ERR_CUDA;
-  return BI_OK;
+  // the caller's stream resumes once every copy enqueued so far has landed
+  // (also after an error, so that no copy outlives the call's buffers
+  // unseen by the caller's stream)
+  const bool joined_in = ok(cudaEventRecord(c.end, c.in)) && ok(cudaStreamWaitEvent(s, c.end, 0));
+  const bool joined_out = ok(cudaEventRecord(c.end, c.out)) && ok(cudaStreamWaitEvent(s, c.end, 0));
+  if (result == BI_OK && !(joined_in && joined_out)) result = BI_ERR_CUDA;
+  return result;
 }
 
 BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return workspace_bytes(M, K); }
