@@ -21,14 +21,17 @@ Pins (checks against things other than the oracle itself) live in
   - ``bf16_rne``: pinned against hand-derived bit patterns (ties, NaN, overflow).
   - ``silu_mul``, ``residual_add``, ``attention_ctx1``, ``decode_layer``:
     pinned by closed forms (silu(0)=0, large-|x| limits, zero weights give the
-    identity layer, selector weights route v exactly).
+    identity layer, selector weights route v exactly, and selector gate/up and
+    down weights with a gain for the second RMSNorm that differs from the
+    first reproduce a numpy closed form of the MLP half).
   - ``log_softmax``, ``token_logprobs``: pinned by closed forms (uniform rows
     give -log V, two-logit rows the stable softplus form), normalisation
     (sum of exp = 1), shift invariance, -Inf entries and undefined rows.
   - ``e4m3_encode``/``e4m3_decode``, ``quantize_rows_e4m3``, ``gemm_e4m3``:
     pinned by hand-derived codes (1.0, 448, subnormals, ties, saturation,
     NaN), the decode/encode round trip over all codes, exact scales for
-    power-of-two rows, and integer-exact GEMMs.
+    power-of-two rows, integer-exact GEMMs, and non-power-of-two scales for
+    which each other order of applying sx and sw changes the bf16 result.
   - ``decode_attention``: pinned by closed forms (one position gives its
     value row; equal keys or scale 0 give the mean of the values; two
     positions give the logistic form; a dominant key selects its value),

@@ -413,6 +413,118 @@ def test_decode_layer_attention_path_wiring(oracle):
     assert np.array_equal(out, want)
 
 
+def test_decode_layer_mlp_path_wiring(oracle):
+    """The MLP half with non-zero weights, against a numpy closed form.
+
+    Wo = 0 makes the attention half exact (h = x + 0 = x).  g_mlp is not
+    g_attn.  Wgu's gate rows are selectors (gate_j = hn_j) and its up rows
+    selectors of another column (up_j = hn_(j+5) mod 16); Wd is a permutation
+    (d_i = s_(3i+1) mod 16).  Each selected value is one exact product plus
+    zeros, so only RMSNorm_2, SiLU(gate) * up and the residual round.  hn is
+    computed from the RMSNorm definition in numpy float32 (small-integer rows
+    make the sum of squares and the mean exact), silu in fp64.  Wiring slips
+    this catches: RMSNorm_2 skipped (gu = h . Wgu^T), RMSNorm_2 with g_attn,
+    gate and up swapped, and d = gu . Wd^T in place of s . Wd^T."""
+    Hd, nq, nkv, D, I = 16, 2, 1, 8, 16
+    layer = _layer(Hd, nq, nkv, D, I, seed=20, zero=True)
+    g_attn = np.ones(Hd, dtype=np.float32)
+    g_mlp = (0.5 + np.arange(Hd) / 16.0).astype(np.float32)       # exact in bf16, far from 1
+    layer["g_attn"] = inputs.bits(inputs.to_bf16(g_attn))
+    layer["g_mlp"] = inputs.bits(inputs.to_bf16(g_mlp))
+    layer["Wqkv"] = inputs.bits(inputs.to_bf16(np.full(((nq + 2 * nkv) * D, Hd), 0.25, dtype=np.float32)))
+    up_src = [(j + 5) % Hd for j in range(I)]
+    perm = [(3 * i + 1) % I for i in range(Hd)]
+    Wgu = np.zeros((2 * I, Hd), dtype=np.float32)
+    for j in range(I):
+        Wgu[j, j] = 1.0
+        Wgu[I + j, up_src[j]] = 1.0
+    Wd = np.zeros((Hd, I), dtype=np.float32)
+    for i in range(Hd):
+        Wd[i, perm[i]] = 1.0
+    layer["Wgu"] = inputs.bits(inputs.to_bf16(Wgu))
+    layer["Wd"] = inputs.bits(inputs.to_bf16(Wd))
+    # positive integer rows with an RMS far from 1 (so skipping the norm shows)
+    x = np.array([[1 + (3 * k) % 7 for k in range(Hd)],
+                  [8 - (5 * k) % 6 for k in range(Hd)]], dtype=np.float32)
+    xb = inputs.bits(inputs.to_bf16(x))
+    out = oracle.decode_layer(xb, layer, nq, nkv, D, EPS)
+
+    want = []
+    for row in x:
+        ss = np.float32(0.0)
+        for v in row:
+            ss = np.float32(ss + np.float32(v * v))
+        mean = np.float32(ss / np.float32(Hd))
+        r = np.float32(np.float32(1.0) / np.sqrt(np.float32(mean + np.float32(EPS))))
+        hn = bf16_val(bf16_of_f64(((row * r).astype(np.float32) * g_mlp).astype(np.float32).astype(np.float64)))
+        gate = hn[:I].astype(np.float64)
+        up = hn[up_src].astype(np.float64)
+        s = bf16_val(bf16_of_f64(gate / (1.0 + np.exp(-gate)) * up)).astype(np.float64)
+        d = s[perm]
+        want.append(bf16_of_f64(row.astype(np.float64) + d))
+    want = np.array(want, dtype=np.uint16)
+    # silu goes through expf on one side and exp in fp64 on the other: one ulp
+    assert np.abs(ordered(out) - ordered(want)).max() <= 1
+    assert not np.array_equal(out, xb)   # the MLP half changed every row
+
+
+# Three (acc, sx, sw) triples where the three orders of applying the scales
+# give different bf16 results: bf16((acc*sx)*sw) differs from
+# bf16(acc*(sx*sw)) and from bf16((acc*sw)*sx) in fp32.  Found by a search
+# over random fp32 scales and confirmed below with exact rational arithmetic.
+_SCALE_ORDER_CASES = [
+    (3, 0.05462578684091568, 0.9683547019958496),
+    (11, 0.023879144340753555, 1.3570051193237305),
+    (19, 0.05306759104132652, 1.9913160800933838),
+]
+
+
+def _rne_frac(a: Fraction, bits: int) -> Fraction:
+    """Exact round-to-nearest-even of a rational to `bits` significant bits
+    (normal range only)."""
+    if a == 0:
+        return Fraction(0)
+    sign = -1 if a < 0 else 1
+    a = abs(a)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (e - bits + 1)
+    n = a / q
+    fl = math.floor(n)
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * q
+
+
+def test_gemm_e4m3_scale_application_order(oracle):
+    """y = bf16((acc * sx[m]) * sw[n]) with each product rounded to fp32, in
+    that order.  The cases are chosen so that each other order changes the
+    bf16 result; the expected value is derived with exact rationals."""
+    f32 = lambda a: _rne_frac(a, 24)
+    bf = lambda a: _rne_frac(a, 8)
+    # acc as a sum of E4M3-exact integers, each times a weight code of 1
+    parts = {3: [3], 11: [8, 3], 19: [16, 3]}
+    for acc, sx, sw in _SCALE_ORDER_CASES:
+        fsx, fsw = Fraction(float(np.float32(sx))), Fraction(float(np.float32(sw)))
+        assert fsx == Fraction(sx) and fsw == Fraction(sw)   # the scales are fp32 values
+        want = bf(f32(f32(acc * fsx) * fsw))
+        assert want != bf(f32(acc * f32(fsx * fsw)))
+        assert want != bf(f32(f32(acc * fsw) * fsx))
+        vals = parts[acc]
+        vx = np.zeros((1, 32), dtype=np.float32)
+        vw = np.zeros((1, 32), dtype=np.float32)
+        vx[0, :len(vals)] = vals
+        vw[0, :len(vals)] = 1.0
+        qx, qw = oracle.e4m3_encode(vx), oracle.e4m3_encode(vw)
+        yf, yb = oracle.gemm_e4m3(qx, np.array([sx], np.float32), qw, np.array([sw], np.float32))
+        assert yf[0, 0] == acc
+        assert Fraction(float(bf16_val(yb)[0, 0])) == want
+
+
 def test_rmsnorm_single_final_rounding(oracle):
     """The reading adopted for RMSNorm rounds once, after the gain: bf16((x*r)*g).
     The alternative (round x*r to bf16, then multiply by g and round again) gives
