@@ -57,7 +57,7 @@ NCU_TRAFFIC = {
 }
 
 
-def build_fingerprint(kernel_files=("gemm.cu", "ptx.cuh", "internal.h")):
+def build_fingerprint(kernel_files=("gemm_kernel.cuh", "gemm.cu", "ptx.cuh", "internal.h", "rowmath.cuh")):
     """SHA-256 of the sources one kernel is compiled from (default: the GEMM
     kernel's) and the compiler flags: DRAM counters taken by ncu stay valid
     while this is unchanged.  The public header is left out: the kernel uses

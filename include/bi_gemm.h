@@ -7,7 +7,8 @@
  *   RMSNorm   y_h = bf16_rne((x_h * r) * g_h),  r = 1 / sqrt(mean_h(x_h^2) + eps),
  *             per row, with fp32 arithmetic.
  *   Fused     RMSNorm followed by the GEMM, bit for bit equal to the two calls
- *             made one after the other.
+ *             made one after the other, with the normalisation applied to X
+ *             in shared memory: the normalised rows never reach device memory.
  *   Glue      the element-wise steps of a Llama-style decode layer (residual
  *             add, SiLU(gate) * up, and the attention stand-in for a context of
  *             one token).
@@ -44,7 +45,11 @@
  *     an error launched nothing and wrote nothing.
  *   - M == 0 is a successful no-op.
  *   - The library allocates no device memory on any call.  The fused call
- *     takes a caller-provided workspace.
+ *     takes a caller-provided workspace (4 bytes per row).
+ *   - Device addresses of the library's own static device variables (the
+ *     stall word, the no-alloc scratch) are looked up once per device and
+ *     cached; they do not survive cudaDeviceReset, after which the library
+ *     must not be called again in the same process.
  *   - Entry points are reentrant; calls on different streams may overlap.
  */
 #ifndef BI_GEMM_H
@@ -109,8 +114,23 @@ typedef struct CUstream_st* bi_stream_t;
  * otherwise one K tile per copy.  The MMAs consume K tiles one by one in the
  * same order either way, so the flag never changes a bit of Y. */
 #define BI_FLAG_KTILE_PAIRS 0x400u
-#define BI_FLAG_KNOWN_MASK \
-  (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER | BI_FLAG_PREFETCH_W | BI_FLAG_KTILE_PAIRS)
+/* Speed only, read by the fused call (bi_rmsnorm_gemm_bf16 and its no-alloc
+ * form) alone.  The fused call applies the RMSNorm to X in one of two ways,
+ * with the same bits: staged, the standalone RMSNorm kernel writing the
+ * normalised rows to the workspace for the GEMM to read (the default), or in
+ * shared memory, as each X tile arrives for the tensor cores, so that the
+ * normalised rows never reach device memory.  In shared memory the
+ * normalisation is repeated for every W tile that meets an X tile, and each
+ * CTA's first stage waits for the rows' scales; measured on GB300 it is the
+ * slower form at every batch size of the Llama-3.1-8B projections (by about
+ * 2% at one token, 3x at thousands), so it is used only when forced
+ * (BI_FLAG_NORM_SMEM) or when the no-alloc call has no room to stage.  Both
+ * flags set: illegal. */
+#define BI_FLAG_NORM_SMEM 0x800u
+#define BI_FLAG_NORM_STAGED 0x1000u
+#define BI_FLAG_KNOWN_MASK                                                                              \
+  (BI_FLAG_SCHEDULE_MASK | BI_FLAG_DEBUG_STALL_PRODUCER | BI_FLAG_PREFETCH_W | BI_FLAG_KTILE_PAIRS | \
+   BI_FLAG_NORM_SMEM | BI_FLAG_NORM_STAGED)
 
 typedef struct bi_pins {
   int32_t abi_version; /* BI_PINS_ABI_VERSION */
@@ -251,38 +271,65 @@ bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_host, int
 bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
                           bi_stream_t stream);
 
-/* Bytes of workspace bi_rmsnorm_gemm_bf16 needs for M rows of width K. */
+/* Bytes of workspace bi_rmsnorm_gemm_bf16 needs for M rows of width K: one
+ * fp32 value per row, then room for the normalised rows [M,K] bf16 (used by
+ * the staged form only), each part rounded up to 256 bytes.  0 for M = 0. */
 size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K);
 
-/* Y = bi_gemm_bf16(bi_rmsnorm_bf16(X; g, eps), W), bit for bit.  The
- * normalised rows are staged in `workspace` (caller-owned device memory of at
- * least bi_rmsnorm_gemm_workspace_bytes(M, K) bytes, 256-byte aligned; its
- * contents on return are unspecified).  H of the RMSNorm is K.
- * Errors: as the two calls, plus BI_ERR_WORKSPACE. */
+/* Y = bi_gemm_bf16(bi_rmsnorm_bf16(X; g, eps), W), bit for bit, with
+ * X [M,K] the raw activations, g [K] the gain, W [N,K], Y [M,N]; H of the
+ * RMSNorm is K.
+ * Defines: LLM-42 (Enabling Determinism in LLM Inference with Verified
+ * Speculation), Sec. 2.1: the normalisation reduces over the hidden dimension
+ * of each token, so it is row-local and its tree depends on K alone; the
+ * fused layer is read as the composition of the two batch-invariant
+ * operators, through the bf16 normalised rows.
+ * How: by default the standalone RMSNorm kernel writes the normalised rows
+ * to the workspace and the GEMM reads them (the two calls in sequence, on
+ * the caller's stream).  With BI_FLAG_NORM_SMEM, r[m] = 1 / sqrt(mean(x^2) +
+ * eps) of each row is computed first with the RMSNorm's lane partition and
+ * butterfly (the same bits; by the GEMM itself for at most 4 rows, else by a
+ * row-scale kernel), and the GEMM applies bf16_rne((x * r[m]) * g[k]) to each
+ * X tile in shared memory between its arrival and the tensor-core reads, so
+ * the normalised rows never reach device memory.  Both forms give the same
+ * bits.
+ * Workspace: room for r and for the staged rows, in `workspace` (caller-owned device memory of at least
+ * bi_rmsnorm_gemm_workspace_bytes(M, K) bytes, 256-byte aligned; its contents
+ * on return are unspecified).  The library allocates nothing, so the caller
+ * provides it; bi_rmsnorm_gemm_bf16_noalloc takes none.
+ * Errors: as the two calls, plus BI_ERR_WORKSPACE.  Everything is checked and
+ * the GEMM planned before the first kernel is launched. */
 bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void* Y, int64_t M,
                                int64_t N, int64_t K, float eps, const bi_pins* pins,
                                void* workspace, size_t workspace_bytes, bi_stream_t stream);
 
 /* Capacity in bytes of the static scratch array used by
- * bi_rmsnorm_gemm_bf16_noalloc: M * K * 2 must not exceed it. */
+ * bi_rmsnorm_gemm_bf16_noalloc: r takes 4 bytes per row (rounded up to 256),
+ * so M may not exceed 4194240; the staged form also needs M * K * 2 bytes. */
 #define BI_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/* BI_NOALLOC_SCRATCH_BYTES as compiled into the library (for bindings that
+ * do not read this header). */
+size_t bi_noalloc_scratch_bytes(void);
 
 /* The fused layer for callers that cannot allocate device memory -- for
  * example a plugin inside a host runtime that has reserved the device's memory
  * and offers no allocator, or a latency-critical path where cudaMalloc /
  * cudaFree would synchronise the device.  Same arguments, result and bits as
- * bi_rmsnorm_gemm_bf16, but no workspace: the normalised rows are staged in a
- * static device array of BI_NOALLOC_SCRATCH_BYTES that the library holds on
- * every GPU that loads it, until the process exits.  The call allocates
- * nothing.
+ * bi_rmsnorm_gemm_bf16, but no workspace: the per-row RMSNorm scales (and
+ * the staged normalised rows, when that form is used) are kept in a static
+ * device array of BI_NOALLOC_SCRATCH_BYTES that the library holds on every
+ * GPU that loads it, until the process exits.  Where the staged rows would
+ * not fit, the rows are normalised in shared memory instead (same bits).  The
+ * call allocates nothing.
  *   - The first call on a device looks the array's address up (with that
  *     device current) and caches it; make that first call before any stream
- *     capture.
+ *     capture.  The cache does not survive cudaDeviceReset.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents; calls whose work overlaps on the GPU (e.g. on two streams)
  *     race on it and must be serialised by the caller.
- * Errors: as bi_rmsnorm_gemm_bf16; BI_ERR_WORKSPACE when M * K * 2 exceeds
- * BI_NOALLOC_SCRATCH_BYTES (nothing is launched).
+ * Errors: as bi_rmsnorm_gemm_bf16; BI_ERR_WORKSPACE when M * 4 (rounded up
+ * to 256) exceeds BI_NOALLOC_SCRATCH_BYTES (nothing is launched).
  * The paper has no counterpart to this entry point. */
 bi_status bi_rmsnorm_gemm_bf16_noalloc(const void* X, const void* g, const void* W, void* Y,
                                        int64_t M, int64_t N, int64_t K, float eps,

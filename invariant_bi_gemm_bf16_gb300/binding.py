@@ -39,6 +39,8 @@ BI_FLAG_SCHEDULE_CHAIN = 0x3
 BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
 BI_FLAG_PREFETCH_W = 0x200
 BI_FLAG_KTILE_PAIRS = 0x400
+BI_FLAG_NORM_SMEM = 0x800
+BI_FLAG_NORM_STAGED = 0x1000
 
 
 class Pins(ctypes.Structure):
@@ -117,6 +119,7 @@ _SIGNATURES = {
                                             ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
     "bi_rmsnorm_gemm_bf16_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
                                                     ctypes.POINTER(Pins), _vp]),
+    "bi_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "bi_residual_add_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "bi_silu_mul_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
@@ -169,6 +172,13 @@ def _stream(stream=None) -> int:
     return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
 
 
+def _on_current_device(t: torch.Tensor, name: str):
+    # the library runs on the current device and reads every pointer there
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("%s is on %s, but the current CUDA device is cuda:%d" %
+                         (name, t.device, torch.cuda.current_device()))
+
+
 def _dev(t: torch.Tensor, name: str, shape=None) -> int:
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
@@ -176,6 +186,7 @@ def _dev(t: torch.Tensor, name: str, shape=None) -> int:
         raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    _on_current_device(t, name)
     return t.data_ptr()
 
 
@@ -268,11 +279,10 @@ def bi_gemm_bf16_host(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None
     need = bi_gemm_bf16_host_workspace_bytes(M, N, K)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=w.device)
-    if not workspace.is_cuda or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_ptr, ws_bytes = _workspace(workspace)
     st = load().bi_gemm_bf16_host(_host(x, "x", (M, K)), _dev(w, "w"), _host(out, "out", (M, N)), M, N, K,
-                                  ctypes.byref(pins) if pins is not None else None, workspace.data_ptr(),
-                                  workspace.numel() * workspace.element_size(), _stream(stream))
+                                  ctypes.byref(pins) if pins is not None else None, ws_ptr, ws_bytes,
+                                  _stream(stream))
     _check(st, "bi_gemm_bf16_host")
     if _call_hooks:
         _report(M, N, K)
@@ -293,6 +303,13 @@ def bi_rmsnorm_bf16(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-5, out: to
     return out
 
 
+def _workspace(ws: torch.Tensor, name: str = "workspace") -> tuple:
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _on_current_device(ws, name)
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
 def bi_rmsnorm_gemm_workspace_bytes(M: int, K: int) -> int:
     return int(load().bi_rmsnorm_gemm_workspace_bytes(M, K))
 
@@ -310,28 +327,30 @@ def bi_rmsnorm_gemm_bf16(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, eps:
     need = bi_rmsnorm_gemm_workspace_bytes(M, K)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
-    if not workspace.is_cuda or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA tensor")
-    ws_bytes = workspace.numel() * workspace.element_size()
+    ws_ptr, ws_bytes = _workspace(workspace)
     st = load().bi_rmsnorm_gemm_bf16(_dev(x, "x"), _dev(g, "g", (K,)), _dev(w, "w"),
                                      _dev(out, "out", (M, N)), M, N, K, float(eps),
                                      ctypes.byref(pins) if pins is not None else None,
-                                     workspace.data_ptr(), ws_bytes, _stream(stream))
+                                     ws_ptr, ws_bytes, _stream(stream))
     _check(st, "bi_rmsnorm_gemm_bf16")
     if _call_hooks:
         _report(M, N, K)
     return out
 
 
-BI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+def bi_noalloc_scratch_bytes() -> int:
+    """Capacity of the library's static scratch array (BI_NOALLOC_SCRATCH_BYTES
+    as compiled into the library)."""
+    return int(load().bi_noalloc_scratch_bytes())
 
 
 def bi_rmsnorm_gemm_bf16_noalloc(x: torch.Tensor, g: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
                                  eps: float = 1e-5, pins: Pins | None = None, stream=None) -> torch.Tensor:
     """The fused layer for callers that cannot allocate device memory: the
-    caller passes the output, and the normalised rows are staged in the
-    library's static device array (M*K*2 <= BI_NOALLOC_SCRATCH_BYTES).  Calls
-    that overlap on the GPU race on that array."""
+    caller passes the output, and each row's RMSNorm scale (and the staged
+    normalised rows, where they fit) is kept in the library's static device
+    array (M * 4 <= bi_noalloc_scratch_bytes()).  Calls that overlap on the
+    GPU race on that array."""
     if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
         raise ValueError("expected x [M,K] and w [N,K]")
     M, K = x.shape
@@ -363,6 +382,7 @@ def _dev_as(t: torch.Tensor, name: str, dtype, shape) -> int:
         raise ValueError("%s must be a contiguous %s CUDA tensor" % (name, dtype))
     if tuple(t.shape) != tuple(shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    _on_current_device(t, name)
     return t.data_ptr()
 
 
@@ -444,9 +464,8 @@ def bi_log_softmax_bf16(x: torch.Tensor, out: torch.Tensor | None = None, stream
     M, V = x.shape
     if out is None:
         out = torch.empty((M, V), dtype=torch.float32, device=x.device)
-    if out.dtype != torch.float32 or not out.is_cuda or not out.is_contiguous() or tuple(out.shape) != (M, V):
-        raise ValueError("out must be a contiguous fp32 CUDA tensor [M,V]")
-    st = load().bi_log_softmax_bf16(_dev(x, "x"), out.data_ptr(), M, V, _stream(stream))
+    st = load().bi_log_softmax_bf16(_dev(x, "x"), _dev_as(out, "out", torch.float32, (M, V)), M, V,
+                                    _stream(stream))
     _check(st, "bi_log_softmax_bf16")
     return out
 
@@ -457,13 +476,10 @@ def bi_token_logprobs_bf16(x: torch.Tensor, ids: torch.Tensor, out: torch.Tensor
     if x.dim() != 2:
         raise ValueError("expected x [M,V]")
     M, V = x.shape
-    if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous() or tuple(ids.shape) != (M,):
-        raise ValueError("ids must be a contiguous int32 CUDA tensor [M]")
     if out is None:
         out = torch.empty(M, dtype=torch.float32, device=x.device)
-    if out.dtype != torch.float32 or not out.is_cuda or tuple(out.shape) != (M,):
-        raise ValueError("out must be an fp32 CUDA tensor [M]")
-    st = load().bi_token_logprobs_bf16(_dev(x, "x"), ids.data_ptr(), out.data_ptr(), M, V, _stream(stream))
+    st = load().bi_token_logprobs_bf16(_dev(x, "x"), _dev_i32(ids, "ids", (M,)),
+                                       _dev_as(out, "out", torch.float32, (M,)), M, V, _stream(stream))
     _check(st, "bi_token_logprobs_bf16")
     return out
 
@@ -515,6 +531,7 @@ def _dev_i32(t: torch.Tensor, name: str, shape=None) -> int:
         raise ValueError("%s must be a contiguous int32 CUDA tensor" % name)
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    _on_current_device(t, name)
     return t.data_ptr()
 
 
@@ -541,13 +558,11 @@ def bi_decode_attention_bf16(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
     need = bi_decode_attention_workspace_bytes(B, Hq, Hkv, max_seq_len, split_size)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    if not workspace.is_cuda or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_ptr, ws_bytes = _workspace(workspace)
     st = load().bi_decode_attention_bf16(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache", tuple(k_cache.shape)),
         _dev_i32(block_table, "block_table", (B, block_table.shape[1])), block_table.shape[1],
         _dev_i32(seq_lens, "seq_lens", (B,)), _dev(out, "out", (B, Hq, D)), B, Hq, Hkv, D, num_pages,
-        page_size, int(max_seq_len), int(split_size), float(scale), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream(stream))
+        page_size, int(max_seq_len), int(split_size), float(scale), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "bi_decode_attention_bf16")
     return out

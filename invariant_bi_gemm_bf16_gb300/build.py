@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbi_gemm.so")
-SOURCES = ["api.cu", "gemm.cu", "rmsnorm.cu", "glue.cu", "noalloc.cu", "logsoftmax.cu", "quant.cu", "attention.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "attention.h", "rowmath.cuh"]
+SOURCES = ["api.cu", "gemm.cu", "gemm_fused.cu", "rmsnorm.cu", "glue.cu", "noalloc.cu", "logsoftmax.cu", "quant.cu", "attention.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "attention.h", "rowmath.cuh", "gemm_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",

@@ -367,6 +367,7 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p, Elem e = Elem::BF16) 
     }
   }
   if (p->flags & ~BI_FLAG_KNOWN_MASK) return BI_ERR_ILLEGAL_PINS;
+  if ((p->flags & BI_FLAG_NORM_SMEM) && (p->flags & BI_FLAG_NORM_STAGED)) return BI_ERR_ILLEGAL_PINS;
   const uint32_t sched = p->flags & BI_FLAG_SCHEDULE_MASK;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * (p->mma_ctas == 2 ? 2 : 1) > 16)
     return BI_ERR_ILLEGAL_PINS;
@@ -426,6 +427,18 @@ bi_status resolve_pins(int64_t N, int64_t K, const bi_pins* pins, Resolved* r, E
   return BI_OK;
 }
 
+bi_status check_rmsnorm_args(const void* X, const void* g, const void* Y, int64_t M, int64_t H,
+                             float eps) {
+  if (M < 0 || H < 1) return BI_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !(eps < 3.0e38f)) return BI_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > 65536) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return BI_OK;
+  if (!X || !g || !Y) return BI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(g) || !aligned16(Y)) return BI_ERR_ALIGNMENT;
+  return BI_OK;
+}
+
 bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M, int64_t N,
                           int64_t K, Elem e = Elem::BF16) {
   if (M < 0) return BI_ERR_INVALID_ARG;
@@ -438,8 +451,10 @@ bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M
   return BI_OK;
 }
 
-bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
-                    const bi_pins* pins, cudaStream_t stream, Elem e = Elem::BF16,
+// Step 1 of a GEMM launch: argument checks, pins and the plan, with no CUDA
+// call.  L->M == 0 means there is nothing to launch.
+bi_status plan_gemm(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                    const bi_pins* pins, cudaStream_t stream, GemmLaunch* out, Elem e = Elem::BF16,
                     const float* sx = nullptr, const float* sw = nullptr) {
   bi_status st = check_gemm_args(X, W, Y, M, N, K, e);
   if (st != BI_OK) return st;
@@ -450,18 +465,14 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   Resolved r;
   st = resolve_pins(N, K, pins, &r, e);
   if (st != BI_OK) return st;
+  GemmLaunch& L = *out;
+  std::memset(&L, 0, sizeof(L));
   if (M == 0) return BI_OK;
   bi_gemm_plan plan;
   st = make_plan(M, N, K, r, sm_count_current(), &plan);
   if (st != BI_OK) return st;
-  GemmLaunch L;
-  std::memset(&L, 0, sizeof(L));
-  // two K tiles per copy (3-D maps) on paired MMAs; single-CTA MMAs with two
-  // K tiles per stage take them as two 2-D copies
-  const bool copy2d = plan.kps > 1 && plan.mma_ctas == 1;
-  const bool map3d = plan.kps > 1 && !copy2d;
-  if (!encode_kmajor(&L.tmW, W, N, K, kTileN, map3d, map3d ? plan.kps : 1, e)) return BI_ERR_CUDA;
-  if (!encode_kmajor(&L.tmX, X, M, K, plan.x_box_rows, map3d, map3d ? plan.kps : 1, e)) return BI_ERR_CUDA;
+  L.X = X;
+  L.W = W;
   L.fp8 = e == Elem::E4M3;
   L.sx = sx;
   L.sw = sw;
@@ -487,29 +498,96 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.grid_z = plan.grid_z;
   L.smem = plan.smem_bytes;
   L.flags = r.flags;
+  // two K tiles per copy (3-D maps) on paired MMAs; single-CTA MMAs with two
+  // K tiles per stage take them as two 2-D copies
+  if (plan.kps > 1 && plan.mma_ctas == 1) L.flags |= kFlagCopy2D;
   if (plan.x_box_rows < plan.tok_tile / plan.mma_ctas) L.flags |= kFlagZeroX;
-  if (copy2d) L.flags |= kFlagCopy2D;
   if (plan.m_tiles == 1) L.flags |= kFlagStreamW;
   L.stream = stream;
-  return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
-}
-
-bi_status check_rmsnorm_args(const void* X, const void* g, const void* Y, int64_t M, int64_t H,
-                             float eps) {
-  if (M < 0 || H < 1) return BI_ERR_INVALID_ARG;
-  if (!(eps > 0.0f) || !(eps < 3.0e38f)) return BI_ERR_INVALID_ARG;
-  if (H % 8 != 0 || H > 65536) return BI_ERR_UNSUPPORTED_SHAPE;
-  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
-  if (M == 0) return BI_OK;
-  if (!X || !g || !Y) return BI_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(g) || !aligned16(Y)) return BI_ERR_ALIGNMENT;
   return BI_OK;
 }
 
-size_t workspace_bytes(int64_t M, int64_t K) {
+// Step 2: the tensor maps and the status word (driver calls, no launch).
+bi_status encode_gemm(GemmLaunch& L) {
+  const Elem e = L.fp8 ? Elem::E4M3 : Elem::BF16;
+  const bool map3d = L.kps > 1 && !(L.flags & kFlagCopy2D);
+  if (!encode_kmajor(&L.tmW, L.W, L.N, L.K, kTileN, map3d, map3d ? L.kps : 1, e)) return BI_ERR_CUDA;
+  if (!encode_kmajor(&L.tmX, L.X, L.M, L.K, L.x_box_rows, map3d, map3d ? L.kps : 1, e)) return BI_ERR_CUDA;
+  L.status = device_status_word();
+  if (!L.status) return BI_ERR_CUDA;
+  return BI_OK;
+}
+
+}  // namespace
+
+// The RMSNorm -> GEMM layer, checked and planned (no CUDA call): X [M,K] raw
+// activations, g [K], W [N,K], Y [M,N].
+bi_status plan_fused(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L) {
+  bi_status st = check_gemm_args(X, W, Y, M, N, K);
+  if (st != BI_OK) return st;
+  st = check_rmsnorm_args(X, g, Y, M, K, eps);
+  if (st != BI_OK) return st;
+  st = plan_gemm(X, W, Y, M, N, K, pins, stream, L);
+  if (st != BI_OK) return st;
+  L->g = g;
+  L->eps = eps;
+  return BI_OK;
+}
+
+// The staged form unless the pins force shared memory: measured faster on
+// GB300 at every batch size of the Llama-3.1-8B projections.
+bool fused_in_smem(const GemmLaunch& L) { return (L.flags & BI_FLAG_NORM_SMEM) != 0; }
+
+size_t fused_r_bytes(int64_t M) { return (size_t)(((uint64_t)M * 4u + 255u) & ~(uint64_t)255u); }
+
+size_t fused_staged_bytes(int64_t M, int64_t K) {
+  return (size_t)(((uint64_t)M * (uint64_t)K * 2u + 255u) & ~(uint64_t)255u);
+}
+
+size_t fused_workspace_bytes(int64_t M, int64_t K) {
   if (M <= 0 || K <= 0) return 0;
-  const uint64_t b = (uint64_t)M * (uint64_t)K * 2u;
-  return (size_t)((b + 255u) & ~(uint64_t)255u);
+  return fused_r_bytes(M) + fused_staged_bytes(M, K);
+}
+
+// Encodes the planned layer's tensor maps, then launches it.  In shared
+// memory: the row-scale kernel (r[m] of every row into the workspace's
+// first part) and the GEMM that normalises X in shared memory with it.
+// Staged: the RMSNorm kernel writes the normalised rows to the workspace's
+// second part and the GEMM reads them.  An encoding failure returns before
+// the first launch.
+bi_status launch_fused(GemmLaunch& L, void* ws, bool in_smem) {
+  if (L.M == 0) return BI_OK;
+  const void* X = L.X;
+  if (!in_smem) L.X = static_cast<char*>(ws) + fused_r_bytes(L.M);
+  bi_status st = encode_gemm(L);
+  if (st != BI_OK) return st;
+  if (!in_smem) {
+    if (launch_rmsnorm(X, L.g, const_cast<void*>(L.X), L.M, L.K, L.eps, L.stream) != cudaSuccess)
+      return BI_ERR_CUDA;
+    return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+  }
+  if (L.M <= kRowScaleInKernelMax && L.m_tiles == 1) {
+    L.rrow = nullptr;  // the GEMM computes the few rows' r itself: one launch
+    return launch_gemm_fused(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+  }
+  float* r = static_cast<float*>(ws);
+  L.rrow = r;
+  if (launch_row_scale(X, r, L.M, L.K, L.eps, L.stream) != cudaSuccess) return BI_ERR_CUDA;
+  return launch_gemm_fused(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+namespace {
+
+bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                    const bi_pins* pins, cudaStream_t stream, Elem e = Elem::BF16,
+                    const float* sx = nullptr, const float* sw = nullptr) {
+  GemmLaunch L;
+  bi_status st = plan_gemm(X, W, Y, M, N, K, pins, stream, &L, e, sx, sw);
+  if (st != BI_OK || L.M == 0) return st;
+  st = encode_gemm(L);
+  if (st != BI_OK) return st;
+  return launch_gemm(L) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
 // ---- the GEMM on host buffers: rows in chunks through a ring of device buffers
@@ -739,25 +817,18 @@ BI_API bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_ho
   return result;
 }
 
-BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return workspace_bytes(M, K); }
+BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return fused_workspace_bytes(M, K); }
 
 BI_API bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void* Y,
                                       int64_t M, int64_t N, int64_t K, float eps,
                                       const bi_pins* pins, void* workspace, size_t ws_bytes,
                                       bi_stream_t stream) {
-  bi_status st = check_gemm_args(X, W, Y, M, N, K);
-  if (st != BI_OK) return st;
-  st = check_rmsnorm_args(X, g, workspace ? workspace : Y, M, K, eps);
-  if (st != BI_OK) return st;
-  Resolved r;
-  st = resolve_pins(N, K, pins, &r);
-  if (st != BI_OK) return st;
-  if (M == 0) return BI_OK;
-  if (!workspace || ws_bytes < workspace_bytes(M, K)) return BI_ERR_WORKSPACE;
+  GemmLaunch L;
+  bi_status st = plan_fused(X, g, W, Y, M, N, K, eps, pins, reinterpret_cast<cudaStream_t>(stream), &L);
+  if (st != BI_OK || L.M == 0) return st;
+  if (!workspace || ws_bytes < fused_workspace_bytes(M, K)) return BI_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_rmsnorm(X, g, workspace, M, K, eps, s) != cudaSuccess) return BI_ERR_CUDA;
-  return gemm_impl(workspace, W, Y, M, N, K, pins, s);
+  return launch_fused(L, workspace, fused_in_smem(L));
 }
 
 BI_API bi_status bi_residual_add_bf16(const void* a, const void* b, void* out, int64_t count,

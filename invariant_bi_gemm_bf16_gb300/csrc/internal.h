@@ -17,6 +17,12 @@ constexpr int kMmaK = 16;          // K per tcgen05.mma.kind::f16 instruction
 constexpr int kEpiWarps = 16;      // epilogue warps (four per TMEM lane quadrant)
 constexpr int kFirstEpiWarp = 3;   // warps 0..2: W producer, MMA issuer, X producer
 constexpr int kGemmThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kXformWarps = 4;     // fused RMSNorm prologue: warps that normalise X stages
+constexpr int kFirstXformWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int gemm_threads(bool fused) { return kGemmThreads + (fused ? 32 * kXformWarps : 0); }
+// Fused layer, in shared memory: up to this many rows, the GEMM computes the
+// rows' RMSNorm scales itself instead of a separate row-scale kernel.
+constexpr int kRowScaleInKernelMax = 4;
 constexpr int kMaxStages = 16;
 constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 
@@ -55,6 +61,12 @@ struct GemmLaunch {
   bool fp8;          // E4M3 operands (kind::f8f6f4), K tiles of 128 values; Y scaled by sx, sw
   const float* sx;   // fp8: per-token scales [M]
   const float* sw;   // fp8: per-channel scales [N]
+  const void* X;     // operands, for the tensor maps
+  const void* W;
+  const void* g;     // fused: RMSNorm gain [K] (bf16)
+  float eps;         // fused: RMSNorm epsilon
+  const float* rrow; // fused: per-row r = 1 / sqrt(mean(x^2) + eps) [M], or nullptr (computed in the GEMM)
+  int* status;       // device status word (bounded waits report there)
   bool cluster;      // one chain per CTA (pair), folded through DSMEM
   bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;
@@ -98,10 +110,17 @@ cudaError_t launch_overlapped_smem(void (*kern)(KArgs...), dim3 grid, dim3 block
 }
 
 
-// Device address of the status word that bi_last_device_status() reads.
+// Device address of the status word that bi_last_device_status() reads
+// (looked up once per device).
 int* device_status_word();
 
 cudaError_t launch_gemm(const GemmLaunch& L);
+// The GEMM with the RMSNorm prologue applied to X in shared memory (L.g and
+// L.rrow set; bf16 only).
+cudaError_t launch_gemm_fused(const GemmLaunch& L);
+// r[m] = 1 / sqrt(mean_h(x[m,h]^2) + eps) of each row of X [M,H], by the
+// lane partition and butterfly of the RMSNorm kernels (the same bits).
+cudaError_t launch_row_scale(const void* X, float* r, int64_t M, int64_t H, float eps, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const void* X, const void* g, void* Y, int64_t M, int64_t H, float eps,
                            cudaStream_t stream);
 cudaError_t launch_residual_add(const void* a, const void* b, void* out, int64_t count,
@@ -114,6 +133,26 @@ cudaError_t launch_token_logprobs(const void* X, const int32_t* ids, float* out,
                                   cudaStream_t stream);
 cudaError_t launch_attention_ctx1(const void* qkv, void* out, int64_t M, int64_t nq, int64_t nkv,
                                   int64_t D, cudaStream_t stream);
+// The fused RMSNorm -> GEMM layer in two steps, so that a caller can check
+// and plan everything before it launches anything.  plan_fused checks the
+// arguments (as bi_rmsnorm_gemm_bf16, less the workspace), resolves the pins
+// and plans the GEMM, with no CUDA call; L->M == 0 means nothing to do.
+// launch_fused encodes the tensor maps (returning BI_ERR_CUDA before any
+// launch if that fails) and launches the layer in one of its two forms:
+// in shared memory (r in the first fused_r_bytes(M) bytes of `ws`) or staged
+// (r's part unused, the normalised rows in the fused_staged_bytes(M, K) bytes
+// after it).
+bi_status plan_fused(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L);
+bi_status launch_fused(GemmLaunch& L, void* ws, bool in_smem);
+// The form the pins choose: in shared memory with BI_FLAG_NORM_SMEM, else staged.
+bool fused_in_smem(const GemmLaunch& L);
+// Workspace bytes: r (4 bytes a row), the staged rows (M * K * 2), and both,
+// each part rounded up to 256.
+size_t fused_r_bytes(int64_t M);
+size_t fused_staged_bytes(int64_t M, int64_t K);
+size_t fused_workspace_bytes(int64_t M, int64_t K);
+
 // Reads and clears the current device's stall word (asynchronously on
 // `stream`; the caller synchronises).
 cudaError_t fetch_and_clear_stall(int* host_dst, cudaStream_t stream);

@@ -144,6 +144,44 @@ __global__ void __launch_bounds__(32 * kRmsWarps)
   for (int64_t i = lane; i < nvec; i += 32) y[i] = norm8(x[i], __ldg(g + i), r);
 }
 
+// r[m] = 1 / sqrt(ss / H + eps) of each row, for the GEMM that applies the
+// RMSNorm to X in shared memory.  The lane partition, the order of the
+// squares within a lane and the butterfly are those of the kernels above
+// (vectors lane, lane + 32, ... in ascending order, each vector's 8 values in
+// order), so r has their bits.  Eight vector loads per lane are issued before
+// they are summed, in the same order.
+__global__ void __launch_bounds__(32 * kRmsWarps)
+    row_scale_kernel(const uint4* X, float* R, int64_t M, int64_t H, float eps) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int64_t nvec = H / 8;
+  const uint4* x = X + row * nvec;
+  float ss = 0.0f;
+  int64_t i = lane;
+  for (; i + 32 * 7 < nvec; i += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = x[i + 32 * j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = sumsq8(v[j], ss);
+  }
+  for (; i < nvec; i += 32) ss = sumsq8(x[i], ss);
+  ss = butterfly_sum(ss);
+  if (lane == 0) R[row] = inv_rms(ss, H, eps);
+}
+
+cudaError_t launch_row_scale(const void* X, float* r, int64_t M, int64_t H, float eps, cudaStream_t stream) {
+  int64_t wpb = (M + kRmsSmCount - 1) / kRmsSmCount;
+  wpb = wpb < 1 ? 1 : (wpb > kRmsWarps ? kRmsWarps : wpb);
+  const int64_t blocks = (M + wpb - 1) / wpb;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_overlapped(row_scale_kernel, dim3((unsigned)blocks), dim3((unsigned)(32 * wpb)), stream,
+                           static_cast<const uint4*>(X), r, M, H, eps);
+}
+
 // Kernel per width and batch size, measured on GB300 as fractions of the
 // copy bandwidth at M = 16384: registers for H <= 2048 (2048: 1.00); for
 // H = 4096 and 8192 the row in shared memory from full blocks on every SM

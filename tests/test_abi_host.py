@@ -105,8 +105,20 @@ def test_null_and_bad_arguments_rejected_before_any_launch(bd):
     assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, None, 0, None) == \
         bd.BI_ERR_WORKSPACE
     ws = bd.bi_rmsnorm_gemm_workspace_bytes(4, 256)
-    assert ws >= 4 * 256 * 2 and ws % 256 == 0
+    assert ws >= 4 * 4 + 4 * 256 * 2 and ws % 256 == 0     # r, then room for the staged rows
+    assert bd.bi_rmsnorm_gemm_workspace_bytes(1000, 4096) == 4096 + 1000 * 4096 * 2
+    assert bd.bi_rmsnorm_gemm_workspace_bytes(0, 4096) == 0
+    # the two forms of the fused layer cannot both be forced
+    both = p.replace(flags=p.flags | bd.BI_FLAG_NORM_SMEM | bd.BI_FLAG_NORM_STAGED)
+    assert lib.bi_pins_validate(128, 256, ctypes.byref(both)) == bd.BI_ERR_ILLEGAL_PINS
+    for one in (bd.BI_FLAG_NORM_SMEM, bd.BI_FLAG_NORM_STAGED):
+        assert lib.bi_pins_validate(128, 256, ctypes.byref(p.replace(flags=p.flags | one))) == bd.BI_OK
     assert lib.bi_rmsnorm_gemm_bf16(16, 32, 48, 64, 4, 128, 256, 1e-5, None, 256, ws - 1, None) == \
+        bd.BI_ERR_WORKSPACE
+    # the no-alloc capacity: one fp32 per row, refused before any CUDA call
+    cap = lib.bi_noalloc_scratch_bytes()
+    assert cap == 16 * 1024 * 1024
+    assert lib.bi_rmsnorm_gemm_bf16_noalloc(16, 32, 48, 64, cap // 4 + 1, 128, 64, 1e-5, None, None) == \
         bd.BI_ERR_WORKSPACE
     # RMSNorm fused with the quantisation: H % 16 == 0 and at most 16384
     assert lib.bi_rmsnorm_quantize_e4m3(None, None, None, None, 0, 4096, 1e-5, None) == bd.BI_OK

@@ -3,7 +3,7 @@
 bi_rmsnorm_gemm_bf16_noalloc serves callers with no allocator of their own
 (for instance a plugin inside a host runtime that has reserved all device
 memory up front, or a latency-critical path where cudaMalloc/cudaFree would
-synchronise the device).  It stages the normalised rows in the library's
+synchronise the device).  It keeps each row's RMSNorm scale in the library's
 static device array instead of a caller workspace.  Its output must match the
 workspace entry point bi_rmsnorm_gemm_bf16 on two calls in a row (the array
 keeps the previous call's contents), and an oversized call must be refused
@@ -26,7 +26,10 @@ def _problem(M, N, K, seed):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(lib):
-    cases = [(37, 640, 4096, 1), (300, 384, 1024, 2)]   # the second call reuses the array
+    # in shared memory; staged in the array (the second call reuses it); and a
+    # batch whose staged rows would not fit the array, normalised in shared
+    # memory instead
+    cases = [(37, 640, 4096, 1), (300, 384, 1024, 2), (2100, 256, 4096, 3)]
     for M, N, K, seed in cases:
         X, g, W = _problem(M, N, K, seed)
         want = lib.bi_rmsnorm_gemm_bf16(X, g, W, EPS)
@@ -50,13 +53,13 @@ def test_noalloc_allocates_nothing_and_refuses_oversize(lib):
     lib.bi_rmsnorm_gemm_bf16_noalloc(X, g, W, out, EPS)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free_before
-    # M * K * 2 above the static capacity: refused, output untouched
-    Kb = 4096
-    Mb = lib.BI_NOALLOC_SCRATCH_BYTES // (Kb * 2) + 1
+    # one fp32 value per row: M * 4 above the static capacity is refused, output untouched
+    Kb, Nb = 8, 8
+    Mb = lib.bi_noalloc_scratch_bytes() // 4 + 1
     xb = torch.zeros((Mb, Kb), dtype=torch.bfloat16, device="cuda")
     gb = torch.ones(Kb, dtype=torch.bfloat16, device="cuda")
-    wb = torch.zeros((128, Kb), dtype=torch.bfloat16, device="cuda")
-    ob = torch.full((Mb, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    wb = torch.zeros((Nb, Kb), dtype=torch.bfloat16, device="cuda")
+    ob = torch.full((Mb, Nb), 5.0, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(lib.BiError) as e:
         lib.bi_rmsnorm_gemm_bf16_noalloc(xb, gb, wb, ob, EPS)
     assert e.value.status == lib.BI_ERR_WORKSPACE
