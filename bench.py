@@ -1,7 +1,7 @@
 """Benchmark of the batch-invariant linear layer on GB300.
 
 Default workload (one GPU): the Llama-3.1-8B down_proj GEMM, W [4096, 14336],
-swept over M = 1, 2, 4, ..., 8192 tokens.  One step = one bi_gemm_bf16 call at
+swept over M = 1, 2, 4, ..., 8192 tokens.  One step = one bi_gemm_bf16_ws call at
 every M of the sweep.  `value` = the sweep's FLOPs / its device time (TFLOPS).
 Per-M times, TFLOPS, GB/s, roofline fractions and the torch.mm (cuBLAS) time on
 the same tensors are in "sweep".
@@ -327,6 +327,10 @@ class DownProjSweep:
         # the weight copies are never written while the sweep runs
         self.pins = bd.bi_pins_default(self.N, self.K)
         self.pins = self.pins.replace(flags=self.pins.flags | bd.BI_FLAG_PREFETCH_W)
+        # one fold workspace for every M (bi_gemm_bf16_ws): its counters are
+        # zeroed once and every call leaves them zero
+        fold = max(bd.bi_gemm_bf16_workspace_bytes(M, self.N, self.K, self.pins) for M in self.ms)
+        self.ws = torch.zeros(max(fold, 256), dtype=torch.uint8, device=dev)
         self.it = 0
 
     def launches_per_step(self):
@@ -342,7 +346,7 @@ class DownProjSweep:
             if use_torch:
                 torch.mm(x, w.t(), out=self.Y[M])
             else:
-                self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins)
+                self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins, workspace=self.ws)
             if events is not None:
                 events[j][1].record()
             self.it += 1
@@ -385,7 +389,7 @@ class DownProjSweep:
         if use_torch:
             torch.mm(x, w.t(), out=self.Y[M])
         else:
-            self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins)
+            self.bd.bi_gemm_bf16(x, w, out=self.Y[M], pins=self.pins, workspace=self.ws)
 
     def work(self):
         f = sum(gemm_work(M, self.N, self.K)[0] for M in self.ms)
@@ -563,7 +567,9 @@ def run_fused(args, dist, peaks):
             xs = [inputs.device_normal((M, K), seed=dist.rank, stream=inputs.STREAM_X + 16 * i, device=dev)
                   for i in range(nx)]
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            ws = torch.empty(max(bd.bi_rmsnorm_gemm_workspace_bytes(M, K), 1), dtype=torch.uint8, device=dev)
+            # the RMSNorm's scratch, with the GEMM's fold workspace in front (zeroed)
+            ws = torch.zeros(bd.bi_rmsnorm_gemm_workspace_bytes(M, K) + bd.bi_gemm_bf16_workspace_bytes(M, N, K, pins),
+                             dtype=torch.uint8, device=dev)
             us = time_graph(lambda i: bd.bi_rmsnorm_gemm_bf16(xs[i % nx], g, W[i % nw], 1e-5, pins=pins, out=y,
                                                              workspace=ws), args.per_m_reps)
             tus = time_graph(lambda i: torch.mm(F.rms_norm(xs[i % nx], (K,), g, 1e-5), W[i % nw].t(), out=y),
@@ -894,7 +900,7 @@ def run_ours(args, dist):
     ach_big = f_big / (float(per_launch[0, j_big]) * 1e-6) / 1e12
     roof = {"bound": "tensor", "achieved": round(ach_big, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(ach_big / peaks["bf16_tflops"], 3), "traffic": traffic.get(M_big),
-            "algorithmic_bytes": int(b_big), "launch": "bi_gemm_bf16 at M=%d (%.0f%% of the step's time)" % (
+            "algorithmic_bytes": int(b_big), "launch": "bi_gemm_bf16_ws at M=%d (%.0f%% of the step's time)" % (
                 M_big, 100.0 * float(per_launch[0, j_big]) / float(per_launch.sum())),
             "peak_source": peaks["source"] + " (burst bf16; launches timed back to back)"}
     # the decode end of the sweep: HBM-bound
@@ -903,7 +909,7 @@ def run_ours(args, dist):
     ach_s = b_s / (float(per_launch[0, 0]) * 1e-6) / 1e9
     roof_decode = {"bound": "hbm", "achieved": round(ach_s, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                    "frac": round(ach_s / peaks["hbm_gbs"], 3), "traffic": traffic.get(M_small),
-                   "algorithmic_bytes": int(b_s), "launch": "bi_gemm_bf16 at M=%d" % M_small,
+                   "algorithmic_bytes": int(b_s), "launch": "bi_gemm_bf16_ws at M=%d" % M_small,
                    "peak_source": peaks["source"] + " (copy bandwidth)"}
     sweep_roof = {"tflops": round(sweep_tflops, 1), "frac_of_bf16_peak": round(sweep_tflops / peaks["bf16_tflops"], 3),
                   "time_weighted_roofline_frac": round(sum_roof / sum_meas, 3),

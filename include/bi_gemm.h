@@ -87,12 +87,21 @@ typedef struct CUstream_st* bi_stream_t;
  *   CHAIN    a cluster of ceil(S/2) CTAs (or pairs) per tile; each computes
  *            two consecutive chains (one for the first when S is odd).  Each
  *            adds its chains, in order, to the running sum the previous one
- *            left in shared memory (S >= 3). */
+ *            left in shared memory (S >= 3).
+ *   GLOBAL   (bi_gemm_bf16_ws with a fold workspace; one token tile,
+ *            single-CTA MMAs, 2 <= S <= 8) persistent CTAs take the S * tiles
+ *            chains one by one, with no cluster co-residency limit; each
+ *            chain's partial goes to the workspace, and the chain that
+ *            finishes its tile's set last folds the S partials there in
+ *            ascending order.  Elsewhere the flag falls back to AUTO. */
 #define BI_FLAG_SCHEDULE_AUTO 0x0u
 #define BI_FLAG_SCHEDULE_LOCAL 0x1u
 #define BI_FLAG_SCHEDULE_CLUSTER 0x2u
 #define BI_FLAG_SCHEDULE_CHAIN 0x3u
-#define BI_FLAG_SCHEDULE_MASK 0x3u
+#define BI_FLAG_SCHEDULE_GLOBAL 0x4u
+#define BI_FLAG_SCHEDULE_MASK 0x7u
+/* Splits the GLOBAL schedule folds at most. */
+#define BI_GLOBAL_MAX_SPLIT_K 8
 /* Diagnostic only: the load producer withholds its first load so that the
  * tensor-core warp's bounded wait runs out.  The kernel then abandons the call
  * (Y is left unspecified), frees its tensor memory and returns, and
@@ -197,7 +206,7 @@ typedef struct bi_gemm_plan {
   int64_t k_tiles;                         /* tree */
   int64_t split_begin[BI_MAX_SPLIT_K + 1]; /* tree: K-tile boundaries, split s = [begin[s], begin[s+1]) */
   /* schedule: may depend on M */
-  int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL, _CLUSTER or _CHAIN */
+  int32_t schedule;                        /* BI_FLAG_SCHEDULE_LOCAL, _CLUSTER, _CHAIN or _GLOBAL */
   int32_t units;                           /* cluster schedules: CTAs (or pairs) per tile */
   int32_t w_stages, x_stages;              /* depths of the W and X shared-memory rings */
   int32_t x_box_rows;                      /* token rows per X copy (< tok_tile for small M) */
@@ -230,6 +239,39 @@ bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi_pins* 
  * BI_ERR_ILLEGAL_PINS, BI_ERR_CUDA. */
 bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                        const bi_pins* pins, bi_stream_t stream);
+
+/* Bytes of fold workspace bi_gemm_bf16_ws can use for this call: the GLOBAL
+ * schedule's per-tile arrival counters (the first 256-byte-rounded
+ * ceil(N/128) * 4 bytes) and chain partials (ceil(N/128) * S * T * 128 * 4
+ * bytes, T the launch's token tile).  0 when the GLOBAL schedule does not
+ * apply (more than one token tile, paired MMAs, S outside 2..8), or on
+ * invalid arguments.  Host only. */
+size_t bi_gemm_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K, const bi_pins* pins);
+
+/* bi_gemm_bf16 with a fold workspace: the same bits for the same pins (the
+ * tree never depends on the schedule), and one more schedule the planner may
+ * choose for a single token tile (decode): GLOBAL (see the schedule flags).
+ * It puts a tile's S split chains on any SMs with no cluster co-residency
+ * limit, so a decode step streams W through every SM.
+ * Workspace: caller-owned device memory of at least
+ * bi_gemm_bf16_workspace_bytes(M, N, K, pins) bytes (smaller or NULL: the
+ * call runs as bi_gemm_bf16), 256-byte aligned.  Its counter part must be
+ * zero before the first call (cudaMemset); every call that completes leaves
+ * it zero again, so a workspace is zeroed once.  A call abandoned by a
+ * bounded wait (BI_ERR_DEVICE_TIMEOUT) may leave counts behind: zero it
+ * again.  Calls that may overlap on the GPU need workspaces of their own.
+ * Defines: LLM-42, Sec. 2.2, Fig. 3 and CoRun, Sec. III-A, Fig. 3(b): the
+ * split count and the order in which split partials are added are fixed by
+ * (N, K, pins); here they are added in ascending split order wherever they
+ * are folded.
+ * Errors: as bi_gemm_bf16, plus BI_ERR_ALIGNMENT for the workspace. */
+bi_status bi_gemm_bf16_ws(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                          const bi_pins* pins, void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
+/* As bi_gemm_plan_describe, for bi_gemm_bf16_ws with a workspace of
+ * `workspace_bytes` bytes. */
+bi_status bi_gemm_plan_describe_ws(int64_t M, int64_t N, int64_t K, const bi_pins* pins, int32_t sm_count,
+                                   size_t workspace_bytes, bi_gemm_plan* plan);
 
 /* Bytes of device workspace bi_gemm_bf16_host needs for M rows (0 for M = 0). */
 size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -293,10 +335,15 @@ size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K);
  * X tile in shared memory between its arrival and the tensor-core reads, so
  * the normalised rows never reach device memory.  Both forms give the same
  * bits.
- * Workspace: room for r and for the staged rows, in `workspace` (caller-owned device memory of at least
- * bi_rmsnorm_gemm_workspace_bytes(M, K) bytes, 256-byte aligned; its contents
- * on return are unspecified).  The library allocates nothing, so the caller
- * provides it; bi_rmsnorm_gemm_bf16_noalloc takes none.
+ * Workspace: caller-owned device memory, 256-byte aligned, of at least
+ * bi_rmsnorm_gemm_workspace_bytes(M, K) bytes: the RMSNorm's scratch (r and
+ * the staged rows), taken from the workspace's end; its contents there on
+ * return are unspecified.  Bytes in front of that part serve as the GEMM's
+ * fold workspace (as for bi_gemm_bf16_ws) when there are at least
+ * bi_gemm_bf16_workspace_bytes(M, N, K, pins) of them: then the workspace's
+ * first bytes hold the fold counters, which must be zero before the first
+ * call and which every completed call leaves zero.  The library allocates
+ * nothing, so the caller provides it; bi_rmsnorm_gemm_bf16_noalloc takes none.
  * Errors: as the two calls, plus BI_ERR_WORKSPACE.  Everything is checked and
  * the GEMM planned before the first kernel is launched. */
 bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* W, void* Y, int64_t M,

@@ -36,6 +36,8 @@ BI_FLAG_SCHEDULE_AUTO = 0x0
 BI_FLAG_SCHEDULE_LOCAL = 0x1
 BI_FLAG_SCHEDULE_CLUSTER = 0x2
 BI_FLAG_SCHEDULE_CHAIN = 0x3
+BI_FLAG_SCHEDULE_GLOBAL = 0x4
+BI_GLOBAL_MAX_SPLIT_K = 8
 BI_FLAG_DEBUG_STALL_PRODUCER = 0x100
 BI_FLAG_PREFETCH_W = 0x200
 BI_FLAG_KTILE_PAIRS = 0x400
@@ -109,6 +111,11 @@ _SIGNATURES = {
     "bi_gemm_plan_describe": (ctypes.c_int, [_i64, _i64, _i64, ctypes.POINTER(Pins), ctypes.c_int32,
                                              ctypes.POINTER(Plan)]),
     "bi_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp]),
+    "bi_gemm_bf16_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.POINTER(Pins)]),
+    "bi_gemm_bf16_ws": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp, ctypes.c_size_t,
+                                       _vp]),
+    "bi_gemm_plan_describe_ws": (ctypes.c_int, [_i64, _i64, _i64, ctypes.POINTER(Pins), ctypes.c_int32,
+                                                ctypes.c_size_t, ctypes.POINTER(Plan)]),
     "bi_rmsnorm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
     "bi_rmsnorm_quantize_e4m3": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float, _vp]),
     "bi_gemm_bf16_host_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
@@ -233,18 +240,47 @@ def _report(M: int, N: int, K: int):
         fn(M, N, K)
 
 
+def _workspace(ws: torch.Tensor, name: str = "workspace") -> tuple:
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _on_current_device(ws, name)
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def bi_gemm_plan_describe_ws(M: int, N: int, K: int, pins: Pins | None = None, sm_count: int = 0,
+                             workspace_bytes: int = 0) -> Plan:
+    plan = Plan()
+    _check(load().bi_gemm_plan_describe_ws(M, N, K, ctypes.byref(pins) if pins is not None else None, sm_count,
+                                           int(workspace_bytes), ctypes.byref(plan)), "bi_gemm_plan_describe_ws")
+    return plan
+
+
+def bi_gemm_bf16_workspace_bytes(M: int, N: int, K: int, pins: Pins | None = None) -> int:
+    """Fold-workspace bytes the call can use (0: the GLOBAL schedule does not apply)."""
+    return int(load().bi_gemm_bf16_workspace_bytes(M, N, K, ctypes.byref(pins) if pins is not None else None))
+
+
 def bi_gemm_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
-                 pins: Pins | None = None, stream=None) -> torch.Tensor:
-    """Y = X . W^T (bf16, fp32 accumulation).  x [M,K], w [N,K] -> [M,N]."""
+                 pins: Pins | None = None, stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = X . W^T (bf16, fp32 accumulation).  x [M,K], w [N,K] -> [M,N].
+    With `workspace` (device memory whose counter part is zero, see
+    bi_gemm_bf16_workspace_bytes) the call goes through bi_gemm_bf16_ws."""
     if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
         raise ValueError("expected x [M,K] and w [N,K]")
     M, K = x.shape
     N = w.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    st = load().bi_gemm_bf16(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
-                             ctypes.byref(pins) if pins is not None else None, _stream(stream))
-    _check(st, "bi_gemm_bf16")
+    if workspace is not None:
+        ws_ptr, ws_bytes = _workspace(workspace)
+        st = load().bi_gemm_bf16_ws(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
+                                    ctypes.byref(pins) if pins is not None else None, ws_ptr, ws_bytes,
+                                    _stream(stream))
+        _check(st, "bi_gemm_bf16_ws")
+    else:
+        st = load().bi_gemm_bf16(_dev(x, "x"), _dev(w, "w"), _dev(out, "out", (M, N)), M, N, K,
+                                 ctypes.byref(pins) if pins is not None else None, _stream(stream))
+        _check(st, "bi_gemm_bf16")
     if _call_hooks:
         _report(M, N, K)
     return out
@@ -301,13 +337,6 @@ def bi_rmsnorm_bf16(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-5, out: to
                                 float(eps), _stream(stream))
     _check(st, "bi_rmsnorm_bf16")
     return out
-
-
-def _workspace(ws: torch.Tensor, name: str = "workspace") -> tuple:
-    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
-        raise ValueError("%s must be a contiguous CUDA tensor" % name)
-    _on_current_device(ws, name)
-    return ws.data_ptr(), ws.numel() * ws.element_size()
 
 
 def bi_rmsnorm_gemm_workspace_bytes(M: int, K: int) -> int:

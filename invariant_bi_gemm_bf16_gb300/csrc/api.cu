@@ -5,6 +5,7 @@
 // resolve and validate the pins, then touch the device.  A call that returns
 // an error has launched nothing.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -209,7 +210,11 @@ struct LaunchChoice {
 // A single short token tile (decode) streams W from HBM: there the schedule
 // that puts the most CTAs on the W stream wins, which the rounds of LOCAL
 // against those of CLUSTER capture (CHAIN is not used).
-LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N, int32_t sm_count) {
+// GLOBAL (a fold workspace at hand, one token tile, single-CTA MMAs,
+// 2 <= S <= BI_GLOBAL_MAX_SPLIT_K): rounds of ceil(tiles * S / SMs) chains on
+// persistent CTAs, with no co-residency limit.
+LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N, int32_t sm_count,
+                           bool fold_ok) {
   const uint32_t forced = r.flags & BI_FLAG_SCHEDULE_MASK;
   const int64_t n_tiles = ceil_div(N, (int64_t)kTileN * ctas);
   const int64_t m_tiles = ceil_div(M, r.T);
@@ -225,14 +230,28 @@ LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N
                   (double)ceil_div(tiles, max_clusters(r.S * ctas, sm_count)) * (chain + 30.0)};
   LaunchChoice ch{ctas, BI_FLAG_SCHEDULE_CHAIN, uc,
                   (double)ceil_div(tiles, max_clusters(uc * ctas, sm_count)) * (2.0 * chain + 30.0)};
+  const bool global_ok = fold_ok && ctas == 1 && m_tiles == 1 && r.S >= 2 && r.S <= BI_GLOBAL_MAX_SPLIT_K &&
+                         tiles * r.S <= 0x7FFFFFFF;
+  const LaunchChoice gl{ctas, BI_FLAG_SCHEDULE_GLOBAL, 1, 0.0};
   if (r.S == 1 || forced == BI_FLAG_SCHEDULE_LOCAL || !grid_ok) return local;
   if (forced == BI_FLAG_SCHEDULE_CLUSTER) return cl;
   if (forced == BI_FLAG_SCHEDULE_CHAIN) return ch;
+  if (forced == BI_FLAG_SCHEDULE_GLOBAL && global_ok) return gl;
   if (m_tiles == 1 && M <= r.T / 2) {
-    // decode: rounds of chain work per unit; CLUSTER charged 15%
+    // decode: rounds of chain work per unit.  CLUSTER runs in waves of the
+    // clusters that fit at once, charged 15%; GLOBAL spreads the chains over
+    // every SM, but its fold through L2 costs more than one DSMEM fold
+    // (measured on GB300: 1-2 us at M = 32), so it is taken where it runs
+    // fewer rounds than the clusters' waves, or where the clusters need
+    // several waves (each wave pays its start and its fold; Llama-3.1-8B
+    // gate_up at decode: 3 waves in 47 us, 3 GLOBAL rounds in 38 us).
     const double local_rounds = (double)ceil_div(tiles, slots) * r.S;
-    const double cluster_rounds = (double)ceil_div(tiles * r.S, slots);
-    return (r.S * ctas <= 8 && cluster_rounds * 1.15 < local_rounds) ? cl : local;
+    const int64_t waves = r.S * ctas <= 8 ? ceil_div(tiles, max_clusters(r.S * ctas, sm_count)) : INT64_MAX;
+    const double cluster_rounds = waves == INT64_MAX ? 1e30 : (double)waves * 1.15;
+    const int64_t rounds = global_ok ? ceil_div(tiles * r.S, sm_count) : INT64_MAX;
+    if (rounds != INT64_MAX && (rounds < waves || (waves > 1 && rounds <= waves)) && (double)rounds <= local_rounds)
+      return gl;
+    return cluster_rounds < local_rounds ? cl : local;
   }
   LaunchChoice best = local;
   if (r.S * ctas <= 8 && cl.cost < best.cost) best = cl;
@@ -248,11 +267,11 @@ LaunchChoice best_schedule(const Resolved& r, int32_t ctas, int64_t M, int64_t N
 // half-empty X box, and decode is bound by the W stream, which S-CTA clusters
 // spread over the most SMs.  A forced one-split CLUSTER schedule also keeps
 // one CTA (a pair would need clusters of 2S).
-LaunchChoice choose_launch(int64_t M, int64_t N, const Resolved& r, int32_t sm_count) {
-  if (r.ctas != 0) return best_schedule(r, r.ctas, M, N, sm_count);
-  const LaunchChoice one = best_schedule(r, 1, M, N, sm_count);
+LaunchChoice choose_launch(int64_t M, int64_t N, const Resolved& r, int32_t sm_count, bool fold_ok) {
+  if (r.ctas != 0) return best_schedule(r, r.ctas, M, N, sm_count, fold_ok);
+  const LaunchChoice one = best_schedule(r, 1, M, N, sm_count, fold_ok);
   if (M <= r.T / 2 || (r.flags & BI_FLAG_SCHEDULE_MASK) == BI_FLAG_SCHEDULE_CLUSTER) return one;
-  LaunchChoice two = best_schedule(r, 2, M, N, sm_count);
+  LaunchChoice two = best_schedule(r, 2, M, N, sm_count, fold_ok);
   // A persistent paired launch may also narrow its token tile so that the
   // tiles fill the last wave (224, 192 or 160 instead of 256).  Its per-K-tile
   // cost follows the operand bytes each CTA receives: 16 KB of W and T/2 rows
@@ -274,11 +293,19 @@ LaunchChoice choose_launch(int64_t M, int64_t N, const Resolved& r, int32_t sm_c
   return two.cost < one.cost ? two : one;
 }
 
-bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int32_t sm_count,
-                    bi_gemm_plan* plan) {
+// Fold workspace bytes of a GLOBAL plan: the per-tile arrival counters
+// (rounded up to 256 bytes), then the chain partials [tiles * S][T][128] fp32.
+size_t fold_bytes(const bi_gemm_plan& plan) {
+  const uint64_t tiles = (uint64_t)plan.n_tiles * (uint64_t)plan.m_tiles;
+  const uint64_t counters = (tiles * 4u + 255u) & ~(uint64_t)255u;
+  return (size_t)(counters + tiles * (uint64_t)plan.split_k * (uint64_t)plan.tok_tile * kTileN * 4u);
+}
+
+bi_status make_plan_once(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int32_t sm_count, bool fold_ok,
+                         bi_gemm_plan* plan) {
   std::memset(plan, 0, sizeof(*plan));
   Resolved r = pinned;
-  const LaunchChoice choice = choose_launch(M, N, r, sm_count);
+  const LaunchChoice choice = choose_launch(M, N, r, sm_count, fold_ok);
   r.ctas = choice.ctas;
   if (choice.T != 0) r.T = choice.T;
   // Decode (M <= 128 on single-CTA MMAs, the CTA grouping and the W depth
@@ -319,8 +346,15 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   const int64_t tiles = plan->n_tiles * plan->m_tiles;
   plan->schedule = choice.schedule;
   plan->units = choice.units;
-  const bool cluster = plan->schedule != BI_FLAG_SCHEDULE_LOCAL;
-  if (cluster) {
+  const bool cluster = plan->schedule == BI_FLAG_SCHEDULE_CLUSTER || plan->schedule == BI_FLAG_SCHEDULE_CHAIN;
+  if (plan->schedule == BI_FLAG_SCHEDULE_GLOBAL) {
+    const int64_t chains = tiles * r.S;
+    plan->grid_x = (int32_t)(chains < sm_count ? chains : sm_count);
+    plan->grid_y = 1;
+    plan->grid_z = 1;
+    plan->cluster_x = 1;
+    plan->group_n = 1;
+  } else if (cluster) {
     if (plan->n_tiles > 65535 || plan->m_tiles > 65535) return BI_ERR_UNSUPPORTED_SHAPE;
     plan->grid_x = choice.units * r.ctas;
     plan->grid_y = (int32_t)plan->n_tiles;
@@ -343,6 +377,16 @@ bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int
   if (plan->w_stages < 2 || plan->x_stages < 2) return BI_ERR_ILLEGAL_PINS;
   if (plan->smem_bytes > kMaxDynSmem) return BI_ERR_ILLEGAL_PINS;
   return BI_OK;
+}
+
+// The plan for a call with `fold_avail` bytes of fold workspace: GLOBAL only
+// where the planner picks it and its workspace fits.
+bi_status make_plan(int64_t M, int64_t N, int64_t K, const Resolved& pinned, int32_t sm_count,
+                    bi_gemm_plan* plan, size_t fold_avail = 0) {
+  bi_status st = make_plan_once(M, N, K, pinned, sm_count, fold_avail > 0, plan);
+  if (st == BI_OK && plan->schedule == BI_FLAG_SCHEDULE_GLOBAL && fold_bytes(*plan) > fold_avail)
+    st = make_plan_once(M, N, K, pinned, sm_count, false, plan);
+  return st;
 }
 
 bi_status validate(int64_t N, int64_t K, const bi_pins* p, Elem e = Elem::BF16) {
@@ -372,6 +416,7 @@ bi_status validate(int64_t N, int64_t K, const bi_pins* p, Elem e = Elem::BF16) 
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k * (p->mma_ctas == 2 ? 2 : 1) > 16)
     return BI_ERR_ILLEGAL_PINS;
   if (sched == BI_FLAG_SCHEDULE_CLUSTER && p->split_k > 8) return BI_ERR_ILLEGAL_PINS;
+  if (sched > BI_FLAG_SCHEDULE_GLOBAL) return BI_ERR_ILLEGAL_PINS;
   // CHAIN: ceil(S/2) >= 2 units per tile; an open grouping may choose pairs
   if (sched == BI_FLAG_SCHEDULE_CHAIN &&
       (p->split_k < 3 || (p->split_k + 1) / 2 * (p->mma_ctas == 1 ? 1 : 2) > 16))
@@ -455,7 +500,8 @@ bi_status check_gemm_args(const void* X, const void* W, const void* Y, int64_t M
 // call.  L->M == 0 means there is nothing to launch.
 bi_status plan_gemm(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                     const bi_pins* pins, cudaStream_t stream, GemmLaunch* out, Elem e = Elem::BF16,
-                    const float* sx = nullptr, const float* sw = nullptr) {
+                    const float* sx = nullptr, const float* sw = nullptr, void* fold_ws = nullptr,
+                    size_t fold_avail = 0) {
   bi_status st = check_gemm_args(X, W, Y, M, N, K, e);
   if (st != BI_OK) return st;
   if (e == Elem::E4M3 && M > 0) {
@@ -469,8 +515,13 @@ bi_status plan_gemm(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   std::memset(&L, 0, sizeof(L));
   if (M == 0) return BI_OK;
   bi_gemm_plan plan;
-  st = make_plan(M, N, K, r, sm_count_current(), &plan);
+  st = make_plan(M, N, K, r, sm_count_current(), &plan, fold_ws ? fold_avail : 0);
   if (st != BI_OK) return st;
+  if (plan.schedule == BI_FLAG_SCHEDULE_GLOBAL) {
+    const uint64_t tiles = (uint64_t)plan.n_tiles * (uint64_t)plan.m_tiles;
+    L.fold_count = static_cast<uint32_t*>(fold_ws);
+    L.fold_part = reinterpret_cast<float*>(static_cast<char*>(fold_ws) + ((tiles * 4u + 255u) & ~(uint64_t)255u));
+  }
   L.X = X;
   L.W = W;
   L.fp8 = e == Elem::E4M3;
@@ -491,7 +542,7 @@ bi_status plan_gemm(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   L.kps = plan.kps;
   L.group_n = plan.group_n > 0 ? plan.group_n : 1;
   L.units = plan.units;
-  L.cluster = plan.schedule != BI_FLAG_SCHEDULE_LOCAL;
+  L.cluster = plan.schedule == BI_FLAG_SCHEDULE_CLUSTER || plan.schedule == BI_FLAG_SCHEDULE_CHAIN;
   L.pair = plan.mma_ctas == 2;
   L.grid_x = plan.grid_x;
   L.grid_y = plan.grid_y;
@@ -523,12 +574,13 @@ bi_status encode_gemm(GemmLaunch& L) {
 // The RMSNorm -> GEMM layer, checked and planned (no CUDA call): X [M,K] raw
 // activations, g [K], W [N,K], Y [M,N].
 bi_status plan_fused(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
-                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L) {
+                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L, void* fold_ws,
+                     size_t fold_avail) {
   bi_status st = check_gemm_args(X, W, Y, M, N, K);
   if (st != BI_OK) return st;
   st = check_rmsnorm_args(X, g, Y, M, K, eps);
   if (st != BI_OK) return st;
-  st = plan_gemm(X, W, Y, M, N, K, pins, stream, L);
+  st = plan_gemm(X, W, Y, M, N, K, pins, stream, L, Elem::BF16, nullptr, nullptr, fold_ws, fold_avail);
   if (st != BI_OK) return st;
   L->g = g;
   L->eps = eps;
@@ -581,9 +633,10 @@ namespace {
 
 bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                     const bi_pins* pins, cudaStream_t stream, Elem e = Elem::BF16,
-                    const float* sx = nullptr, const float* sw = nullptr) {
+                    const float* sx = nullptr, const float* sw = nullptr, void* fold_ws = nullptr,
+                    size_t fold_avail = 0) {
   GemmLaunch L;
-  bi_status st = plan_gemm(X, W, Y, M, N, K, pins, stream, &L, e, sx, sw);
+  bi_status st = plan_gemm(X, W, Y, M, N, K, pins, stream, &L, e, sx, sw, fold_ws, fold_avail);
   if (st != BI_OK || L.M == 0) return st;
   st = encode_gemm(L);
   if (st != BI_OK) return st;
@@ -688,6 +741,34 @@ BI_API bi_status bi_gemm_plan_describe(int64_t M, int64_t N, int64_t K, const bi
 BI_API bi_status bi_gemm_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
                               const bi_pins* pins, bi_stream_t stream) {
   return gemm_impl(X, W, Y, M, N, K, pins, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API size_t bi_gemm_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K, const bi_pins* pins) {
+  if (M <= 0 || check_nk(N, K) != BI_OK || M > 0x7FFFFFFFll) return 0;
+  Resolved r;
+  if (resolve_pins(N, K, pins, &r) != BI_OK) return 0;
+  bi_gemm_plan plan;
+  if (make_plan(M, N, K, r, sm_count_current(), &plan, (size_t)-1) != BI_OK) return 0;
+  return plan.schedule == BI_FLAG_SCHEDULE_GLOBAL ? fold_bytes(plan) : 0;
+}
+
+BI_API bi_status bi_gemm_plan_describe_ws(int64_t M, int64_t N, int64_t K, const bi_pins* pins, int32_t sm_count,
+                                          size_t workspace_bytes, bi_gemm_plan* plan) {
+  if (!plan) return BI_ERR_INVALID_ARG;
+  if (M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  return make_plan(M, N, K, r, sm_count > 0 ? sm_count : kDefaultSmCount, plan, workspace_bytes);
+}
+
+BI_API bi_status bi_gemm_bf16_ws(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                                 const bi_pins* pins, void* workspace, size_t ws_bytes, bi_stream_t stream) {
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
+  return gemm_impl(X, W, Y, M, N, K, pins, reinterpret_cast<cudaStream_t>(stream), Elem::BF16, nullptr, nullptr,
+                   workspace, workspace ? ws_bytes : 0);
 }
 
 BI_API bi_status bi_pins_default_fp8(int64_t N, int64_t K, bi_pins* out) {
@@ -823,12 +904,19 @@ BI_API bi_status bi_rmsnorm_gemm_bf16(const void* X, const void* g, const void* 
                                       int64_t M, int64_t N, int64_t K, float eps,
                                       const bi_pins* pins, void* workspace, size_t ws_bytes,
                                       bi_stream_t stream) {
+  // The workspace: the RMSNorm's scratch (r, the staged rows) at its end,
+  // and in front of it, when there is room, the GEMM's fold workspace (its
+  // counters at offset 0 whatever M is, so that they stay zero between calls).
+  const size_t base = fused_workspace_bytes(M, K);
+  const bool ws_ok = workspace && ws_bytes >= base && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0;
+  const size_t front = ws_ok ? ((ws_bytes - base) & ~(size_t)255) : 0;
   GemmLaunch L;
-  bi_status st = plan_fused(X, g, W, Y, M, N, K, eps, pins, reinterpret_cast<cudaStream_t>(stream), &L);
+  bi_status st = plan_fused(X, g, W, Y, M, N, K, eps, pins, reinterpret_cast<cudaStream_t>(stream), &L,
+                            front ? workspace : nullptr, front);
   if (st != BI_OK || L.M == 0) return st;
-  if (!workspace || ws_bytes < fused_workspace_bytes(M, K)) return BI_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < base) return BI_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
-  return launch_fused(L, workspace, fused_in_smem(L));
+  return launch_fused(L, static_cast<char*>(workspace) + front, fused_in_smem(L));
 }
 
 BI_API bi_status bi_residual_add_bf16(const void* a, const void* b, void* out, int64_t count,

@@ -76,6 +76,8 @@ struct GemmParams {
                            // nullptr: computed in the kernel (M <= kRowScaleInKernelMax)
   const __nv_bfloat16* xraw;  // FUSED with rrow == nullptr: X [M,K], for the sums of squares
   float eps;
+  float* fold_part;        // GLOBAL: chain partials [n_tiles * S][T][128] fp32, or nullptr (other schedules)
+  uint32_t* fold_count;    // GLOBAL: per-tile arrival counts, zero between calls
   int* status;             // device status word: 0, or the bi_status of a call that gave up
   uint32_t flags;  // BI_FLAG_DEBUG_STALL_PRODUCER | kFlagStreamW | kFlagZeroX
 };
@@ -92,6 +94,7 @@ struct __align__(8) SmemCtl {
   uint32_t tmem_base;
   int abort;
   float rrow[kRowScaleInKernelMax];  // FUSED, tiny batches: r of the CTA's rows, computed here
+  int fold_last;                     // GLOBAL: this chain was its tile's last to finish
 };
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block too large");
 
@@ -159,6 +162,104 @@ __device__ __forceinline__ void tile_coords(int64_t t, int32_t n_tiles, int32_t 
     const int64_t r = t - full;
     *n_tile = (int32_t)((n_tiles / G) * G + r % w);
     *m_tile = (int32_t)(r / w);
+  }
+}
+
+// Epilogue of the GLOBAL schedule (single-CTA MMAs, one chain per work
+// item).  Each chain's partial goes to the workspace as [item][column][W row]
+// fp32, columns below M only.  The epilogue warps then publish it (fence,
+// barrier) and count the chain in on its tile's arrival counter; the chain
+// whose arrival completes the count folds the tile's S partials from the
+// workspace in ascending split order, (((P0 + P1) + P2) + ...), the order of
+// the register and shared-memory folds, writes Y and sets the counter back to
+// zero.  Nobody waits on anybody: the count only decides who folds.  The
+// atomic touches the count, never a value.  Every barrier is taken by all
+// 16 epilogue warps; a bounded wait that runs out is agreed on by all of
+// them (bar.red.and) before anyone leaves.
+constexpr int kFoldMaxS = BI_GLOBAL_MAX_SPLIT_K;  // splits the GLOBAL schedule folds (one column group's loads in flight together)
+
+template <int T, bool FP8, typename Work>
+__device__ __forceinline__ void global_fold_epilogue(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
+                                                     volatile int* abort, int64_t tile_first, int64_t tile_step,
+                                                     int64_t tile_end, int32_t S, Work&& work) {
+  constexpr int kColGroups = kEpiWarps / 4;
+  constexpr int kHalf = T / kColGroups;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - kFirstEpiWarp;
+  const int quad = warp & 3, half = ew >> 2;
+  const int n_local = quad * 32 + lane;
+  const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+  const int et = (int)threadIdx.x - 32 * kFirstEpiWarp;  // 0 .. 511
+  const int frow = et & (kTileN - 1);                      // fold: this thread's W row
+  const int fcol = et >> 7;                                // and first column (then every 4th)
+  uint32_t acc_iter = 0;
+  for (int64_t t = tile_first; t < tile_end; t += tile_step) {
+    int32_t n_tile, m_tile, s_lo, s_hi;
+    work(t, n_tile, m_tile, s_lo, s_hi);
+    const int64_t tile = t / S;
+    const uint32_t buf = acc_iter & 1u;
+    const uint32_t acc_phase = (acc_iter >> 1) & 1u;
+    const bool got = wait_or_abort(smem_u32(&ctl->acc_full[buf]), acc_phase, abort, p.status);
+    if (!named_barrier_and(2, 32 * kEpiWarps, got)) return;
+    tc_fence_after();
+    const int64_t mt0 = (int64_t)m_tile * T;              // the tile's first token
+    const int64_t mrem = p.M - mt0;
+    const int mvt = mrem < T ? (int)mrem : T;              // valid tokens of the tile
+    const int mv = min(max(mvt - half * kHalf, 0), kHalf);  // ... in this warp's columns
+    float* part = p.fold_part + ((int64_t)t * T + half * kHalf) * kTileN + n_local;
+    const uint32_t taddr = tmem_base + t_lane + buf * (uint32_t)T + (uint32_t)(half * kHalf);
+#pragma unroll
+    for (int c = 0; c < kHalf; c += 4) {
+      if (c < mv) {
+        float v[4];
+        tmem_ld4(taddr + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (c + i < mv) __stcg(part + (int64_t)(c + i) * kTileN, v[i]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+    ++acc_iter;
+    __threadfence();  // the partial is visible before the count
+    named_barrier_sync(2, 32 * kEpiWarps);
+    if (et == 0) {
+      const uint32_t before = atomicAdd(p.fold_count + tile, 1u);
+      const int last = before == (uint32_t)(S - 1);
+      if (last) p.fold_count[tile] = 0u;  // all S chains counted in: zero for the next call
+      ctl->fold_last = last;
+    }
+    named_barrier_sync(2, 32 * kEpiWarps);
+    if (!ctl->fold_last) continue;
+    __threadfence();
+    const int64_t n = (int64_t)n_tile * kTileN + frow;
+    if (n < p.N) {
+      const float* P0 = p.fold_part + tile * S * T * kTileN + frow;  // split 0 of this tile, column 0
+      const float swn = FP8 ? p.sw[n] : 1.0f;
+      // columns fcol, fcol + 4, ...: four of them at a time, all S loads in flight
+      for (int c0 = fcol; c0 < mvt; c0 += 16) {
+        float v[4][kFoldMaxS];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int q = 0; q < kFoldMaxS; ++q) {
+            const int c = c0 + 4 * i;
+            v[i][q] = (q < S && c < mvt) ? __ldcg(P0 + ((int64_t)q * T + c) * kTileN) : 0.0f;
+          }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + 4 * i;
+          if (c >= mvt) break;
+          float acc = v[i][0];
+#pragma unroll
+          for (int q = 1; q < kFoldMaxS; ++q)
+            if (q < S) acc = __fadd_rn(acc, v[i][q]);
+          if (FP8) acc = __fmul_rn(__fmul_rn(acc, p.sx[mt0 + c]), swn);
+          p.Y[(mt0 + c) * p.N + n] = __float2bfloat16_rn(acc);
+        }
+      }
+    }
   }
 }
 
@@ -267,17 +368,35 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
   // (the cluster rank, counted in pairs when PAIR) of U runs splits
   // [floor(u*S/U), floor((u+1)*S/U)): one split each when U = S, one or two
   // when U = ceil(S/2) (chained).  LOCAL: tiles u, u + U, ... for unit u of U
-  // (a unit is a CTA, or a CTA pair), all S splits of each.
+  // (a unit is a CTA, or a CTA pair), all S splits of each.  GLOBAL (a LOCAL
+  // kernel of single-CTA MMAs given a fold workspace): the work items are
+  // the chains (tile, split), unit u taking items u, u + U, ...; each chain's
+  // partial goes to the workspace, and the last of a tile's S chains to
+  // finish folds them there in ascending split order.
   const int32_t U = CLUSTER ? p.units : 1;
   const bool chained = CLUSTER && U != S;
+  const bool gfold = !CLUSTER && !PAIR && p.fold_part != nullptr;
   const int32_t my_unit = CLUSTER ? (int32_t)(PAIR ? (crank >> 1) : crank) : 0;
   const int64_t unit = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
   const int64_t units = PAIR ? (gridDim.x >> 1) : gridDim.x;
   const int64_t tile_first = CLUSTER ? 0 : unit;
   const int64_t tile_step = CLUSTER ? 1 : units;
-  const int64_t tile_end = CLUSTER ? 1 : num_tiles;
+  const int64_t tile_end = CLUSTER ? 1 : (gfold ? num_tiles * S : num_tiles);
   const int32_t s_first = CLUSTER ? (int32_t)(((int64_t)my_unit * S) / U) : 0;
   const int32_t s_end = CLUSTER ? (int32_t)(((int64_t)(my_unit + 1) * S) / U) : S;
+  // work item t -> its tile and its splits [s_lo, s_hi)
+  auto work = [&](int64_t t, int32_t& n_tile, int32_t& m_tile, int32_t& s_lo, int32_t& s_hi) {
+    if (CLUSTER) {
+      n_tile = (int32_t)blockIdx.y;
+      m_tile = (int32_t)blockIdx.z;
+      s_lo = s_first;
+      s_hi = s_end;
+      return;
+    }
+    tile_coords(gfold ? t / S : t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
+    s_lo = gfold ? (int32_t)(t % S) : 0;
+    s_hi = gfold ? s_lo + 1 : S;
+  };
   const bool stream_w = (p.flags & kFlagStreamW) != 0;
   bool chain_ok = false;  // epilogue threads of a CLUSTER unit: its chains completed
 
@@ -319,16 +438,11 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
-        int32_t n_tile, m_tile;
-        if (CLUSTER) {
-          n_tile = (int32_t)blockIdx.y;
-          m_tile = (int32_t)blockIdx.z;
-        } else {
-          tile_coords(t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
-        }
+        int32_t n_tile, m_tile, s_lo, s_hi;
+        work(t, n_tile, m_tile, s_lo, s_hi);
         const int32_t row = is_w ? n_tile * kMmaM + (int32_t)peer * kTileN
                                  : m_tile * T + (int32_t)peer * kXRows;
-        for (int32_t s = s_first; ok && s < s_end; ++s) {
+        for (int32_t s = s_lo; ok && s < s_hi; ++s) {
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
           // the last copy of a split may reach one K tile past it (loaded, unused)
           for (int64_t kt = k0; kt < k1; kt += KP) {
@@ -422,7 +536,9 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
       uint32_t acc_iter = 0;
       bool ok = true;
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
-        for (int32_t s = s_first; ok && s < s_end; ++s) {
+        int32_t n_tile, m_tile, s_lo, s_hi;
+        work(t, n_tile, m_tile, s_lo, s_hi);
+        for (int32_t s = s_lo; ok && s < s_hi; ++s) {
           const uint32_t buf = acc_iter & 1u;
           const uint32_t acc_phase = (acc_iter >> 1) & 1u;
           if (!wait_or_abort(smem_u32(&ctl->acc_empty[buf]), acc_phase ^ 1u, abort, p.status)) {
@@ -525,11 +641,21 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
     // g is a weight: with BI_FLAG_PREFETCH_W the caller allows reading it
     // before the previous kernel in the stream has finished
     const bool g_early = (p.flags & BI_FLAG_PREFETCH_W) != 0;
-    if (g_early && tile_first < tile_end)
-      load_g(split_begin(s_first, S, KT), split_begin(s_first + 1, S, KT), gcur);
+    // the first split of work item t
+    auto first_split = [&](int64_t t) -> int32_t {
+      int32_t nt, mt, lo, hi;
+      work(t, nt, mt, lo, hi);
+      return lo;
+    };
+    if (g_early && tile_first < tile_end) {
+      const int32_t s0 = first_split(tile_first);
+      load_g(split_begin(s0, S, KT), split_begin(s0 + 1, S, KT), gcur);
+    }
     grid_dep_wait();  // r, X and g may come from the previous kernel in the stream
-    if (!g_early && tile_first < tile_end)
-      load_g(split_begin(s_first, S, KT), split_begin(s_first + 1, S, KT), gcur);
+    if (!g_early && tile_first < tile_end) {
+      const int32_t s0 = first_split(tile_first);
+      load_g(split_begin(s0, S, KT), split_begin(s0 + 1, S, KT), gcur);
+    }
     if (p.rrow == nullptr) {
       // Tiny batch (M <= kRowScaleInKernelMax, one token tile): r of each row
       // here, one transform warp per row with the RMSNorm's lane partition,
@@ -566,12 +692,8 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
     // run in the X producer's order: tile, split, K tile), so their latency
     // overlaps the wait for the stage before.
     for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
-      int32_t n_tile, m_tile;
-      if (CLUSTER) {
-        m_tile = (int32_t)blockIdx.z;
-      } else {
-        tile_coords(t, p.n_tiles, p.m_tiles, p.group_n, &n_tile, &m_tile);
-      }
+      int32_t n_tile, m_tile, s_lo, s_hi;
+      work(t, n_tile, m_tile, s_lo, s_hi);
       const int64_t m0 = (int64_t)m_tile * T + (int64_t)peer * kXRows;  // this CTA's first token row
       if (m0 != have_m0) {
         have_m0 = m0;
@@ -581,17 +703,19 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
         for (int j = 0; j < kRowsPer; ++j)
           rr[j] = j >= nrows ? 0.0f : (p.rrow ? p.rrow[m0 + r0 + 16 * j] : ctl->rrow[m0 + r0 + 16 * j]);
       }
-      for (int32_t s = s_first; ok && s < s_end; ++s) {
+      for (int32_t s = s_lo; ok && s < s_hi; ++s) {
         const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
         for (int64_t kt = k0; kt < k1; kt += KP) {
           // the next stage: the next K tiles of this split, else the next
-          // split's first, else the first split of this CTA's next tile
-          if (kt + KP < k1)
+          // split's first, else the first split of this CTA's next work item
+          if (kt + KP < k1) {
             load_g(kt + KP, k1, gnext);
-          else if (s + 1 < s_end)
+          } else if (s + 1 < s_hi) {
             load_g(k1, split_begin(s + 2, S, KT), gnext);
-          else if (t + tile_step < tile_end)
-            load_g(split_begin(s_first, S, KT), split_begin(s_first + 1, S, KT), gnext);
+          } else if (t + tile_step < tile_end) {
+            const int32_t s0 = first_split(t + tile_step);
+            load_g(split_begin(s0, S, KT), split_begin(s0 + 1, S, KT), gnext);
+          }
           ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&ctl->x_full[xi]), xph, abort, p.status));
           if (!ok) break;
 #pragma unroll
@@ -640,6 +764,12 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
     const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
     uint32_t acc_iter = 0;
     bool ok = true;
+    if constexpr (!CLUSTER && !PAIR) {
+      if (gfold) {
+        global_fold_epilogue<T, FP8>(p, ctl, tmem_base, abort, tile_first, tile_step, tile_end, S, work);
+        ok = false;  // the loop below is for the other schedules
+      }
+    }
     if constexpr (!CLUSTER) {
       for (int64_t t = tile_first; ok && t < tile_end; t += tile_step) {
         int32_t n_tile, m_tile;
@@ -888,6 +1018,8 @@ static cudaError_t launch_t(const GemmLaunch& L) {
   prm.rrow = L.rrow;
   prm.xraw = static_cast<const __nv_bfloat16*>(L.X);
   prm.eps = L.eps;
+  prm.fold_part = L.fold_part;
+  prm.fold_count = L.fold_count;
   prm.status = L.status;
   prm.K = L.K;
   prm.flags = L.flags;

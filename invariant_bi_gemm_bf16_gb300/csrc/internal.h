@@ -67,6 +67,8 @@ struct GemmLaunch {
   float eps;         // fused: RMSNorm epsilon
   const float* rrow; // fused: per-row r = 1 / sqrt(mean(x^2) + eps) [M], or nullptr (computed in the GEMM)
   int* status;       // device status word (bounded waits report there)
+  float* fold_part;        // GLOBAL schedule: chain partials in the fold workspace (else nullptr)
+  uint32_t* fold_count;    // GLOBAL schedule: per-tile arrival counters
   bool cluster;      // one chain per CTA (pair), folded through DSMEM
   bool pair;         // cta_group::2 MMA across a CTA pair
   int32_t grid_x, grid_y, grid_z;
@@ -136,14 +138,17 @@ cudaError_t launch_attention_ctx1(const void* qkv, void* out, int64_t M, int64_t
 // The fused RMSNorm -> GEMM layer in two steps, so that a caller can check
 // and plan everything before it launches anything.  plan_fused checks the
 // arguments (as bi_rmsnorm_gemm_bf16, less the workspace), resolves the pins
-// and plans the GEMM, with no CUDA call; L->M == 0 means nothing to do.
+// and plans the GEMM (with the GLOBAL schedule where `fold_avail` bytes of
+// fold workspace at `fold_ws` allow it), with no CUDA call; L->M == 0 means
+// nothing to do.
 // launch_fused encodes the tensor maps (returning BI_ERR_CUDA before any
 // launch if that fails) and launches the layer in one of its two forms:
 // in shared memory (r in the first fused_r_bytes(M) bytes of `ws`) or staged
 // (r's part unused, the normalised rows in the fused_staged_bytes(M, K) bytes
 // after it).
 bi_status plan_fused(const void* X, const void* g, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
-                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L);
+                     float eps, const bi_pins* pins, cudaStream_t stream, GemmLaunch* L, void* fold_ws = nullptr,
+                     size_t fold_avail = 0);
 bi_status launch_fused(GemmLaunch& L, void* ws, bool in_smem);
 // The form the pins choose: in shared memory with BI_FLAG_NORM_SMEM, else staged.
 bool fused_in_smem(const GemmLaunch& L);

@@ -474,6 +474,21 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Barrier `id` among `threads` threads that also ANDs a predicate across
+// them: every participant gets true only if every participant passed true.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 // 16-byte shared-memory load and store at a shared::cta address.
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
   uint4 v;

@@ -89,7 +89,24 @@ class DecodeStack:
                     self.pins[name] = p.replace(flags=p.flags | bd.BI_FLAG_PREFETCH_W)
         if pins:
             self.pins.update(pins)
+        self._nk = {"qkv": (s.qkv_width, s.hidden), "o": (s.hidden, s.n_q * s.head_dim),
+                    "gu": (2 * s.inter, s.hidden), "d": (s.hidden, s.inter)}
         self._bufs = {}
+        self._fold = {}
+
+    def _workspace(self, name: str, M: int, scratch: int, device) -> torch.Tensor:
+        """The projection's workspace for M rows: room for the GEMM's fold in
+        front (its counters at offset 0, zeroed once and left zero by every
+        call, so one buffer serves every M) and `scratch` bytes at the end for
+        the fused call's RMSNorm.  Grown, as a new zeroed buffer, when a call
+        needs more."""
+        N, K = self._nk[name]
+        need = bd.bi_gemm_bf16_workspace_bytes(M, N, K, self.pins[name]) + scratch
+        buf = self._fold.get(name)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
+            self._fold[name] = buf
+        return buf
 
     def _buffers(self, M: int, device):
         if M not in self._bufs:
@@ -97,6 +114,10 @@ class DecodeStack:
             e = dict(dtype=torch.bfloat16, device=device)
             ws = bd.bi_rmsnorm_gemm_workspace_bytes(M, s.hidden)
             self._bufs[M] = {
+                "ws_qkv": self._workspace("qkv", M, ws, device),
+                "ws_o": self._workspace("o", M, 0, device),
+                "ws_gu": self._workspace("gu", M, ws, device),
+                "ws_d": self._workspace("d", M, 0, device),
                 "qkv": torch.empty((M, s.qkv_width), **e),
                 "att": torch.empty((M, s.n_q * s.head_dim), **e),
                 "o": torch.empty((M, s.hidden), **e),
@@ -105,7 +126,6 @@ class DecodeStack:
                 "act": torch.empty((M, s.inter), **e),
                 "d": torch.empty((M, s.hidden), **e),
                 "x": [torch.empty((M, s.hidden), **e), torch.empty((M, s.hidden), **e)],
-                "ws": torch.empty(max(ws, 256), dtype=torch.uint8, device=device),
             }
         return self._bufs[M]
 
@@ -120,14 +140,14 @@ class DecodeStack:
         cur = x
         for i, L in enumerate(self.layers):
             bd.bi_rmsnorm_gemm_bf16(cur, L["g_attn"], L["Wqkv"], s.eps, pins=self.pins["qkv"], out=b["qkv"],
-                                    workspace=b["ws"])
+                                    workspace=b["ws_qkv"])
             bd.bi_attention_ctx1_bf16(b["qkv"], s.n_q, s.n_kv, s.head_dim, out=b["att"])
-            bd.bi_gemm_bf16(b["att"], L["Wo"], out=b["o"], pins=self.pins["o"])
+            bd.bi_gemm_bf16(b["att"], L["Wo"], out=b["o"], pins=self.pins["o"], workspace=b["ws_o"])
             bd.bi_residual_add_bf16(cur, b["o"], out=b["h"])
             bd.bi_rmsnorm_gemm_bf16(b["h"], L["g_mlp"], L["Wgu"], s.eps, pins=self.pins["gu"], out=b["gu"],
-                                    workspace=b["ws"])
+                                    workspace=b["ws_gu"])
             bd.bi_silu_mul_bf16(b["gu"], out=b["act"])
-            bd.bi_gemm_bf16(b["act"], L["Wd"], out=b["d"], pins=self.pins["d"])
+            bd.bi_gemm_bf16(b["act"], L["Wd"], out=b["d"], pins=self.pins["d"], workspace=b["ws_d"])
             nxt = b["x"][i % 2]
             bd.bi_residual_add_bf16(b["h"], b["d"], out=nxt)
             cur = nxt

@@ -26,10 +26,12 @@ heads, key/value heads, page size); its calls are decode steps, each a list of
 request lengths with a count; the split size is the argmin of the family's
 summed time over the legal sizes (multiples of 64 up to 4096), all measured.
 
-Timing: each (candidate, M) is timed as back-to-back calls between two CUDA
-events on rotating weight copies (more bytes than L2), after warm-up calls,
-and a candidate's cost takes the fastest of a few repeats (the SM clock drifts
-under the power cap).  The winner must then beat the default tuple by a margin
+Timing: each (candidate, M) is timed as back-to-back calls of bi_gemm_bf16_ws
+(with a fold workspace, so that the GLOBAL schedule is open to split counts
+whose clusters would not fit the GPU at once) between two CUDA events on
+rotating weight copies (more bytes than L2), after warm-up calls, and a
+candidate's cost takes the fastest of a few repeats (the SM clock drifts under
+the power cap).  The winner must then beat the default tuple by a margin
 in interleaved re-measurements (``confirm``), else the default is kept.
 """
 from __future__ import annotations
@@ -45,10 +47,10 @@ FORMAT = "bi_gemm_pins/1"
 L2_BYTES = 129 * 1024 * 1024
 
 # Axes of the legal grid of one family, in the order coordinate descent visits them.
-SPLITS = (1, 2, 3, 4, 5, 6, 8, 12, 16)
+SPLITS = (1, 2, 3, 4, 5, 6, 7, 8, 12, 16)
 TOK_TILES = (128, 256)
 GROUPINGS = (0, 1, 2)
-STAGES = (0,)
+STAGES = (0, 4)
 COPY_FLAGS = (0, bd.BI_FLAG_KTILE_PAIRS)
 
 
@@ -208,18 +210,29 @@ class GemmTimer:
                          for i in range(nx)]
         self.Y = {M: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in Ms}
         self.reps = reps
+        self.ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+
+    def _workspace(self, M: int, pins: bd.Pins):
+        """A zeroed fold workspace large enough for this call (the counters
+        stay zero between calls, so it is only replaced when too small)."""
+        import torch
+        need = bd.bi_gemm_bf16_workspace_bytes(M, self.N, self.K, pins)
+        if need > self.ws.numel():
+            self.ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        return self.ws
 
     def __call__(self, M: int, pins: bd.Pins) -> float:
         import torch
         xs, W, Y = self.X[M], self.W, self.Y[M]
+        ws = self._workspace(M, pins)
         for i in range(3):
-            bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins)
+            bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins, workspace=ws)
         torch.cuda.synchronize()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()
         for i in range(self.reps):
-            bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins)
+            bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins, workspace=ws)
         e.record()
         torch.cuda.synchronize()
         if bd.bi_last_device_status() != bd.BI_OK:

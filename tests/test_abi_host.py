@@ -374,3 +374,34 @@ def test_plan_ktile_pairs(bd):
     deep = p.replace(stages=6)
     assert bd.bi_pins_validate(4096, 14336, deep) == bd.BI_OK
     assert bd.bi_pins_validate(4096, 14336, deep.replace(flags=bd.BI_FLAG_KTILE_PAIRS)) == bd.BI_ERR_ILLEGAL_PINS
+
+
+def test_global_schedule_plans_and_workspace_sizes(bd):
+    """The fold workspace a GLOBAL plan needs (host only): the per-tile
+    counters rounded up to 256 bytes, then one T x 128 fp32 partial per chain;
+    nothing for plans the schedule does not apply to."""
+    lib = bd.load()
+    p = bd.bi_pins_default(6144, 4096).replace(split_k=3)
+    pg = p.replace(flags=p.flags | bd.BI_FLAG_SCHEDULE_GLOBAL)
+    need = bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg)
+    assert need == 256 + 48 * 3 * 64 * 128 * 4
+    plan = bd.bi_gemm_plan_describe_ws(32, 6144, 4096, pg, 152, need)
+    assert plan.schedule == bd.BI_FLAG_SCHEDULE_GLOBAL and plan.grid_x == 144 and plan.cluster_x == 1
+    # the same tree as the other schedules
+    other = bd.bi_gemm_plan_describe(32, 6144, 4096, p.replace(flags=p.flags | bd.BI_FLAG_SCHEDULE_LOCAL), 152)
+    assert plan.tree() == other.tree()
+    # too little workspace, several token tiles, paired MMAs, S = 1 or S > 8: no GLOBAL
+    assert bd.bi_gemm_plan_describe_ws(32, 6144, 4096, pg, 152, need - 1).schedule != bd.BI_FLAG_SCHEDULE_GLOBAL
+    assert bd.bi_gemm_bf16_workspace_bytes(300, 6144, 4096, pg) == 0
+    assert bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg.replace(mma_ctas=2)) == 0
+    # a pinned single-CTA grouping keeps the pinned 256-token tile: larger partials
+    assert bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg.replace(mma_ctas=1)) == 256 + 48 * 3 * 256 * 128 * 4
+    assert bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg.replace(split_k=1)) == 0
+    assert bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg.replace(split_k=9)) == 0
+    assert bd.bi_gemm_bf16_workspace_bytes(32, 6144, 4096, pg.replace(split_k=8)) == 256 + 48 * 8 * 64 * 128 * 4
+    # schedule values past GLOBAL are illegal
+    for sched in (5, 6, 7):
+        assert lib.bi_pins_validate(6144, 4096, ctypes.byref(p.replace(flags=(p.flags & ~0x7) | sched))) == \
+            bd.BI_ERR_ILLEGAL_PINS
+    # the workspace entry point checks its alignment before anything else touches the GPU
+    assert lib.bi_gemm_bf16_ws(16, 32, 48, 4, 6144, 4096, None, 264, 1 << 20, None) == bd.BI_ERR_ALIGNMENT

@@ -196,3 +196,27 @@ def test_fused_tiny_batches_every_m(lib):
             torch.cuda.synchronize()
             assert same_bits(got, comp[:M]), "M=%d flags=%#x" % (M, p.flags)
     assert lib.bi_last_device_status() == lib.BI_OK
+
+
+@pytest.mark.parametrize("M", [1, 9, 64, 100])
+def test_fused_with_a_fold_workspace(lib, M):
+    """A fused-call workspace with room for the GEMM's fold in front: the
+    GLOBAL schedule folds the split partials there; both forms keep the
+    composition's bits, and the fold counters at the front are zero after
+    every call, whatever M the calls use."""
+    N, K = 1024, 4096
+    X, g, W = problem(128, N, K, seed=15)
+    x, gg, w = X.cuda(), g.cuda(), W.cuda()
+    pins = lib.bi_pins_default(N, K).replace(split_k=3)
+    pins = pins.replace(flags=pins.flags | lib.BI_FLAG_SCHEDULE_GLOBAL)
+    front = max(lib.bi_gemm_bf16_workspace_bytes(m, N, K, pins) for m in (1, 128))
+    assert front > 0
+    ws = torch.zeros(front + lib.bi_rmsnorm_gemm_workspace_bytes(128, K), dtype=torch.uint8, device="cuda")
+    comp = lib.bi_gemm_bf16(lib.bi_rmsnorm_bf16(x, gg, EPS), w, pins=pins)
+    for p in forms(lib, pins):
+        for m in (M, 128, M):
+            got = lib.bi_rmsnorm_gemm_bf16(x[:m], gg, w, EPS, pins=p, workspace=ws)
+            torch.cuda.synchronize()
+            assert same_bits(got, comp[:m]), "M=%d flags=%#x" % (m, p.flags)
+            assert bool((ws[: 8 * 4] == 0).all())        # the counters of the 8 W tiles
+    assert lib.bi_last_device_status() == lib.BI_OK

@@ -39,8 +39,9 @@ def test_family_cost_is_the_weighted_sum():
 
 def separable_cost(p):
     # a made-up cost, separable over the axes, with a unique optimum
-    return ({1: 9, 2: 5, 3: 4, 4: 1, 5: 3, 6: 6, 8: 7, 12: 8, 16: 9}[p.split_k] + {128: 2, 256: 0}[p.tok_tile]
-            + {0: 0, 1: 1, 2: 3}[p.mma_ctas] + (0 if p.flags & bd.BI_FLAG_KTILE_PAIRS else 0.5))
+    return ({1: 9, 2: 5, 3: 4, 4: 1, 5: 3, 6: 6, 7: 6.5, 8: 7, 12: 8, 16: 9}[p.split_k] + {128: 2, 256: 0}[p.tok_tile]
+            + {0: 0, 1: 1, 2: 3}[p.mma_ctas] + (0 if p.flags & bd.BI_FLAG_KTILE_PAIRS else 0.5)
+            + (0 if p.stages == 0 else 0.25))
 
 
 def test_search_finds_the_optimum_of_a_separable_cost_with_few_measurements(lib):
