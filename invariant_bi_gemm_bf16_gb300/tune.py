@@ -8,6 +8,8 @@ Workloads (synthetic inputs, random-init weights of the named shapes):
                       1, 2, 4, 2, 1, 1 (recorded by running the stack);
   llama31-8b-prefill  the Llama-3.1-8B qkv, gate_up and down_proj projections at
                       M = 1, 8, 32, 128, 1024, 4096, 8192, one call each.
+  llama31-8b-decode   the same projections at decode batch sizes 1, 8, 16, 32,
+                      64 with weights 1, 2, 2, 4, 1.
   decode-attention-70b  decode attention with Llama-3.1-70B heads (64 query, 8
                       key/value, pages of 16) over three decode steps, one each:
                       64 requests with lengths uniform on [512, 8192], 256 on
@@ -30,19 +32,27 @@ from . import tuner
 
 DECODE_MIX = {1: 1, 8: 2, 32: 4, 64: 2, 128: 1, 256: 1}
 PREFILL_MS = (1, 8, 32, 128, 1024, 4096, 8192)
+DECODE8B_MIX = {1: 1, 8: 2, 16: 2, 32: 4, 64: 1}
 
 
 def stack_time_us(stack, xs, reps=5):
+    """Device time of the decode mix (each batch size its weight's number of
+    steps), captured in a CUDA graph and replayed, like the families' timing."""
     for x in xs.values():
         stack.forward(x)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for M, x in xs.items():
+            for _ in range(DECODE_MIX[M]):
+                stack.forward(x)
+    g.replay()
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record()
     for _ in range(reps):
-        for M, x in xs.items():
-            for _ in range(DECODE_MIX[M]):
-                stack.forward(x)
+        g.replay()
     e.record()
     torch.cuda.synchronize()
     return s.elapsed_time(e) * 1e3 / reps
@@ -88,19 +98,29 @@ def run_decode(args):
     return entries, meta
 
 
-def run_prefill(args):
+def run_projections(args, calls_of_m, name):
     flags = bd.BI_FLAG_SCHEDULE_AUTO | bd.BI_FLAG_PREFETCH_W
     entries = []
     for N, K in ((6144, 4096), (28672, 4096), (4096, 14336)):
-        calls = [(M, 1) for M in PREFILL_MS]
+        calls = list(calls_of_m)
         e = tuner.tune_family(N, K, calls, mode=args.mode, reps=args.reps, base_flags=flags)
         print(json.dumps({k: e[k] for k in ("N", "K", "T_us", "T_default_us", "measured", "legal")}),
               file=sys.stderr, flush=True)
         entries.append(e)
-    meta = {"workload": "llama31-8b-prefill: qkv, gate_up, down_proj at M = %s, one call each" % (PREFILL_MS,),
-            "device": torch.cuda.get_device_name(), "sm_count": torch.cuda.get_device_properties(0).multi_processor_count,
-            "mode": args.mode}
+    meta = {"workload": name, "device": torch.cuda.get_device_name(),
+            "sm_count": torch.cuda.get_device_properties(0).multi_processor_count, "mode": args.mode}
     return entries, meta
+
+
+def run_prefill(args):
+    return run_projections(args, [(M, 1) for M in PREFILL_MS],
+                           "llama31-8b-prefill: qkv, gate_up, down_proj at M = %s, one call each" % (PREFILL_MS,))
+
+
+def run_decode8b(args):
+    return run_projections(args, sorted(DECODE8B_MIX.items()),
+                           "llama31-8b-decode: qkv, gate_up, down_proj at the decode batch mix %s"
+                           % json.dumps(DECODE8B_MIX))
 
 
 ATTN_STEPS = ((64, 512, 8192), (256, 64, 2048), (1, 32768, 32768))
@@ -120,8 +140,8 @@ def run_attention(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", choices=["llama31-70b-decode", "llama31-8b-prefill", "decode-attention-70b"],
-                    required=True)
+    ap.add_argument("--workload", choices=["llama31-70b-decode", "llama31-8b-prefill", "llama31-8b-decode",
+                                           "decode-attention-70b"], required=True)
     ap.add_argument("--mode", choices=["search", "exhaustive"], default="search")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--out", required=True)
@@ -131,6 +151,8 @@ def main(argv=None):
         entries, meta = run_decode(args)
     elif args.workload == "llama31-8b-prefill":
         entries, meta = run_prefill(args)
+    elif args.workload == "llama31-8b-decode":
+        entries, meta = run_decode8b(args)
     else:
         entries, meta = run_attention(args)
     tuner.dump(entries, args.out, **meta)

@@ -26,10 +26,13 @@ heads, key/value heads, page size); its calls are decode steps, each a list of
 request lengths with a count; the split size is the argmin of the family's
 summed time over the legal sizes (multiples of 64 up to 4096), all measured.
 
-Timing: each (candidate, M) is timed as back-to-back calls of bi_gemm_bf16_ws
-(with a fold workspace, so that the GLOBAL schedule is open to split counts
-whose clusters would not fit the GPU at once) between two CUDA events on
-rotating weight copies (more bytes than L2), after warm-up calls, and a
+Timing: each (candidate, M) is timed as calls of bi_gemm_bf16_ws (with a fold
+workspace, so that the GLOBAL schedule is open to split counts whose clusters
+would not fit the GPU at once) captured in a CUDA graph and replayed between
+two CUDA events, on rotating weight copies (more bytes than L2), after
+warm-up calls.  The graph keeps the binding's per-call host time out of the
+measurement: a decode call takes about as long on the host as on the GPU, and
+timed back to back from Python every candidate would look alike.  A
 candidate's cost takes the fastest of a few repeats (the SM clock drifts under
 the power cap).  The winner must then beat the default tuple by a margin
 in interleaved re-measurements (``confirm``), else the default is kept.
@@ -228,11 +231,16 @@ class GemmTimer:
         for i in range(3):
             bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins, workspace=ws)
         torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(self.reps):
+                bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins, workspace=ws)
+        g.replay()
+        torch.cuda.synchronize()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()
-        for i in range(self.reps):
-            bd.bi_gemm_bf16(xs[i % len(xs)], W[i % len(W)], out=Y, pins=pins, workspace=ws)
+        g.replay()
         e.record()
         torch.cuda.synchronize()
         if bd.bi_last_device_status() != bd.BI_OK:
