@@ -211,8 +211,9 @@ static cudaError_t launch_rows_vpt(const void* X, void* Q, float* scale, int64_t
 // order; the xor butterfly combines the lanes), then the E4M3 codes of y with
 // the row's scale, as bi_quantize_rows_e4m3 takes them from y.  One warp per
 // row; the block stages g once and each warp its row in shared memory by
-// 16-byte asynchronous copies, so X is read once and y never leaves the chip;
-// y is recomputed, with the same bits, for the amax and for the codes.
+// 16-byte asynchronous copies, so X is read once and y never leaves the chip.
+// Three passes over the staged row: the sum of squares; y (written back over
+// x) with its packed NaN-propagating maximum; the codes of y.
 constexpr int kRqSmemBudget = 100 * 1024;  // shared memory per block: rows and g
 
 int rq_rows_per_block(int64_t H) {
@@ -243,34 +244,27 @@ __global__ void __launch_bounds__(256)
   __syncthreads();  // g was copied by the whole block
   if (!live) return;
   float ss = 0.0f;
+#pragma unroll 4
   for (int i = lane; i < nvec; i += 32) ss = sumsq8(buf[i], ss);
   ss = butterfly_sum(ss);
   const float r = inv_rms(ss, H, eps);
-  float amax = 0.0f;
-  bool bad = false;
+  uint32_t am = 0u;
+#pragma unroll 4
   for (int i = lane; i < nvec; i += 32) {
     const uint4 y = norm8(buf[i], gs[i], r);
-    amax2(y.x, amax, bad);
-    amax2(y.y, amax, bad);
-    amax2(y.z, amax, bad);
-    amax2(y.w, amax, bad);
+    buf[i] = y;  // each lane reads back only its own vectors
+    am = absmax8(am, y);
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
-  }
+  const float amax = warp_amax(am);
+  const bool bad = !isfinite(amax);
   const float s = e4m3_row_scale(amax, bad);
   const float inv = e4m3_row_inv(amax);
   if (lane == 0) scale[row] = s;
   uint2* q = Q + row * nvec;
+#pragma unroll 4
   for (int i = lane; i < nvec; i += 32) {
-    if (bad) {
-      q[i] = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    } else {
-      const uint4 y = norm8(buf[i], gs[i], r);
-      q[i] = make_uint2(codes4(y.x, y.y, inv), codes4(y.z, y.w, inv));
-    }
+    const uint4 y = buf[i];
+    q[i] = bad ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : make_uint2(codes4(y.x, y.y, inv), codes4(y.z, y.w, inv));
   }
 }
 
@@ -295,21 +289,14 @@ __global__ void __launch_bounds__(256)
   for (int i = 0; i < VPL; ++i) ss = sumsq8(v[i], ss);
   ss = butterfly_sum(ss);
   const float r = inv_rms(ss, (int64_t)kVecs * 8, eps);
-  float amax = 0.0f;
-  bool bad = false;
+  uint32_t am = 0u;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     v[i] = norm8(v[i], __ldg(g + lane + 32 * i), r);
-    amax2(v[i].x, amax, bad);
-    amax2(v[i].y, amax, bad);
-    amax2(v[i].z, amax, bad);
-    amax2(v[i].w, amax, bad);
+    am = absmax8(am, v[i]);
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    bad = __shfl_xor_sync(0xffffffffu, (int)bad, off) || bad;
-  }
+  const float amax = warp_amax(am);
+  const bool bad = !isfinite(amax);
   const float s = e4m3_row_scale(amax, bad);
   const float inv = e4m3_row_inv(amax);
   if (lane == 0) scale[row] = s;
@@ -335,7 +322,10 @@ cudaError_t launch_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, 
     configured.fetch_or(bit);
   }
   // the row in registers for H = 2048, 4096 below 4096 rows (measured at
-  // H = 4096: 8.8 against 12.4 us at M = 2048; 30.2 against 26.4 at 8192)
+  // H = 4096: 8.8 against 12.4 us at M = 2048).  At M = 8192 the staged kernel
+  // takes 20.7 us (0.72 of HBM; 26.4 before y was written back and the
+  // maximum taken packed); a persistent variant with two rows per warp in
+  // flight took 23.1.
   if ((H == 2048 || H == 4096) && M < 4096) {
     // rows (warps) per block: ceil(M / 152) up to 8, as for the RMSNorm
     int64_t wpb = (M + 151) / 152;

@@ -66,6 +66,37 @@ __device__ __forceinline__ void amax2(uint32_t w, float& amax, bool& bad) {
   amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
 }
 
+// The largest |value| of packed bf16 pairs, NaN-propagating (max.NaN): a NaN
+// anywhere gives NaN, an infinity gives infinity, so one test of the row's
+// final maximum finds a row holding either.  The maximum is exact in any
+// order, and the sign is cleared first (so -0 and +0 both count as 0).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w & 0x7FFF7FFFu));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t absmax8(uint32_t acc, const uint4& v) {
+  acc = absmax_bf16x2(acc, v.x);
+  acc = absmax_bf16x2(acc, v.y);
+  acc = absmax_bf16x2(acc, v.z);
+  return absmax_bf16x2(acc, v.w);
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// The packed maxima of a warp's lanes -> the row's amax (all lanes agree).
+__device__ __forceinline__ float warp_amax(uint32_t acc) {
+  float m = fmax_nan(bf_lo(acc), bf_hi(acc));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
+  return m;
+}
+
 // Four E4M3 codes of x[0..3] * inv, x[0] in the lowest byte.
 __device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float inv) {
   const uint32_t lo = cvt_e4m3x2(__fmul_rn(bf_lo(w0), inv), __fmul_rn(bf_hi(w0), inv));

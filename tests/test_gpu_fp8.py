@@ -130,6 +130,9 @@ def test_rmsnorm_quantize_is_the_composition(lib, oracle, M, H):
     if M >= 3:
         X[1] = 0
         X[2, H // 3] = float("nan")
+    if M >= 5:
+        X[3, 7] = -float("inf")   # an infinity flags its row like a NaN
+        X[4] = -0.0               # signed zeros: the row's maximum is 0
     g = inputs.normal((H,), std=0.1, mean=1.0, seed=45, stream=2)
     x, gg = X.cuda(), g.cuda()
     q, sc = lib.bi_rmsnorm_quantize_e4m3(x, gg, 1e-5)
