@@ -52,8 +52,8 @@ EPS = 1e-5
 # (summaries in profiles/), keyed by build_fingerprint() of the GEMM kernel's
 # sources: valid only for the kernel build they were taken on.
 NCU_TRAFFIC = {
-    "f7bf86b71357c45995abf076d048fc0408fc349e71b191afc8cf003c605012b4": {8192: 965384960 + 63719424,
-                                                                        1: 117513472 + 2791168},
+    "5cc490084eac77fa506237ba28375c9a76e61dfc9fdd93e40a88d72774595f36": {8192: 962298880 + 65127680,
+                                                                        1: 117516032 + 2732288},
 }
 
 
@@ -977,6 +977,35 @@ def run_single_m(args, dist):
         raise RuntimeError(bd.status_string(st))
 
 
+def run_single_gemm(args, dist):
+    """Launches bi_gemm_bf16_ws with the default pins (plus the early weight
+    stream) and a zeroed fold workspace on one shape N:K:M, --launches times
+    on rotating weight copies larger than L2, for an ncu capture of those
+    launches (the decode projections' GLOBAL schedule, for one)."""
+    from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+    bd.load()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    N, K, M = (int(v) for v in args.single_gemm.split(":"))
+    nw = copies_for(N * K * 2, cap=8)
+    W = [inputs.device_normal((N, K), std=0.02, seed=dist.rank, stream=inputs.STREAM_W + 16 * i, device=dev)
+         for i in range(nw)]
+    x = inputs.device_normal((M, K), seed=dist.rank, stream=inputs.STREAM_X, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    pins = bd.bi_pins_default(N, K)
+    pins = pins.replace(flags=pins.flags | bd.BI_FLAG_PREFETCH_W)
+    ws = torch.zeros(max(bd.bi_gemm_bf16_workspace_bytes(M, N, K, pins), 256), dtype=torch.uint8, device=dev)
+    plan = bd.bi_gemm_plan_describe_ws(M, N, K, pins, 0, ws.numel())
+    print(json.dumps({"single_gemm": [N, K, M], "schedule": plan.schedule, "split_k": plan.split_k,
+                      "tok_tile": plan.tok_tile, "grid": [plan.grid_x, plan.grid_y, plan.grid_z]}), flush=True)
+    for i in range(args.launches):
+        bd.bi_gemm_bf16(x, W[i % nw], out=y, pins=pins, workspace=ws)
+    torch.cuda.synchronize()
+    st = bd.bi_last_device_status()
+    if st != bd.BI_OK:
+        raise RuntimeError(bd.status_string(st))
+
+
 def run_single_attention(args, dist):
     """Launches decode attention on one request mix (MIX:SPLIT), --launches
     times, for an ncu capture of those launches."""
@@ -1100,6 +1129,8 @@ def main():
                     help="H:M -- only launch RMSNorm on that shape (for ncu)")
     ap.add_argument("--single-attention", default="",
                     help="MIX:SPLIT -- only launch decode attention on that request mix (for ncu)")
+    ap.add_argument("--single-gemm", default="",
+                    help="N:K:M -- only launch bi_gemm_bf16_ws on that shape --launches times (for ncu)")
     ap.add_argument("--single-m", type=int, default=0,
                     help="profiling helper: only launch the sweep's GEMM at this M --launches times")
     ap.add_argument("--launches", type=int, default=3)
@@ -1122,6 +1153,9 @@ def main():
             return
         if args.single_m:
             run_single_m(args, dist)
+            return
+        if args.single_gemm:
+            run_single_gemm(args, dist)
             return
         if args.impl == "reference":
             res = run_reference(args, dist)
