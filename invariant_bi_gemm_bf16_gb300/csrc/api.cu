@@ -982,6 +982,12 @@ bi_status attn_geometry(int64_t B, int64_t Hq, int64_t Hkv, int64_t max_seq_len,
   return BI_OK;
 }
 
+int32_t log2_pow2(int64_t v) {
+  int32_t s = 0;
+  while (((int64_t)1 << s) < v) ++s;
+  return s;
+}
+
 // Workspace: 256 bytes of control words (ticket counter, item count), the
 // item list (one uint32 per (request, split), padded to 256 bytes), then the
 // split records (B * Hkv * n_split of (128 + 2) * GP floats).
@@ -991,16 +997,18 @@ int64_t attn_ws_bytes(int64_t B, int64_t Hkv, int64_t n_split, int64_t gp) {
   return 256 + attn_list_bytes(B, n_split) + B * Hkv * n_split * (BI_ATTN_HEAD_DIM + 2) * gp * 4;
 }
 
-// A paged cache [num_pages, page_size, Hkv, 128] seen as rows of Hkv * 128
-// values; a box is box_rows positions of one 64-value half of one head.
+// A paged cache [num_pages, page_size, Hkv, 128] seen as [rows][2 Hkv][64]:
+// position, 64-value half of a head, value.  A box is {64 values, the two
+// halves of one head, box_rows positions}, landing as 2 box_rows rows of
+// 128 bytes (position-major).
 bool encode_cache(CUtensorMap* map, const void* ptr, int64_t rows, int64_t Hkv, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)(Hkv * BI_ATTN_HEAD_DIM), (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(Hkv * BI_ATTN_HEAD_DIM * 2)};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  cuuint64_t dims[3] = {64, (cuuint64_t)(Hkv * 2), (cuuint64_t)rows};
+  cuuint64_t strides[2] = {128, (cuuint64_t)(Hkv * BI_ATTN_HEAD_DIM * 2)};
+  cuuint32_t box[3] = {64, 2, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1038,7 +1046,7 @@ BI_API bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, co
     return BI_ERR_ALIGNMENT;
   if (ws_bytes < (size_t)attn_ws_bytes(B, Hkv, n_split, gp)) return BI_ERR_WORKSPACE;
   AttnLaunch A = {};
-  const int box_rows = (int)std::min<int64_t>(page_size, 32);
+  const int box_rows = (int)std::min<int64_t>(page_size, 32);  // one 32-position tile at most
   if (!encode_cache(&A.tmK, k_cache, num_pages * page_size, Hkv, box_rows) ||
       !encode_cache(&A.tmV, v_cache, num_pages * page_size, Hkv, box_rows))
     return BI_ERR_CUDA;
@@ -1056,6 +1064,9 @@ BI_API bi_status bi_decode_attention_bf16(const void* q, const void* k_cache, co
   A.p.G = (int32_t)(Hq / Hkv);
   A.p.page_size = (int32_t)page_size;
   A.p.box_rows = box_rows;
+  A.p.page_shift = log2_pow2(page_size);
+  A.p.box_shift = log2_pow2(box_rows);
+  A.p.nreq = (int32_t)B;
   A.p.split_size = (int32_t)split_size;
   A.p.n_split = (int32_t)n_split;
   A.p.qk_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
