@@ -356,9 +356,6 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
   __shared__ __align__(8) uint64_t full[NS];
   __shared__ AttnItem queue[W][kQ];
 
-  grid_dep_launch_dependents();
-  grid_dep_wait();  // the item list, q and the cache come from earlier kernels
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const uint32_t smem0 = (smem_u32(attn_smem_raw) + 1023u) & ~1023u;
@@ -368,6 +365,10 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  grid_dep_wait();  // the item list, q, the lengths and the cache come from earlier kernels
+  // Only now may the combine start: its CTAs read the lengths before their
+  // own wait, which is safe once every earlier kernel has completed.
+  grid_dep_launch_dependents();
   const uint32_t n_tickets = STATIC ? 0u : p.ctl[1] * (uint32_t)p.Hkv;
   AttnItem* Q = queue[warp];
   // Positions stay below 2^28 (n_split <= 65535 splits of <= 4096) and cache
@@ -503,14 +504,44 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
     }
   };
 
-  // ---- cache rows of one tile: lane j < nb holds the row of box j.
-  auto tile_rows = [&](const AttnItem& it, int t, int& nb) -> int32_t {
+  // ---- page ids.  A window is 32 consecutive pages of an item (from the
+  // page holding its first position), lane j holding page 32 w + j of
+  // window w (-1 past the item's last page).  The issue side keeps the
+  // window in use (wcur) and the next one (wnx: the item's next window, or
+  // the next item's first), loaded while the current one is in use, so that
+  // no tile waits for the block table.
+  auto win_load = [&](const AttnItem& it, int w) -> int32_t {
+    const int32_t fp = it.p0 >> pshift;
+    const int32_t np = ((it.p1 - 1) >> pshift) - fp + 1;
+    const int32_t j = 32 * w + lane;
+    return j < np ? it.bt[fp + j] : -1;
+  };
+  int32_t wcur = -1, wnx = -1;
+  int wcur_item = -1, wcur_w = 0, wnx_item = -1, wnx_w = 0;
+  int wpf_ready = -1;  // nready when the last prefetch attempt found nothing to load
+
+  // ---- cache rows of tile t of item number ii: lane j < nb holds the row
+  // of box j.
+  auto tile_rows = [&](const AttnItem& it, int ii, int t, int& nb) -> int32_t {
     const int32_t tp = it.p0 + t * kAttnTile, left = it.p1 - tp;
     nb = left >= kAttnTile ? full_nb : (left + (1 << bshift) - 1) >> bshift;
+    const int32_t pos = tp + (lane << bshift);
+    const int32_t rel = (pos >> pshift) - (it.p0 >> pshift);  // page of the item
+    const int w = ((tp >> pshift) - (it.p0 >> pshift)) >> 5;  // a tile never spans two windows
+    if (wcur_item != ii || wcur_w != w) {
+      if (wnx_item == ii && wnx_w == w) {
+        wcur = wnx;
+      } else {
+        wcur = win_load(it, w);  // not prefetched (the item was not fetched in time)
+      }
+      wcur_item = ii;
+      wcur_w = w;
+      wnx_item = -1;
+      wpf_ready = -1;
+    }
+    const int32_t pg = __shfl_sync(0xffffffffu, wcur, rel & 31);
     int32_t y = 0;
     if (lane < nb) {
-      const int32_t pos = tp + (lane << bshift);
-      const int32_t pg = it.bt[pos >> pshift];
       if ((uint32_t)pg >= npages) {
         attn_flag(p.status, (int)BI_ERR_INVALID_ARG);
         y = rows;  // past the cache's end: zeros
@@ -519,6 +550,24 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
       }
     }
     return y;
+  };
+  // Loads the window after the one in use, if it is known and not loaded
+  // (tried again only once another item has been fetched).
+  auto win_prefetch = [&]() {
+    if (wnx_item >= 0 || wcur_item < 0 || wpf_ready == nready) return;
+    const AttnItem& it = Q[wcur_item & (kQ - 1)];
+    const int32_t np = ((it.p1 - 1) >> pshift) - (it.p0 >> pshift) + 1;
+    if (32 * (wcur_w + 1) < np) {
+      wnx = win_load(it, wcur_w + 1);
+      wnx_item = wcur_item;
+      wnx_w = wcur_w + 1;
+    } else if (wcur_item + 1 < nready) {
+      wnx = win_load(Q[(wcur_item + 1) & (kQ - 1)], 0);
+      wnx_item = wcur_item + 1;
+      wnx_w = 0;
+    } else {
+      wpf_ready = nready;
+    }
   };
 
   // Issues tile t of item it into stage st (rows y from tile_rows): the K and
@@ -548,8 +597,8 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
   int pi = 0, pt = 0, ci = 0, ct = 0, issued = 0, consumed = 0;
   int ist = 0, cst = 0;  // stages of the next issue and of the next tile consumed
   uint32_t cph = 0;      // phase parity of stage cst
-  int pf_item = -1, pf_tile = 0, pf_nb = 0;  // the tile whose rows pf_y holds
-  int32_t pf_y = 0;
+  AttnItem iit, cit;     // the items being issued (number iit_n) and consumed
+  int iit_n = -1;
   bool ok = true;
   while (ok) {
     fetch_step(pi);
@@ -558,25 +607,21 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
       // an item's first tile overwrites the q buffer: not before the
       // previous item has read it (its first tile consumed)
       if (pt == 0 && ci < pi && !(ci == pi - 1 && ct > 0)) break;
-      const AttnItem it = Q[pi & (kQ - 1)];
-      int nb = pf_nb;
-      int32_t y = pf_y;
-      if (pf_item != pi || pf_tile != pt) y = tile_rows(it, pt, nb);
-      issue(it, pt, ist, nb, y);
+      if (iit_n != pi) {
+        iit = Q[pi & (kQ - 1)];
+        iit_n = pi;
+      }
+      int nb = 0;
+      const int32_t y = tile_rows(iit, pi, pt, nb);
+      issue(iit, pt, ist, nb, y);
       ++issued;
       if (++ist == nst) ist = 0;
-      if (++pt == it.ntiles) {
+      if (++pt == iit.ntiles) {
         pt = 0;
         ++pi;
       }
-      // the next tile's rows load while this one is in flight
-      pf_item = -1;
-      if (pi < nready) {
-        pf_y = tile_rows(Q[pi & (kQ - 1)], pt, pf_nb);
-        pf_item = pi;
-        pf_tile = pt;
-      }
     }
+    win_prefetch();
     if (consumed == issued) {
       if (fetch_done && pi == nready && fs == 0) break;
       continue;  // waiting for the next item's fetch
@@ -588,7 +633,8 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
       ok = false;
       break;
     }
-    const AttnItem it = Q[ci & (kQ - 1)];
+    if (ct == 0) cit = Q[ci & (kQ - 1)];
+    const AttnItem& it = cit;
     const uint32_t kb = ring + (uint32_t)(st * SB);
     if (ct == 0) {
       // a new split: fresh state, and q as the MMA's B operand (k = d, n =
@@ -695,12 +741,14 @@ __global__ void __launch_bounds__(CT) decode_attn_combine_kernel(const AttnParam
   static_assert(DPT >= 1 && SD % DSTEP == 0, "combine layout");
   // records whose loads are in flight together (about 32 values per thread)
   constexpr int A = 32 / DPT < 4 ? 4 : (32 / DPT > 32 ? 32 : 32 / DPT);
-  grid_dep_launch_dependents();
-  grid_dep_wait();  // the split records come from the previous kernel
   const int kvh = blockIdx.x / SL, slice = blockIdx.x % SL;
   const int t = threadIdx.x, h = t % GP, d0 = slice * SD + t / GP;
   const int64_t b = blockIdx.y;
+  // The stream kernel lets this grid start only after its own wait, so the
+  // kernels that wrote the lengths have completed: read them before waiting.
   const int64_t L = p.seq_lens[b];
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // the split records come from the previous kernel
   __nv_bfloat16* ob = out + (b * p.Hq + (int64_t)kvh * p.G + h) * kAttnD + d0;
   if (L <= 0 || L > p.max_len) {
     // an empty request gives zeros; an invalid length (flagged by the plan
