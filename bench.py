@@ -1025,19 +1025,27 @@ def run_single_attention(args, dist):
 
 
 def run_single_rmsnorm(args, dist):
-    """Launches RMSNorm on one shape (H:M), --launches times on rotating
-    inputs, for an ncu capture of those launches."""
+    """Launches RMSNorm on one shape (H:M), or RMSNorm with the E4M3
+    quantisation (H:M:q), --launches times on rotating inputs, for an ncu
+    capture of those launches."""
     from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
     bd.load()
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
-    H, M = (int(x) for x in args.single_rmsnorm.split(":"))
+    parts = args.single_rmsnorm.split(":")
+    H, M = int(parts[0]), int(parts[1])
+    quant = len(parts) > 2 and parts[2] == "q"
     n = copies_for(M * H * 2, cap=8)
     xs = [inputs.device_normal((M, H), seed=dist.rank, stream=60 + i, device=dev) for i in range(n)]
     g = inputs.device_normal((H,), std=0.1, mean=1.0, seed=dist.rank, stream=inputs.STREAM_G, device=dev)
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    q = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    sc = torch.empty(M, dtype=torch.float32, device=dev)
     for i in range(args.launches):
-        bd.bi_rmsnorm_bf16(xs[i % n], g, EPS, out=y)
+        if quant:
+            bd.bi_rmsnorm_quantize_e4m3(xs[i % n], g, EPS, q=q, scale=sc)
+        else:
+            bd.bi_rmsnorm_bf16(xs[i % n], g, EPS, out=y)
     torch.cuda.synchronize()
 
 
@@ -1126,7 +1134,7 @@ def main():
     ap.add_argument("--single-logsoftmax", default="",
                     help="M: only launch the log-softmax kernels on M rows of V = 128256 logits (for ncu)")
     ap.add_argument("--single-rmsnorm", default="",
-                    help="H:M -- only launch RMSNorm on that shape (for ncu)")
+                    help="H:M -- only launch RMSNorm on that shape (H:M:q: RMSNorm with the E4M3 quantisation) (for ncu)")
     ap.add_argument("--single-attention", default="",
                     help="MIX:SPLIT -- only launch decode attention on that request mix (for ncu)")
     ap.add_argument("--single-gemm", default="",

@@ -42,12 +42,17 @@ constexpr int kLsmStride = kLsmCtas * kLsmThreads;  // vectors between a thread'
 __device__ __forceinline__ float lsm_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float lsm_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// m = max(m, m2), s = s exp(m_old - m) + s2 exp(m2 - m).  The side holding
+// the maximum is multiplied by exp(0) = 1, which is exact, so only the other
+// side's factor is evaluated (the same bits as evaluating both).
 __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) {
     s = 0.0f;
   } else {
-    s = __fadd_rn(__fmul_rn(s, expf(m - mm)), __fmul_rn(s2, expf(m2 - mm)));
+    const bool keep = m == mm;                 // this side holds the maximum
+    const float e = expf((keep ? m2 : m) - mm);
+    s = keep ? __fadd_rn(s, __fmul_rn(s2, e)) : __fadd_rn(__fmul_rn(s, e), s2);
   }
   m = mm;
 }
