@@ -170,7 +170,9 @@ typedef enum bi_status {
   BI_ERR_ILLEGAL_PINS = 4,      /* bi_pins_validate() refused the pins */
   BI_ERR_CUDA = 5,              /* a CUDA runtime call failed (launch, no device, ...) */
   BI_ERR_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait ran out (see bi_last_device_status) */
-  BI_ERR_WORKSPACE = 7          /* workspace missing or smaller than required */
+  BI_ERR_WORKSPACE = 7,         /* workspace missing or smaller than required */
+  BI_ERR_DEBUG_BOUNDS = 8       /* (debug-bounds build only) a kernel's index check failed; the
+                                   access was skipped (see bi_debug_bounds_detail) */
 } bi_status;
 
 /* Version of this ABI (BI_PINS_ABI_VERSION). */
@@ -178,6 +180,24 @@ int32_t bi_abi_version(void);
 
 /* Human-readable name of a status.  Never NULL; static storage. */
 const char* bi_status_string(bi_status status);
+
+/* 1 in the debug-bounds build of the library (libbi_gemm_debug.so, compiled
+ * with -DBI_DEBUG_BOUNDS), 0 in the ordinary one.  In the debug-bounds build
+ * the GEMM and decode-attention kernels check, before each access, their tile
+ * coordinates (W and X rows, K tiles) and their ring-stage, tensor-memory
+ * column, fold-workspace and split-record indices against the bounds of what
+ * they address.  A failed check skips the access (it never traps), records
+ * BI_ERR_DEBUG_BOUNDS for bi_last_device_status(), and keeps the first
+ * failure's check number and value for bi_debug_bounds_detail(); the kernel
+ * then gives up through its bounded waits.  Same ABI and same bits otherwise:
+ * a speed-only variant for tests.  Host only. */
+int32_t bi_debug_bounds_enabled(void);
+
+/* The first failed check since the last call, as (check << 48) | value, and
+ * clears it (0 when none failed).  The check numbers are listed in the
+ * library's bounds.cuh.  Synchronises `stream`.  Errors: BI_ERR_INVALID_ARG
+ * (detail NULL), BI_ERR_CUDA. */
+bi_status bi_debug_bounds_detail(uint64_t* detail, bi_stream_t stream);
 
 /* The library's pins for a GEMM with N output features and reduction length
  * K.  There is no M argument: the table is keyed on (N, K) alone (Detent,

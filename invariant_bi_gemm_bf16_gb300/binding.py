@@ -18,6 +18,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbi_gemm.so")
+LIB_DEBUG_PATH = os.path.join(_PKG, "libbi_gemm_debug.so")  # the debug-bounds build
 
 BI_OK = 0
 BI_ERR_INVALID_ARG = 1
@@ -27,6 +28,7 @@ BI_ERR_ILLEGAL_PINS = 4
 BI_ERR_CUDA = 5
 BI_ERR_DEVICE_TIMEOUT = 6
 BI_ERR_WORKSPACE = 7
+BI_ERR_DEBUG_BOUNDS = 8
 
 BI_PINS_ABI_VERSION = 1
 BI_BK = 64
@@ -131,6 +133,8 @@ _SIGNATURES = {
     "bi_silu_mul_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "bi_attention_ctx1_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "bi_last_device_status": (ctypes.c_int, [_vp]),
+    "bi_debug_bounds_enabled": (ctypes.c_int32, []),
+    "bi_debug_bounds_detail": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), _vp]),
     "bi_log_softmax_bf16": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "bi_quantize_rows_e4m3": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "bi_pins_default_fp8": (ctypes.c_int, [_i64, _i64, ctypes.POINTER(Pins)]),
@@ -148,11 +152,13 @@ _SIGNATURES = {
 
 
 def load(path: str | None = None):
-    """Loads libbi_gemm.so (built by ``__graft_entry__.build()``); raises if absent."""
+    """Loads libbi_gemm.so (built by ``__graft_entry__.build()``), or the
+    library named by the BI_GEMM_LIB environment variable (the debug-bounds
+    variant, for one); raises if absent."""
     global _lib
     with _lock:
         if _lib is None:
-            p = path or LIB_PATH
+            p = path or os.environ.get("BI_GEMM_LIB") or LIB_PATH
             if not os.path.exists(p):
                 raise RuntimeError("libbi_gemm.so is not built (%s); run __graft_entry__.build()" % p)
             lib = ctypes.CDLL(p)
@@ -537,6 +543,19 @@ def bi_attention_ctx1_bf16(qkv: torch.Tensor, nq: int, nkv: int, D: int, out: to
 def bi_last_device_status(stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device's stall status."""
     return int(load().bi_last_device_status(_stream(stream)))
+
+
+def bi_debug_bounds_enabled() -> bool:
+    """True for the debug-bounds build of the library."""
+    return bool(load().bi_debug_bounds_enabled())
+
+
+def bi_debug_bounds_detail(stream=None) -> int:
+    """The first failed index check since the last call, (check << 48) | value
+    (0 if none), then cleared.  Synchronises the stream."""
+    out = ctypes.c_uint64(0)
+    _check(load().bi_debug_bounds_detail(ctypes.byref(out), _stream(stream)), "bi_debug_bounds_detail")
+    return int(out.value)
 
 
 # ---------------------------------------------------------------------------

@@ -716,8 +716,23 @@ BI_API const char* bi_status_string(bi_status s) {
     case BI_ERR_CUDA: return "BI_ERR_CUDA: CUDA runtime error";
     case BI_ERR_DEVICE_TIMEOUT: return "BI_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
     case BI_ERR_WORKSPACE: return "BI_ERR_WORKSPACE: workspace missing or too small";
+    case BI_ERR_DEBUG_BOUNDS: return "BI_ERR_DEBUG_BOUNDS: a kernel's index check failed (debug-bounds build)";
   }
   return "BI_ERR_UNKNOWN";
+}
+
+BI_API int32_t bi_debug_bounds_enabled(void) {
+#ifdef BI_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+BI_API bi_status bi_debug_bounds_detail(uint64_t* detail, bi_stream_t stream) {
+  if (!detail) return BI_ERR_INVALID_ARG;
+  return fetch_and_clear_bounds_detail(detail, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? BI_OK
+                                                                                                      : BI_ERR_CUDA;
 }
 
 BI_API bi_status bi_pins_default(int64_t N, int64_t K, bi_pins* out) { return pins_default(N, K, out); }

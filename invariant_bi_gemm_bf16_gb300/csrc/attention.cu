@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include "attention.h"
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -574,6 +575,11 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
   // V boxes (one per lane, lanes < nb), and q into the q buffer with the
   // item's first tile.
   auto issue = [&](const AttnItem& it, int t, int st, int nb, int32_t y) {
+    // debug-bounds build: the stage within the pool, the item within range
+    if (!bounds_ok(st >= 0 && st < nst && sbase + nst <= NS, p.status, kChkAttnStage, (uint64_t)(sbase + st)) ||
+        !bounds_ok(it.b >= 0 && it.b < p.nreq && it.kvh >= 0 && it.kvh < p.Hkv && it.s >= 0 && it.s < p.n_split,
+                   p.status, kChkAttnItem, ((uint64_t)(uint32_t)it.b << 32) | (uint32_t)it.s))
+      return;  // the stage's barrier stays short: the wait gives up
     const uint32_t stage = ring + (uint32_t)(st * SB);
     const uint32_t fb = smem_u32(&full[sbase + st]);
     if (lane == 0)
@@ -681,8 +687,14 @@ __global__ void __launch_bounds__(32 * AttnCfg<NT>::warps, 1)
           l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 8));
           l[j][cc] = __fadd_rn(l[j][cc], __shfl_xor_sync(0xffffffffu, l[j][cc], 16));
         }
-      float* rec = p.part + (((int64_t)it.b * p.Hkv + it.kvh) * (int64_t)p.n_split + it.s) *
-                                (int64_t)((kAttnD + 2) * GP);
+      const int64_t rec_i = ((int64_t)it.b * p.Hkv + it.kvh) * (int64_t)p.n_split + it.s;
+      if (!bounds_ok(rec_i >= 0 && rec_i < (int64_t)p.nreq * p.Hkv * p.n_split, p.status, kChkAttnRecord,
+                     (uint64_t)rec_i)) {
+        ct = 0;
+        ++ci;
+        continue;
+      }
+      float* rec = p.part + rec_i * (int64_t)((kAttnD + 2) * GP);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll

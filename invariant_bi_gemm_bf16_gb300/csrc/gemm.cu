@@ -6,7 +6,9 @@
 
 namespace bi {
 
-__device__ int g_stall_status;  // 0, or a bi_status code set by a kernel that gave up
+// [0]: 0, or a bi_status code set by a kernel that gave up; [2..3]: the
+// debug-bounds build's detail word (the first failed index check)
+__device__ __align__(8) int g_stall_status[4];
 
 // ---------------------------------------------------------------------------
 // host side
@@ -80,6 +82,19 @@ cudaError_t fetch_and_clear_stall(int* host_dst, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int zero = 0;
   e = cudaMemcpyToSymbolAsync(g_stall_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
+
+cudaError_t fetch_and_clear_bounds_detail(uint64_t* host_dst, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(host_dst, g_stall_status, sizeof(uint64_t), 2 * sizeof(int),
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  const uint64_t zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_stall_status, &zero, sizeof(uint64_t), 2 * sizeof(int), cudaMemcpyHostToDevice,
+                              stream);
   if (e != cudaSuccess) return e;
   return cudaStreamSynchronize(stream);
 }

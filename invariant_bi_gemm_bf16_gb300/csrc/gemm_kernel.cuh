@@ -55,6 +55,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "bounds.cuh"
 #include "ptx.cuh"
 #include "rowmath.cuh"
 
@@ -208,9 +209,15 @@ __device__ __forceinline__ void global_fold_epilogue(const GemmParams& p, SmemCt
     const int mv = min(max(mvt - half * kHalf, 0), kHalf);  // ... in this warp's columns
     float* part = p.fold_part + ((int64_t)t * T + half * kHalf) * kTileN + n_local;
     const uint32_t taddr = tmem_base + t_lane + buf * (uint32_t)T + (uint32_t)(half * kHalf);
+    // debug-bounds build: the chain's partial within the workspace's tiles * S
+    // partials, its columns within the allocation
+    const bool part_ok =
+        bounds_ok(t >= 0 && t < (int64_t)p.n_tiles * p.m_tiles * S, p.status, kChkFoldPart, (uint64_t)t) &&
+        bounds_ok(buf * (uint32_t)T + (uint32_t)(half * kHalf + kHalf) <= 2u * (uint32_t)T, p.status, kChkTmemCol,
+                  (uint64_t)(buf * T + half * kHalf));
 #pragma unroll
     for (int c = 0; c < kHalf; c += 4) {
-      if (c < mv) {
+      if (c < mv && part_ok) {
         float v[4];
         tmem_ld4(taddr + (uint32_t)c, v);
 #pragma unroll
@@ -225,9 +232,12 @@ __device__ __forceinline__ void global_fold_epilogue(const GemmParams& p, SmemCt
     __threadfence();  // the partial is visible before the count
     named_barrier_sync(2, 32 * kEpiWarps);
     if (et == 0) {
-      const uint32_t before = atomicAdd(p.fold_count + tile, 1u);
-      const int last = before == (uint32_t)(S - 1);
-      if (last) p.fold_count[tile] = 0u;  // all S chains counted in: zero for the next call
+      int last = 0;
+      if (bounds_ok(tile >= 0 && tile < (int64_t)p.n_tiles * p.m_tiles, p.status, kChkFoldTile, (uint64_t)tile)) {
+        const uint32_t before = atomicAdd(p.fold_count + tile, 1u);
+        last = before == (uint32_t)(S - 1);
+        if (last) p.fold_count[tile] = 0u;  // all S chains counted in: zero for the next call
+      }
       ctl->fold_last = last;
     }
     named_barrier_sync(2, 32 * kEpiWarps);
@@ -450,7 +460,13 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
               ok = false;
               break;
             }
-            if (!(stall && issued == 0)) {
+            // debug-bounds build: the stage, the K tile and the row of the copy
+            const bool in_bounds =
+                bounds_ok(stage < nst, p.status, is_w ? kChkWStage : kChkXStage, (uint64_t)stage) &&
+                bounds_ok(kt >= 0 && kt < KT, p.status, kChkKTile, (uint64_t)kt) &&
+                bounds_ok(is_w ? row < p.n_tiles * kMmaM : row < p.m_tiles * T, p.status, is_w ? kChkWRow : kChkXRow,
+                          (uint64_t)row);
+            if (!(stall && issued == 0) && in_bounds) {
               const uint32_t full = smem_u32(&full_bar[stage]);
               const uint32_t dst = ring + (uint32_t)stage * stage_sz;
               const int32_t kx = (int32_t)(kt * kTileElems);  // 2-D maps: element column
@@ -546,6 +562,11 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
             break;
           }
           tc_fence_after();
+          if (!bounds_ok(buf * (uint32_t)T + (uint32_t)T <= kTmemCols && wi < ws && xi < xs, p.status, kChkTmemCol,
+                         (uint64_t)buf * T)) {
+            ok = false;
+            break;
+          }
           const uint32_t d_tmem = tmem_base + buf * (uint32_t)T;
           const int64_t k0 = split_begin(s, S, KT), k1 = split_begin(s + 1, S, KT);
           for (int64_t kt = k0; kt < k1; kt += KP) {
@@ -790,6 +811,11 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
             break;
           }
           tc_fence_after();
+          if (!bounds_ok(buf * (uint32_t)T + (uint32_t)(half * kHalf + kHalf) <= kTmemCols, p.status, kChkTmemCol,
+                         (uint64_t)(buf * T + half * kHalf))) {
+            ok = false;
+            break;
+          }
           const uint32_t taddr = tmem_base + t_lane + buf * (uint32_t)T + (uint32_t)(half * kHalf);
           // four columns per load: with the 64-float sum live, wider loads
           // push the epilogue past its register budget (and into local memory)
@@ -841,7 +867,11 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
         const int64_t m0 = (int64_t)blockIdx.z * T;
         const int64_t rem = p.M - m0;
         const int mv = rem < T ? (int)rem : T;              // valid tokens in this tile
-        const int c_end = min(half * kHalf + kHalf, (mv + 7) & ~7);
+        int c_end = min(half * kHalf + kHalf, (mv + 7) & ~7);
+        // debug-bounds build: the partial's rows within the [T][128] tile, the
+        // chains' columns within the allocation
+        if (!bounds_ok(c_end <= T && (uint32_t)(nch * T) <= kTmemCols, p.status, kChkClusterPart, (uint64_t)c_end))
+          c_end = 0;
         float* P = reinterpret_cast<float*>(smem);
         for (int c = half * kHalf; c < c_end; c += 8) {
           float v[8];

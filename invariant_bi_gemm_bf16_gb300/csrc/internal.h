@@ -161,5 +161,7 @@ size_t fused_workspace_bytes(int64_t M, int64_t K);
 // Reads and clears the current device's stall word (asynchronously on
 // `stream`; the caller synchronises).
 cudaError_t fetch_and_clear_stall(int* host_dst, cudaStream_t stream);
+// the debug-bounds build's detail word (bounds.cuh), then cleared
+cudaError_t fetch_and_clear_bounds_detail(uint64_t* host_dst, cudaStream_t stream);
 
 }  // namespace bi
