@@ -269,21 +269,30 @@ __global__ void __launch_bounds__(256)
 }
 
 // The same with the row in registers (H = 256 * VPL): every vector of a
-// lane is loaded at once, normalised in place, and quantised from there.
+// lane is loaded at once, normalised in place, and quantised from there.  The
+// block stages g in shared memory first, so that the norm pass holds one
+// gain vector at a time beside the row (at most 128 registers: two blocks of
+// 8 rows per SM).
 template <int VPL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     rmsnorm_quantize_regs_kernel(const uint4* X, const uint4* __restrict__ g, uint2* Q, float* scale, int64_t M,
                                  float eps) {
+  constexpr int kVecs = VPL * 32;
+  __shared__ uint4 gs[kVecs];
+  for (int i = threadIdx.x; i < kVecs; i += blockDim.x) gs[i] = __ldg(g + i);  // g is a weight
   grid_dep_launch_dependents();
   grid_dep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= M) return;
-  constexpr int kVecs = VPL * 32;
-  const uint4* x = X + row * kVecs;
+  const bool live = row < M;
   uint4 v[VPL];
+  if (live) {
+    const uint4* x = X + row * kVecs;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) v[i] = __ldcs(x + lane + 32 * i);
+    for (int i = 0; i < VPL; ++i) v[i] = __ldcs(x + lane + 32 * i);
+  }
+  __syncthreads();  // gs is complete
+  if (!live) return;
   float ss = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) ss = sumsq8(v[i], ss);
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(256)
   uint32_t am = 0u;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    v[i] = norm8(v[i], __ldg(g + lane + 32 * i), r);
+    v[i] = norm8(v[i], gs[lane + 32 * i], r);
     am = absmax8(am, v[i]);
   }
   const float amax = warp_amax(am);
@@ -322,10 +331,11 @@ cudaError_t launch_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, 
     configured.fetch_or(bit);
   }
   // the row in registers for H = 2048, 4096 below 4096 rows (measured at
-  // H = 4096: 8.8 against 12.4 us at M = 2048).  At M = 8192 the staged kernel
-  // takes 20.7 us (0.72 of HBM; 26.4 before y was written back and the
-  // maximum taken packed); a persistent variant with two rows per warp in
-  // flight took 23.1.
+  // H = 4096, M = 2048: 7.5 us with g staged in shared memory and 128
+  // registers, 8.8 with g from L2 and 205 registers, 12.4 staged).  At
+  // M = 8192 the staged kernel takes 20.7 us (0.72 of HBM; 26.4 before y was
+  // written back and the maximum taken packed) against 23.1 for the register
+  // kernel; a persistent variant with two rows per warp in flight took 23.1.
   if ((H == 2048 || H == 4096) && M < 4096) {
     // rows (warps) per block: ceil(M / 152) up to 8, as for the RMSNorm
     int64_t wpb = (M + 151) / 152;
