@@ -255,3 +255,43 @@ def test_attention_full_size_sampled(lib, oracle):
         v = f64(vc[pages, pos % P, kvh])
         tol = head_tolerance(ref[i], got[i], qf[b, h], k, v, 1 / math.sqrt(D))
         assert np.all(np.abs(got[i] - ref[i]) <= tol), (b, h)
+
+
+def test_attention_one_long_request(lib, oracle):
+    """The benchmark's long-context workload (one request of 32768 positions,
+    Llama-3.1-70B heads, pages of 16 in shuffled order) at split 512: few
+    requests take the static schedule, and their warps share the CTA's stage
+    pool.  Sampled heads against the oracle; and the request's bits are those
+    it gets at row 5 of 12 requests (ticket schedule, two stages per warp,
+    its pages re-laid out)."""
+    L, Hq, Hkv, P, S = 32768, 64, 8, 16, 512
+    kc, vc, bt, sl = inputs.device_paged_kv([L], Hkv, D, P, seed=68)
+    q = inputs.device_normal((1, Hq, D), seed=68, stream=0)
+    alone = lib.bi_decode_attention_bf16(q, kc, vc, bt, sl, 1 / math.sqrt(D), split_size=S)
+    torch.cuda.synchronize()
+    assert lib.bi_last_device_status() == lib.BI_OK
+    heads = [0, 7, 8, 31, 63]
+    pairs = np.array([[0, h] for h in heads])
+    ref = oracle.decode_attention(inputs.bits(q.cpu()), inputs.bits(kc.cpu()), inputs.bits(vc.cpu()),
+                                  bt.cpu().numpy(), sl.cpu().numpy(), 1 / math.sqrt(D), pairs=pairs)
+    got = f64(alone)[0, heads]
+    qf = f64(q)
+    pos = torch.arange(L, device="cuda")
+    pages = bt[0].long()[pos // P]
+    for i, h in enumerate(heads):
+        k = f64(kc[pages, pos % P, h // 8])
+        v = f64(vc[pages, pos % P, h // 8])
+        tol = head_tolerance(ref[i], got[i], qf[0, h], k, v, 1 / math.sqrt(D))
+        assert np.all(np.abs(got[i] - ref[i]) <= tol), h
+    # the same request among eleven others
+    lens = [300, 4000, 17, 900, 2500, L, 64, 1, 700, 5000, 128, 3333]
+    kc2, vc2, bt2, sl2 = inputs.device_paged_kv(lens, Hkv, D, P, seed=69)
+    n = L // P
+    kc2[bt2[5, :n].long()] = kc[bt[0, :n].long()]
+    vc2[bt2[5, :n].long()] = vc[bt[0, :n].long()]
+    q2 = inputs.device_normal((len(lens), Hq, D), seed=69, stream=0)
+    q2[5] = q[0]
+    batch = lib.bi_decode_attention_bf16(q2, kc2, vc2, bt2, sl2, 1 / math.sqrt(D), split_size=S)
+    torch.cuda.synchronize()
+    assert lib.bi_last_device_status() == lib.BI_OK
+    assert np.array_equal(bf16_bits(batch)[5], bf16_bits(alone)[0])
