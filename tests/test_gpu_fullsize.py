@@ -64,3 +64,30 @@ def test_fullsize_fused_sampled_parity(lib, oracle, N):
         sub = list(range(0, M, max(1, M // 16)))
         check_ulp(bf16_bits(xh[sub]), oracle.rmsnorm(inputs.bits(X[sub]), inputs.bits(g), EPS), 1, "norm")
         sampled_parity(oracle, xh, W, Y, 6, seed=M, what="fused N=%d M=%d" % (N, M))
+
+
+def test_fullsize_fp8_sampled_parity(lib, oracle):
+    """The FP8 workload at full size (down_proj W [4096, 14336]; M = 1, 512,
+    8192), in the benchmark's launch configuration (the FP8 default pins plus
+    the early weight stream): whole sampled rows against the oracle's E4M3
+    GEMM on the same codes and scales, with the same GEMM tolerance."""
+    N, K = 4096, 14336
+    W = inputs.device_normal((N, K), std=0.02, seed=1, stream=inputs.STREAM_W)
+    wq, sw = lib.bi_quantize_rows_e4m3(W)
+    pins = lib.bi_pins_default_fp8(N, K)
+    pins = pins.replace(flags=pins.flags | lib.BI_FLAG_PREFETCH_W)
+    wq_np = wq.cpu().numpy()
+    sw_np = sw.cpu().numpy()
+    for M in (1, 512, 8192):
+        X = inputs.device_normal((M, K), seed=1, stream=inputs.STREAM_X)
+        xq, sx = lib.bi_quantize_rows_e4m3(X)
+        Y = lib.bi_gemm_fp8(xq, sx, wq, sw, pins=pins)
+        torch.cuda.synchronize()
+        assert lib.bi_last_device_status() == lib.BI_OK
+        r = np.random.default_rng(M)
+        rows = np.unique(np.concatenate([[0, M - 1], r.integers(0, M, 4)]))
+        sx_np = sx.cpu().numpy()[rows]
+        yf, _ = oracle.gemm_e4m3(xq.cpu().numpy()[rows], sx_np, wq_np, sw_np)
+        ref = (yf.astype(np.float64) * sx_np[:, None] * sw_np[None, :]).astype(np.float32)
+        idx = torch.from_numpy(rows).cuda()
+        check_gemm_parity(bf16_bits(Y[idx]), ref, K, "fp8 N=%d K=%d M=%d" % (N, K, M))
