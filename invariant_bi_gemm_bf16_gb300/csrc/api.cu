@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -554,6 +555,12 @@ bi_status plan_gemm(const void* X, const void* W, void* Y, int64_t M, int64_t N,
   if (plan.kps > 1 && plan.mma_ctas == 1) L.flags |= kFlagCopy2D;
   if (plan.x_box_rows < plan.tok_tile / plan.mma_ctas) L.flags |= kFlagZeroX;
   if (plan.m_tiles == 1) L.flags |= kFlagStreamW;
+#ifdef BI_DEBUG_BOUNDS
+  {
+    const char* poke = std::getenv("BI_DEBUG_POKE");
+    if (poke && std::strcmp(poke, "wrow") == 0) L.flags |= kFlagDebugPokeWRow;
+  }
+#endif
   L.stream = stream;
   return BI_OK;
 }

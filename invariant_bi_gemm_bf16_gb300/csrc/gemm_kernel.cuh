@@ -461,11 +461,16 @@ __global__ void __launch_bounds__(gemm_threads(FUSED), 1)
               break;
             }
             // debug-bounds build: the stage, the K tile and the row of the copy
+#ifdef BI_DEBUG_BOUNDS
+            const int32_t row_c = (is_w && issued == 0 && (p.flags & kFlagDebugPokeWRow)) ? row + (1 << 24) : row;
+#else
+            const int32_t row_c = row;
+#endif
             const bool in_bounds =
                 bounds_ok(stage < nst, p.status, is_w ? kChkWStage : kChkXStage, (uint64_t)stage) &&
                 bounds_ok(kt >= 0 && kt < KT, p.status, kChkKTile, (uint64_t)kt) &&
-                bounds_ok(is_w ? row < p.n_tiles * kMmaM : row < p.m_tiles * T, p.status, is_w ? kChkWRow : kChkXRow,
-                          (uint64_t)row);
+                bounds_ok(is_w ? row_c < p.n_tiles * kMmaM : row_c < p.m_tiles * T, p.status,
+                          is_w ? kChkWRow : kChkXRow, (uint64_t)row_c);
             if (!(stall && issued == 0) && in_bounds) {
               const uint32_t full = smem_u32(&full_bar[stage]);
               const uint32_t dst = ring + (uint32_t)stage * stage_sz;

@@ -30,6 +30,10 @@ constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in per block on sm_100-class 
 constexpr uint32_t kFlagStreamW = 1u << 16;  // W read once: evict-first, X evict-last in L2
 constexpr uint32_t kFlagZeroX = 1u << 17;    // X boxes hold fewer rows than T: zero the ring once
 constexpr uint32_t kFlagCopy2D = 1u << 18;   // KP = 2 by two 2-D copies per stage (single-CTA MMAs only)
+// Debug-bounds build only: the first W copy of each CTA is aimed past the
+// tile grid, for the negative test of the index checks (set from the
+// BI_DEBUG_POKE=wrow environment variable; never in the ordinary build).
+constexpr uint32_t kFlagDebugPokeWRow = 1u << 19;
 
 // Shared-memory bytes of one W stage [128 x 64] and one X stage [rows x 64]
 // (rows = T, or T/2 per CTA of a pair).

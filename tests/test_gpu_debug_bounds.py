@@ -117,3 +117,52 @@ def test_debug_bounds_build_runs_clean_with_the_same_bits(lib, tmp_path):
             a, b = a.view(torch.int32), b.view(torch.int32)
         assert torch.equal(a, b), k
     assert lib.bi_last_device_status() == lib.BI_OK
+
+
+POKE_CHILD = r'''
+import json, os, sys, torch
+sys.path.insert(0, sys.argv[1])
+from invariant_bi_gemm_bf16_gb300 import binding as bd, inputs
+bd.load()
+x = inputs.normal((3, 256), seed=3, stream=0).cuda()
+w = inputs.normal((128, 256), std=0.02, seed=3, stream=1).cuda()
+res = {}
+os.environ["BI_DEBUG_POKE"] = "wrow"       # the first W copy of each CTA aimed past the tile grid
+bd.bi_gemm_bf16(x, w)
+res["poked_status"] = bd.bi_last_device_status()
+res["poked_detail"] = bd.bi_debug_bounds_detail()
+del os.environ["BI_DEBUG_POKE"]
+y = bd.bi_gemm_bf16(x, w)
+res["clean_status"] = bd.bi_last_device_status()
+res["clean_detail"] = bd.bi_debug_bounds_detail()
+torch.save(y.cpu(), sys.argv[2])
+print(json.dumps(res))
+'''
+
+
+def test_debug_bounds_check_reports_and_recovers(lib, tmp_path):
+    """Negative control: in the debug-bounds build, a W copy aimed past the tile
+    grid (planted by the host of that build only) is caught by the kernel's
+    own row check: the copy is skipped, the call reports BI_ERR_DEBUG_BOUNDS
+    with the check number of the W row and the offending row, the kernel gives
+    up through its bounded waits, and the next call runs clean with the
+    ordinary bits."""
+    from invariant_bi_gemm_bf16_gb300 import build, inputs
+    dbg = build.build(debug=True)
+    child = tmp_path / "poke.py"
+    child.write_text(POKE_CHILD)
+    out = tmp_path / "clean.pt"
+    env = dict(os.environ, BI_GEMM_LIB=dbg)
+    env.pop("BI_DEBUG_POKE", None)
+    r = subprocess.run([sys.executable, str(child), ROOT, str(out)], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["poked_status"] == lib.BI_ERR_DEBUG_BOUNDS
+    assert res["poked_detail"] >> 48 == 4                       # the W-row check
+    assert res["poked_detail"] & (2 ** 48 - 1) >= 1 << 24       # the planted row
+    assert res["clean_status"] == lib.BI_OK and res["clean_detail"] == 0
+    x = inputs.normal((3, 256), seed=3, stream=0).cuda()
+    w = inputs.normal((128, 256), std=0.02, seed=3, stream=1).cuda()
+    ref = lib.bi_gemm_bf16(x, w).cpu()
+    assert torch.equal(torch.load(out).view(torch.int16), ref.view(torch.int16))
