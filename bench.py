@@ -396,20 +396,29 @@ class DownProjSweep:
         b = sum(gemm_work(M, self.N, self.K)[1] for M in self.ms)
         return f, b
 
-    def e2e_step(self, host_x, host_y):
-        """Through the public API with host buffers: bi_gemm_bf16_host for each
-        M, which copies the rows in from pinned memory in chunks, multiplies
-        them and copies the results back into pinned memory, the copies of one
-        chunk overlapping the GEMM of the next."""
-        if getattr(self, "host_ws", None) is None:
-            need = self.bd.bi_gemm_bf16_host_workspace_bytes(max(self.ms), self.N, self.K)
+    def e2e_step(self, host_x, host_y, batched=True, depth=2, chunk_rows=0):
+        """Through the public API with host buffers: the rows of every M are
+        copied in from pinned memory in chunks, multiplied and copied back into
+        pinned memory, the copies of one chunk overlapping the GEMMs of the
+        others.  batched: one bi_gemm_bf16_host_batch call over the sweep (one
+        pipeline across the M boundaries); else bi_gemm_bf16_host once per M.
+        depth: ring slots in the workspace; chunk_rows: rows per chunk of the
+        batched call (0: the library's default)."""
+        need = depth * self.bd.bi_gemm_bf16_host_slot_bytes(list(self.ms), self.N, self.K,
+                                                            chunk_rows if batched else 0)
+        if getattr(self, "host_ws", None) is None or self.host_ws.numel() != need:
             self.host_ws = torch.empty(need, dtype=torch.uint8, device=self.dev)
-        h2d = d2h = 0
+        h2d = sum(M * self.K * 2 for M in self.ms)
+        d2h = sum(M * self.N * 2 for M in self.ms)
+        if batched:
+            ws = [self.W[(self.it + j) % self.nw] for j in range(len(self.ms))]
+            self.bd.bi_gemm_bf16_host_batch([host_x[M] for M in self.ms], ws, outs=[host_y[M] for M in self.ms],
+                                            pins=self.pins, workspace=self.host_ws, chunk_rows=chunk_rows)
+            self.it += len(self.ms)
+            return h2d, d2h
         for M in self.ms:
             self.bd.bi_gemm_bf16_host(host_x[M], self.W[self.it % self.nw], out=host_y[M], pins=self.pins,
                                       workspace=self.host_ws)
-            h2d += M * self.K * 2
-            d2h += M * self.N * 2
             self.it += 1
         return h2d, d2h
 
@@ -879,15 +888,21 @@ def run_ours(args, dist):
     # e2e through the C ABI with host buffers
     host_x = {M: wl.X[M][0].cpu().pin_memory() for M in wl.ms}
     host_y = {M: torch.empty((M, wl.N), dtype=torch.bfloat16).pin_memory() for M in wl.ms}
-    for _ in range(max(1, args.warmup // 2)):
-        wl.e2e_step(host_x, host_y)
-    torch.cuda.synchronize()
     holder = {}
+    # chunks of about e2e_chunk_mb MB of X for the batched call (a multiple of 128 rows)
+    chunk_rows = max(128, ((args.e2e_chunk_mb << 20) // (2 * wl.K)) // 128 * 128)
 
-    def e2e():
-        holder["b"] = wl.e2e_step(host_x, host_y)
-    e2e_wall = dist.max(time_steps(e2e, args.steps, dist))
-    e2e_value = dist.sum(flops * args.steps) / e2e_wall / 1e12
+    def e2e_time(batched):
+        for _ in range(max(1, args.warmup // 2)):
+            wl.e2e_step(host_x, host_y, batched, args.e2e_depth, chunk_rows)
+        torch.cuda.synchronize()
+
+        def e2e():
+            holder["b"] = wl.e2e_step(host_x, host_y, batched, args.e2e_depth, chunk_rows)
+        wall = dist.max(time_steps(e2e, args.steps, dist))
+        return dist.sum(flops * args.steps) / wall / 1e12
+    e2e_per_call = e2e_time(False)
+    e2e_value = e2e_time(True)
     h2d, d2h = holder["b"]
 
     launch_sum = float(per_launch.sum()) / 1e6          # one sweep, seconds
@@ -930,7 +945,12 @@ def run_ours(args, dist):
         "sweep_roofline": sweep_roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "api": "bi_gemm_bf16_host per M (pinned host X and Y, chunked copies overlapping the GEMMs)"},
+                "api": "one bi_gemm_bf16_host_batch call over the sweep's 14 jobs (pinned host X and Y, "
+                       "chunks of %d rows copied in and out while other chunks multiply, across the M "
+                       "boundaries; ring of %d slots)" % (chunk_rows, args.e2e_depth)},
+        "e2e_per_call": {"value": round(e2e_per_call, 2), "unit": "TFLOP/s",
+                         "api": "bi_gemm_bf16_host once per M (default chunks of about 16 MB of X; ring of %d "
+                                "slots)" % args.e2e_depth},
         "gpu_launches": L * args.steps,
         "per_m_timing": ("us: %d back-to-back launches of that M between two CUDA events (mean); us_median50: "
                          "median of 50 launches, each between its own events, after 10 warm-up launches; "
@@ -1129,6 +1149,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--per-m-reps", type=int, default=20)
+    ap.add_argument("--e2e-depth", type=int, default=8, help="ring slots of the host-buffer GEMM's workspace")
+    ap.add_argument("--e2e-chunk-mb", type=int, default=64, help="MB of X per chunk of the batched host GEMM")
     ap.add_argument("--single-quantize", default="",
                     help="M:K: only launch the E4M3 quantisation on that shape (for ncu)")
     ap.add_argument("--single-logsoftmax", default="",

@@ -293,17 +293,21 @@ bi_status bi_gemm_bf16_ws(const void* X, const void* W, void* Y, int64_t M, int6
 bi_status bi_gemm_plan_describe_ws(int64_t M, int64_t N, int64_t K, const bi_pins* pins, int32_t sm_count,
                                    size_t workspace_bytes, bi_gemm_plan* plan);
 
-/* Bytes of device workspace bi_gemm_bf16_host needs for M rows (0 for M = 0). */
+/* Bytes of device workspace bi_gemm_bf16_host needs for M rows (0 for M = 0):
+ * a ring of two chunk slots, or one when one chunk holds every row. */
 size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Y_host[M,N] = bf16(X_host[M,K] . W[N,K]^T) with X and Y in host memory and W
  * on the device: the same bits as bi_gemm_bf16 on device copies of X and Y.
- * The rows travel in chunks of about 16 MB of X through a ring of two
- * buffers in `workspace`: a chunk is copied in on a library stream, multiplied
- * on `stream` and copied out on a second library stream, so copies and GEMMs
- * of consecutive chunks overlap.  Chunking is free because the tree of a row
+ * The rows travel in chunks of about 16 MB of X through a ring of buffers in
+ * `workspace`: a chunk is copied in on a library stream, multiplied on
+ * `stream` and copied out on a second library stream, so copies and GEMMs of
+ * consecutive chunks overlap.  Chunking is free because the tree of a row
  * never depends on M (Detent, Sec. 3: a batch-invariant operator gives each
  * row the same bits whatever batch it is computed in).
+ * Ring depth: as many slots of bi_gemm_bf16_host_slot_bytes bytes as
+ * `workspace_bytes` holds, at most 8 and at most the number of chunks; the
+ * size the workspace query returns gives two.
  * Ownership: X_host and Y_host are caller-owned host memory (page-locked for
  * the copies to overlap; pageable memory works, with synchronous copies);
  * W and `workspace` are caller-owned device memory, `workspace` at least
@@ -315,9 +319,52 @@ size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * `stream` before reading Y_host.
  * Requirements: as bi_gemm_bf16 (W 16-byte aligned; X_host and Y_host need no
  * alignment).
- * Errors: as bi_gemm_bf16, plus BI_ERR_WORKSPACE. */
+ * Errors: as bi_gemm_bf16, plus BI_ERR_WORKSPACE.  Every argument is checked
+ * before any work is enqueued. */
 bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_host, int64_t M, int64_t N, int64_t K,
                             const bi_pins* pins, void* workspace, size_t workspace_bytes, bi_stream_t stream);
+
+/* One job of bi_gemm_bf16_host_batch: Y_host[M,N] = X_host[M,K] . W[N,K]^T. */
+typedef struct bi_host_gemm_job {
+  const void* X_host; /* [M, K] bf16, row-major, host memory */
+  const void* W;      /* [N, K] bf16, row-major, device memory, 16-byte aligned */
+  void* Y_host;       /* [M, N] bf16, row-major, host memory */
+  int64_t M;          /* rows; 0 skips the job (its pointers may then be NULL) */
+} bi_host_gemm_job;
+
+/* Bytes of device workspace bi_gemm_bf16_host_batch needs for `jobs` and
+ * `chunk_rows` (0 when no job has rows, or for an invalid argument): two
+ * chunk slots, or one when one chunk holds every row of every job. */
+size_t bi_gemm_bf16_host_batch_workspace_bytes(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                               int64_t chunk_rows);
+
+/* Bytes of one ring slot (a chunk's X and Y) for `jobs` and `chunk_rows`; a
+ * workspace of d slots gives a ring of depth d (at most 8).  With one job of
+ * M rows and chunk_rows 0 this is the slot of bi_gemm_bf16_host. */
+size_t bi_gemm_bf16_host_slot_bytes(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                    int64_t chunk_rows);
+
+/* The GEMMs of a list of jobs of one shape (N, K) and one set of pins, with X
+ * and Y in host memory: each job gives the bits bi_gemm_bf16 gives on device
+ * copies of its X and Y.  The jobs' rows run as one sequence of chunks through
+ * one ring, in job order, so the copies of one job overlap the GEMMs of its
+ * neighbours as they overlap those of its own chunks (Detent, Sec. 3: the
+ * bits of a row do not depend on the launch it is computed in).  The jobs may
+ * share W or not.
+ * chunk_rows: rows per chunk (capped at the largest job's rows); 0 takes the
+ * rule of bi_gemm_bf16_host for the largest job (about 16 MB of X, a multiple
+ * of 128 rows).  Larger chunks run the GEMMs faster and stretch the last
+ * chunk's GEMM and copy-out; the chunk size changes no bit.
+ * Ownership, asynchrony and the ring depth: as bi_gemm_bf16_host, with
+ * `workspace` at least bi_gemm_bf16_host_batch_workspace_bytes bytes.  The
+ * job array itself is read during the call only.
+ * Errors: BI_ERR_INVALID_ARG for n_jobs < 0, a NULL `jobs` with n_jobs > 0, a
+ * negative M or chunk_rows, or a NULL pointer of a job with rows;
+ * BI_ERR_UNSUPPORTED_SHAPE for chunk_rows above 2^31 - 1; otherwise as
+ * bi_gemm_bf16_host.  Every argument is checked before any work is enqueued. */
+bi_status bi_gemm_bf16_host_batch(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                  const bi_pins* pins, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
+                                  bi_stream_t stream);
 
 /* Y[M,H] = RMSNorm(X[M,H]) with gain g[H], one warp per row: each lane sums
  * the squares of its 16-byte vectors in ascending order, the 32 lane sums are

@@ -92,6 +92,12 @@ class Plan(ctypes.Structure):
         return tuple(getattr(self, f) for f in self.LAYOUT_FIELDS)
 
 
+class HostGemmJob(ctypes.Structure):
+    """bi_host_gemm_job: one GEMM of bi_gemm_bf16_host_batch."""
+    _fields_ = [("X_host", ctypes.c_void_p), ("W", ctypes.c_void_p), ("Y_host", ctypes.c_void_p),
+                ("M", ctypes.c_int64)]
+
+
 class BiError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -123,6 +129,12 @@ _SIGNATURES = {
     "bi_gemm_bf16_host_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "bi_gemm_bf16_host": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Pins), _vp,
                                          ctypes.c_size_t, _vp]),
+    "bi_gemm_bf16_host_batch_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(HostGemmJob), ctypes.c_int32,
+                                                                  _i64, _i64, _i64]),
+    "bi_gemm_bf16_host_slot_bytes": (ctypes.c_size_t, [ctypes.POINTER(HostGemmJob), ctypes.c_int32, _i64, _i64,
+                                                       _i64]),
+    "bi_gemm_bf16_host_batch": (ctypes.c_int, [ctypes.POINTER(HostGemmJob), ctypes.c_int32, _i64, _i64,
+                                               ctypes.POINTER(Pins), _i64, _vp, ctypes.c_size_t, _vp]),
     "bi_rmsnorm_gemm_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "bi_rmsnorm_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
                                             ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
@@ -329,6 +341,61 @@ def bi_gemm_bf16_host(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None
     if _call_hooks:
         _report(M, N, K)
     return out
+
+
+def _job_array(ms, xs=None, ws=None, outs=None):
+    arr = (HostGemmJob * max(len(ms), 1))()
+    for j, M in enumerate(ms):
+        arr[j].M = int(M)
+        if xs is not None:
+            arr[j].X_host, arr[j].W, arr[j].Y_host = xs[j], ws[j], outs[j]
+    return arr
+
+
+def bi_gemm_bf16_host_batch_workspace_bytes(ms, N: int, K: int, chunk_rows: int = 0) -> int:
+    """Workspace of bi_gemm_bf16_host_batch for jobs of ms[j] rows (a ring of
+    two slots)."""
+    return int(load().bi_gemm_bf16_host_batch_workspace_bytes(_job_array(ms), len(ms), N, K, chunk_rows))
+
+
+def bi_gemm_bf16_host_slot_bytes(ms, N: int, K: int, chunk_rows: int = 0) -> int:
+    """Bytes of one ring slot for jobs of ms[j] rows; d slots give a ring of
+    depth d (at most 8)."""
+    return int(load().bi_gemm_bf16_host_slot_bytes(_job_array(ms), len(ms), N, K, chunk_rows))
+
+
+def bi_gemm_bf16_host_batch(xs, ws, outs=None, pins: Pins | None = None, workspace: torch.Tensor | None = None,
+                            stream=None, chunk_rows: int = 0) -> list:
+    """outs[j] = xs[j] . ws[j]^T for a list of jobs of one shape (N, K): x [M_j,K]
+    and the results [M_j,N] in host memory, w [N,K] on the device (the jobs may
+    share one).  One pipeline of chunks over all jobs (chunk_rows rows each, 0
+    for the default of about 16 MB of X); each job gets the bits bi_gemm_bf16
+    gives it alone.  Asynchronous on `stream`."""
+    if len(xs) != len(ws) or (outs is not None and len(outs) != len(xs)):
+        raise ValueError("xs, ws and outs must have one entry per job")
+    if not xs:
+        return []
+    N, K = ws[0].shape
+    ms = []
+    for x, w in zip(xs, ws):
+        if x.dim() != 2 or w.dim() != 2 or tuple(w.shape) != (N, K) or x.shape[1] != K:
+            raise ValueError("expected x [M,K] and w [N,K] of one (N, K) for every job")
+        ms.append(int(x.shape[0]))
+    if outs is None:
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True) for M in ms]
+    arr = _job_array(ms, [_host(x, "x", (M, K)) for x, M in zip(xs, ms)], [_dev(w, "w") for w in ws],
+                     [_host(o, "out", (M, N)) for o, M in zip(outs, ms)])
+    need = int(load().bi_gemm_bf16_host_batch_workspace_bytes(arr, len(ms), N, K, chunk_rows))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=ws[0].device)
+    ws_ptr, ws_bytes = _workspace(workspace)
+    st = load().bi_gemm_bf16_host_batch(arr, len(ms), N, K, ctypes.byref(pins) if pins is not None else None,
+                                        chunk_rows, ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "bi_gemm_bf16_host_batch")
+    if _call_hooks:
+        for M in ms:
+            _report(M, N, K)
+    return outs
 
 
 def bi_rmsnorm_bf16(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-5, out: torch.Tensor | None = None,

@@ -655,8 +655,11 @@ bi_status gemm_impl(const void* X, const void* W, void* Y, int64_t M, int64_t N,
 // Chunk c's rows are copied in on one stream, multiplied on the caller's
 // stream and copied out on another, so the copies of one chunk overlap the
 // GEMM of the next.  Batch invariance makes this free: a row's bits do not
-// depend on the chunk (the M of the launch) it travels in.
-constexpr int kHostSlots = 2;
+// depend on the chunk (the M of the launch) it travels in.  A list of jobs of
+// one (N, K) runs as one sequence of chunks, so the copies of one job overlap
+// the GEMMs of its neighbours too.
+constexpr int kHostSlots = 2;     // ring depth of the workspace size the query returns
+constexpr int kHostMaxSlots = 8;  // deepest ring a larger workspace buys
 
 int64_t host_chunk_rows(int64_t M, int64_t K) {
   int64_t r = (int64_t{16} << 20) / (2 * K);  // about 16 MB of X per chunk
@@ -672,10 +675,28 @@ uint64_t host_slot_bytes(int64_t R, int64_t N, int64_t K) {
   return round256((uint64_t)R * (uint64_t)K * 2u) + round256((uint64_t)R * (uint64_t)N * 2u);
 }
 
-size_t host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
-  const int64_t R = host_chunk_rows(M, K);
-  const int64_t chunks = (M + R - 1) / R;
+// Chunk rows R (chunk_rows, else the rule above for the largest job, and at
+// most the largest job's rows) and the number of chunks of all jobs; false for
+// a negative or oversized M or chunk_rows.
+bool host_chunking(const bi_host_gemm_job* jobs, int32_t n, int64_t K, int64_t chunk_rows, int64_t* R,
+                   int64_t* chunks) {
+  if (chunk_rows < 0 || chunk_rows > 0x7FFFFFFFll) return false;
+  int64_t mmax = 0;
+  for (int32_t j = 0; j < n; ++j) {
+    if (jobs[j].M < 0 || jobs[j].M > 0x7FFFFFFFll) return false;
+    mmax = jobs[j].M > mmax ? jobs[j].M : mmax;
+  }
+  *R = chunk_rows > 0 ? (chunk_rows < mmax ? chunk_rows : mmax) : host_chunk_rows(mmax, K);
+  *chunks = 0;
+  for (int32_t j = 0; j < n; ++j)
+    if (jobs[j].M > 0) *chunks += (jobs[j].M + *R - 1) / *R;
+  return true;
+}
+
+size_t host_workspace_bytes(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t K, int64_t chunk_rows) {
+  if (n <= 0 || !jobs || N <= 0 || K <= 0) return 0;
+  int64_t R = 0, chunks = 0;
+  if (!host_chunking(jobs, n, K, chunk_rows, &R, &chunks) || chunks == 0) return 0;
   return (size_t)((chunks < kHostSlots ? chunks : kHostSlots) * host_slot_bytes(R, N, K));
 }
 
@@ -684,7 +705,7 @@ size_t host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 struct HostCtx {
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
-  cudaEvent_t copied_in[kHostSlots] = {}, multiplied[kHostSlots] = {}, copied_out[kHostSlots] = {};
+  cudaEvent_t copied_in[kHostMaxSlots] = {}, multiplied[kHostMaxSlots] = {}, copied_out[kHostMaxSlots] = {};
   bool ready = false;
 };
 HostCtx g_host_ctx[64];
@@ -697,13 +718,90 @@ bool host_ctx_init(HostCtx& c) {
   if (cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (cudaEventCreateWithFlags(&c.start, ef) != cudaSuccess) return false;
   if (cudaEventCreateWithFlags(&c.end, ef) != cudaSuccess) return false;
-  for (int i = 0; i < kHostSlots; ++i) {
+  for (int i = 0; i < kHostMaxSlots; ++i) {
     if (cudaEventCreateWithFlags(&c.copied_in[i], ef) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&c.multiplied[i], ef) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&c.copied_out[i], ef) != cudaSuccess) return false;
   }
   c.ready = true;
   return true;
+}
+
+// Every argument is checked before anything is enqueued.
+bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t K, const bi_pins* pins,
+                    int64_t chunk_rows, void* workspace, size_t ws_bytes, cudaStream_t s) {
+  if (n < 0 || (n > 0 && !jobs) || chunk_rows < 0) return BI_ERR_INVALID_ARG;
+  for (int32_t j = 0; j < n; ++j)
+    if (jobs[j].M < 0) return BI_ERR_INVALID_ARG;
+  bi_status st = check_nk(N, K);
+  if (st != BI_OK) return st;
+  for (int32_t j = 0; j < n; ++j)
+    if (jobs[j].M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  if (chunk_rows > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  Resolved r;
+  st = resolve_pins(N, K, pins, &r);
+  if (st != BI_OK) return st;
+  int64_t R = 0, chunks = 0;
+  host_chunking(jobs, n, K, chunk_rows, &R, &chunks);
+  if (chunks == 0) return BI_OK;
+  for (int32_t j = 0; j < n; ++j) {
+    if (jobs[j].M == 0) continue;
+    if (!jobs[j].X_host || !jobs[j].W || !jobs[j].Y_host) return BI_ERR_INVALID_ARG;
+    if (!aligned16(jobs[j].W)) return BI_ERR_ALIGNMENT;
+  }
+  const uint64_t slot = host_slot_bytes(R, N, K), xoff = round256((uint64_t)R * (uint64_t)K * 2u);
+  if (!workspace || ws_bytes < host_workspace_bytes(jobs, n, N, K, chunk_rows)) return BI_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
+  // ring depth: as many slots as the workspace holds, up to kHostMaxSlots
+  int64_t depth = (int64_t)(ws_bytes / slot);
+  depth = depth > kHostMaxSlots ? kHostMaxSlots : depth;
+  depth = depth > chunks ? chunks : depth;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mu[dev]);
+  HostCtx& c = g_host_ctx[dev];
+  if (!host_ctx_init(c)) return BI_ERR_CUDA;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // everything before this call on `s` (W, the workspace's last users) comes first
+  if (!ok(cudaEventRecord(c.start, s)) || !ok(cudaStreamWaitEvent(c.in, c.start, 0)) ||
+      !ok(cudaStreamWaitEvent(c.out, c.start, 0)))
+    return BI_ERR_CUDA;
+  bi_status result = BI_OK;
+  int64_t ch = 0;  // chunk index over all jobs
+  for (int32_t j = 0; j < n && result == BI_OK; ++j) {
+    const bi_host_gemm_job& job = jobs[j];
+    for (int64_t r0 = 0; r0 < job.M && result == BI_OK; r0 += R, ++ch) {
+      const int i = (int)(ch % depth);
+      const int64_t rows = job.M - r0 < R ? job.M - r0 : R;
+      char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
+      char* yd = xd + xoff;
+      // the slot's previous chunk has been copied out (so also multiplied)
+      if (ch >= depth && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) {
+        result = BI_ERR_CUDA;
+        break;
+      }
+      if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(job.X_host) + (uint64_t)r0 * K * 2,
+                              (size_t)rows * K * 2, cudaMemcpyHostToDevice, c.in)) ||
+          !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0))) {
+        result = BI_ERR_CUDA;
+        break;
+      }
+      result = gemm_impl(xd, job.W, yd, rows, N, K, pins, s);
+      if (result != BI_OK) break;
+      if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
+          !ok(cudaMemcpyAsync(static_cast<char*>(job.Y_host) + (uint64_t)r0 * N * 2, yd, (size_t)rows * N * 2,
+                              cudaMemcpyDeviceToHost, c.out)) ||
+          !ok(cudaEventRecord(c.copied_out[i], c.out)))
+        result = BI_ERR_CUDA;
+    }
+  }
+  // the caller's stream resumes once every copy enqueued so far has landed
+  // (also after an error, so that no copy outlives the call's buffers
+  // unseen by the caller's stream)
+  const bool joined_in = ok(cudaEventRecord(c.end, c.in)) && ok(cudaStreamWaitEvent(s, c.end, 0));
+  const bool joined_out = ok(cudaEventRecord(c.end, c.out)) && ok(cudaStreamWaitEvent(s, c.end, 0));
+  if (result == BI_OK && !(joined_in && joined_out)) result = BI_ERR_CUDA;
+  return result;
 }
 
 }  // namespace
@@ -854,70 +952,35 @@ BI_API bi_status bi_rmsnorm_bf16(const void* X, const void* g, void* Y, int64_t 
 }
 
 BI_API size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  return host_workspace_bytes(M, N, K);
+  const bi_host_gemm_job job = {nullptr, nullptr, nullptr, M};
+  return host_workspace_bytes(&job, 1, N, K, 0);
 }
 
 BI_API bi_status bi_gemm_bf16_host(const void* X_host, const void* W, void* Y_host, int64_t M, int64_t N,
                                    int64_t K, const bi_pins* pins, void* workspace, size_t ws_bytes,
                                    bi_stream_t stream) {
-  if (M < 0) return BI_ERR_INVALID_ARG;
-  bi_status st = check_nk(N, K);
-  if (st != BI_OK) return st;
-  if (M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
-  Resolved r;
-  st = resolve_pins(N, K, pins, &r);
-  if (st != BI_OK) return st;
-  if (M == 0) return BI_OK;
-  if (!X_host || !W || !Y_host) return BI_ERR_INVALID_ARG;
-  if (!aligned16(W)) return BI_ERR_ALIGNMENT;
-  if (!workspace || ws_bytes < host_workspace_bytes(M, N, K)) return BI_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_host_mu[dev]);
-  HostCtx& c = g_host_ctx[dev];
-  if (!host_ctx_init(c)) return BI_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t R = host_chunk_rows(M, K);
-  const int64_t chunks = (M + R - 1) / R;
-  const uint64_t slot = host_slot_bytes(R, N, K), xoff = round256((uint64_t)R * (uint64_t)K * 2u);
-  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-  // everything before this call on `stream` (W, the workspace's last users) comes first
-  if (!ok(cudaEventRecord(c.start, s)) || !ok(cudaStreamWaitEvent(c.in, c.start, 0)) ||
-      !ok(cudaStreamWaitEvent(c.out, c.start, 0)))
-    return BI_ERR_CUDA;
-  bi_status result = BI_OK;
-  for (int64_t ch = 0; ch < chunks && result == BI_OK; ++ch) {
-    const int i = (int)(ch % kHostSlots);
-    const int64_t rows = M - ch * R < R ? M - ch * R : R;
-    char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
-    char* yd = xd + xoff;
-    // the slot's previous chunk has been copied out (so also multiplied)
-    if (ch >= kHostSlots && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) {
-      result = BI_ERR_CUDA;
-      break;
-    }
-    if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(X_host) + (uint64_t)ch * R * K * 2, (size_t)rows * K * 2,
-                            cudaMemcpyHostToDevice, c.in)) ||
-        !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0))) {
-      result = BI_ERR_CUDA;
-      break;
-    }
-    result = gemm_impl(xd, W, yd, rows, N, K, pins, s);
-    if (result != BI_OK) break;
-    if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
-        !ok(cudaMemcpyAsync(static_cast<char*>(Y_host) + (uint64_t)ch * R * N * 2, yd, (size_t)rows * N * 2,
-                            cudaMemcpyDeviceToHost, c.out)) ||
-        !ok(cudaEventRecord(c.copied_out[i], c.out)))
-      result = BI_ERR_CUDA;
-  }
-  // the caller's stream resumes once every copy enqueued so far has landed
-  // (also after an error, so that no copy outlives the call's buffers
-  // unseen by the caller's stream)
-  const bool joined_in = ok(cudaEventRecord(c.end, c.in)) && ok(cudaStreamWaitEvent(s, c.end, 0));
-  const bool joined_out = ok(cudaEventRecord(c.end, c.out)) && ok(cudaStreamWaitEvent(s, c.end, 0));
-  if (result == BI_OK && !(joined_in && joined_out)) result = BI_ERR_CUDA;
-  return result;
+  const bi_host_gemm_job job = {X_host, W, Y_host, M};
+  return host_gemm(&job, 1, N, K, pins, 0, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API size_t bi_gemm_bf16_host_batch_workspace_bytes(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N,
+                                                      int64_t K, int64_t chunk_rows) {
+  return host_workspace_bytes(jobs, n_jobs, N, K, chunk_rows);
+}
+
+BI_API size_t bi_gemm_bf16_host_slot_bytes(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                           int64_t chunk_rows) {
+  if (n_jobs <= 0 || !jobs || N <= 0 || K <= 0) return 0;
+  int64_t R = 0, chunks = 0;
+  if (!host_chunking(jobs, n_jobs, K, chunk_rows, &R, &chunks) || chunks == 0) return 0;
+  return (size_t)host_slot_bytes(R, N, K);
+}
+
+BI_API bi_status bi_gemm_bf16_host_batch(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                         const bi_pins* pins, int64_t chunk_rows, void* workspace,
+                                         size_t ws_bytes, bi_stream_t stream) {
+  return host_gemm(jobs, n_jobs, N, K, pins, chunk_rows, workspace, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return fused_workspace_bytes(M, K); }

@@ -221,6 +221,77 @@ def test_host_gemm_workspace_is_two_chunk_slots(bd):
     assert bd.bi_gemm_bf16_host_workspace_bytes(5000, 6144, 4096) == 2 * slot(2048, 6144, 4096)
     assert bd.bi_gemm_bf16_host_workspace_bytes(100000, 128, 256) == 2 * slot(8192, 128, 256)
 
+def test_host_batch_workspace_follows_the_largest_job(bd):
+    """A job list chunks every job with the row count of its largest job; the
+    workspace is two slots of that chunk, or one when a single chunk holds
+    every row of every job; one job sizes as bi_gemm_bf16_host."""
+    def r256(b):
+        return (b + 255) // 256 * 256
+
+    def slot(R, N, K):
+        return r256(R * K * 2) + r256(R * N * 2)
+    N, K = 4096, 14336
+    sweep = [1 << i for i in range(14)]
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes(sweep, N, K) == 2 * slot(512, N, K)
+    assert bd.bi_gemm_bf16_host_slot_bytes(sweep, N, K) == slot(512, N, K)
+    # 3 rows and 5 rows: one 5-row chunk each, two chunks in all
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([3, 5], N, K) == 2 * slot(5, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([0, 7, 0], N, K) == slot(7, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([0, 0], N, K) == 0
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([], N, K) == 0
+    assert bd.bi_gemm_bf16_host_slot_bytes([0], N, K) == 0
+    for M in (1, 300, 512, 513, 8192, 100000):
+        assert bd.bi_gemm_bf16_host_batch_workspace_bytes([M], N, K) == \
+            bd.bi_gemm_bf16_host_workspace_bytes(M, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([-1, 4], N, K) == 0
+    # an explicit chunk: capped at the largest job; negative is refused (0)
+    assert bd.bi_gemm_bf16_host_slot_bytes(sweep, N, K, 2304) == slot(2304, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes(sweep, N, K, 2304) == 2 * slot(2304, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([3, 5], N, K, 1000) == 2 * slot(5, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([10], N, K, 1000) == slot(10, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([10], N, K, 3) == 2 * slot(3, N, K)
+    assert bd.bi_gemm_bf16_host_batch_workspace_bytes([10], N, K, -1) == 0
+    assert bd.bi_gemm_bf16_host_slot_bytes([10], N, K, 1 << 40) == 0
+
+
+def test_host_batch_arguments_rejected_before_any_launch(bd):
+    """Every argument of a job list is checked before anything is enqueued
+    (so these calls need no GPU)."""
+    lib = bd.load()
+    J = bd.HostGemmJob
+
+    def jobs(*rows):
+        arr = (J * len(rows))()
+        for j, (x, w, y, M) in enumerate(rows):
+            arr[j].X_host, arr[j].W, arr[j].Y_host, arr[j].M = x, w, y, M
+        return arr
+    def call(arr, n, N, K, ws, ws_bytes, chunk_rows=0):
+        return lib.bi_gemm_bf16_host_batch(arr, n, N, K, None, chunk_rows, ws, ws_bytes, None)
+    assert call(None, 0, 128, 256, None, 0) == bd.BI_OK
+    assert call(None, 1, 128, 256, None, 0) == bd.BI_ERR_INVALID_ARG
+    assert call(None, -1, 128, 256, None, 0) == bd.BI_ERR_INVALID_ARG
+    assert call(jobs((None, None, None, 0), (None, None, None, 0)), 2, 128, 256, None, 0) == bd.BI_OK
+    assert call(jobs((16, 32, 48, 4), (None, None, None, -1)), 2, 128, 256, 256, 1 << 20) == \
+        bd.BI_ERR_INVALID_ARG
+    assert call(jobs((16, 32, 48, 4)), 1, 128, 250, 256, 1 << 20) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    assert call(jobs((16, 32, 48, 4)), 1, 128, 256, 256, 1 << 20, -1) == bd.BI_ERR_INVALID_ARG
+    assert call(jobs((16, 32, 48, 4)), 1, 128, 256, 256, 1 << 20, 1 << 40) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    # the second job's null W or misaligned W is found before the first job runs
+    assert call(jobs((16, 32, 48, 4), (16, None, 48, 4)), 2, 128, 256, 256, 1 << 20) == bd.BI_ERR_INVALID_ARG
+    assert call(jobs((16, 32, 48, 4), (16, 40, 48, 4)), 2, 128, 256, 256, 1 << 20) == bd.BI_ERR_ALIGNMENT
+    arr = jobs((16, 32, 48, 4), (16, 32, 48, 6))
+    need = lib.bi_gemm_bf16_host_batch_workspace_bytes(arr, 2, 128, 256, 0)
+    assert need == 2 * lib.bi_gemm_bf16_host_slot_bytes(arr, 2, 128, 256, 0)
+    assert call(arr, 2, 128, 256, 256, need - 1) == bd.BI_ERR_WORKSPACE
+    assert call(arr, 2, 128, 256, 512 + 16, need) == bd.BI_ERR_ALIGNMENT
+    # 2-row chunks: five chunks, a larger slot count, a smaller slot
+    need2 = lib.bi_gemm_bf16_host_batch_workspace_bytes(arr, 2, 128, 256, 2)
+    assert need2 == 2 * lib.bi_gemm_bf16_host_slot_bytes(arr, 2, 128, 256, 2) and need2 < need
+    assert call(arr, 2, 128, 256, 256, need2 - 1, 2) == bd.BI_ERR_WORKSPACE
+    with pytest.raises(ValueError):
+        bd.bi_gemm_bf16_host_batch([], [None])
+
+
 @pytest.mark.parametrize("N,K", TABLE_SHAPES + [(300, 200), (20000, 1000)])
 def test_reduction_tree_never_depends_on_m(bd, N, K):
     """Detent Sec. 8.2: the batch reaches no GEMM selection point.  The plan's

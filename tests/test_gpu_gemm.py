@@ -222,3 +222,49 @@ def test_host_buffer_calls_back_to_back(lib):
     torch.cuda.synchronize()
     for x, y in zip(xs, outs):
         assert np.array_equal(bf16_bits(y), bf16_bits(lib.bi_gemm_bf16(x.cuda(), W)))
+
+
+@pytest.mark.parametrize("depth,chunk_rows", [(0, 0), (3, 0), (8, 0), (0, 1000), (4, 128), (2, 4999), (8, 2304)])
+def test_host_batch_gives_each_job_its_device_bits(lib, depth, chunk_rows):
+    """bi_gemm_bf16_host_batch over jobs of one (N, K) (an empty job, one row,
+    ragged counts, jobs sharing W and jobs with their own W) gives each job
+    the bits of bi_gemm_bf16 alone, with the two-slot ring the workspace query
+    sizes (depth 0 here) or a deeper one, and the default chunk (2048 rows at
+    K = 4096) or an explicit one (ragged, small, larger than most jobs)."""
+    N, K = 6144, 4096
+    Wa = inputs.device_normal((N, K), std=0.02, seed=32, stream=1)
+    Wb = inputs.device_normal((N, K), std=0.02, seed=32, stream=2)
+    Ms = (0, 1, 5000, 3, 2049, 700)
+    Wl = [Wa, Wb, Wa, Wb, Wb, Wa]
+    xs = [inputs.normal((M, K), seed=32, stream=10 + i).pin_memory() for i, M in enumerate(Ms)]
+    ws = None
+    if depth:
+        ws = torch.empty(depth * lib.bi_gemm_bf16_host_slot_bytes(list(Ms), N, K, chunk_rows), dtype=torch.uint8,
+                         device="cuda")
+    outs = lib.bi_gemm_bf16_host_batch(xs, Wl, workspace=ws, chunk_rows=chunk_rows)
+    torch.cuda.synchronize()
+    for x, w, y in zip(xs, Wl, outs):
+        assert y.shape == (x.shape[0], N)
+        if x.shape[0]:
+            assert np.array_equal(bf16_bits(y), bf16_bits(lib.bi_gemm_bf16(x.cuda(), w)))
+
+
+def test_host_batch_calls_back_to_back(lib):
+    """Two job lists enqueued on one stream and one workspace without a
+    synchronisation between them, then a single-job call: each keeps its own
+    bits (down_proj shape, 512-row chunks)."""
+    N, K = 4096, 14336
+    W = inputs.device_normal((N, K), std=0.02, seed=33, stream=1)
+    lists = [(1, 1100, 64), (513, 2, 1024)]
+    ws = torch.empty(lib.bi_gemm_bf16_host_batch_workspace_bytes([1100, 1024, 700], N, K), dtype=torch.uint8,
+                     device="cuda")
+    xs = [[inputs.normal((M, K), seed=33, stream=100 * a + i).pin_memory() for i, M in enumerate(Ms)]
+          for a, Ms in enumerate(lists)]
+    outs = [lib.bi_gemm_bf16_host_batch(x, [W] * len(x), workspace=ws) for x in xs]
+    x1 = inputs.normal((700, K), seed=33, stream=999).pin_memory()
+    y1 = lib.bi_gemm_bf16_host(x1, W, workspace=ws)
+    torch.cuda.synchronize()
+    for xl, yl in zip(xs, outs):
+        for x, y in zip(xl, yl):
+            assert np.array_equal(bf16_bits(y), bf16_bits(lib.bi_gemm_bf16(x.cuda(), W)))
+    assert np.array_equal(bf16_bits(y1), bf16_bits(lib.bi_gemm_bf16(x1.cuda(), W)))
