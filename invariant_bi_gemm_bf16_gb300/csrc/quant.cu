@@ -316,6 +316,166 @@ __global__ void __launch_bounds__(256, 2)
                            : make_uint2(codes4(v[i].x, v[i].y, inv), codes4(v[i].z, v[i].w, inv));
 }
 
+// {a.x * b.x, a.y * b.y}: two IEEE fp32 products rounded to nearest even in
+// one packed instruction (the same two results as two __fmul_rn)
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\t"
+      "mul.rn.f32x2 pd, pa, pb;\n\t"
+      "mov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// norm2 with the products taken in pairs (the same bits)
+__device__ __forceinline__ uint32_t norm2_packed(uint32_t x, uint32_t g, float r) {
+  const float2 t = mul2_rn(make_float2(bf_lo(x), bf_hi(x)), make_float2(r, r));
+  const float2 y = mul2_rn(t, make_float2(bf_lo(g), bf_hi(g)));
+  __nv_bfloat162 o = __floats2bfloat162_rn(y.x, y.y);
+  return *reinterpret_cast<uint32_t*>(&o);
+}
+
+__device__ __forceinline__ uint4 norm8_packed(const uint4& x, const uint4& g, float r) {
+  uint4 o;
+  o.x = norm2_packed(x.x, g.x, r);
+  o.y = norm2_packed(x.y, g.y, r);
+  o.z = norm2_packed(x.z, g.z, r);
+  o.w = norm2_packed(x.w, g.w, r);
+  return o;
+}
+
+// codes4 with the products taken in pairs (the same bits)
+__device__ __forceinline__ uint32_t codes4_packed(uint32_t w0, uint32_t w1, float inv) {
+  const float2 a = mul2_rn(make_float2(bf_lo(w0), bf_hi(w0)), make_float2(inv, inv));
+  const float2 b = mul2_rn(make_float2(bf_lo(w1), bf_hi(w1)), make_float2(inv, inv));
+  return (uint32_t)cvt_e4m3x2(a.x, a.y) | ((uint32_t)cvt_e4m3x2(b.x, b.y) << 16);
+}
+
+// The same one pass with the rows streamed: a persistent grid of one block
+// per SM, whose warps take rows w, w + G, w + 2G, ... (G warps in all,
+// numbered warp-major across the blocks, so that the last, partial round of
+// rows is spread over every SM).  Each warp keeps NB of its rows in flight
+// through its own ring in shared memory: each lane copies its own vectors of
+// a row by 16-byte cp.async, one commit group per row (an empty group past
+// the warp's last row, so that every wait leaves NB - 1 newer groups
+// pending).  A lane reads back only what it copied, so its own wait (the
+// hardware's, no spin) is the only synchronisation.  It reads its vectors of
+// the row once, into registers, and normalises, takes the maximum and
+// quantises there.  The lane-to-vector split, and so every operation and its
+// order, is the register kernel's; the products go in packed pairs (the same
+// IEEE products).
+constexpr int kRqRingWarps = 12;
+constexpr int64_t kRqRingMinRows = 1024;  // from this many rows the ring kernel runs
+
+template <int VPL, int NB>
+struct RqRing {
+  static constexpr int vecs = VPL * 32;
+  static constexpr int smem = (1 + kRqRingWarps * NB) * vecs * 16;  // g, then the warps' rings
+  static_assert(smem <= kMaxDynSmem, "ring too large");
+};
+
+// The per-row work once a lane holds its vectors v of the row: the sum of
+// squares (split out so that the caller can refill the row's slot once every
+// vector has been consumed), then the norm, the maximum and the codes.
+template <int VPL>
+__device__ __forceinline__ float rq_row_sumsq(const uint4 (&v)[VPL]) {
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) ss = sumsq8(v[i], ss);
+  return butterfly_sum(ss);
+}
+
+template <int VPL>
+__device__ __forceinline__ void rq_row_finish(uint4 (&v)[VPL], float ss, const uint4* gs, int lane, float eps,
+                                              int64_t row, uint2* Q, float* scale) {
+  const float r = inv_rms(ss, (int64_t)VPL * 256, eps);
+  uint32_t am = 0u;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    v[i] = norm8_packed(v[i], gs[lane + 32 * i], r);
+    am = absmax8(am, v[i]);
+  }
+  const float amax = warp_amax(am);
+  const bool bad = !isfinite(amax);
+  const float s = e4m3_row_scale(amax, bad);
+  const float inv = e4m3_row_inv(amax);
+  if (lane == 0) scale[row] = s;
+  uint2* q = Q + row * (VPL * 32);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    q[lane + 32 * i] = bad ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu)
+                           : make_uint2(codes4_packed(v[i].x, v[i].y, inv), codes4_packed(v[i].z, v[i].w, inv));
+}
+
+template <int VPL, int NB>
+__global__ void __launch_bounds__(32 * kRqRingWarps, 1)
+    rmsnorm_quantize_ring_kernel(const uint4* X, const uint4* __restrict__ g, uint2* Q, float* scale, int64_t M,
+                                 float eps) {
+  constexpr int kVecs = VPL * 32;
+  extern __shared__ __align__(128) uint4 rr_smem[];
+  uint4* gs = rr_smem;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4* ring = rr_smem + (1 + warp * NB) * kVecs;
+  for (int i = threadIdx.x; i < kVecs; i += blockDim.x) gs[i] = __ldg(g + i);  // g is a weight
+  __syncthreads();
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the previous kernel in the stream
+  const int64_t G = (int64_t)gridDim.x * kRqRingWarps;
+  const int64_t w0 = (int64_t)warp * gridDim.x + blockIdx.x;
+  const int64_t n = w0 < M ? (M - 1 - w0) / G + 1 : 0;  // rows of this warp
+  auto issue = [&](int64_t k) {
+    if (k < n) {
+      const uint4* x = X + (w0 + k * G) * kVecs + lane;
+      const uint32_t dst = smem_u32(ring + (int)(k % NB) * kVecs + lane);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 512u * i), "l"(x + 32 * i) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+#pragma unroll
+  for (int b = 0; b < NB; ++b) issue(b);
+  for (int64_t k = 0; k < n; ++k) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(NB - 1) : "memory");  // row k has landed
+    uint4 v[VPL];
+    const uint4* buf = ring + (int)(k % NB) * kVecs + lane;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = buf[32 * i];
+    const float ss = rq_row_sumsq(v);
+    asm volatile("" ::"f"(ss) : "memory");  // every vector of the slot has been read: refill it
+    issue(k + NB);
+    rq_row_finish<VPL>(v, ss, gs, lane, eps, w0 + k * G, Q, scale);
+  }
+}
+
+template <int VPL, int NB>
+cudaError_t launch_rq_ring(const void* X, const void* g, void* Q, float* scale, int64_t M, float eps,
+                           cudaStream_t stream) {
+  using C = RqRing<VPL, NB>;
+  static std::atomic<uint64_t> configured{0};  // the shared-memory limit is per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(rmsnorm_quantize_ring_kernel<VPL, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = (M + kRqRingWarps - 1) / kRqRingWarps;
+  blocks = blocks < sms ? blocks : sms;
+  return launch_overlapped_smem(rmsnorm_quantize_ring_kernel<VPL, NB>, dim3((unsigned)blocks),
+                                dim3(32 * kRqRingWarps), (size_t)C::smem, stream, static_cast<const uint4*>(X),
+                                static_cast<const uint4*>(g), static_cast<uint2*>(Q), scale, M, eps);
+}
+
 cudaError_t launch_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, float* scale, int64_t M, int64_t H,
                                          float eps, cudaStream_t stream) {
   // the shared-memory limit is per device: set it once for each
@@ -330,13 +490,16 @@ cudaError_t launch_rmsnorm_quantize_e4m3(const void* X, const void* g, void* Q, 
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  // the row in registers for H = 2048, 4096 below 4096 rows (measured at
-  // H = 4096, M = 2048: 7.5 us with g staged in shared memory and 128
-  // registers, 8.8 with g from L2 and 205 registers, 12.4 staged).  At
-  // M = 8192 the staged kernel takes 20.7 us (0.72 of HBM; 26.4 before y was
-  // written back and the maximum taken packed) against 23.1 for the register
-  // kernel; a persistent variant with two rows per warp in flight took 23.1.
-  if ((H == 2048 || H == 4096) && M < 4096) {
+  // H = 2048, 4096: the streamed ring from 1024 rows, the row in registers
+  // below.  Measured (H = 4096, graph-replayed): ring against registers 4.8
+  // against 5.9 us at M = 1024, 9.1 against 10.6 at 3072, 18.0 against 20.7
+  // (the staged kernel) at 8192; 4.2 against 3.0 at M = 128.  At H = 2048 the
+  // ring wins from 1024 rows too (4.5 against 6.1 at 2560) except around
+  // 2048 rows (4.1 against 3.7), where the warps take two rows each.
+  if ((H == 2048 || H == 4096) && M >= kRqRingMinRows)
+    return H == 2048 ? launch_rq_ring<8, 4>(X, g, Q, scale, M, eps, stream)
+                     : launch_rq_ring<16, 2>(X, g, Q, scale, M, eps, stream);
+  if (H == 2048 || H == 4096) {
     // rows (warps) per block: ceil(M / 152) up to 8, as for the RMSNorm
     int64_t wpb = (M + 151) / 152;
     wpb = wpb < 1 ? 1 : (wpb > 8 ? 8 : wpb);

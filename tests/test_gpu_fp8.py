@@ -121,7 +121,7 @@ def test_fp8_rows_independent_of_batch(lib):
 
 
 @pytest.mark.parametrize("M,H", [(1, 4096), (37, 8192), (300, 4096), (5, 16384), (3, 1040), (2000, 2048),
-                                 (4100, 4096)])
+                                 (1023, 4096), (1024, 4096), (4100, 4096), (8192, 4096), (5001, 2048)])
 def test_rmsnorm_quantize_is_the_composition(lib, oracle, M, H):
     """One pass gives the codes and scales of bi_quantize_rows_e4m3 applied to
     bi_rmsnorm_bf16's output, bit for bit, and those are the oracle's
@@ -146,3 +146,25 @@ def test_rmsnorm_quantize_is_the_composition(lib, oracle, M, H):
     assert np.array_equal(np.isnan(got_s), np.isnan(want_s))
     ok = ~np.isnan(want_s)
     assert np.array_equal(got_s[ok].view(np.uint32), want_s[ok].view(np.uint32))
+
+
+@pytest.mark.parametrize("H", [2048, 4096])
+def test_rmsnorm_quantize_bits_across_the_kernel_switch(lib, H):
+    """Below 1024 rows a warp holds its row in registers; from 1024 rows the
+    rows stream through per-warp rings in shared memory (a persistent grid,
+    each warp taking every G-th row).  A row's codes and scale are the same
+    bits either way, and whatever batch the row is in: every row of a
+    4096 + 1900 row batch equals the same row computed in batches of 1000
+    (registers), 1 (registers), 3099 and 3000 (the ring)."""
+    M = 4096 + 1900
+    X = inputs.rows_loguniform(M, H, lo=1e-2, hi=1e2, seed=46, stream=0)
+    X[5] = 0
+    X[4097, 11] = float("nan")
+    g = inputs.normal((H,), std=0.1, mean=1.0, seed=46, stream=2)
+    x, gg = X.cuda(), g.cuda()
+    q, sc = lib.bi_rmsnorm_quantize_e4m3(x, gg, 1e-5)
+    q, sc = u8(q), sc.cpu().numpy().view(np.uint32)
+    for a, b in ((0, 1000), (1000, 1001), (1001, 4100), (M - 3000, M)):
+        qa, sa = lib.bi_rmsnorm_quantize_e4m3(x[a:b].contiguous(), gg, 1e-5)
+        assert np.array_equal(u8(qa), q[a:b]), (a, b)
+        assert np.array_equal(sa.cpu().numpy().view(np.uint32), sc[a:b]), (a, b)
