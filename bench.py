@@ -764,7 +764,7 @@ def run_attention(args, dist, peaks):
         max_len = bt.shape[1] * P
         alg = sum(lens) * Hkv * D * 2 * 2 + 2 * B * Hq * D * 2
         row = {"mix": name, "kv_bytes": sum(lens) * Hkv * D * 4, "splits": []}
-        for S in (128, 256, 320, 512, 1024):
+        for S in (128, 256, 320, 512, 576, 1024):
             ws = torch.empty(bd.bi_decode_attention_workspace_bytes(B, Hq, Hkv, max_len, S), dtype=torch.uint8,
                              device=dev)
             us = time_graph(lambda i: bd.bi_decode_attention_bf16(q, kc, vc, bt, sl, D ** -0.5, max_seq_len=max_len,

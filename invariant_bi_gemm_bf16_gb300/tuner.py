@@ -311,7 +311,10 @@ def load(path: str) -> Dict[tuple, object]:
 
 # --------------------------------------------------------------------------- decode attention
 
-ATTN_SPLITS = (64, 128, 256, 512, 1024, 2048, 4096)
+# Powers of two, and every multiple of 64 between 256 and 1024: a few long
+# requests are shared out among the CTAs (request, split) item by item, so the
+# split size that balances them need not be a power of two.
+ATTN_SPLITS = (64, 128, 256, 320, 384, 448, 512, 576, 640, 704, 768, 832, 896, 960, 1024, 2048, 4096)
 
 
 def attn_legal_splits(splits: Sequence[int] = ATTN_SPLITS) -> List[int]:

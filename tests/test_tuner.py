@@ -119,7 +119,8 @@ def test_attention_split_grid_is_the_legal_sizes(lib):
 
 def test_tune_attention_takes_the_argmin_and_keeps_the_default_within_the_margin(lib):
     # Detent, Sec. 7: the split stride is tuned like a pin.  A made-up cost per split size.
-    costs = {64: 10.0, 128: 8.0, 256: 9.0, 512: 5.0, 1024: 6.0, 2048: 7.0, 4096: 12.0}
+    costs = {S: 11.0 for S in tuner.ATTN_SPLITS}
+    costs.update({64: 10.0, 128: 8.0, 256: 9.0, 448: 5.5, 512: 5.0, 1024: 6.0, 2048: 7.0, 4096: 12.0})
     e = tuner.tune_attention(64, 8, 16, [([100, 200], 1)], timer=costs.__getitem__, repeats=1)
     att = e["attention"]
     assert att["split_size"] == 512 and att["T_us"] == 5.0 and att["T_default_us"] == 9.0
