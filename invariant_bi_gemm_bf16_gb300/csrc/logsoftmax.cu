@@ -252,8 +252,19 @@ __global__ void __launch_bounds__(kLsmThreads)
 // vectors g + kLsmStride i for i < 3 in shared memory (96 KB, staged by
 // 16-byte asynchronous copies) and its vector i = 3 in a register.  Rows
 // longer than kLsmCache * 8 * kLsmStride logits read their further vectors
-// from global memory in each pass.  Two CTAs share an SM, so one's loads
-// overlap the other's arithmetic and stores.
+// from global memory in each pass.
+//
+// Pair p takes rows p, p + P, p + 2P, ... for a grid of P pairs.  A thread
+// stages only its own vectors and reads back only those, so as soon as it
+// has written a slot's outputs (or, for the token variant, finished its sums)
+// it copies the next row's vector into that slot: the next row's loads
+// overlap this row's stores and reductions.  The token variant runs one pair
+// per SM from kLsmPersistRows rows (M = 256: 23.2 against 25.6 us with a
+// pair per row; M = 1024: 68.1 against 76.9).  Full rows run one pair per
+// row, the loop once: persistent pairs move in step, all reducing at once
+// while HBM idles, and took longer (M = 256: 56.8 against 55.2 us; M = 1024:
+// 171 against 161), where pairs that start wave by wave drift apart and fill
+// each other's gaps.
 constexpr int kLsmCtaThreads = 512;
 constexpr int kLsmHalf = kLsmCtas * kLsmThreads / 2;                 // cluster threads per CTA
 constexpr int kLsmVirt = kLsmHalf / kLsmCtaThreads;                   // cluster threads per thread
@@ -263,6 +274,7 @@ static_assert(kLsmVirt * 2 == kLsmCtas && kLsmThreads == kLsmCtaThreads, "rank j
 #ifndef BI_LSM_CTA_MIN_ROWS
 #define BI_LSM_CTA_MIN_ROWS 128  // measured: 8-CTA clusters win below (M = 96: 28 against 31 us)
 #endif
+constexpr int64_t kLsmPersistRows = 256;  // token variant: one pair per SM from this many rows
 
 struct LsmPairShared {
   float m[kLsmVirt][kLsmWarps], s[kLsmVirt][kLsmWarps];
@@ -275,123 +287,161 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Holds until the thread's load of v has completed (before a copy may
+// rewrite the shared-memory slot v came from).
+__device__ __forceinline__ void lsm_consumed(const uint4& v) {
+  asm volatile("" ::"r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 
 template <bool FULL>
 __global__ void __launch_bounds__(kLsmCtaThreads, 2)
     lsm_rows_kernel(const uint4* __restrict__ X, float4* __restrict__ Y, const int32_t* ids, float* out,
-                    int64_t nvec) {
+                    int64_t nvec, int64_t M) {
   extern __shared__ __align__(16) uint4 lsm_row[];
   __shared__ LsmPairShared sh;
   grid_dep_launch_dependents();
   grid_dep_wait();  // the logits may come from the previous kernel in the stream
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t rank = cluster_ctarank();
-  const int64_t row = blockIdx.x >> 1;
-  const uint4* x = X + row * nvec;
+  const int64_t pairs = gridDim.x >> 1;
   const int64_t g0 = (int64_t)rank * kLsmHalf;  // this CTA's first cluster thread
-  // stage vectors i < 3 (shared memory) and i = 3 (registers)
-#pragma unroll
-  for (int i = 0; i < kLsmCache - 1; ++i)
-#pragma unroll
-    for (int j = 0; j < kLsmVirt; ++j) {
-      const int h = t + j * kLsmCtaThreads;
-      const int64_t k = g0 + h + (int64_t)i * kLsmStride;
-      if (k < nvec) cp_async16(smem_u32(lsm_row + i * kLsmHalf + h), x + k);
-    }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  uint4 r[kLsmVirt];
-#pragma unroll
-  for (int j = 0; j < kLsmVirt; ++j) {
-    const int64_t k = g0 + t + j * kLsmCtaThreads + (int64_t)(kLsmCache - 1) * kLsmStride;
-    r[j] = k < nvec ? __ldg(x + k) : make_uint4(0, 0, 0, 0);
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
   const int64_t per = (nvec + kLsmStride - 1) / kLsmStride;  // vectors of cluster thread 0
+  int nvs[kLsmVirt];  // vectors of each played cluster thread (the same for every row)
 #pragma unroll
   for (int j = 0; j < kLsmVirt; ++j) {
-    const int h = t + j * kLsmCtaThreads;
-    const int64_t g = g0 + h;
-    const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
-    // vectors i < 3 (shared memory), i = 3 (register), i >= 4 (global), in order
-    float m = -INFINITY, s = 0.0f;
+    const int64_t g = g0 + t + j * kLsmCtaThreads;
+    nvs[j] = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
+  }
+  // the first row: vectors i < 3 into shared memory, i = 3 into registers
+  int64_t row = blockIdx.x >> 1;
+  uint4 r[kLsmVirt];
+  {
+    const uint4* x = X + row * nvec;
 #pragma unroll
     for (int i = 0; i < kLsmCache - 1; ++i)
-      if (i < nv) m = fmax_nan(m, max8(lsm_row[i * kLsmHalf + h]));
-    if (nv >= kLsmCache) m = fmax_nan(m, max8(r[j]));
-    for (int i = kLsmCache; i < nv; ++i) m = fmax_nan(m, max8(__ldg(x + g + (int64_t)i * kLsmStride)));
-    bool bad = bad_max(m);
-    if (m != -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < kLsmCache - 1; ++i)
-        if (i < nv) s = sumexp8(lsm_row[i * kLsmHalf + h], m, s);
-      if (nv >= kLsmCache) s = sumexp8(r[j], m, s);
-      for (int i = kLsmCache; i < nv; ++i) s = sumexp8(__ldg(x + g + (int64_t)i * kLsmStride), m, s);
-    }
-    ms_butterfly(m, s, bad);
-    if (lane == 0) {  // cluster CTA 4 rank + j, warp `warp`
-      sh.m[j][warp] = m;
-      sh.s[j][warp] = s;
-      sh.bad[j][warp] = bad;
-    }
+      for (int j = 0; j < kLsmVirt; ++j) {
+        const int h = t + j * kLsmCtaThreads;
+        if (i < nvs[j]) cp_async16(smem_u32(lsm_row + i * kLsmHalf + h), x + g0 + h + (int64_t)i * kLsmStride);
+      }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < kLsmVirt; ++j)
+      r[j] = nvs[j] >= kLsmCache ? __ldg(x + g0 + t + j * kLsmCtaThreads + (int64_t)(kLsmCache - 1) * kLsmStride)
+                                 : make_uint4(0, 0, 0, 0);
   }
-  __syncthreads();
-  if (warp < kLsmVirt) {  // warp j plays warp 0 of cluster CTA 4 rank + j
-    float m = lane < kLsmWarps ? sh.m[warp][lane] : -INFINITY;
-    float s = lane < kLsmWarps ? sh.s[warp][lane] : 0.0f;
-    bool bad = lane < kLsmWarps ? sh.bad[warp][lane] != 0 : false;
-    ms_butterfly(m, s, bad);
-    if (lane == 0) {
-      sh.cm[warp] = m;
-      sh.cs[warp] = s;
-      sh.cb[warp] = bad ? 1.0f : 0.0f;
-    }
-  }
-  cluster_sync();  // both CTAs' results are in their shared memory
-  if (rank == 0 && warp == 0) {  // warp 0 of cluster CTA 0
-    float m = -INFINITY, s = 0.0f;
-    bool bad = false;
-    if (lane < kLsmCtas) {
-      const uint32_t src = (uint32_t)(lane / kLsmVirt), w = (uint32_t)(lane % kLsmVirt);
-      m = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cm[w]), src));
-      s = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cs[w]), src));
-      bad = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cb[w]), src)) != 0.0f;
-    }
-    ms_butterfly(m, s, bad);
-    if (lane == 0) sh.lse = (bad || m == -INFINITY) ? __int_as_float(0x7fc00000) : m + logf(s);
-  }
-  cluster_sync();  // rank 0 has the lse
-  const float lse = ld_dsmem_f32(mapa_shared(smem_u32(&sh.lse), 0u));
-  cluster_sync();  // nobody leaves while its shared memory may still be read
-  if constexpr (FULL) {
-    float4* y = Y + row * nvec * 2;
+  for (; row < M; row += pairs) {
+    const uint4* x = X + row * nvec;
+    const int64_t next = row + pairs;
+    const uint4* xn = X + (next < M ? next : row) * nvec;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's copies of the row have landed
 #pragma unroll
     for (int j = 0; j < kLsmVirt; ++j) {
       const int h = t + j * kLsmCtaThreads;
       const int64_t g = g0 + h;
-      const int nv = (int)(per - (g >= nvec - (per - 1) * kLsmStride ? 1 : 0));
-      auto put = [&](const uint4& v, int i) {
-        const int64_t k = g + (int64_t)i * kLsmStride;
-        __stcs(y + 2 * k, make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse));
-        __stcs(y + 2 * k + 1,
-               make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse));
-      };
+      const int nv = nvs[j];
+      // vectors i < 3 (shared memory), i = 3 (register), i >= 4 (global), in order
+      float m = -INFINITY, s = 0.0f;
 #pragma unroll
       for (int i = 0; i < kLsmCache - 1; ++i)
-        if (i < nv) put(lsm_row[i * kLsmHalf + h], i);
-      if (nv >= kLsmCache) put(r[j], kLsmCache - 1);
-      for (int i = kLsmCache; i < nv; ++i) put(__ldg(x + g + (int64_t)i * kLsmStride), i);
+        if (i < nv) m = fmax_nan(m, max8(lsm_row[i * kLsmHalf + h]));
+      if (nv >= kLsmCache) m = fmax_nan(m, max8(r[j]));
+      for (int i = kLsmCache; i < nv; ++i) m = fmax_nan(m, max8(__ldg(x + g + (int64_t)i * kLsmStride)));
+      bool bad = bad_max(m);
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kLsmCache - 1; ++i)
+          if (i < nv) s = sumexp8(lsm_row[i * kLsmHalf + h], m, s);
+        if (nv >= kLsmCache) s = sumexp8(r[j], m, s);
+        for (int i = kLsmCache; i < nv; ++i) s = sumexp8(__ldg(x + g + (int64_t)i * kLsmStride), m, s);
+      }
+      if (!FULL && next < M) {
+        // the token variant is done with the staged row (m holds every
+        // staged value's maximum, so every load has completed): stage the next one
+        asm volatile("" ::"f"(m) : "memory");
+#pragma unroll
+        for (int i = 0; i < kLsmCache - 1; ++i)
+          if (i < nv) cp_async16(smem_u32(lsm_row + i * kLsmHalf + h), xn + g + (int64_t)i * kLsmStride);
+        if (nv >= kLsmCache) r[j] = __ldg(xn + g + (int64_t)(kLsmCache - 1) * kLsmStride);
+      }
+      ms_butterfly(m, s, bad);
+      if (lane == 0) {  // cluster CTA 4 rank + j, warp `warp`
+        sh.m[j][warp] = m;
+        sh.s[j][warp] = s;
+        sh.bad[j][warp] = bad;
+      }
     }
-  } else if (rank == 0 && t == 0) {
-    const int32_t id = ids[row];
-    const int64_t V = nvec * 8;
-    float res = __int_as_float(0x7fc00000);
-    if (id >= 0 && id < V) {
-      const uint16_t b = reinterpret_cast<const uint16_t*>(x)[id];
-      res = __uint_as_float((uint32_t)b << 16) - lse;
+    if (!FULL) asm volatile("cp.async.commit_group;" ::: "memory");
+    __syncthreads();
+    if (warp < kLsmVirt) {  // warp j plays warp 0 of cluster CTA 4 rank + j
+      float m = lane < kLsmWarps ? sh.m[warp][lane] : -INFINITY;
+      float s = lane < kLsmWarps ? sh.s[warp][lane] : 0.0f;
+      bool bad = lane < kLsmWarps ? sh.bad[warp][lane] != 0 : false;
+      ms_butterfly(m, s, bad);
+      if (lane == 0) {
+        sh.cm[warp] = m;
+        sh.cs[warp] = s;
+        sh.cb[warp] = bad ? 1.0f : 0.0f;
+      }
     }
-    out[row] = res;
+    cluster_sync();  // both CTAs' results are in their shared memory
+    if (rank == 0 && warp == 0) {  // warp 0 of cluster CTA 0
+      float m = -INFINITY, s = 0.0f;
+      bool bad = false;
+      if (lane < kLsmCtas) {
+        const uint32_t src = (uint32_t)(lane / kLsmVirt), w = (uint32_t)(lane % kLsmVirt);
+        m = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cm[w]), src));
+        s = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cs[w]), src));
+        bad = ld_dsmem_f32(mapa_shared(smem_u32(&sh.cb[w]), src)) != 0.0f;
+      }
+      ms_butterfly(m, s, bad);
+      if (lane == 0) sh.lse = (bad || m == -INFINITY) ? __int_as_float(0x7fc00000) : m + logf(s);
+    }
+    cluster_sync();  // rank 0 has the lse
+    const float lse = ld_dsmem_f32(mapa_shared(smem_u32(&sh.lse), 0u));
+    cluster_sync();  // the lse is read everywhere before the next row rewrites the pairs
+    if constexpr (FULL) {
+      float4* y = Y + row * nvec * 2;
+#pragma unroll
+      for (int j = 0; j < kLsmVirt; ++j) {
+        const int h = t + j * kLsmCtaThreads;
+        const int64_t g = g0 + h;
+        const int nv = nvs[j];
+        auto put = [&](const uint4& v, int i) {
+          const int64_t k = g + (int64_t)i * kLsmStride;
+          __stcs(y + 2 * k, make_float4(lsm_lo(v.x) - lse, lsm_hi(v.x) - lse, lsm_lo(v.y) - lse, lsm_hi(v.y) - lse));
+          __stcs(y + 2 * k + 1,
+                 make_float4(lsm_lo(v.z) - lse, lsm_hi(v.z) - lse, lsm_lo(v.w) - lse, lsm_hi(v.w) - lse));
+        };
+#pragma unroll
+        for (int i = 0; i < kLsmCache - 1; ++i)
+          if (i < nv) {
+            const uint4 v = lsm_row[i * kLsmHalf + h];
+            put(v, i);
+            if (next < M) {  // the slot is free: stage the next row's vector
+              lsm_consumed(v);
+              cp_async16(smem_u32(lsm_row + i * kLsmHalf + h), xn + g + (int64_t)i * kLsmStride);
+            }
+          }
+        if (nv >= kLsmCache) {
+          put(r[j], kLsmCache - 1);
+          if (next < M) r[j] = __ldg(xn + g + (int64_t)(kLsmCache - 1) * kLsmStride);
+        }
+        for (int i = kLsmCache; i < nv; ++i) put(__ldg(x + g + (int64_t)i * kLsmStride), i);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    } else if (rank == 0 && t == 0) {
+      const int32_t id = ids[row];
+      const int64_t V = nvec * 8;
+      float res = __int_as_float(0x7fc00000);
+      if (id >= 0 && id < V) {
+        const uint16_t b = reinterpret_cast<const uint16_t*>(x)[id];
+        res = __uint_as_float((uint32_t)b << 16) - lse;
+      }
+      out[row] = res;
+    }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the block
 }
 
 template <bool FULL>
@@ -408,8 +458,14 @@ static cudaError_t launch_lsm_rows(const void* X, void* Y, const int32_t* ids, f
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
+  // pairs: one per row, or for the token variant from kLsmPersistRows rows
+  // one per SM (two CTAs of a pair's size fit on an SM)
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t pairs = (!FULL && M >= kLsmPersistRows && M > sms) ? sms : M;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * M));
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
   cfg.blockDim = dim3(kLsmCtaThreads);
   cfg.dynamicSmemBytes = kLsmSmemBytes;
   cfg.stream = stream;
@@ -423,7 +479,7 @@ static cudaError_t launch_lsm_rows(const void* X, void* Y, const int32_t* ids, f
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, lsm_rows_kernel<FULL>, static_cast<const uint4*>(X), static_cast<float4*>(Y), ids,
-                            out, V / 8);
+                            out, V / 8, M);
 }
 
 template <typename... KArgs, typename... Args>

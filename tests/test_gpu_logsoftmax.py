@@ -142,3 +142,33 @@ def test_lm_head_logprobs_batch_invariant(lib, oracle):
     ref = oracle.token_logprobs(bf16_bits(logits), ids[:4].cpu().numpy())
     got = lib.bi_token_logprobs_bf16(logits, ids[:4]).cpu().numpy()
     assert np.all(np.abs(got - ref) <= 300 * 2.0 ** -23 + 2.0 ** -21 * np.abs(ref))
+
+
+@pytest.mark.parametrize("V", [1000, 128256, 140008])
+def test_token_logprobs_on_persistent_pairs(lib, V):
+    """From 256 rows the token variant runs one CTA pair per SM, each pair
+    taking every P-th row and staging its next row while it reduces this one.
+    Each row's log-probability keeps its bits: equal to the full
+    log-softmax's element (one pair per row) and to the row computed alone
+    (an 8-CTA cluster), for rows longer than the on-chip cache and special
+    rows; ids outside [0, V) give NaN."""
+    M = 400
+    X = inputs.normal((M, V), std=4.0, seed=25, stream=0)
+    X[5, :] = float("-inf")
+    X[160, V // 3] = float("nan")
+    X[399, V - 1] = float("inf")
+    X = X.cuda()
+    ids = torch.from_numpy(np.random.default_rng(25).integers(0, V, size=M).astype(np.int32))
+    ids[11] = -1
+    ids[300] = V
+    tok = lib.bi_token_logprobs_bf16(X, ids.cuda()).cpu().numpy().view(np.uint32)
+    full = lib.bi_log_softmax_bf16(X).cpu().numpy().view(np.uint32)
+    idn = ids.numpy()
+    for r in range(M):
+        if r in (11, 300):
+            assert np.isnan(tok[r].view(np.float32)), r
+        else:
+            assert tok[r] == full[r, idn[r]], r
+    for r in (0, 5, 151, 152, 160, 303, 304, 399):
+        t1 = lib.bi_token_logprobs_bf16(X[r:r + 1].contiguous(), ids[r:r + 1].cuda()).cpu().numpy().view(np.uint32)
+        assert t1[0] == tok[r], r
