@@ -307,7 +307,10 @@ size_t bi_gemm_bf16_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * row the same bits whatever batch it is computed in).
  * Ring depth: as many slots of bi_gemm_bf16_host_slot_bytes bytes as
  * `workspace_bytes` holds, at most 8 and at most the number of chunks; the
- * size the workspace query returns gives two.
+ * size the workspace query returns gives two.  With three or more slots the
+ * last rows go in halving chunks (multiples of 128 rows, the last 256 or
+ * fewer whole), so that little is left to multiply and copy out after the
+ * last copy-in.
  * Ownership: X_host and Y_host are caller-owned host memory (page-locked for
  * the copies to overlap; pageable memory works, with synchronous copies);
  * W and `workspace` are caller-owned device memory, `workspace` at least
