@@ -91,3 +91,26 @@ def test_fullsize_fp8_sampled_parity(lib, oracle):
         ref = (yf.astype(np.float64) * sx_np[:, None] * sw_np[None, :]).astype(np.float32)
         idx = torch.from_numpy(rows).cuda()
         check_gemm_parity(bf16_bits(Y[idx]), ref, K, "fp8 N=%d K=%d M=%d" % (N, K, M))
+
+
+def test_fullsize_host_batch_sweep(lib, oracle):
+    """The end-to-end launch configuration of the benchmark: the whole
+    down_proj M sweep (M = 1, 2, 4 .. 8192, 16383 rows) as one
+    bi_gemm_bf16_host_batch call from page-locked memory, 2304-row chunks and
+    a ring of 8 slots (so the last rows go in halving chunks), two weight
+    copies alternating between the jobs.  Every job's rows are the bits
+    bi_gemm_bf16 gives on device copies; sampled whole rows of the largest
+    job are the oracle's within the GEMM tolerance."""
+    N, K = 4096, 14336
+    Ws = [inputs.device_normal((N, K), std=0.02, seed=0, stream=inputs.STREAM_W + 16 * i) for i in range(2)]
+    Ms = [1 << i for i in range(14)]
+    xs = [inputs.device_normal((M, K), seed=0, stream=inputs.STREAM_X + 16 * j).cpu().pin_memory()
+          for j, M in enumerate(Ms)]
+    wl = [Ws[j % 2] for j in range(len(Ms))]
+    ws = torch.empty(8 * lib.bi_gemm_bf16_host_slot_bytes(Ms, N, K, 2304), dtype=torch.uint8, device="cuda")
+    outs = lib.bi_gemm_bf16_host_batch(xs, wl, workspace=ws, chunk_rows=2304)
+    torch.cuda.synchronize()
+    assert lib.bi_last_device_status() == lib.BI_OK
+    for x, w, y in zip(xs, wl, outs):
+        assert np.array_equal(bf16_bits(y), bf16_bits(lib.bi_gemm_bf16(x.cuda(), w))), x.shape[0]
+    sampled_parity(oracle, xs[-1], Ws[13 % 2].cpu(), outs[-1], 4, 7, "host batch M=8192")
