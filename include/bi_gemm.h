@@ -369,6 +369,27 @@ bi_status bi_gemm_bf16_host_batch(const bi_host_gemm_job* jobs, int32_t n_jobs, 
                                   const bi_pins* pins, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
                                   bi_stream_t stream);
 
+/* One chunk of the schedule bi_gemm_bf16_host_batch follows. */
+typedef struct bi_host_chunk {
+  int32_t job;  /* index of the job in the list */
+  int32_t slot; /* ring slot holding the chunk's X and Y */
+  int64_t row0; /* first row of the job in the chunk */
+  int64_t rows; /* rows in the chunk */
+} bi_host_chunk;
+
+/* The chunk schedule of bi_gemm_bf16_host_batch for these arguments (only
+ * each job's M is read): the chunks in the order they are copied in,
+ * multiplied and copied out, each job's rows covered once and in order.
+ * Writes the first min(*n_chunks, max_chunks) chunks to `chunks` and the
+ * count to *n_chunks (0 when no job has rows).  A host-only call.
+ * Errors: BI_ERR_INVALID_ARG for a NULL n_chunks, max_chunks < 0 or a NULL
+ * `chunks` with max_chunks > 0; BI_ERR_WORKSPACE for workspace_bytes below
+ * bi_gemm_bf16_host_batch_workspace_bytes; otherwise as
+ * bi_gemm_bf16_host_batch for the rows, the shape and chunk_rows. */
+bi_status bi_gemm_bf16_host_schedule(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                     int64_t chunk_rows, size_t workspace_bytes, bi_host_chunk* chunks,
+                                     int64_t max_chunks, int64_t* n_chunks);
+
 /* Y[M,H] = RMSNorm(X[M,H]) with gain g[H], one warp per row: each lane sums
  * the squares of its 16-byte vectors in ascending order, the 32 lane sums are
  * combined by a fixed xor-butterfly, r = 1/sqrt(sum/H + eps) (IEEE division

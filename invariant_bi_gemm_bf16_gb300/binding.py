@@ -98,6 +98,12 @@ class HostGemmJob(ctypes.Structure):
                 ("M", ctypes.c_int64)]
 
 
+class HostChunk(ctypes.Structure):
+    """bi_host_chunk: one chunk of bi_gemm_bf16_host_batch's schedule."""
+    _fields_ = [("job", ctypes.c_int32), ("slot", ctypes.c_int32), ("row0", ctypes.c_int64),
+                ("rows", ctypes.c_int64)]
+
+
 class BiError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -135,6 +141,9 @@ _SIGNATURES = {
                                                        _i64]),
     "bi_gemm_bf16_host_batch": (ctypes.c_int, [ctypes.POINTER(HostGemmJob), ctypes.c_int32, _i64, _i64,
                                                ctypes.POINTER(Pins), _i64, _vp, ctypes.c_size_t, _vp]),
+    "bi_gemm_bf16_host_schedule": (ctypes.c_int, [ctypes.POINTER(HostGemmJob), ctypes.c_int32, _i64, _i64, _i64,
+                                                  ctypes.c_size_t, ctypes.POINTER(HostChunk), _i64,
+                                                  ctypes.POINTER(_i64)]),
     "bi_rmsnorm_gemm_workspace_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "bi_rmsnorm_gemm_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float,
                                             ctypes.POINTER(Pins), _vp, ctypes.c_size_t, _vp]),
@@ -362,6 +371,22 @@ def bi_gemm_bf16_host_slot_bytes(ms, N: int, K: int, chunk_rows: int = 0) -> int
     """Bytes of one ring slot for jobs of ms[j] rows; d slots give a ring of
     depth d (at most 8)."""
     return int(load().bi_gemm_bf16_host_slot_bytes(_job_array(ms), len(ms), N, K, chunk_rows))
+
+
+def bi_gemm_bf16_host_schedule(ms, N: int, K: int, chunk_rows: int = 0, workspace_bytes: int | None = None) -> list:
+    """The chunks bi_gemm_bf16_host_batch would run for jobs of ms[j] rows, as
+    (job, slot, row0, rows) tuples in order; workspace_bytes (the size of the
+    workspace, which sets the ring depth) defaults to the workspace query's."""
+    if workspace_bytes is None:
+        workspace_bytes = bi_gemm_bf16_host_batch_workspace_bytes(ms, N, K, chunk_rows)
+    arr = _job_array(ms)
+    n = _i64(0)
+    _check(load().bi_gemm_bf16_host_schedule(arr, len(ms), N, K, chunk_rows, int(workspace_bytes), None, 0,
+                                             ctypes.byref(n)), "bi_gemm_bf16_host_schedule")
+    out = (HostChunk * max(n.value, 1))()
+    _check(load().bi_gemm_bf16_host_schedule(arr, len(ms), N, K, chunk_rows, int(workspace_bytes), out, n.value,
+                                             ctypes.byref(n)), "bi_gemm_bf16_host_schedule")
+    return [(c.job, c.slot, c.row0, c.rows) for c in out[:n.value]]
 
 
 def bi_gemm_bf16_host_batch(xs, ws, outs=None, pins: Pins | None = None, workspace: torch.Tensor | None = None,

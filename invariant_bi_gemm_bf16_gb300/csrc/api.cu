@@ -743,9 +743,10 @@ bool host_ctx_init(HostCtx& c) {
   return true;
 }
 
-// Every argument is checked before anything is enqueued.
-bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t K, const bi_pins* pins,
-                    int64_t chunk_rows, void* workspace, size_t ws_bytes, cudaStream_t s) {
+// The checks the call and its schedule query share: the list, the rows, the
+// shape and chunk_rows.  Sets R and the chunk count before the taper.
+bi_status host_check_rows(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t K, int64_t chunk_rows,
+                          int64_t* R, int64_t* chunks) {
   if (n < 0 || (n > 0 && !jobs) || chunk_rows < 0) return BI_ERR_INVALID_ARG;
   for (int32_t j = 0; j < n; ++j)
     if (jobs[j].M < 0) return BI_ERR_INVALID_ARG;
@@ -754,11 +755,46 @@ bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t 
   for (int32_t j = 0; j < n; ++j)
     if (jobs[j].M > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
   if (chunk_rows > 0x7FFFFFFFll) return BI_ERR_UNSUPPORTED_SHAPE;
+  *R = 0;
+  *chunks = 0;
+  host_chunking(jobs, n, K, chunk_rows, R, chunks);
+  return BI_OK;
+}
+
+// Ring depth: as many slots as the workspace holds, up to kHostMaxSlots and
+// the chunk count.
+int64_t host_depth(size_t ws_bytes, uint64_t slot, int64_t chunks) {
+  int64_t depth = (int64_t)(ws_bytes / slot);
+  depth = depth > kHostMaxSlots ? kHostMaxSlots : depth;
+  return depth > chunks ? chunks : depth;
+}
+
+// Calls fn(job, slot, row0, rows, index) for every chunk of the list in order
+// (the schedule the call follows); stops when fn returns false.
+template <typename F>
+void host_for_each_chunk(const bi_host_gemm_job* jobs, int32_t n, int64_t R, int64_t depth, F fn) {
+  int32_t last = -1;  // the last job with rows
+  for (int32_t j = 0; j < n; ++j)
+    if (jobs[j].M > 0) last = j;
+  int64_t ch = 0;
+  for (int32_t j = 0; j < n; ++j) {
+    int64_t rows = 0;
+    for (int64_t r0 = 0; r0 < jobs[j].M; r0 += rows, ++ch) {
+      rows = host_next_rows(jobs[j].M - r0, R, j == last && depth >= 3);
+      if (!fn(j, (int)(ch % depth), r0, rows, ch)) return;
+    }
+  }
+}
+
+// Every argument is checked before anything is enqueued.
+bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t K, const bi_pins* pins,
+                    int64_t chunk_rows, void* workspace, size_t ws_bytes, cudaStream_t s) {
+  int64_t R = 0, chunks = 0;
+  bi_status st = host_check_rows(jobs, n, N, K, chunk_rows, &R, &chunks);
+  if (st != BI_OK) return st;
   Resolved r;
   st = resolve_pins(N, K, pins, &r);
   if (st != BI_OK) return st;
-  int64_t R = 0, chunks = 0;
-  host_chunking(jobs, n, K, chunk_rows, &R, &chunks);
   if (chunks == 0) return BI_OK;
   for (int32_t j = 0; j < n; ++j) {
     if (jobs[j].M == 0) continue;
@@ -768,10 +804,7 @@ bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t 
   const uint64_t slot = host_slot_bytes(R, N, K), xoff = round256((uint64_t)R * (uint64_t)K * 2u);
   if (!workspace || ws_bytes < host_workspace_bytes(jobs, n, N, K, chunk_rows)) return BI_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BI_ERR_ALIGNMENT;
-  // ring depth: as many slots as the workspace holds, up to kHostMaxSlots
-  int64_t depth = (int64_t)(ws_bytes / slot);
-  depth = depth > kHostMaxSlots ? kHostMaxSlots : depth;
-  depth = depth > chunks ? chunks : depth;
+  const int64_t depth = host_depth(ws_bytes, slot, chunks);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BI_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_host_mu[dev]);
@@ -783,38 +816,32 @@ bi_status host_gemm(const bi_host_gemm_job* jobs, int32_t n, int64_t N, int64_t 
       !ok(cudaStreamWaitEvent(c.out, c.start, 0)))
     return BI_ERR_CUDA;
   bi_status result = BI_OK;
-  int64_t ch = 0;  // chunk index over all jobs
-  int32_t last = -1;  // the last job with rows
-  for (int32_t j = 0; j < n; ++j)
-    if (jobs[j].M > 0) last = j;
-  for (int32_t j = 0; j < n && result == BI_OK; ++j) {
+  host_for_each_chunk(jobs, n, R, depth, [&](int32_t j, int i, int64_t r0, int64_t rows, int64_t ch) {
     const bi_host_gemm_job& job = jobs[j];
-    int64_t rows = 0;
-    for (int64_t r0 = 0; r0 < job.M && result == BI_OK; r0 += rows, ++ch) {
-      const int i = (int)(ch % depth);
-      rows = host_next_rows(job.M - r0, R, j == last && depth >= 3);
-      char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
-      char* yd = xd + xoff;
-      // the slot's previous chunk has been copied out (so also multiplied)
-      if (ch >= depth && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) {
-        result = BI_ERR_CUDA;
-        break;
-      }
-      if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(job.X_host) + (uint64_t)r0 * K * 2,
-                              (size_t)rows * K * 2, cudaMemcpyHostToDevice, c.in)) ||
-          !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0))) {
-        result = BI_ERR_CUDA;
-        break;
-      }
-      result = gemm_impl(xd, job.W, yd, rows, N, K, pins, s);
-      if (result != BI_OK) break;
-      if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
-          !ok(cudaMemcpyAsync(static_cast<char*>(job.Y_host) + (uint64_t)r0 * N * 2, yd, (size_t)rows * N * 2,
-                              cudaMemcpyDeviceToHost, c.out)) ||
-          !ok(cudaEventRecord(c.copied_out[i], c.out)))
-        result = BI_ERR_CUDA;
+    char* xd = static_cast<char*>(workspace) + (uint64_t)i * slot;
+    char* yd = xd + xoff;
+    // the slot's previous chunk has been copied out (so also multiplied)
+    if (ch >= depth && !ok(cudaStreamWaitEvent(c.in, c.copied_out[i], 0))) {
+      result = BI_ERR_CUDA;
+      return false;
     }
-  }
+    if (!ok(cudaMemcpyAsync(xd, static_cast<const char*>(job.X_host) + (uint64_t)r0 * K * 2, (size_t)rows * K * 2,
+                            cudaMemcpyHostToDevice, c.in)) ||
+        !ok(cudaEventRecord(c.copied_in[i], c.in)) || !ok(cudaStreamWaitEvent(s, c.copied_in[i], 0))) {
+      result = BI_ERR_CUDA;
+      return false;
+    }
+    result = gemm_impl(xd, job.W, yd, rows, N, K, pins, s);
+    if (result != BI_OK) return false;
+    if (!ok(cudaEventRecord(c.multiplied[i], s)) || !ok(cudaStreamWaitEvent(c.out, c.multiplied[i], 0)) ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(job.Y_host) + (uint64_t)r0 * N * 2, yd, (size_t)rows * N * 2,
+                            cudaMemcpyDeviceToHost, c.out)) ||
+        !ok(cudaEventRecord(c.copied_out[i], c.out))) {
+      result = BI_ERR_CUDA;
+      return false;
+    }
+    return true;
+  });
   // the caller's stream resumes once every copy enqueued so far has landed
   // (also after an error, so that no copy outlives the call's buffers
   // unseen by the caller's stream)
@@ -1001,6 +1028,26 @@ BI_API bi_status bi_gemm_bf16_host_batch(const bi_host_gemm_job* jobs, int32_t n
                                          size_t ws_bytes, bi_stream_t stream) {
   return host_gemm(jobs, n_jobs, N, K, pins, chunk_rows, workspace, ws_bytes,
                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_gemm_bf16_host_schedule(const bi_host_gemm_job* jobs, int32_t n_jobs, int64_t N, int64_t K,
+                                            int64_t chunk_rows, size_t workspace_bytes, bi_host_chunk* chunks,
+                                            int64_t max_chunks, int64_t* n_chunks) {
+  if (!n_chunks || max_chunks < 0 || (max_chunks > 0 && !chunks)) return BI_ERR_INVALID_ARG;
+  *n_chunks = 0;
+  int64_t R = 0, count = 0;
+  bi_status st = host_check_rows(jobs, n_jobs, N, K, chunk_rows, &R, &count);
+  if (st != BI_OK || count == 0) return st;
+  if (workspace_bytes < host_workspace_bytes(jobs, n_jobs, N, K, chunk_rows)) return BI_ERR_WORKSPACE;
+  const int64_t depth = host_depth(workspace_bytes, host_slot_bytes(R, N, K), count);
+  int64_t total = 0;
+  host_for_each_chunk(jobs, n_jobs, R, depth, [&](int32_t j, int i, int64_t r0, int64_t rows, int64_t ch) {
+    if (ch < max_chunks) chunks[ch] = bi_host_chunk{j, i, r0, rows};
+    total = ch + 1;
+    return true;
+  });
+  *n_chunks = total;
+  return BI_OK;
 }
 
 BI_API size_t bi_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K) { return fused_workspace_bytes(M, K); }

@@ -292,6 +292,90 @@ def test_host_batch_arguments_rejected_before_any_launch(bd):
         bd.bi_gemm_bf16_host_batch([], [None])
 
 
+def test_host_schedule_of_the_benchmark_sweep(bd):
+    """The down_proj sweep as one list, 2304-row chunks: with a ring of two
+    slots every job goes in whole chunks; with eight the last job's last rows
+    go in halving chunks (multiples of 128, the last 256 whole), so that
+    little is left after the last copy-in."""
+    N, K = 4096, 14336
+    sweep = [1 << i for i in range(14)]
+    slot = bd.bi_gemm_bf16_host_slot_bytes(sweep, N, K, 2304)
+    two = bd.bi_gemm_bf16_host_schedule(sweep, N, K, 2304)
+    assert [c[3] for c in two if c[0] == 13] == [2304, 2304, 2304, 1280]
+    assert [c[1] for c in two] == [i % 2 for i in range(len(two))]
+    eight = bd.bi_gemm_bf16_host_schedule(sweep, N, K, 2304, 8 * slot)
+    assert [c[3] for c in eight if c[0] == 13] == [2304, 2304, 1792, 896, 384, 256, 256]
+    assert [c[3] for c in eight if c[0] == 12] == [2304, 1792]
+    assert [c[1] for c in eight] == [i % 8 for i in range(len(eight))]
+    # the default chunk (512 rows here) and three slots: the taper starts at 1024 rows left
+    three = bd.bi_gemm_bf16_host_schedule([8192], N, K, 0, 3 * bd.bi_gemm_bf16_host_slot_bytes([8192], N, K))
+    assert [c[3] for c in three][-4:] == [512, 512, 256, 256] and len(three) == 17
+    assert bd.bi_gemm_bf16_host_schedule([0, 0], N, K) == []
+
+
+def test_host_schedule_covers_every_row_once(bd):
+    """On random lists: the chunks cover each job's rows once, in order, job
+    after job; no chunk is above the chunk rows; the slots rotate through a
+    ring of at most 8 slots and at most what the workspace holds; only the
+    last job with rows is cut finer than the chunk rows, only with a ring of
+    three slots or more, and then into multiples of 128 rows (its last piece
+    aside)."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    N, K = 1024, 4096
+    for _ in range(300):
+        ms = [int(rng.choice([0, rng.integers(1, 300), rng.integers(1, 6000)])) for _ in range(rng.integers(1, 7))]
+        cr = int(rng.choice([0, 128, 300, 1000, 2304]))
+        if sum(ms) == 0:
+            assert bd.bi_gemm_bf16_host_schedule(ms, N, K, cr) == []
+            continue
+        slot = bd.bi_gemm_bf16_host_slot_bytes(ms, N, K, cr)
+        ws = max(bd.bi_gemm_bf16_host_batch_workspace_bytes(ms, N, K, cr), int(rng.integers(1, 11)) * slot)
+        sched = bd.bi_gemm_bf16_host_schedule(ms, N, K, cr, ws)
+        if cr:
+            assert max(c[3] for c in sched) <= min(cr, max(ms))
+        pieces = {j: [] for j in range(len(ms))}
+        prev = -1
+        for j, _slot, r0, rows in sched:
+            assert j >= prev and rows >= 1 and r0 == sum(pieces[j])
+            prev = j
+            pieces[j].append(rows)
+        assert all(sum(pieces[j]) == M for j, M in enumerate(ms))
+        slots = [c[1] for c in sched]
+        depth = max(slots) + 1
+        assert slots == [i % depth for i in range(len(sched))]
+        assert depth <= min(8, ws // slot)
+        last = max(j for j, M in enumerate(ms) if M > 0)
+        for j, M in enumerate(ms):
+            p = pieces[j]
+            if M == 0:
+                continue
+            if j != last or depth < 3:
+                # whole chunks of the chunk rows, the remainder last
+                assert all(r == p[0] for r in p[:-1]) and p[-1] <= p[0], (ms, cr, j, p)
+            else:
+                assert all(r % 128 == 0 and r >= 128 for r in p[:-1] if r < p[0]), (ms, cr, p)
+
+
+def test_host_schedule_arguments(bd):
+    lib = bd.load()
+    arr = bd._job_array([5, 9])
+    n = ctypes.c_int64(0)
+    call = lib.bi_gemm_bf16_host_schedule
+    assert call(arr, 2, 128, 256, 0, 1 << 30, None, 0, None) == bd.BI_ERR_INVALID_ARG
+    assert call(arr, 2, 128, 256, 0, 1 << 30, None, 1, ctypes.byref(n)) == bd.BI_ERR_INVALID_ARG
+    assert call(arr, 2, 128, 256, 0, 1 << 30, None, -1, ctypes.byref(n)) == bd.BI_ERR_INVALID_ARG
+    assert call(arr, 2, 128, 256, -1, 1 << 30, None, 0, ctypes.byref(n)) == bd.BI_ERR_INVALID_ARG
+    assert call(arr, 2, 128, 250, 0, 1 << 30, None, 0, ctypes.byref(n)) == bd.BI_ERR_UNSUPPORTED_SHAPE
+    need = lib.bi_gemm_bf16_host_batch_workspace_bytes(arr, 2, 128, 256, 0)
+    assert call(arr, 2, 128, 256, 0, need - 1, None, 0, ctypes.byref(n)) == bd.BI_ERR_WORKSPACE
+    assert call(arr, 2, 128, 256, 0, need, None, 0, ctypes.byref(n)) == bd.BI_OK and n.value == 2
+    # fewer entries than chunks: the first ones are written, the count is whole
+    out = (bd.HostChunk * 1)()
+    assert call(arr, 2, 128, 256, 0, need, out, 1, ctypes.byref(n)) == bd.BI_OK and n.value == 2
+    assert (out[0].job, out[0].slot, out[0].row0, out[0].rows) == (0, 0, 0, 5)
+
+
 @pytest.mark.parametrize("N,K", TABLE_SHAPES + [(300, 200), (20000, 1000)])
 def test_reduction_tree_never_depends_on_m(bd, N, K):
     """Detent Sec. 8.2: the batch reaches no GEMM selection point.  The plan's
